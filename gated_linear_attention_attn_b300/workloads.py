@@ -1,0 +1,116 @@
+"""Workload shapes and seeded synthetic inputs for the linear-attention forward.
+
+This module holds no arithmetic of the layer itself: it only names the shapes
+and draws the random inputs, so both the CUDA path and the fp64 oracle can be
+fed the same values.
+
+Shapes come from the latent token grids of SANA-Video 2.0 (NVlabs/Sana
+docs/sana_video2.md, "Architecture": 20 heads x 128 for 5B, 32 heads x 128 for
+14B; (1, 1, 1) latent patches over an LTX 2.3 latent with (8, 32, 32)
+temporal/spatial strides, so N = T * (height/32) * (width/32) with
+T = (frames - 1)/8 + 1).
+
+Input recipe: one CPU ``torch.Generator`` seeded with ``seed`` draws q, k, v, g
+in that order as float32 N(0, 1) tensors of shape [B, H, N, d]; k is then
+scaled by ``k_scale``; all four are cast to the workload dtype.  Values are
+i.i.d., so no dataset is needed.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional, Tuple
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    grid: Tuple[int, int, int]          # (T, Hs, Ws) latent token grid
+    d: int = 128
+    dtype: torch.dtype = torch.bfloat16
+    rope: bool = False
+    split: Tuple[int, int, int] = (44, 42, 42)   # head-dim bands for t, h, w
+    base: float = 10000.0
+    eps: float = 1e-6
+    k_scale: float = 1.0
+    tol: float = 1e-2                   # max|err| / max|ref| bound for parity
+    description: str = ""
+
+    @property
+    def N(self) -> int:
+        T, Hs, Ws = self.grid
+        return T * Hs * Ws
+
+    @property
+    def token_heads(self) -> int:
+        return self.B * self.H * self.N
+
+    @property
+    def elem_size(self) -> int:
+        return torch.empty((), dtype=self.dtype).element_size()
+
+    @property
+    def algorithmic_bytes(self) -> int:
+        """Reads of q, k, v, g and the write of o: 5 * B*H*N*d elements."""
+        return 5 * self.B * self.H * self.N * self.d * self.elem_size
+
+    @property
+    def algorithmic_flops(self) -> int:
+        """Two d x d contractions per token: 4 * B*H*N*d^2."""
+        return 4 * self.B * self.H * self.N * self.d * self.d
+
+    def with_(self, **kw) -> "Workload":
+        fields = dict(self.__dict__)
+        fields.update(kw)
+        return Workload(**fields)
+
+
+WORKLOADS = {
+    "tiny_fp32": Workload(
+        "tiny_fp32", B=1, H=2, grid=(4, 8, 8), dtype=torch.float32, tol=1e-5,
+        description="oracle-size check: B=1 H=2 N=256 (4x8x8) fp32, no RoPE"),
+    "5b_480p": Workload(
+        "5b_480p", B=2, H=20, grid=(11, 15, 26),
+        description="5B shape, 480p/81 frames: B=2 H=20 N=4290 (11x15x26) bf16, no RoPE"),
+    "5b_720p": Workload(
+        "5b_720p", B=2, H=20, grid=(25, 22, 40), rope=True,
+        description="5B shape, 720p/193 frames: B=2 H=20 N=22000 (25x22x40) bf16, 3D RoPE 44/42/42"),
+    "14b_480p": Workload(
+        "14b_480p", B=2, H=32, grid=(11, 15, 26), rope=True,
+        description="14B shape, 480p/81 frames: B=2 H=32 N=4290 bf16, 3D RoPE 44/42/42"),
+    "5b_720p_60s": Workload(
+        "5b_720p_60s", B=1, H=20, grid=(181, 22, 40), rope=True, k_scale=0.5,
+        description="long clip, 720p/60 s: B=1 H=20 N=159280 (181x22x40) bf16, 3D RoPE, k x 0.5"),
+}
+
+# The workload the throughput metric is quoted on (5B shape at 720p).
+HEADLINE = "5b_720p"
+
+
+def make_inputs(wl: Workload, seed: int = 0, device: Optional[str] = None):
+    """Draw (q, k, v, g) for ``wl``: see the module docstring for the recipe."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    shape = (wl.B, wl.H, wl.N, wl.d)
+    out = []
+    for name in ("q", "k", "v", "g"):
+        x = torch.randn(shape, generator=gen, dtype=torch.float32)
+        if name == "k" and wl.k_scale != 1.0:
+            x.mul_(wl.k_scale)
+        x = x.to(wl.dtype)
+        if device is not None:
+            x = x.to(device)
+        out.append(x)
+    return tuple(out)
+
+
+def sample_rows(N: int, count: int, seed: int = 1):
+    """Token rows to check at full size: the first, the last, and a seeded spread."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    picks = torch.randint(0, N, (max(count - 2, 0),), generator=gen).tolist()
+    rows = sorted(set([0, N - 1] + picks))
+    return rows
