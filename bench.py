@@ -1,0 +1,377 @@
+"""Throughput of the gated linear-attention forward on synthetic latent-grid inputs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl sla|reference]
+
+One step is one forward (state reduction + apply, every head) over the whole
+workload, inputs already resident in HBM.  The metric is token-heads per
+second (B*H*N / step time); the roofline object gives the achieved HBM
+bandwidth of the dominant kernel against the measured peak.  Prints one JSON
+line on rank 0.  Under torchrun each rank runs its own replica on its own GPU
+(the heads are independent; nothing is exchanged), so `value` is the sum over
+ranks of the work divided by the slowest rank's time.
+
+`--impl reference` times the fp64 CPU oracle instead (one head of the
+workload per step, on the host cores), for the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gated_linear_attention_attn_b300.workloads import HEADLINE, WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "linear-attn fwd token-heads/s; HBM GB/s as % of B300 peak (5B 720p shape)"
+UNIT = "token-heads/s"
+FALLBACK_HBM_GBS = 6400.0
+L2_BYTES = 126 * 1024 * 1024
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="sla", choices=["sla", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip timing the oracle on the host")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            data = json.load(fh)
+        return float(data["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons through NVML while the GPU works.
+
+    NVML is called through ctypes on the driver's libnvidia-ml.so.1; the GPU
+    is matched to the CUDA device by PCI bus id.
+    """
+
+    REASONS = {0x2: "applications_clocks", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+               0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown", 0x100: "display_clock"}
+    NVML_CLOCK_SM = 1
+
+    def __init__(self, device: torch.device, period_s: float = 0.005):
+        import ctypes
+        self.samples, self.reasons = [], set()
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._period = period_s
+        self._thread = None
+        self.error = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit failed")
+            bus = ctypes.create_string_buffer(64)
+            cudart = ctypes.CDLL("libcudart.so.13")
+            if cudart.cudaDeviceGetPCIBusId(bus, 64, int(device.index or 0)) != 0:
+                raise RuntimeError("cudaDeviceGetPCIBusId failed")
+            self._h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(bus.value, ctypes.byref(self._h)) != 0:
+                raise RuntimeError(f"no NVML handle for {bus.value!r}")
+            mx = ctypes.c_uint()
+            nv.nvmlDeviceGetMaxClockInfo(self._h, self.NVML_CLOCK_SM, ctypes.byref(mx))
+            self.max_mhz = mx.value
+            self._nv, self._ct = nv, ctypes
+            self.sample()
+        except Exception as exc:  # no NVML: report why instead of clocks
+            self._nv = None
+            self.error = repr(exc)
+
+    def sample(self):
+        ct, nv = self._ct, self._nv
+        clk, bits = ct.c_uint(), ct.c_ulonglong()
+        if nv.nvmlDeviceGetClockInfo(self._h, self.NVML_CLOCK_SM, ct.byref(clk)) == 0:
+            self.samples.append(clk.value)
+        if nv.nvmlDeviceGetCurrentClocksEventReasons(self._h, ct.byref(bits)) == 0:
+            for bit, name in self.REASONS.items():
+                if bits.value & bit:
+                    self.reasons.add(name)
+
+    def _run(self):
+        while not self._stop.is_set():
+            self.sample()
+            time.sleep(self._period)
+
+    def start(self):
+        if self._nv is not None:
+            self.samples.clear()
+            self.reasons.clear()
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+
+    def stop(self):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+        if self._nv is None:
+            return {"error": self.error or "NVML unavailable"}
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "samples": len(self.samples),
+                "reasons": sorted(self.reasons)}
+
+
+def source_hash():
+    """Hash of the CUDA sources, to tell whether a stored ncu traffic figure is current."""
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "gated_linear_attention_attn_b300", "csrc", "*"))):
+        with open(p, "rb") as fh:
+            h.update(os.path.basename(p).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from profiles/dram_traffic.txt, if taken on the current sources.
+
+    Lines: `<kernel> <workload> <bytes_per_launch> <source_hash>`.
+    """
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    current = source_hash()
+    with open(path) as fh:
+        for line in fh:
+            parts = line.split()
+            if len(parts) == 4 and not line.startswith("#") and parts[0] == kernel \
+                    and parts[1] == workload and parts[3] == current:
+                return float(parts[2])
+    return None
+
+
+# ------------------------------------------------------------ CPU oracle ----
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [p.get("num_threads", 0) for p in threadpool_info() if p.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_heads(wl, tensors, heads):
+    """Run the fp64 oracle on the given (b, h) heads at full N; returns elapsed seconds."""
+    import oracle.linattn as ol   # the CPU baseline is the one place bench.py runs the oracle
+    spec = ol.RopeSpec(*wl.grid, *wl.split, base=wl.base) if wl.rope else None
+    q, k, v, g = tensors
+    t0 = time.perf_counter()
+    for b, h in heads:
+        ang = ol.rope3d_angles(spec) if spec is not None else None
+        ol.linattn_head(q[b, h].double().numpy(), k[b, h].double().numpy(),
+                        v[b, h].double().numpy(), g[b, h].double().numpy(), wl.eps, ang)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(wl, tensors, budget_s=10.0):
+    """The oracle as it stands on the host cores: heads of the workload, one after another,
+    until about `budget_s` seconds have passed (at least one head)."""
+    all_heads = [(b, h) for b in range(wl.B) for h in range(wl.H)]
+    done, elapsed = 0, 0.0
+    while elapsed < budget_s and done < 4 * len(all_heads):
+        elapsed += oracle_heads(wl, tensors, [all_heads[done % len(all_heads)]])
+        done += 1
+    return {"value": done * wl.N / elapsed, "unit": UNIT, "cores": _blas_threads(),
+            "kind": "oracle",
+            "sample": f"{done} heads of {wl.name} at full N={wl.N} (fp64 numpy, "
+                      f"{elapsed:.1f} s); token-heads = heads x N"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 oracle on the host, one head of the workload per step."""
+    if rank != 0:
+        return
+    wl = WORKLOADS[args.workload]
+    tensors = make_inputs(wl, seed=0)
+    heads = [(b, h) for b in range(wl.B) for h in range(wl.H)]
+    for i in range(args.warmup):
+        oracle_heads(wl, tensors, [heads[i % len(heads)]])
+    total = 0.0
+    for i in range(args.steps):
+        total += oracle_heads(wl, tensors, [heads[i % len(heads)]])
+    value = args.steps * wl.N / total
+    cores = _blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(wl, world, note="one head (full N) per step on the host cores"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} heads of {wl.name}, one per step, full N"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config(wl, world, note=""):
+    cfg = {"workload": wl.name, "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d,
+           "grid": list(wl.grid), "rope": wl.rope,
+           "rope_split": list(wl.split) if wl.rope else None, "eps": wl.eps,
+           "k_scale": wl.k_scale, "input_dtype": str(wl.dtype).replace("torch.", ""),
+           "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+           "l2": ("inputs larger than L2 (%.0f MB vs 126 MB)" % (wl.algorithmic_bytes / 1e6)
+                  if wl.algorithmic_bytes > 2 * L2_BYTES else "L2 flushed between steps")}
+    if note:
+        cfg["note"] = note
+    return cfg
+
+
+# ------------------------------------------------------------------ GPU -----
+
+def _max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def run_sla(args, rank, world, local):
+    from gated_linear_attention_attn_b300 import sla
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    wl = WORKLOADS[args.workload]
+    host = make_inputs(wl, seed=0)
+    q, k, v, g = (t.to(dev) for t in host)
+    rope = sla.RopeTable(wl.grid, wl.split, wl.base, device=dev) if wl.rope else None
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        sla.linattn_forward(q, k, v, g, out=out, rope=rope, eps=wl.eps, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    status = sla.last_device_status(stream, dev)
+    if status != sla.OK:
+        raise RuntimeError(f"device status after warm-up: {sla.status_string(status)}")
+
+    # -------- device-resident timing: K steps between two events
+    _barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(dev)
+    sampler.start()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    _barrier(world)
+    secs = _max_over_ranks(t0.elapsed_time(t1) / 1e3, world, dev)
+    status = sla.last_device_status(stream, dev)
+    if status != sla.OK:
+        raise RuntimeError(f"device status after timing: {sla.status_string(status)}")
+    per_step = secs / args.steps
+    value = world * wl.token_heads / per_step
+
+    # -------- end to end through the public call, host buffers in pinned memory
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hg = (t.pin_memory() for t in host)
+        hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        bi = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg))
+        bo = hout.numel() * hout.element_size()
+
+        def e2e_step():
+            for dst, src in ((q, hq), (k, hk), (v, hv), (g, hg)):
+                dst.copy_(src, non_blocking=True)
+            step()
+            hout.copy_(out, non_blocking=True)
+
+        e2e_step()
+        ke = max(3, min(args.steps, 10))
+        _barrier(world)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        _barrier(world)
+        esecs = _max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
+        e2e = {"value": world * wl.token_heads * ke / esecs, "unit": UNIT,
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": ke,
+               "ms_per_step": 1e3 * esecs / ke}
+
+    if rank != 0:
+        return
+    peak, peak_src = measured_peaks()
+    achieved = wl.algorithmic_bytes / per_step / 1e9
+    kernels = sla.launches_per_forward(wl.dtype)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": 1e3 * per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if wl.dtype == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded N(0,1) q,k,v,g on the latent token grid)",
+        "config": _config(wl, world),
+        "roofline": {"bound": "hbm", "kernel": "forward (all launches of one call)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_src} copy bandwidth",
+                     "algorithmic_bytes_per_launch": wl.algorithmic_bytes,
+                     "traffic": stored_traffic("forward", wl.name)},
+        "e2e": e2e,
+        "gpu_launches": kernels * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, host)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_sla(args, rank, world, local)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

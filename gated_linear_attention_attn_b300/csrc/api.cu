@@ -1,0 +1,223 @@
+// C ABI of the linear-attention library: argument checks, the per-stream
+// workspace, and dispatch to the kernels.  Every check runs before anything
+// is launched, so a call that returns an error has launched nothing.
+#include <cmath>
+#include <cstdint>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "../../include/sla.h"
+#include "launch.h"
+
+namespace sla {
+namespace {
+
+struct DeviceState {
+    bool ready = false;
+    int num_sms = 0;
+    unsigned* status = nullptr;   // device status word (kStatusTimeout, ...)
+};
+
+struct Workspace {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+
+std::mutex g_mutex;
+std::map<int, DeviceState> g_devices;
+std::map<std::pair<int, uintptr_t>, Workspace> g_workspaces;
+
+// Per-device set-up: SM count and the status word.  Called with g_mutex held.
+sla_status_t device_state(int dev, DeviceState** out) {
+    DeviceState& st = g_devices[dev];
+    if (!st.ready) {
+        if (cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) !=
+            cudaSuccess)
+            return SLA_ERR_CUDA;
+        if (cudaMalloc(&st.status, 256) != cudaSuccess) return SLA_ERR_CUDA;
+        if (cudaMemset(st.status, 0, 256) != cudaSuccess) return SLA_ERR_CUDA;
+        st.ready = true;
+    }
+    *out = &st;
+    return SLA_OK;
+}
+
+// The workspace of (dev, stream), grown to at least `bytes`.  Calls on one
+// stream are ordered, so they can share it; calls on different streams get
+// different workspaces.  Growing frees the old buffer (cudaFree waits for the
+// device).  Called with g_mutex held.
+sla_status_t workspace(int dev, cudaStream_t stream, size_t bytes, void** out) {
+    Workspace& ws = g_workspaces[{dev, reinterpret_cast<uintptr_t>(stream)}];
+    if (ws.bytes < bytes) {
+        if (ws.ptr) {
+            cudaFree(ws.ptr);
+            ws.ptr = nullptr;
+            ws.bytes = 0;
+        }
+        const size_t rounded = (bytes + (1u << 20) - 1) & ~size_t((1u << 20) - 1);
+        if (cudaMalloc(&ws.ptr, rounded) != cudaSuccess) {
+            cudaGetLastError();
+            return SLA_ERR_CUDA;
+        }
+        ws.bytes = rounded;
+    }
+    *out = ws.ptr;
+    return SLA_OK;
+}
+
+bool misaligned(const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a != 0; }
+
+bool overlaps(const void* a, const void* b, size_t bytes) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + bytes && y < x + bytes;
+}
+
+}  // namespace
+
+// Checks shared by both dtypes.  `elem` is the element size in bytes.
+static sla_status_t check_forward(const void* q, const void* k, const void* v, const void* g,
+                                  const void* out, int B, int H, int N, int d,
+                                  const sla_rope_table_t* rope, float eps, size_t elem,
+                                  RopeView* rv) {
+    if (!q || !k || !v || !g || !out) return SLA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1 || d < 1) return SLA_ERR_INVALID_ARG;
+    if (!std::isfinite(eps) || eps < 0.f) return SLA_ERR_INVALID_ARG;
+    if (d != kHeadDim) return SLA_ERR_UNSUPPORTED;
+    // B*H heads of N rows each; the kernels index rows with 32-bit ints
+    const long long rows = (long long)B * H * N;
+    if (rows > 0x7fffffffLL) return SLA_ERR_UNSUPPORTED;
+    const void* ins[4] = {q, k, v, g};
+    for (const void* p : ins)
+        if (misaligned(p, 16)) return SLA_ERR_ALIGNMENT;
+    if (misaligned(out, 16)) return SLA_ERR_ALIGNMENT;
+    const size_t bytes = (size_t)rows * d * elem;
+    for (const void* p : ins)
+        if (overlaps(out, p, bytes)) return SLA_ERR_INVALID_ARG;
+    if (rope) {
+        if (!rope->table) return SLA_ERR_INVALID_ARG;
+        if (rope->T < 1 || rope->Hs < 1 || rope->Ws < 1) return SLA_ERR_INVALID_ARG;
+        if (rope->dt < 0 || rope->dh < 0 || rope->dw < 0) return SLA_ERR_INVALID_ARG;
+        if ((rope->dt | rope->dh | rope->dw) & 1) return SLA_ERR_INVALID_ARG;
+        if (rope->dt + rope->dh + rope->dw != d) return SLA_ERR_INVALID_ARG;
+        if ((long long)rope->T * rope->Hs * rope->Ws != N) return SLA_ERR_INVALID_ARG;
+        if (misaligned(rope->table, 8)) return SLA_ERR_ALIGNMENT;
+        const float2* base = reinterpret_cast<const float2*>(rope->table);
+        rv->pt = rope->dt / 2;
+        rv->ph = rope->dh / 2;
+        rv->pw = rope->dw / 2;
+        rv->T = rope->T;
+        rv->Hs = rope->Hs;
+        rv->Ws = rope->Ws;
+        rv->tab_t = base;
+        rv->tab_h = base + (size_t)rope->T * rv->pt;
+        rv->tab_w = rv->tab_h + (size_t)rope->Hs * rv->ph;
+    }
+    return SLA_OK;
+}
+
+}  // namespace sla
+
+using namespace sla;
+
+extern "C" {
+
+size_t sla_rope_table_floats(int T, int Hs, int Ws, int dt, int dh, int dw) {
+    if (T < 1 || Hs < 1 || Ws < 1 || dt < 0 || dh < 0 || dw < 0) return 0;
+    if ((dt | dh | dw) & 1) return 0;
+    return (size_t)T * dt + (size_t)Hs * dh + (size_t)Ws * dw;
+}
+
+sla_status_t sla_rope_table_fill(float* table, int T, int Hs, int Ws, int dt, int dh, int dw,
+                                 float base, sla_stream_t stream) {
+    if (!table) return SLA_ERR_INVALID_ARG;
+    if (T < 1 || Hs < 1 || Ws < 1 || dt < 0 || dh < 0 || dw < 0) return SLA_ERR_INVALID_ARG;
+    if ((dt | dh | dw) & 1) return SLA_ERR_INVALID_ARG;
+    if (!std::isfinite(base) || base <= 0.f) return SLA_ERR_INVALID_ARG;
+    if (misaligned(table, 8)) return SLA_ERR_ALIGNMENT;
+    if ((long long)T * dt + (long long)Hs * dh + (long long)Ws * dw > 0x7fffffffLL)
+        return SLA_ERR_UNSUPPORTED;
+    if (launch_rope_fill(table, T, Hs, Ws, dt, dh, dw, base, (cudaStream_t)stream) !=
+        cudaSuccess)
+        return SLA_ERR_CUDA;
+    return SLA_OK;
+}
+
+// Shared body of both forward entry points.
+static sla_status_t forward(const void* q, const void* k, const void* v, const void* g,
+                            void* out, int B, int H, int N, int d,
+                            const sla_rope_table_t* rope, float eps, sla_stream_t stream,
+                            bool is_f32) {
+    RopeView rv{};
+    sla_status_t st = check_forward(q, k, v, g, out, B, H, N, d, rope, eps,
+                                    is_f32 ? sizeof(float) : 2, &rv);
+    if (st != SLA_OK) return st;
+    const RopeView* rp = rope ? &rv : nullptr;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SLA_ERR_CUDA;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* ds = nullptr;
+    if ((st = device_state(dev, &ds)) != SLA_OK) return st;
+    const int BH = B * H;
+    const int C = simt_chunks(BH, N, ds->num_sms);
+    void* ws = nullptr;
+    if ((st = workspace(dev, s, simt_workspace_bytes(BH, C), &ws)) != SLA_OK) return st;
+    cudaError_t err;
+    if (is_f32)
+        err = launch_simt_f32((const float*)q, (const float*)k, (const float*)v,
+                              (const float*)g, (float*)out, B, H, N, rp, eps, (float*)ws, C, s);
+    else
+        err = launch_simt_bf16(q, k, v, g, out, B, H, N, rp, eps, (float*)ws, C, s);
+    return err == cudaSuccess ? SLA_OK : SLA_ERR_CUDA;
+}
+
+sla_status_t sla_linattn_forward(const void* q, const void* k, const void* v, const void* g,
+                                 void* out, int B, int H, int N, int d,
+                                 const sla_rope_table_t* rope_table, float eps,
+                                 sla_stream_t stream) {
+    return forward(q, k, v, g, out, B, H, N, d, rope_table, eps, stream, false);
+}
+
+sla_status_t sla_linattn_forward_f32(const float* q, const float* k, const float* v,
+                                     const float* g, float* out, int B, int H, int N, int d,
+                                     const sla_rope_table_t* rope_table, float eps,
+                                     sla_stream_t stream) {
+    return forward(q, k, v, g, out, B, H, N, d, rope_table, eps, stream, true);
+}
+
+const char* sla_status_string(sla_status_t status) {
+    switch (status) {
+        case SLA_OK: return "ok";
+        case SLA_ERR_INVALID_ARG: return "invalid argument";
+        case SLA_ERR_UNSUPPORTED: return "unsupported shape";
+        case SLA_ERR_ALIGNMENT: return "misaligned pointer";
+        case SLA_ERR_CUDA: return "CUDA runtime error";
+        case SLA_ERR_DEVICE_TIMEOUT: return "a kernel wait timed out";
+    }
+    return "unknown status";
+}
+
+sla_status_t sla_last_device_status(sla_stream_t stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return SLA_ERR_CUDA;
+    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SLA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* ds = nullptr;
+    sla_status_t st = device_state(dev, &ds);
+    if (st != SLA_OK) return st;
+    unsigned word = 0;
+    if (cudaMemcpy(&word, ds->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SLA_ERR_CUDA;
+    if (word != 0 && cudaMemset(ds->status, 0, sizeof(word)) != cudaSuccess)
+        return SLA_ERR_CUDA;
+    return (word & kStatusTimeout) ? SLA_ERR_DEVICE_TIMEOUT : SLA_OK;
+}
+
+}  // extern "C"

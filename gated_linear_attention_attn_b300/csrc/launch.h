@@ -1,0 +1,25 @@
+// Internal launchers of the linear-attention library (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "common.cuh"
+
+namespace sla {
+
+// fp32 SIMT path (simt.cu).
+int simt_chunks(int BH, int N, int num_sms);
+size_t simt_workspace_bytes(int BH, int C);
+cudaError_t launch_simt_f32(const float* q, const float* k, const float* v, const float* g,
+                            float* out, int B, int H, int N, const RopeView* rope, float eps,
+                            float* workspace, int C, cudaStream_t stream);
+cudaError_t launch_simt_bf16(const void* q, const void* k, const void* v, const void* g,
+                             void* out, int B, int H, int N, const RopeView* rope, float eps,
+                             float* workspace, int C, cudaStream_t stream);
+
+// RoPE table (rope_table.cu).
+cudaError_t launch_rope_fill(float* table, int T, int Hs, int Ws, int dt, int dh, int dw,
+                             float base, cudaStream_t stream);
+
+}  // namespace sla

@@ -1,0 +1,173 @@
+"""Python binding of libsla.so: the gated bidirectional linear-attention forward.
+
+This module only marshals arguments: it turns torch CUDA tensors into device
+pointers, sizes and the current stream, and calls the C ABI declared in
+``include/sla.h``.  Every step of the computation runs in the library's CUDA
+kernels.  Importing it fails loudly if the library has not been built
+(``python -m gated_linear_attention_attn_b300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsla.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -m gated_linear_attention_attn_b300.build`"
+        " (the forward has no other implementation)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+OK, INVALID_ARG, UNSUPPORTED, ALIGNMENT, CUDA_ERROR, DEVICE_TIMEOUT = range(6)
+HEAD_DIM = 128
+
+
+class RopeTableC(ctypes.Structure):
+    """Mirror of sla_rope_table_t."""
+    _fields_ = [("table", ctypes.c_void_p),
+                ("T", ctypes.c_int), ("Hs", ctypes.c_int), ("Ws", ctypes.c_int),
+                ("dt", ctypes.c_int), ("dh", ctypes.c_int), ("dw", ctypes.c_int)]
+
+
+_vp, _int, _flt = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+_lib.sla_rope_table_floats.argtypes = [_int] * 6
+_lib.sla_rope_table_floats.restype = ctypes.c_size_t
+_lib.sla_rope_table_fill.argtypes = [_vp] + [_int] * 6 + [_flt, _vp]
+_lib.sla_rope_table_fill.restype = _int
+_FWD_ARGS = [_vp] * 5 + [_int] * 4 + [ctypes.POINTER(RopeTableC), _flt, _vp]
+for _name in ("sla_linattn_forward", "sla_linattn_forward_f32"):
+    getattr(_lib, _name).argtypes = _FWD_ARGS
+    getattr(_lib, _name).restype = _int
+_lib.sla_status_string.argtypes = [_int]
+_lib.sla_status_string.restype = ctypes.c_char_p
+_lib.sla_last_device_status.argtypes = [_vp]
+_lib.sla_last_device_status.restype = _int
+
+EXPORTED = ("sla_rope_table_floats", "sla_rope_table_fill", "sla_linattn_forward",
+            "sla_linattn_forward_f32", "sla_status_string", "sla_last_device_status")
+
+
+class SlaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+def status_string(status: int) -> str:
+    return _lib.sla_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != OK:
+        raise SlaError(status, where)
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream], device: torch.device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream
+
+
+class RopeTable:
+    """A filled 3D RoPE table on one device, plus its grid and band split.
+
+    The table holds, for each axis, the (cos, sin) of every coordinate value
+    times every frequency of that axis's band (see ``sla_rope_table_t``).
+    """
+
+    def __init__(self, grid: Sequence[int], split: Sequence[int] = (44, 42, 42),
+                 base: float = 10000.0, device="cuda", stream=None):
+        T, Hs, Ws = (int(x) for x in grid)
+        dt, dh, dw = (int(x) for x in split)
+        n = _lib.sla_rope_table_floats(T, Hs, Ws, dt, dh, dw)
+        if n == 0 and (dt or dh or dw):
+            raise SlaError(INVALID_ARG, "sla_rope_table_floats")
+        self.device = torch.device(device)
+        self.grid, self.split, self.base = (T, Hs, Ws), (dt, dh, dw), float(base)
+        self.table = torch.empty(max(int(n), 2), dtype=torch.float32, device=self.device)
+        with torch.cuda.device(self.device):
+            _check(_lib.sla_rope_table_fill(self.table.data_ptr(), T, Hs, Ws, dt, dh, dw,
+                                            self.base, _stream_handle(stream, self.device)),
+                   "sla_rope_table_fill")
+
+    @property
+    def n_tokens(self) -> int:
+        T, Hs, Ws = self.grid
+        return T * Hs * Ws
+
+    def c_struct(self) -> RopeTableC:
+        return RopeTableC(self.table.data_ptr(), *self.grid, *self.split)
+
+    def axis_tables(self):
+        """The (cos, sin) rows of each axis as [extent, pairs, 2] float tensors."""
+        T, Hs, Ws = self.grid
+        dt, dh, dw = self.split
+        flat = self.table.view(-1, 2)
+        a = T * (dt // 2)
+        b = a + Hs * (dh // 2)
+        return (flat[:a].view(T, dt // 2, 2), flat[a:b].view(Hs, dh // 2, 2),
+                flat[b:b + Ws * (dw // 2)].view(Ws, dw // 2, 2))
+
+
+def linattn_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                    out: Optional[torch.Tensor] = None, rope: Optional[RopeTable] = None,
+                    eps: float = 1e-6, stream: Optional[torch.cuda.Stream] = None
+                    ) -> torch.Tensor:
+    """o = sigmoid(g) * (R phi(q)) S / (phi(q) . z + eps) for [B, H, N, d] CUDA tensors.
+
+    bf16 tensors go to ``sla_linattn_forward``, fp32 tensors to
+    ``sla_linattn_forward_f32``.  Asynchronous on ``stream`` (default: the
+    current stream).  Raises SlaError with the library's status on bad input.
+    """
+    if q.dim() != 4:
+        raise SlaError(INVALID_ARG, "linattn_forward: q must be [B, H, N, d]")
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g)):
+        if t.shape != q.shape or t.dtype != q.dtype or t.device != q.device:
+            raise SlaError(INVALID_ARG, f"linattn_forward: {name} differs from q")
+        if not t.is_contiguous():
+            raise SlaError(INVALID_ARG, f"linattn_forward: {name} is not contiguous")
+    if q.device.type != "cuda":
+        raise SlaError(INVALID_ARG, "linattn_forward: tensors must be on a CUDA device")
+    if q.dtype == torch.bfloat16:
+        fn = _lib.sla_linattn_forward
+    elif q.dtype == torch.float32:
+        fn = _lib.sla_linattn_forward_f32
+    else:
+        raise SlaError(UNSUPPORTED, f"linattn_forward: dtype {q.dtype}")
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() \
+            or out.device != q.device:
+        raise SlaError(INVALID_ARG, "linattn_forward: out must match q")
+    B, H, N, d = q.shape
+    rope_c = None
+    if rope is not None:
+        rope_c = ctypes.byref(rope.c_struct())
+    with torch.cuda.device(q.device):
+        _check(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(), out.data_ptr(),
+                  B, H, N, d, rope_c, float(eps), _stream_handle(stream, q.device)),
+               fn.__name__)
+    return out
+
+
+def last_device_status(stream: Optional[torch.cuda.Stream] = None, device="cuda") -> int:
+    """Synchronise the stream and read (and clear) the device status word."""
+    dev = torch.device(device)
+    with torch.cuda.device(dev):
+        return _lib.sla_last_device_status(_stream_handle(stream, dev))
+
+
+def launches_per_forward(dtype: torch.dtype) -> int:
+    """Kernels one forward call launches (the state reduction and the apply)."""
+    return 2
+
+
+def raw_lib() -> ctypes.CDLL:
+    """The loaded library, for callers that pass raw pointers."""
+    return _lib

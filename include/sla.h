@@ -1,0 +1,130 @@
+/*
+ * sla.h -- C ABI of the gated bidirectional linear-attention forward
+ * (SANA-Video 2.0), a single-GPU CUDA library for B300 (sm_103a).
+ *
+ * The operation.  "SANA-Video 2.0" (NVlabs/Sana docs/sana_video2.md,
+ * section "Architecture") builds 75% of its attention layers as gated
+ * bidirectional linear attention with Wan 3D rotary position embeddings, 20
+ * heads x 128 in the 5B model and 32 x 128 in the 14B model; the arXiv
+ * abstract of 2607.21553 calls it the gated linear attention used for the
+ * O(N)-dominated token mixing.  For each (batch b, head h), with q, k, v, g
+ * the N x d slices of that head:
+ *
+ *     phi(x) = max(x, 0)
+ *     S      = sum_j R_j phi(k_j) v_j^T          (d x d; R_j = I without RoPE)
+ *     z      = sum_j phi(k_j)                    (d, never rotated)
+ *     o_i    = sigmoid(g_i) * (R_i phi(q_i))^T S / (phi(q_i) . z + eps)
+ *
+ * The sums run over all N tokens (bidirectional: no causal mask).  The gate
+ * g has the shape of q and acts elementwise.  R_n is the 3D rotary embedding
+ * of token n, applied to the numerator only (see sla_rope_table_t).
+ *
+ * Layout.  q, k, v, g and out are [B][H][N][d] row-major and contiguous
+ * (d fastest), all in device memory of the current device.  out has the
+ * element type of the inputs.
+ *
+ * Ownership.  The caller owns every buffer passed in.  The library owns a
+ * workspace per (device, stream) for the split-N partial states
+ * (about 140 KB per SM of the device plus 33 KB per head), allocated with
+ * cudaMalloc on the first call that needs it (or more of it) and kept until
+ * the process exits.  A call that has to grow the workspace synchronises the
+ * device; make the first call of the largest shape outside stream capture.
+ *
+ * Errors.  Every argument is checked before anything is launched; a call
+ * that returns an error has launched nothing.  Calls are asynchronous on
+ * `stream` (NULL = the legacy default stream); SLA_ERR_CUDA reports a launch
+ * error.  Kernels never spin forever: a wait that exceeds its limit (about
+ * one second) sets a device status word and the kernel returns early;
+ * sla_last_device_status() reads (and clears) that word.
+ */
+#ifndef SLA_H_
+#define SLA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (the same object as cudaStream_t). */
+typedef struct CUstream_st* sla_stream_t;
+
+typedef enum sla_status {
+    SLA_OK = 0,
+    SLA_ERR_INVALID_ARG = 1,    /* null pointer, size < 1, bad eps, aliasing, bad RoPE grid */
+    SLA_ERR_UNSUPPORTED = 2,    /* a shape the kernels do not implement (d != 128) */
+    SLA_ERR_ALIGNMENT = 3,      /* a tensor not 16-byte aligned (a RoPE table not 8-byte aligned) */
+    SLA_ERR_CUDA = 4,           /* a CUDA runtime call failed (launch, allocation, no device) */
+    SLA_ERR_DEVICE_TIMEOUT = 5  /* a kernel gave up a wait and returned early */
+} sla_status_t;
+
+/*
+ * The 3D rotary embedding ("Wan 3D rotary position embeddings", NVlabs page,
+ * "Architecture"; RoFormer's rotation).  Token n of a T x Hs x Ws latent grid
+ * (one token per latent cell, "(1, 1, 1) latent patches") sits at
+ * n = (t*Hs + h)*Ws + w.  The head dimension is split into three even bands
+ * [0, dt), [dt, dt+dh), [dt+dh, d) that take t, h and w respectively; inside
+ * a band of width W, pair j = (x_{2p}, x_{2p+1}) turns by pos * base^(-2j/W)
+ * radians (complex multiplication of x_{2p} + i x_{2p+1}).
+ *
+ * `table` is a device buffer of sla_rope_table_floats(...) floats written by
+ * sla_rope_table_fill: (cos, sin) pairs for t in [0,T) x j in [0,dt/2), then
+ * for h in [0,Hs) x j in [0,dh/2), then for w in [0,Ws) x j in [0,dw/2).
+ * The angles are separable by axis, so the table holds
+ * T*dt + Hs*dh + Ws*dw floats rather than one row per token.
+ */
+typedef struct sla_rope_table {
+    const float* table;   /* device pointer, 8-byte aligned */
+    int T, Hs, Ws;        /* latent grid; N must equal T*Hs*Ws */
+    int dt, dh, dw;       /* even band widths, dt + dh + dw == d */
+} sla_rope_table_t;
+
+/* Number of floats of the RoPE table for this grid and split (0 if invalid). */
+size_t sla_rope_table_floats(int T, int Hs, int Ws, int dt, int dh, int dw);
+
+/*
+ * Writes the RoPE table (layout above) for base `base` (10000 for the Wan
+ * embedding) into `table` (device, sla_rope_table_floats(...) floats).  The
+ * angles are formed and the cosine and sine taken in double precision, then
+ * rounded to float.  Asynchronous on `stream`.
+ */
+sla_status_t sla_rope_table_fill(float* table, int T, int Hs, int Ws, int dt, int dh,
+                                 int dw, float base, sla_stream_t stream);
+
+/*
+ * The forward with bf16 q, k, v, g and out (IEEE bfloat16, 2 bytes each),
+ * fp32 accumulation.  B, H, N >= 1; d must be 128.  rope_table: NULL for no
+ * RoPE, else a host pointer to a filled sla_rope_table_t whose grid has N
+ * tokens and whose bands sum to d.  eps: finite, >= 0 (1e-6 in the
+ * workloads).  All five tensors 16-byte aligned; out must not overlap any
+ * input.  Asynchronous on `stream`.
+ */
+sla_status_t sla_linattn_forward(const void* q, const void* k, const void* v, const void* g,
+                                 void* out, int B, int H, int N, int d,
+                                 const sla_rope_table_t* rope_table, float eps,
+                                 sla_stream_t stream);
+
+/*
+ * The same forward for fp32 tensors (fp32 arithmetic throughout, no tensor
+ * cores), same arguments, layout and errors.
+ */
+sla_status_t sla_linattn_forward_f32(const float* q, const float* k, const float* v,
+                                     const float* g, float* out, int B, int H, int N, int d,
+                                     const sla_rope_table_t* rope_table, float eps,
+                                     sla_stream_t stream);
+
+/* A static, human-readable name for a status code. */
+const char* sla_status_string(sla_status_t status);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of the
+ * current device: SLA_ERR_DEVICE_TIMEOUT if a kernel gave up a wait since the
+ * last read, SLA_ERR_CUDA if the synchronisation failed, else SLA_OK.
+ */
+sla_status_t sla_last_device_status(sla_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SLA_H_ */

@@ -1,0 +1,119 @@
+"""The C ABI without a GPU: the library loads, exports what include/sla.h
+declares, and rejects bad arguments before it touches CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gated_linear_attention_attn_b300 import build
+
+build.build()
+from gated_linear_attention_attn_b300 import sla  # noqa: E402
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "sla.h")
+
+# Fake device addresses: the checks below fail before any CUDA call, so the
+# library never dereferences them.
+A = 0x10000000
+STEP = 0x01000000
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sla_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_symbols():
+    assert set(_declared_functions()) == set(sla.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(sla.LIB_PATH)
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings():
+    assert sla.status_string(sla.OK) == "ok"
+    assert "argument" in sla.status_string(sla.INVALID_ARG)
+    assert "timed out" in sla.status_string(sla.DEVICE_TIMEOUT)
+    assert sla.status_string(99) == "unknown status"
+
+
+def _fwd(q=A, k=A + STEP, v=A + 2 * STEP, g=A + 3 * STEP, out=A + 4 * STEP, B=1, H=2, N=256,
+         d=128, rope=None, eps=1e-6, f32=False):
+    fn = sla.raw_lib().sla_linattn_forward_f32 if f32 else sla.raw_lib().sla_linattn_forward
+    r = ctypes.byref(rope) if rope is not None else None
+    return fn(q, k, v, g, out, B, H, N, d, r, eps, None)
+
+
+@pytest.mark.parametrize("f32", [False, True])
+def test_forward_rejects_bad_arguments(f32):
+    bad = [
+        (dict(q=0), sla.INVALID_ARG),
+        (dict(out=0), sla.INVALID_ARG),
+        (dict(g=None), sla.INVALID_ARG),
+        (dict(B=0), sla.INVALID_ARG),
+        (dict(H=-1), sla.INVALID_ARG),
+        (dict(N=0), sla.INVALID_ARG),
+        (dict(eps=-1e-6), sla.INVALID_ARG),
+        (dict(eps=float("nan")), sla.INVALID_ARG),
+        (dict(eps=float("inf")), sla.INVALID_ARG),
+        (dict(d=64), sla.UNSUPPORTED),
+        (dict(d=256), sla.UNSUPPORTED),
+        (dict(B=2, H=1 << 14, N=1 << 20), sla.UNSUPPORTED),
+        (dict(k=A + STEP + 8), sla.ALIGNMENT),
+        (dict(out=A + 4 * STEP + 2), sla.ALIGNMENT),
+        (dict(out=A), sla.INVALID_ARG),                         # out is q
+        (dict(out=A + 3 * STEP + 4096), sla.INVALID_ARG),       # out overlaps g
+    ]
+    for kw, want in bad:
+        assert _fwd(f32=f32, **kw) == want, kw
+
+
+def _rope(**kw):
+    args = dict(table=A + 5 * STEP, T=4, Hs=8, Ws=8, dt=44, dh=42, dw=42)
+    args.update(kw)
+    return sla.RopeTableC(args["table"], args["T"], args["Hs"], args["Ws"], args["dt"],
+                          args["dh"], args["dw"])
+
+
+def test_forward_rejects_bad_rope():
+    bad = [
+        (dict(table=0), sla.INVALID_ARG),
+        (dict(T=5), sla.INVALID_ARG),                 # grid has 320 tokens, N = 256
+        (dict(dt=45, dh=41), sla.INVALID_ARG),        # odd band
+        (dict(dt=40), sla.INVALID_ARG),               # bands sum to 124
+        (dict(dw=-2, dt=46, dh=84), sla.INVALID_ARG),
+        (dict(Hs=0), sla.INVALID_ARG),
+        (dict(table=A + 5 * STEP + 4), sla.ALIGNMENT),
+    ]
+    for kw, want in bad:
+        assert _fwd(rope=_rope(**kw)) == want, kw
+
+
+def test_rope_table_sizes():
+    f = sla.raw_lib().sla_rope_table_floats
+    assert f(25, 22, 40, 44, 42, 42) == 25 * 44 + 22 * 42 + 40 * 42
+    assert f(181, 22, 40, 44, 42, 42) == 10568
+    assert f(0, 1, 1, 2, 2, 2) == 0
+    assert f(1, 1, 1, 3, 2, 2) == 0
+    fill = sla.raw_lib().sla_rope_table_fill
+    assert fill(None, 1, 1, 1, 2, 2, 2, 10000.0, None) == sla.INVALID_ARG
+    assert fill(A, 1, 1, 1, 3, 2, 2, 10000.0, None) == sla.INVALID_ARG
+    assert fill(A, 1, 1, 1, 2, 2, 2, 0.0, None) == sla.INVALID_ARG
+    assert fill(A + 4, 1, 1, 1, 2, 2, 2, 10000.0, None) == sla.ALIGNMENT
+
+
+def test_binding_rejects_mismatched_tensors():
+    import torch
+    q = torch.zeros(1, 2, 8, 128)
+    with pytest.raises(sla.SlaError):
+        sla.linattn_forward(q, q, q, q)                      # CPU tensors
+    with pytest.raises(sla.SlaError):
+        sla.linattn_forward(q, q[:, :1], q, q)
+    with pytest.raises(sla.SlaError):
+        sla.linattn_forward(q.to(torch.float16), q, q, q)

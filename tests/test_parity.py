@@ -1,0 +1,144 @@
+"""CUDA path vs the fp64 oracle, through the C ABI.
+
+Small shapes are compared element by element; they span several 128-token
+tiles and a ragged tail.  The full-size workloads are compared on sampled
+token rows: each head's state is formed by the oracle over all N tokens, the
+outputs at the sampled rows are checked.  The bound is max|err| / max|ref|:
+1e-5 for fp32 inputs, 1e-2 for bf16 inputs with fp32 accumulation.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle.linattn as ol
+from gated_linear_attention_attn_b300.workloads import WORKLOADS, Workload, make_inputs, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.float32: 1e-5, torch.bfloat16: 1e-2}
+
+
+def _sla():
+    from gated_linear_attention_attn_b300 import sla
+    return sla
+
+
+def _np64(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def _rel(out, ref):
+    return float(np.max(np.abs(out - ref)) / np.max(np.abs(ref)))
+
+
+def _spec(wl: Workload):
+    return ol.RopeSpec(*wl.grid, *wl.split, base=wl.base) if wl.rope else None
+
+
+def _rope_table(wl: Workload, device):
+    return _sla().RopeTable(wl.grid, wl.split, wl.base, device=device) if wl.rope else None
+
+
+def _run(wl, tensors, device):
+    q, k, v, g = (t.to(device) for t in tensors)
+    out = _sla().linattn_forward(q, k, v, g, rope=_rope_table(wl, device), eps=wl.eps)
+    assert _sla().last_device_status(device=device) == 0
+    return out
+
+
+SMALL = [
+    # (B, H, grid, dtype, rope)
+    (1, 1, (1, 1, 1), torch.bfloat16, False),
+    (1, 2, (1, 1, 7), torch.bfloat16, True),
+    (2, 3, (1, 1, 127), torch.bfloat16, False),
+    (1, 2, (1, 8, 16), torch.bfloat16, True),
+    (1, 2, (1, 1, 129), torch.bfloat16, False),
+    (1, 3, (3, 10, 10), torch.bfloat16, True),
+    (2, 2, (10, 10, 10), torch.bfloat16, True),
+    (1, 2, (11, 15, 26), torch.bfloat16, False),
+    (4, 16, (1, 1, 3), torch.bfloat16, True),
+    (1, 1, (5, 7, 9), torch.float32, True),
+    (2, 3, (1, 1, 129), torch.float32, False),
+    (1, 2, (4, 8, 8), torch.float32, True),
+]
+
+
+@pytest.mark.parametrize("B,H,grid,dtype,rope", SMALL,
+                         ids=[f"B{b}H{h}N{g[0]*g[1]*g[2]}-{str(dt)[6:]}-{'rope' if r else 'norope'}"
+                              for b, h, g, dt, r in SMALL])
+def test_small_shapes_elementwise(B, H, grid, dtype, rope, cuda_device):
+    wl = Workload("small", B=B, H=H, grid=grid, dtype=dtype, rope=rope)
+    tensors = make_inputs(wl, seed=7)
+    out = _run(wl, tensors, cuda_device)
+    ref = ol.linattn_forward(*tensors, eps=wl.eps, rope=_spec(wl))
+    assert _rel(_np64(out), ref) <= TOL[dtype]
+
+
+def test_tiny_fp32_workload_elementwise(cuda_device):
+    wl = WORKLOADS["tiny_fp32"]
+    tensors = make_inputs(wl, seed=0)
+    out = _run(wl, tensors, cuda_device)
+    ref = ol.linattn_forward(*tensors, eps=wl.eps, rope=_spec(wl))
+    assert _rel(_np64(out), ref) <= 1e-5
+
+
+@pytest.mark.parametrize("name", ["5b_480p", "5b_720p", "14b_480p", "5b_720p_60s"])
+def test_full_size_sampled_rows(name, cuda_device):
+    wl = WORKLOADS[name]
+    tensors = make_inputs(wl, seed=0)
+    out = _run(wl, tensors, cuda_device)
+    rows = sample_rows(wl.N, 48)
+    heads = [(b, h) for b in range(wl.B) for h in range(wl.H)]
+    if wl.N > 50000:          # the longest clip: first, last and two more heads
+        heads = [heads[0], heads[7], heads[13], heads[-1]]
+    q, k, v, g = tensors
+    ref = ol.linattn_forward_rows(q, k, v, g, rows, eps=wl.eps, rope=_spec(wl), heads=heads)
+    got = np.stack([_np64(out[b, h][rows]) for b, h in heads])
+    want = np.stack([ref[bh] for bh in heads])
+    assert _rel(got, want) <= wl.tol
+    assert np.all(np.isfinite(_np64(out[0, 0])))
+
+
+def test_dead_query_rows_are_zero(cuda_device):
+    wl = Workload("dead", B=1, H=2, grid=(3, 10, 10), rope=True)
+    q, k, v, g = make_inputs(wl, seed=3)
+    q[:, :, 5] = -q[:, :, 5].abs() - 0.1         # phi(q) = 0: num = 0, den = eps
+    q[:, :, 299] = -1.0
+    out = _run(wl, (q, k, v, g), cuda_device)
+    assert torch.all(out[:, :, 5] == 0) and torch.all(out[:, :, 299] == 0)
+
+
+def test_constant_values_pass_through(cuda_device):
+    wl = Workload("const", B=1, H=2, grid=(2, 20, 20), rope=False)
+    q, k, _, _ = make_inputs(wl, seed=4)
+    c = torch.linspace(-2, 2, 128).to(torch.bfloat16)
+    v = c.expand(1, 2, wl.N, 128).contiguous()
+    g = torch.full_like(q, 40.0)
+    out = _run(wl, (q, k, v, g), cuda_device)
+    err = (out.float().cpu() - c.float()).abs().max().item()
+    assert err <= 1e-2 * c.float().abs().max().item()
+
+
+def test_large_eps_and_saturated_gate(cuda_device):
+    wl = Workload("eps", B=1, H=2, grid=(1, 9, 30), rope=True, eps=5.0)
+    q, k, v, _ = make_inputs(wl, seed=5)
+    g = torch.full_like(q, 40.0)
+    out = _run(wl, (q, k, v, g), cuda_device)
+    ref = ol.linattn_forward(q, k, v, g, eps=5.0, rope=_spec(wl))
+    assert _rel(_np64(out), ref) <= 1e-2
+
+
+def test_repeatable_and_stream_independent(cuda_device):
+    wl = Workload("rep", B=2, H=3, grid=(4, 11, 13), rope=True)
+    q, k, v, g = (t.to(cuda_device) for t in make_inputs(wl, seed=6))
+    rope = _rope_table(wl, cuda_device)
+    sla = _sla()
+    a = sla.linattn_forward(q, k, v, g, rope=rope)
+    b = sla.linattn_forward(q, k, v, g, rope=rope)
+    s = torch.cuda.Stream(cuda_device)
+    s.wait_stream(torch.cuda.current_stream(cuda_device))
+    with torch.cuda.stream(s):
+        c = sla.linattn_forward(q, k, v, g, rope=rope)
+    s.synchronize()
+    torch.cuda.synchronize(cuda_device)
+    assert torch.equal(a, b) and torch.equal(a, c)
