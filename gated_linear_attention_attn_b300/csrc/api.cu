@@ -163,16 +163,24 @@ static sla_status_t forward(const void* q, const void* k, const void* v, const v
     DeviceState* ds = nullptr;
     if ((st = device_state(dev, &ds)) != SLA_OK) return st;
     const int BH = B * H;
-    const int C = simt_chunks(BH, N, ds->num_sms);
     void* ws = nullptr;
-    if ((st = workspace(dev, s, simt_workspace_bytes(BH, C), &ws)) != SLA_OK) return st;
     cudaError_t err;
-    if (is_f32)
+    if (is_f32) {
+        const int C = simt_chunks(BH, N, ds->num_sms);
+        if ((st = workspace(dev, s, simt_workspace_bytes(BH, C), &ws)) != SLA_OK) return st;
         err = launch_simt_f32((const float*)q, (const float*)k, (const float*)v,
                               (const float*)g, (float*)out, B, H, N, rp, eps, (float*)ws, C, s);
-    else
-        err = launch_simt_bf16(q, k, v, g, out, B, H, N, rp, eps, (float*)ws, C, s);
-    return err == cudaSuccess ? SLA_OK : SLA_ERR_CUDA;
+    } else {
+        if ((st = workspace(dev, s, tc_workspace_bytes(BH, N, ds->num_sms), &ws)) != SLA_OK)
+            return st;
+        err = launch_tc_bf16(q, k, v, g, out, B, H, N, rp, eps, (float*)ws, ds->status,
+                             ds->num_sms, s);
+    }
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return SLA_ERR_CUDA;
+    }
+    return SLA_OK;
 }
 
 sla_status_t sla_linattn_forward(const void* q, const void* k, const void* v, const void* g,
@@ -217,7 +225,8 @@ sla_status_t sla_last_device_status(sla_stream_t stream) {
         return SLA_ERR_CUDA;
     if (word != 0 && cudaMemset(ds->status, 0, sizeof(word)) != cudaSuccess)
         return SLA_ERR_CUDA;
-    return (word & kStatusTimeout) ? SLA_ERR_DEVICE_TIMEOUT : SLA_OK;
+    if (word & kStatusTimeout) return SLA_ERR_DEVICE_TIMEOUT;
+    return word ? SLA_ERR_CUDA : SLA_OK;
 }
 
 }  // extern "C"

@@ -12,7 +12,8 @@ constexpr int kHeadDim = 128;          // d: 128 in both the 5B and the 14B mode
 constexpr int kPairs = kHeadDim / 2;
 
 // Bits of the device status word (one 32-bit word per device).
-constexpr unsigned kStatusTimeout = 1u;
+constexpr unsigned kStatusTimeout = 1u;   // a bounded wait gave up
+constexpr unsigned kStatusLayout = 2u;    // shared memory not 1 KB aligned: nothing ran
 
 // Device view of a filled RoPE table: (cos, sin) pairs per axis, each axis
 // [extent][band pairs], axes in the order t, h, w.

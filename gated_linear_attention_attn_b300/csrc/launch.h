@@ -18,6 +18,12 @@ cudaError_t launch_simt_bf16(const void* q, const void* k, const void* v, const 
                              void* out, int B, int H, int N, const RopeView* rope, float eps,
                              float* workspace, int C, cudaStream_t stream);
 
+// bf16 path on tcgen05 (tc_forward.cu).
+size_t tc_workspace_bytes(int BH, int N, int num_sms);
+cudaError_t launch_tc_bf16(const void* q, const void* k, const void* v, const void* g, void* out,
+                           int B, int H, int N, const RopeView* rope, float eps, float* workspace,
+                           unsigned* status, int num_sms, cudaStream_t stream);
+
 // RoPE table (rope_table.cu).
 cudaError_t launch_rope_fill(float* table, int T, int Hs, int Ws, int dt, int dh, int dw,
                              float base, cudaStream_t stream);
