@@ -75,8 +75,9 @@ bool overlaps(const void* a, const void* b, size_t bytes) {
 
 }  // namespace
 
-// Checks shared by both dtypes.  `elem` is the element size in bytes.
-static sla_status_t check_forward(const void* q, const void* k, const void* v, const void* g,
+// Checks shared by every forward entry point.  `elem` is the element size in
+// bytes.
+sla_status_t check_forward(const void* q, const void* k, const void* v, const void* g,
                                   const void* out, int B, int H, int N, int d,
                                   const sla_rope_table_t* rope, float eps, size_t elem,
                                   RopeView* rv) {

@@ -4,9 +4,15 @@
 #include <cuda_runtime.h>
 #include <stddef.h>
 
+#include "../../include/sla.h"
 #include "common.cuh"
 
 namespace sla {
+
+// Argument checks of the forward entry points (api.cu); fills *rv when RoPE is on.
+sla_status_t check_forward(const void* q, const void* k, const void* v, const void* g,
+                           const void* out, int B, int H, int N, int d,
+                           const sla_rope_table_t* rope, float eps, size_t elem, RopeView* rv);
 
 // fp32 SIMT path (simt.cu).
 int simt_chunks(int BH, int N, int num_sms);

@@ -44,13 +44,16 @@ _FWD_ARGS = [_vp] * 5 + [_int] * 4 + [ctypes.POINTER(RopeTableC), _flt, _vp]
 for _name in ("sla_linattn_forward", "sla_linattn_forward_f32"):
     getattr(_lib, _name).argtypes = _FWD_ARGS
     getattr(_lib, _name).restype = _int
+_lib.sla_linattn_forward_noalloc.argtypes = _FWD_ARGS[:-1] + [_vp, _vp]
+_lib.sla_linattn_forward_noalloc.restype = _int
 _lib.sla_status_string.argtypes = [_int]
 _lib.sla_status_string.restype = ctypes.c_char_p
 _lib.sla_last_device_status.argtypes = [_vp]
 _lib.sla_last_device_status.restype = _int
 
 EXPORTED = ("sla_rope_table_floats", "sla_rope_table_fill", "sla_linattn_forward",
-            "sla_linattn_forward_f32", "sla_status_string", "sla_last_device_status")
+            "sla_linattn_forward_f32", "sla_linattn_forward_noalloc", "sla_status_string",
+            "sla_last_device_status")
 
 
 class SlaError(RuntimeError):

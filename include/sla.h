@@ -113,6 +113,43 @@ sla_status_t sla_linattn_forward_f32(const float* q, const float* k, const float
                                      const sla_rope_table_t* rope_table, float eps,
                                      sla_stream_t stream);
 
+/*
+ * The bf16 forward of sla_linattn_forward for callers that cannot allocate
+ * device memory.  No page has a counterpart: this entry point exists for
+ * library users, not for the method.  Some callers must not see a library
+ * allocate: a framework whose caching allocator has already reserved the
+ * device's memory (a cudaMalloc of ours could fail or fragment its pool), a
+ * runtime whose enqueue path forbids allocation (plugin interfaces), or a
+ * latency-critical loop that cannot afford the device-wide synchronisation of
+ * cudaMalloc and cudaFree.  This call allocates nothing: it runs the same
+ * kernels with their scratch (the split-N partial states) in a fixed 24 MiB
+ * array that is part of the library's device code.  Each GPU that loads the
+ * library holds that array until the process exits.
+ *
+ * Arguments, layout and checks are those of sla_linattn_forward, plus:
+ * device_status: NULL, or a caller-owned device pointer to a 4-byte aligned
+ * unsigned int into which the kernels OR a nonzero value if one of their
+ * waits gives up (the word is never cleared by the library).  With NULL,
+ * such an early return is not reported.
+ *
+ * Size limit: a shape whose scratch does not fit in the 24 MiB array returns
+ * SLA_ERR_UNSUPPORTED before anything is launched.  The scratch is about
+ * 66 KB x (number of SMs + B*H), so B*H up to about 220 heads fits on a
+ * 148-SM B300.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call on a device shares the one array, and nothing in it
+ * has to start at zero: every byte a call reads it has written earlier in the
+ * same call, after which the array keeps the last call's contents.  Calls that
+ * overlap on the GPU (other streams, other host threads) race on the array;
+ * order them on one stream or with events.
+ */
+sla_status_t sla_linattn_forward_noalloc(const void* q, const void* k, const void* v,
+                                         const void* g, void* out, int B, int H, int N, int d,
+                                         const sla_rope_table_t* rope_table, float eps,
+                                         unsigned int* device_status, sla_stream_t stream);
+
 /* A static, human-readable name for a status code. */
 const char* sla_status_string(sla_status_t status);
 

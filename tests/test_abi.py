@@ -117,3 +117,20 @@ def test_binding_rejects_mismatched_tensors():
         sla.linattn_forward(q, q[:, :1], q, q)
     with pytest.raises(sla.SlaError):
         sla.linattn_forward(q.to(torch.float16), q, q, q)
+
+
+def test_noalloc_forward_rejects_bad_arguments_before_cuda():
+    fn = sla.raw_lib().sla_linattn_forward_noalloc
+    ok = dict(q=A, k=A + STEP, v=A + 2 * STEP, g=A + 3 * STEP, out=A + 4 * STEP)
+
+    def call(status=None, **kw):
+        a = dict(ok, **kw)
+        return fn(a["q"], a["k"], a["v"], a["g"], a["out"], 1, 2, 256, 128, None, 1e-6,
+                  status, None)
+
+    assert call(q=0) == sla.INVALID_ARG
+    assert call(out=A) == sla.INVALID_ARG
+    assert call(k=A + STEP + 8) == sla.ALIGNMENT
+    assert call(status=A + 6 * STEP + 2) == sla.ALIGNMENT
+    assert fn(A, A + STEP, A + 2 * STEP, A + 3 * STEP, A + 4 * STEP, 1, 2, 256, 64, None, 1e-6,
+              None, None) == sla.UNSUPPORTED
