@@ -241,8 +241,10 @@ def _config(wl, world, note=""):
            "rope_split": list(wl.split) if wl.rope else None, "eps": wl.eps,
            "k_scale": wl.k_scale, "input_dtype": str(wl.dtype).replace("torch.", ""),
            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-           "l2": ("inputs larger than L2 (%.0f MB vs 126 MB)" % (wl.algorithmic_bytes / 1e6)
-                  if wl.algorithmic_bytes > 2 * L2_BYTES else "L2 flushed between steps")}
+           "l2": ("inputs larger than L2 (%.0f MB vs 126 MB), steps back to back"
+                  % (wl.algorithmic_bytes / 1e6) if wl.algorithmic_bytes >= 4 * L2_BYTES
+                  else "L2 flushed between steps (a 252 MB buffer written outside the "
+                       "timed events)")}
     if note:
         cfg["note"] = note
     return cfg
@@ -263,6 +265,29 @@ def _barrier(world):
         torch.distributed.barrier()
 
 
+def _time_steps(fn, steps, stream, flush=None):
+    """Device seconds of `steps` calls of fn on `stream`: one event pair around
+    all of them, or, with an L2 flush between steps, one pair per step with the
+    flush outside the pairs."""
+    if flush is None:
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(steps):
+            fn()
+        t1.record(stream)
+        t1.synchronize()
+        return t0.elapsed_time(t1) / 1e3
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, b in evs:
+        flush()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    evs[-1][1].synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs) / 1e3
+
+
 def run_sla(args, rank, world, local):
     from gated_linear_attention_attn_b300 import sla
 
@@ -276,6 +301,15 @@ def run_sla(args, rank, world, local):
     rope = sla.RopeTable(wl.grid, wl.split, wl.base, device=dev) if wl.rope else None
     out = torch.empty_like(q)
     stream = torch.cuda.current_stream(dev)
+    bf16 = wl.dtype == torch.bfloat16
+
+    # inputs within a few L2 sizes: overwrite L2 between timed steps
+    scrub = None
+    if wl.algorithmic_bytes < 4 * L2_BYTES:
+        scrub_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+
+        def scrub():
+            scrub_buf.fill_(1)
 
     def step():
         sla.linattn_forward(q, k, v, g, out=out, rope=rope, eps=wl.eps, stream=stream)
@@ -286,25 +320,45 @@ def run_sla(args, rank, world, local):
     if status != sla.OK:
         raise RuntimeError(f"device status after warm-up: {sla.status_string(status)}")
 
-    # -------- device-resident timing: K steps between two events
+    # -------- device-resident timing of the forward: K steps
     _barrier(world)
     torch.cuda.synchronize(dev)
     sampler = ClockSampler(dev)
     sampler.start()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(args.steps):
-        step()
-    t1.record(stream)
-    torch.cuda.synchronize(dev)
+    secs = _time_steps(step, args.steps, stream, scrub)
     clocks = sampler.stop()
+    torch.cuda.synchronize(dev)
     _barrier(world)
-    secs = _max_over_ranks(t0.elapsed_time(t1) / 1e3, world, dev)
+    secs = _max_over_ranks(secs, world, dev)
     status = sla.last_device_status(stream, dev)
     if status != sla.OK:
         raise RuntimeError(f"device status after timing: {sla.status_string(status)}")
     per_step = secs / args.steps
     value = world * wl.token_heads / per_step
+
+    # -------- each kernel on its own (the two phases of the forward), for the roofline
+    kernels = {}
+    if bf16:
+        state = sla.linattn_state(k, v, rope=rope, stream=stream)
+
+        def k_state():
+            sla.linattn_state(k, v, rope=rope, state=state, stream=stream)
+
+        def k_apply():
+            sla.linattn_apply(q, g, state, out=out, rope=rope, eps=wl.eps, stream=stream)
+
+        per_tok = wl.d * wl.elem_size
+        for name, fn, unit_bytes in (("tc_state_kernel", k_state, 2 * per_tok),
+                                     ("tc_apply_kernel", k_apply, 3 * per_tok)):
+            for _ in range(3):
+                fn()
+            ksecs = _time_steps(fn, args.steps, stream, scrub) / args.steps
+            alg = unit_bytes * wl.B * wl.H * wl.N
+            kernels[name] = {"us": 1e6 * ksecs, "algorithmic_bytes": alg,
+                             "gbs": alg / ksecs / 1e9}
+        status = sla.last_device_status(stream, dev)
+        if status != sla.OK:
+            raise RuntimeError(f"device status after kernel timing: {sla.status_string(status)}")
 
     # -------- end to end through the public call, host buffers in pinned memory
     e2e = None
@@ -324,14 +378,8 @@ def run_sla(args, rank, world, local):
         ke = max(3, min(args.steps, 10))
         _barrier(world)
         torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(ke):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
+        esecs = _max_over_ranks(_time_steps(e2e_step, ke, stream), world, dev)
         _barrier(world)
-        esecs = _max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
         e2e = {"value": world * wl.token_heads * ke / esecs, "unit": UNIT,
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": ke,
                "ms_per_step": 1e3 * esecs / ke}
@@ -339,22 +387,36 @@ def run_sla(args, rank, world, local):
     if rank != 0:
         return
     peak, peak_src = measured_peaks()
-    achieved = wl.algorithmic_bytes / per_step / 1e9
-    kernels = sla.launches_per_forward(wl.dtype)
+    if kernels:
+        dom = max(kernels, key=lambda n: kernels[n]["us"])
+        kd = kernels[dom]
+        achieved = kd["gbs"]
+        roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                    "unit": "GB/s", "frac": achieved / peak,
+                    "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                    if peak_src == "measured" else "fallback 6400 GB/s",
+                    "algorithmic_bytes_per_launch": kd["algorithmic_bytes"],
+                    "launch_us": kd["us"],
+                    "traffic": stored_traffic(dom, wl.name),
+                    "forward": {"achieved": wl.algorithmic_bytes / per_step / 1e9,
+                                "frac": wl.algorithmic_bytes / per_step / 1e9 / peak},
+                    "kernels": kernels}
+    else:
+        achieved = wl.algorithmic_bytes / per_step / 1e9
+        roofline = {"bound": "hbm", "kernel": "simt forward (both launches)",
+                    "achieved": achieved, "peak": peak, "unit": "GB/s",
+                    "frac": achieved / peak, "algorithmic_bytes_per_launch": wl.algorithmic_bytes,
+                    "traffic": None}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": 1e3 * per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if wl.dtype == torch.bfloat16 else "f32",
+        "dtype": "bf16" if bf16 else "f32",
         "data": "synthetic (seeded N(0,1) q,k,v,g on the latent token grid)",
         "config": _config(wl, world),
-        "roofline": {"bound": "hbm", "kernel": "forward (all launches of one call)",
-                     "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_source": f"{peak_src} copy bandwidth",
-                     "algorithmic_bytes_per_launch": wl.algorithmic_bytes,
-                     "traffic": stored_traffic("forward", wl.name)},
+        "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": kernels * args.steps,
+        "gpu_launches": sla.launches_per_forward(wl.dtype) * args.steps,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline:

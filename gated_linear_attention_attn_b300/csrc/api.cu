@@ -60,6 +60,13 @@ sla_status_t workspace(int dev, cudaStream_t stream, size_t bytes, void** out) {
             cudaGetLastError();
             return SLA_ERR_CUDA;
         }
+        // the kernels' per-head counters must not start with a stale tag
+        if (cudaMemsetAsync(ws.ptr, 0, rounded, stream) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFree(ws.ptr);
+            ws.ptr = nullptr;
+            return SLA_ERR_CUDA;
+        }
         ws.bytes = rounded;
     }
     *out = ws.ptr;
@@ -68,53 +75,75 @@ sla_status_t workspace(int dev, cudaStream_t stream, size_t bytes, void** out) {
 
 bool misaligned(const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a != 0; }
 
-bool overlaps(const void* a, const void* b, size_t bytes) {
-    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-    return x < y + bytes && y < x + bytes;
+}  // namespace
+
+// Sizes: B, H, N >= 1 and d == 128, with B*H*N rows indexable by 32-bit ints.
+static sla_status_t check_dims(int B, int H, int N, int d) {
+    if (B < 1 || H < 1 || N < 1 || d < 1) return SLA_ERR_INVALID_ARG;
+    if (d != kHeadDim) return SLA_ERR_UNSUPPORTED;
+    if ((long long)B * H * N > 0x7fffffffLL) return SLA_ERR_UNSUPPORTED;
+    return SLA_OK;
 }
 
-}  // namespace
+static bool bad_eps(float eps) { return !std::isfinite(eps) || eps < 0.f; }
+
+// The RoPE grid must have N tokens and bands that sum to d; fills *rv.
+static sla_status_t check_rope(const sla_rope_table_t* rope, int N, int d, RopeView* rv) {
+    if (!rope) return SLA_OK;
+    if (!rope->table) return SLA_ERR_INVALID_ARG;
+    if (rope->T < 1 || rope->Hs < 1 || rope->Ws < 1) return SLA_ERR_INVALID_ARG;
+    if (rope->dt < 0 || rope->dh < 0 || rope->dw < 0) return SLA_ERR_INVALID_ARG;
+    if ((rope->dt | rope->dh | rope->dw) & 1) return SLA_ERR_INVALID_ARG;
+    if (rope->dt + rope->dh + rope->dw != d) return SLA_ERR_INVALID_ARG;
+    if ((long long)rope->T * rope->Hs * rope->Ws != N) return SLA_ERR_INVALID_ARG;
+    if (misaligned(rope->table, 8)) return SLA_ERR_ALIGNMENT;
+    const float2* base = reinterpret_cast<const float2*>(rope->table);
+    rv->pt = rope->dt / 2;
+    rv->ph = rope->dh / 2;
+    rv->pw = rope->dw / 2;
+    rv->T = rope->T;
+    rv->Hs = rope->Hs;
+    rv->Ws = rope->Ws;
+    rv->tab_t = base;
+    rv->tab_h = base + (size_t)rope->T * rv->pt;
+    rv->tab_w = rv->tab_h + (size_t)rope->Hs * rv->ph;
+    rv->div_ws = make_fastdiv(rope->Ws);
+    rv->div_hs = make_fastdiv(rope->Hs);
+    return SLA_OK;
+}
+
+// Buffers: none null, all 16-byte aligned, the output overlapping no input.
+static sla_status_t check_buffers(const void* const* ins, const size_t* in_bytes, int n_ins,
+                                  const void* out, size_t out_bytes) {
+    for (int i = 0; i < n_ins; ++i)
+        if (!ins[i]) return SLA_ERR_INVALID_ARG;
+    if (!out) return SLA_ERR_INVALID_ARG;
+    for (int i = 0; i < n_ins; ++i)
+        if (misaligned(ins[i], 16)) return SLA_ERR_ALIGNMENT;
+    if (misaligned(out, 16)) return SLA_ERR_ALIGNMENT;
+    for (int i = 0; i < n_ins; ++i) {
+        const uintptr_t x = reinterpret_cast<uintptr_t>(out), y = reinterpret_cast<uintptr_t>(ins[i]);
+        if (x < y + in_bytes[i] && y < x + out_bytes) return SLA_ERR_INVALID_ARG;
+    }
+    return SLA_OK;
+}
 
 // Checks shared by every forward entry point.  `elem` is the element size in
 // bytes.
 sla_status_t check_forward(const void* q, const void* k, const void* v, const void* g,
-                                  const void* out, int B, int H, int N, int d,
-                                  const sla_rope_table_t* rope, float eps, size_t elem,
-                                  RopeView* rv) {
+                           const void* out, int B, int H, int N, int d,
+                           const sla_rope_table_t* rope, float eps, size_t elem,
+                           RopeView* rv) {
     if (!q || !k || !v || !g || !out) return SLA_ERR_INVALID_ARG;
-    if (B < 1 || H < 1 || N < 1 || d < 1) return SLA_ERR_INVALID_ARG;
-    if (!std::isfinite(eps) || eps < 0.f) return SLA_ERR_INVALID_ARG;
-    if (d != kHeadDim) return SLA_ERR_UNSUPPORTED;
-    // B*H heads of N rows each; the kernels index rows with 32-bit ints
-    const long long rows = (long long)B * H * N;
-    if (rows > 0x7fffffffLL) return SLA_ERR_UNSUPPORTED;
+    sla_status_t st = check_dims(B, H, N, d);
+    if (st == SLA_ERR_INVALID_ARG) return st;
+    if (bad_eps(eps)) return SLA_ERR_INVALID_ARG;
+    if (st != SLA_OK) return st;
+    const size_t bytes = (size_t)B * H * N * d * elem;
     const void* ins[4] = {q, k, v, g};
-    for (const void* p : ins)
-        if (misaligned(p, 16)) return SLA_ERR_ALIGNMENT;
-    if (misaligned(out, 16)) return SLA_ERR_ALIGNMENT;
-    const size_t bytes = (size_t)rows * d * elem;
-    for (const void* p : ins)
-        if (overlaps(out, p, bytes)) return SLA_ERR_INVALID_ARG;
-    if (rope) {
-        if (!rope->table) return SLA_ERR_INVALID_ARG;
-        if (rope->T < 1 || rope->Hs < 1 || rope->Ws < 1) return SLA_ERR_INVALID_ARG;
-        if (rope->dt < 0 || rope->dh < 0 || rope->dw < 0) return SLA_ERR_INVALID_ARG;
-        if ((rope->dt | rope->dh | rope->dw) & 1) return SLA_ERR_INVALID_ARG;
-        if (rope->dt + rope->dh + rope->dw != d) return SLA_ERR_INVALID_ARG;
-        if ((long long)rope->T * rope->Hs * rope->Ws != N) return SLA_ERR_INVALID_ARG;
-        if (misaligned(rope->table, 8)) return SLA_ERR_ALIGNMENT;
-        const float2* base = reinterpret_cast<const float2*>(rope->table);
-        rv->pt = rope->dt / 2;
-        rv->ph = rope->dh / 2;
-        rv->pw = rope->dw / 2;
-        rv->T = rope->T;
-        rv->Hs = rope->Hs;
-        rv->Ws = rope->Ws;
-        rv->tab_t = base;
-        rv->tab_h = base + (size_t)rope->T * rv->pt;
-        rv->tab_w = rv->tab_h + (size_t)rope->Hs * rv->ph;
-    }
-    return SLA_OK;
+    const size_t sizes[4] = {bytes, bytes, bytes, bytes};
+    if ((st = check_buffers(ins, sizes, 4, out, bytes)) != SLA_OK) return st;
+    return check_rope(rope, N, d, rv);
 }
 
 }  // namespace sla
@@ -196,6 +225,70 @@ sla_status_t sla_linattn_forward_f32(const float* q, const float* k, const float
                                      const sla_rope_table_t* rope_table, float eps,
                                      sla_stream_t stream) {
     return forward(q, k, v, g, out, B, H, N, d, rope_table, eps, stream, true);
+}
+
+size_t sla_linattn_state_bytes(int B, int H, int d) {
+    if (B < 1 || H < 1 || d != kHeadDim) return 0;
+    return tc_state_bytes(B * H);
+}
+
+sla_status_t sla_linattn_state(const void* k, const void* v, void* state, int B, int H, int N,
+                               int d, const sla_rope_table_t* rope_table, sla_stream_t stream) {
+    sla_status_t st = check_dims(B, H, N, d);
+    if (st != SLA_OK) return st;
+    const size_t bytes = (size_t)B * H * N * d * 2;
+    const void* ins[2] = {k, v};
+    const size_t sizes[2] = {bytes, bytes};
+    if ((st = check_buffers(ins, sizes, 2, state, tc_state_bytes(B * H))) != SLA_OK) return st;
+    RopeView rv{};
+    if ((st = check_rope(rope_table, N, d, &rv)) != SLA_OK) return st;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SLA_ERR_CUDA;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* ds = nullptr;
+    if ((st = device_state(dev, &ds)) != SLA_OK) return st;
+    void* ws = nullptr;
+    if ((st = workspace(dev, s, tc_state_workspace_bytes(B * H, N, ds->num_sms), &ws)) != SLA_OK)
+        return st;
+    if (launch_tc_state(k, v, state, B, H, N, rope_table ? &rv : nullptr, ws, ds->status,
+                        ds->num_sms, s) != cudaSuccess) {
+        cudaGetLastError();
+        return SLA_ERR_CUDA;
+    }
+    return SLA_OK;
+}
+
+sla_status_t sla_linattn_apply(const void* q, const void* g, const void* state, void* out, int B,
+                               int H, int N, int d, const sla_rope_table_t* rope_table, float eps,
+                               sla_stream_t stream) {
+    sla_status_t st = check_dims(B, H, N, d);
+    if (st == SLA_ERR_INVALID_ARG) return st;
+    if (bad_eps(eps)) return SLA_ERR_INVALID_ARG;
+    if (st != SLA_OK) return st;
+    const size_t bytes = (size_t)B * H * N * d * 2;
+    const void* ins[3] = {q, g, state};
+    const size_t sizes[3] = {bytes, bytes, tc_state_bytes(B * H)};
+    if ((st = check_buffers(ins, sizes, 3, out, bytes)) != SLA_OK) return st;
+    RopeView rv{};
+    if ((st = check_rope(rope_table, N, d, &rv)) != SLA_OK) return st;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SLA_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* ds = nullptr;
+    if ((st = device_state(dev, &ds)) != SLA_OK) return st;
+    if (launch_tc_apply(q, g, state, out, B, H, N, rope_table ? &rv : nullptr, eps, ds->status,
+                        ds->num_sms, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return SLA_ERR_CUDA;
+    }
+    return SLA_OK;
 }
 
 const char* sla_status_string(sla_status_t status) {

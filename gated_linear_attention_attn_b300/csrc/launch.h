@@ -24,11 +24,22 @@ cudaError_t launch_simt_bf16(const void* q, const void* k, const void* v, const 
                              void* out, int B, int H, int N, const RopeView* rope, float eps,
                              float* workspace, int C, cudaStream_t stream);
 
-// bf16 path on tcgen05 (tc_forward.cu).
+// bf16 path on tcgen05 (tc_forward.cu).  The whole forward needs
+// tc_workspace_bytes of workspace (counters, partial states, the heads'
+// states); the state phase alone needs tc_state_workspace_bytes and writes
+// tc_state_bytes of state.
 size_t tc_workspace_bytes(int BH, int N, int num_sms);
+size_t tc_state_workspace_bytes(int BH, int N, int num_sms);
+size_t tc_state_bytes(int BH);
 cudaError_t launch_tc_bf16(const void* q, const void* k, const void* v, const void* g, void* out,
                            int B, int H, int N, const RopeView* rope, float eps, float* workspace,
                            unsigned* status, int num_sms, cudaStream_t stream);
+cudaError_t launch_tc_state(const void* k, const void* v, void* state, int B, int H, int N,
+                            const RopeView* rope, void* workspace, unsigned* status, int num_sms,
+                            cudaStream_t stream);
+cudaError_t launch_tc_apply(const void* q, const void* g, const void* state, void* out, int B,
+                            int H, int N, const RopeView* rope, float eps, unsigned* status,
+                            int num_sms, cudaStream_t stream);
 
 // RoPE table (rope_table.cu).
 cudaError_t launch_rope_fill(float* table, int T, int Hs, int Ws, int dt, int dh, int dw,

@@ -105,6 +105,17 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* s
         : "memory");
 }
 
+// Contiguous bulk copy global -> shared (16-byte aligned addresses, size a
+// multiple of 16), completion counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -127,6 +138,20 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 // (tensor core operand reads, TMA stores).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------- programmatic launch -----
+
+// Blocks until the grids this one depends on have completed and their memory
+// operations are visible (returns at once when there is no such dependency).
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next grid of the stream, if launched as a programmatic dependent,
+// be scheduled before this one completes.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ------------------------------------------------------------- tcgen05 -----

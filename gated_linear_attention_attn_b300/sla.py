@@ -44,6 +44,12 @@ _FWD_ARGS = [_vp] * 5 + [_int] * 4 + [ctypes.POINTER(RopeTableC), _flt, _vp]
 for _name in ("sla_linattn_forward", "sla_linattn_forward_f32"):
     getattr(_lib, _name).argtypes = _FWD_ARGS
     getattr(_lib, _name).restype = _int
+_lib.sla_linattn_state_bytes.argtypes = [_int] * 3
+_lib.sla_linattn_state_bytes.restype = ctypes.c_size_t
+_lib.sla_linattn_state.argtypes = [_vp] * 3 + [_int] * 4 + [ctypes.POINTER(RopeTableC), _vp]
+_lib.sla_linattn_state.restype = _int
+_lib.sla_linattn_apply.argtypes = [_vp] * 4 + [_int] * 4 + [ctypes.POINTER(RopeTableC), _flt, _vp]
+_lib.sla_linattn_apply.restype = _int
 _lib.sla_linattn_forward_noalloc.argtypes = _FWD_ARGS[:-1] + [_vp, _vp]
 _lib.sla_linattn_forward_noalloc.restype = _int
 _lib.sla_status_string.argtypes = [_int]
@@ -52,7 +58,8 @@ _lib.sla_last_device_status.argtypes = [_vp]
 _lib.sla_last_device_status.restype = _int
 
 EXPORTED = ("sla_rope_table_floats", "sla_rope_table_fill", "sla_linattn_forward",
-            "sla_linattn_forward_f32", "sla_linattn_forward_noalloc", "sla_status_string",
+            "sla_linattn_forward_f32", "sla_linattn_state_bytes", "sla_linattn_state",
+            "sla_linattn_apply", "sla_linattn_forward_noalloc", "sla_status_string",
             "sla_last_device_status")
 
 
@@ -156,6 +163,64 @@ def linattn_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.
         _check(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(), out.data_ptr(),
                   B, H, N, d, rope_c, float(eps), _stream_handle(stream, q.device)),
                fn.__name__)
+    return out
+
+
+def _check_bf16(name, t, like=None):
+    if t.dtype != torch.bfloat16 or t.dim() != 4 or t.device.type != "cuda" \
+            or not t.is_contiguous():
+        raise SlaError(INVALID_ARG, f"{name} must be a contiguous [B, H, N, d] bf16 CUDA tensor")
+    if like is not None and (t.shape != like.shape or t.device != like.device):
+        raise SlaError(INVALID_ARG, f"{name} differs from its partner tensor")
+
+
+def state_bytes(B: int, H: int, d: int = HEAD_DIM) -> int:
+    """Bytes of the per-head state that ``linattn_state`` writes."""
+    return int(_lib.sla_linattn_state_bytes(B, H, d))
+
+
+def linattn_state(k: torch.Tensor, v: torch.Tensor, rope: Optional[RopeTable] = None,
+                  state: Optional[torch.Tensor] = None,
+                  stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Phase 1 (bf16): the heads' S and z from k and v, as a uint8 device buffer."""
+    _check_bf16("k", k)
+    _check_bf16("v", v, like=k)
+    B, H, N, d = k.shape
+    nbytes = state_bytes(B, H, d)
+    if nbytes == 0:
+        raise SlaError(UNSUPPORTED, "linattn_state: shape")
+    if state is None:
+        state = torch.empty(nbytes, dtype=torch.uint8, device=k.device)
+    elif state.numel() * state.element_size() < nbytes or not state.is_contiguous():
+        raise SlaError(INVALID_ARG, "linattn_state: state buffer too small")
+    rope_c = ctypes.byref(rope.c_struct()) if rope is not None else None
+    with torch.cuda.device(k.device):
+        _check(_lib.sla_linattn_state(k.data_ptr(), v.data_ptr(), state.data_ptr(), B, H, N, d,
+                                      rope_c, _stream_handle(stream, k.device)),
+               "sla_linattn_state")
+    return state
+
+
+def linattn_apply(q: torch.Tensor, g: torch.Tensor, state: torch.Tensor,
+                  out: Optional[torch.Tensor] = None, rope: Optional[RopeTable] = None,
+                  eps: float = 1e-6, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Phase 2 (bf16): o from q, g and a state written by ``linattn_state``."""
+    _check_bf16("q", q)
+    _check_bf16("g", g, like=q)
+    B, H, N, d = q.shape
+    if state.device != q.device or not state.is_contiguous() \
+            or state.numel() * state.element_size() < state_bytes(B, H, d):
+        raise SlaError(INVALID_ARG, "linattn_apply: state does not match q")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check_bf16("out", out, like=q)
+    rope_c = ctypes.byref(rope.c_struct()) if rope is not None else None
+    with torch.cuda.device(q.device):
+        _check(_lib.sla_linattn_apply(q.data_ptr(), g.data_ptr(), state.data_ptr(),
+                                      out.data_ptr(), B, H, N, d, rope_c, float(eps),
+                                      _stream_handle(stream, q.device)),
+               "sla_linattn_apply")
     return out
 
 

@@ -24,10 +24,10 @@
  * element type of the inputs.
  *
  * Ownership.  The caller owns every buffer passed in.  The library owns a
- * workspace per (device, stream) for the split-N partial states
- * (about 140 KB per SM of the device plus 33 KB per head), allocated with
- * cudaMalloc on the first call that needs it (or more of it) and kept until
- * the process exits.  A call that has to grow the workspace synchronises the
+ * workspace per (device, stream) for the split-N partial states and the
+ * heads' states (about 68 KB per SM of the device plus 101 KB per head),
+ * allocated with cudaMalloc on the first call that needs it (or more of it)
+ * and kept until the process exits.  A call that has to grow the workspace synchronises the
  * device; make the first call of the largest shape outside stream capture.
  *
  * Errors.  Every argument is checked before anything is launched; a call
@@ -114,6 +114,42 @@ sla_status_t sla_linattn_forward_f32(const float* q, const float* k, const float
                                      sla_stream_t stream);
 
 /*
+ * The two phases of sla_linattn_forward, for callers that reuse a state
+ * (several query sets against one set of keys and values) or time the phases.
+ * sla_linattn_forward is exactly sla_linattn_state followed by
+ * sla_linattn_apply, except that it keeps the state in the library's
+ * workspace and lets the apply kernel start while the state kernel finishes.
+ *
+ * The state of one head is sla_linattn_state_bytes(1, 1, 128) = 33280 bytes:
+ * S^T (row n = output dim, column m = key dim) as bf16 in the layout the
+ * tensor cores read (two 64-column halves of 128 rows x 128 bytes; the
+ * 16-byte chunk c of row n sits at chunk position (c mod 8) xor (n mod 8) of
+ * its row), then z as 128 fp32 values.  Heads follow each other, b-major.
+ */
+size_t sla_linattn_state_bytes(int B, int H, int d);   /* 0 if the shape is invalid */
+
+/*
+ * Phase 1: S~ = sum_j R_j phi(k_j) v_j^T and z = sum_j phi(k_j) for every
+ * head of bf16 k and v ([B][H][N][d], device).  state: device buffer of
+ * sla_linattn_state_bytes(B, H, d) bytes, 16-byte aligned, overlapping
+ * neither input.  rope_table as for sla_linattn_forward (N tokens of k).
+ * Uses the library's per-stream workspace for the split-N partial states.
+ */
+sla_status_t sla_linattn_state(const void* k, const void* v, void* state, int B, int H, int N,
+                               int d, const sla_rope_table_t* rope_table, sla_stream_t stream);
+
+/*
+ * Phase 2: out = sigmoid(g) * (R phi(q)) S~ / (phi(q) . z + eps) for bf16 q
+ * and g ([B][H][N][d], device; N query tokens, which may differ from the N of
+ * the state's keys), with a state written by sla_linattn_state for the same
+ * B and H.  rope_table as for sla_linattn_forward, for the N query tokens.
+ * out must overlap neither q, g nor the state.
+ */
+sla_status_t sla_linattn_apply(const void* q, const void* g, const void* state, void* out, int B,
+                               int H, int N, int d, const sla_rope_table_t* rope_table, float eps,
+                               sla_stream_t stream);
+
+/*
  * The bf16 forward of sla_linattn_forward for callers that cannot allocate
  * device memory.  No page has a counterpart: this entry point exists for
  * library users, not for the method.  Some callers must not see a library
@@ -134,16 +170,18 @@ sla_status_t sla_linattn_forward_f32(const float* q, const float* k, const float
  *
  * Size limit: a shape whose scratch does not fit in the 24 MiB array returns
  * SLA_ERR_UNSUPPORTED before anything is launched.  The scratch is about
- * 66 KB x (number of SMs + B*H), so B*H up to about 220 heads fits on a
- * 148-SM B300.
+ * 68 KB x (number of SMs + B*H) + 33 KB x B*H, so B*H up to about 140 heads
+ * fits on a 148-SM B300.
  *
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
- * capture.  Every call on a device shares the one array, and nothing in it
- * has to start at zero: every byte a call reads it has written earlier in the
- * same call, after which the array keeps the last call's contents.  Calls that
- * overlap on the GPU (other streams, other host threads) race on the array;
- * order them on one stream or with events.
+ * capture.  Every call on a device shares the one array, which keeps the
+ * last call's contents.  Nothing in it has to be cleared between calls: the
+ * only values a call reads before writing them are per-head counters, which
+ * carry the tag of the call that wrote them, so a count left by an earlier
+ * call reads as zero (the array starts zeroed when the library loads).  Calls
+ * that overlap on the GPU (other streams, other host threads) race on the
+ * array; order them on one stream or with events.
  */
 sla_status_t sla_linattn_forward_noalloc(const void* q, const void* k, const void* v,
                                          const void* g, void* out, int B, int H, int N, int d,

@@ -134,3 +134,24 @@ def test_noalloc_forward_rejects_bad_arguments_before_cuda():
     assert call(status=A + 6 * STEP + 2) == sla.ALIGNMENT
     assert fn(A, A + STEP, A + 2 * STEP, A + 3 * STEP, A + 4 * STEP, 1, 2, 256, 64, None, 1e-6,
               None, None) == sla.UNSUPPORTED
+
+
+def test_phase_entry_points_reject_bad_arguments():
+    lib = sla.raw_lib()
+    st = lib.sla_linattn_state
+    ap = lib.sla_linattn_apply
+    K, V, S, Q, G, O = (A + i * STEP for i in range(6))
+    assert lib.sla_linattn_state_bytes(2, 3, 128) == 6 * 33280
+    assert lib.sla_linattn_state_bytes(2, 3, 64) == 0
+    assert st(0, V, S, 1, 2, 256, 128, None, None) == sla.INVALID_ARG
+    assert st(K, V, 0, 1, 2, 256, 128, None, None) == sla.INVALID_ARG
+    assert st(K, V, K + 64, 1, 2, 256, 128, None, None) == sla.INVALID_ARG   # state overlaps k
+    assert st(K, V, S + 8, 1, 2, 256, 128, None, None) == sla.ALIGNMENT
+    assert st(K, V, S, 1, 2, 256, 96, None, None) == sla.UNSUPPORTED
+    assert st(K, V, S, 0, 2, 256, 128, None, None) == sla.INVALID_ARG
+    assert ap(Q, G, S, O, 1, 2, 256, 128, None, -1.0, None) == sla.INVALID_ARG
+    assert ap(Q, G, S, S, 1, 2, 256, 128, None, 1e-6, None) == sla.INVALID_ARG  # out is state
+    assert ap(Q, G, S, O + 4, 1, 2, 256, 128, None, 1e-6, None) == sla.ALIGNMENT
+    assert ap(Q, 0, S, O, 1, 2, 256, 128, None, 1e-6, None) == sla.INVALID_ARG
+    r = ctypes.byref(_rope(T=5))
+    assert ap(Q, G, S, O, 1, 2, 256, 128, r, 1e-6, None) == sla.INVALID_ARG

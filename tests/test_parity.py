@@ -142,3 +142,56 @@ def test_repeatable_and_stream_independent(cuda_device):
     s.synchronize()
     torch.cuda.synchronize(cuda_device)
     assert torch.equal(a, b) and torch.equal(a, c)
+
+
+def test_phases_equal_forward(cuda_device):
+    """sla_linattn_state + sla_linattn_apply give the forward's output bit for bit."""
+    sla = _sla()
+    for rope_on in (False, True):
+        wl = Workload("phases", B=2, H=3, grid=(3, 7, 11), rope=rope_on)
+        q, k, v, g = (t.to(cuda_device) for t in make_inputs(wl, seed=8))
+        rope = _rope_table(wl, cuda_device)
+        fwd = sla.linattn_forward(q, k, v, g, rope=rope)
+        state = sla.linattn_state(k, v, rope=rope)
+        out = sla.linattn_apply(q, g, state, rope=rope)
+        assert sla.last_device_status(device=cuda_device) == 0
+        assert torch.equal(fwd, out)
+        assert state.numel() == sla.state_bytes(2, 3) == 6 * 33280
+
+
+def test_apply_with_other_queries(cuda_device):
+    """A state of one token set applied to queries of another (own grids, own RoPE)."""
+    sla = _sla()
+    wk = Workload("keys", B=1, H=2, grid=(4, 6, 10), rope=True)
+    wq = Workload("queries", B=1, H=2, grid=(2, 5, 13), rope=True)
+    _, k, v, _ = make_inputs(wk, seed=9)
+    q, _, _, g = make_inputs(wq, seed=10)
+    rk, rq = _rope_table(wk, cuda_device), _rope_table(wq, cuda_device)
+    state = sla.linattn_state(k.to(cuda_device), v.to(cuda_device), rope=rk)
+    out = sla.linattn_apply(q.to(cuda_device), g.to(cuda_device), state, rope=rq)
+    assert sla.last_device_status(device=cuda_device) == 0
+    ak, aq = ol.rope3d_angles(_spec(wk)), ol.rope3d_angles(_spec(wq))
+    ref = np.empty((1, 2, wq.N, 128))
+    for h in range(2):
+        S, z = ol.linattn_state(_np64(k[0, h]), _np64(v[0, h]), ak)
+        ref[0, h] = ol.linattn_apply(_np64(q[0, h]), _np64(g[0, h]), S, z, 1e-6, aq)
+    assert _rel(_np64(out), ref) <= 1e-2
+
+
+def test_state_layout_holds_s_and_z(cuda_device):
+    """The documented state layout: S^T in bf16 (swizzled chunks), then z in fp32."""
+    sla = _sla()
+    wl = Workload("layout", B=1, H=1, grid=(1, 3, 100), rope=False)
+    _, k, v, _ = make_inputs(wl, seed=12)
+    state = sla.linattn_state(k.to(cuda_device), v.to(cuda_device)).cpu()
+    S, z = ol.linattn_state(_np64(k[0, 0]), _np64(v[0, 0]))
+    raw = state[:32768].view(torch.bfloat16).float().numpy().reshape(2, 128, 8, 8)
+    st = np.empty((128, 128))                      # S^T[n][m]
+    for n in range(128):
+        for cpos in range(8):
+            for half in range(2):
+                chunk = half * 8 + (cpos ^ (n % 8))
+                st[n, chunk * 8:(chunk + 1) * 8] = raw[half, n, cpos]
+    assert _rel(st, S.T) <= 1e-2
+    zz = state[32768:33280].view(torch.float32).numpy()
+    assert np.max(np.abs(zz - z)) <= 1e-5 * np.max(np.abs(z))
