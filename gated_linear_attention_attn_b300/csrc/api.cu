@@ -96,7 +96,7 @@ static sla_status_t check_rope(const sla_rope_table_t* rope, int N, int d, RopeV
     if ((rope->dt | rope->dh | rope->dw) & 1) return SLA_ERR_INVALID_ARG;
     if (rope->dt + rope->dh + rope->dw != d) return SLA_ERR_INVALID_ARG;
     if ((long long)rope->T * rope->Hs * rope->Ws != N) return SLA_ERR_INVALID_ARG;
-    if (misaligned(rope->table, 8)) return SLA_ERR_ALIGNMENT;
+    if (misaligned(rope->table, 256)) return SLA_ERR_ALIGNMENT;
     const float2* base = reinterpret_cast<const float2*>(rope->table);
     rv->pt = rope->dt / 2;
     rv->ph = rope->dh / 2;
@@ -107,8 +107,8 @@ static sla_status_t check_rope(const sla_rope_table_t* rope, int N, int d, RopeV
     rv->tab_t = base;
     rv->tab_h = base + (size_t)rope->T * rv->pt;
     rv->tab_w = rv->tab_h + (size_t)rope->Hs * rv->ph;
-    rv->div_ws = make_fastdiv(rope->Ws);
-    rv->div_hs = make_fastdiv(rope->Hs);
+    rv->tok = reinterpret_cast<const uint32_t*>(rope->table) +
+              rope_tok_offset_words(rope->T, rope->Hs, rope->Ws, rope->dt, rope->dh, rope->dw);
     return SLA_OK;
 }
 
@@ -155,7 +155,7 @@ extern "C" {
 size_t sla_rope_table_floats(int T, int Hs, int Ws, int dt, int dh, int dw) {
     if (T < 1 || Hs < 1 || Ws < 1 || dt < 0 || dh < 0 || dw < 0) return 0;
     if ((dt | dh | dw) & 1) return 0;
-    return (size_t)T * dt + (size_t)Hs * dh + (size_t)Ws * dw;
+    return rope_total_words(T, Hs, Ws, dt, dh, dw);
 }
 
 sla_status_t sla_rope_table_fill(float* table, int T, int Hs, int Ws, int dt, int dh, int dw,
@@ -164,9 +164,8 @@ sla_status_t sla_rope_table_fill(float* table, int T, int Hs, int Ws, int dt, in
     if (T < 1 || Hs < 1 || Ws < 1 || dt < 0 || dh < 0 || dw < 0) return SLA_ERR_INVALID_ARG;
     if ((dt | dh | dw) & 1) return SLA_ERR_INVALID_ARG;
     if (!std::isfinite(base) || base <= 0.f) return SLA_ERR_INVALID_ARG;
-    if (misaligned(table, 8)) return SLA_ERR_ALIGNMENT;
-    if ((long long)T * dt + (long long)Hs * dh + (long long)Ws * dw > 0x7fffffffLL)
-        return SLA_ERR_UNSUPPORTED;
+    if (misaligned(table, 256)) return SLA_ERR_ALIGNMENT;
+    if (rope_total_words(T, Hs, Ws, dt, dh, dw) > 0x7fffffffULL) return SLA_ERR_UNSUPPORTED;
     if (launch_rope_fill(table, T, Hs, Ws, dt, dh, dw, base, (cudaStream_t)stream) !=
         cudaSuccess)
         return SLA_ERR_CUDA;

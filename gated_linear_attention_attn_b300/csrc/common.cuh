@@ -15,39 +15,30 @@ constexpr int kPairs = kHeadDim / 2;
 constexpr unsigned kStatusTimeout = 1u;   // a bounded wait gave up
 constexpr unsigned kStatusLayout = 2u;    // shared memory not 1 KB aligned: nothing ran
 
-// Division of 0 <= n < 2^31 by an invariant divisor d >= 1 with one high
-// multiply, after Granlund and Montgomery, "Division by invariant integers
-// using multiplication" (PLDI 1994): with s = ceil(log2 d) and
-// m = floor(2^32 (2^s - d) / d) + 1, floor(n / d) = (umulhi(n, m) + n) >> s.
-// The sum cannot overflow because umulhi(n, m) < n < 2^31.
-struct FastDiv {
-    uint32_t mul = 1;
-    uint32_t shift = 0;
-};
-
-inline FastDiv make_fastdiv(int d) {
-    FastDiv f;
-    uint32_t s = 0;
-    while ((1ull << s) < (unsigned long long)d) ++s;
-    const unsigned long long pow2 = 1ull << s;
-    f.mul = (uint32_t)(((1ull << 32) * (pow2 - (unsigned long long)d)) / (unsigned long long)d + 1);
-    f.shift = s;
-    return f;
+// Layout of a RoPE table buffer, in 4-byte words: the separable fp32
+// (cos, sin) pairs of each axis ([T][dt/2], [Hs][dh/2], [Ws][dw/2]), then,
+// from the next 256-byte boundary, one row per token of d/2 (cos, sin) pairs
+// as two fp16 values in a word (cos in the low half).
+inline size_t rope_sep_words(int T, int Hs, int Ws, int dt, int dh, int dw) {
+    return (size_t)T * dt + (size_t)Hs * dh + (size_t)Ws * dw;
 }
-
-__device__ __forceinline__ int fast_div(int n, FastDiv f) {
-    return (int)((__umulhi((uint32_t)n, f.mul) + (uint32_t)n) >> f.shift);
+inline size_t rope_tok_offset_words(int T, int Hs, int Ws, int dt, int dh, int dw) {
+    return (rope_sep_words(T, Hs, Ws, dt, dh, dw) + 63) & ~size_t(63);
+}
+inline size_t rope_total_words(int T, int Hs, int Ws, int dt, int dh, int dw) {
+    return rope_tok_offset_words(T, Hs, Ws, dt, dh, dw) +
+           (size_t)T * Hs * Ws * (size_t)((dt + dh + dw) / 2);
 }
 
 // Device view of a filled RoPE table: (cos, sin) pairs per axis, each axis
-// [extent][band pairs], axes in the order t, h, w.
+// [extent][band pairs], axes in the order t, h, w; and the per-token rows.
 struct RopeView {
     const float2* tab_t;   // [T][pt]
     const float2* tab_h;   // [Hs][ph]
     const float2* tab_w;   // [Ws][pw]
+    const uint32_t* tok;   // [N][64] fp16 (cos, sin) per pair, 256 bytes per token
     int T, Hs, Ws;
     int pt, ph, pw;        // pairs per band: dt/2, dh/2, dw/2
-    FastDiv div_ws, div_hs;   // n / Ws and (n / Ws) / Hs
 };
 
 // Grid coordinates of token n: n = (t*Hs + h)*Ws + w.

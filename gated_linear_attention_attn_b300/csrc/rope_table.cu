@@ -3,14 +3,24 @@
 // "Wan 3D rotary position embeddings" (SANA-Video 2.0, NVlabs/Sana
 // docs/sana_video2.md, "Architecture") rotate the t, h and w bands of the
 // head dimension by the token's frame, row and column index.  The angles of a
-// band depend on one coordinate only, so the table holds one short row per
-// coordinate value instead of one row per token.
+// band depend on one coordinate only, so the first part of the table holds
+// one short fp32 row per coordinate value (read by the fp32 kernels); the
+// second part holds, for every token, all d/2 pairs as fp16 (cos, sin), so
+// that the tensor-core kernels stream a token's rotation with its row of q or
+// k instead of gathering it pair by pair.
+#include <cuda_fp16.h>
+
 #include "launch.h"
 
 namespace sla {
 namespace {
 
-__global__ void rope_fill_kernel(float2* __restrict__ table, int T, int Hs, int Ws, int pt,
+// theta_j = base^(-2j/W) for pair j of a band of width W = 2 * pairs.
+__device__ __forceinline__ double band_angle(double base, int pos, int j, int pairs) {
+    return (double)pos * pow(base, -(double)j / (double)pairs);
+}
+
+__global__ void rope_axes_kernel(float2* __restrict__ table, int T, int Hs, int Ws, int pt,
                                  int ph, int pw, double base) {
     const int total = T * pt + Hs * ph + Ws * pw;
     for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < total;
@@ -31,25 +41,58 @@ __global__ void rope_fill_kernel(float2* __restrict__ table, int T, int Hs, int 
             pos = f / pw;
             j = f - pos * pw;
         }
-        // band width W = 2 * pairs; theta_j = base^(-2j/W) = base^(-j/pairs)
-        const double theta = pow(base, -(double)j / (double)pairs);
         double s, c;
-        sincos((double)pos * theta, &s, &c);
+        sincos(band_angle(base, pos, j, pairs), &s, &c);
         table[e] = make_float2((float)c, (float)s);
     }
+}
+
+// Entry (n, p): pair p of token n = (t*Hs + h)*Ws + w.
+__global__ void rope_tokens_kernel(uint32_t* __restrict__ rows, int T, int Hs, int Ws, int pt,
+                                   int ph, int pw, double base) {
+    const int P = pt + ph + pw;
+    const int total = T * Hs * Ws * P;
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += gridDim.x * blockDim.x) {
+        const int n = e / P, p = e - n * P;
+        const int hw = n / Ws, w = n - hw * Ws;
+        const int t = hw / Hs, h = hw - t * Hs;
+        double ang;
+        if (p < pt)
+            ang = band_angle(base, t, p, pt);
+        else if (p < pt + ph)
+            ang = band_angle(base, h, p - pt, ph);
+        else
+            ang = band_angle(base, w, p - pt - ph, pw);
+        double s, c;
+        sincos(ang, &s, &c);
+        const __half2 cs = __floats2half2_rn((float)c, (float)s);
+        rows[e] = *reinterpret_cast<const uint32_t*>(&cs);
+    }
+}
+
+int grid_for(int total, int threads) {
+    int blocks = (total + threads - 1) / threads;
+    return blocks > 4096 ? 4096 : (blocks < 1 ? 1 : blocks);
 }
 
 }  // namespace
 
 cudaError_t launch_rope_fill(float* table, int T, int Hs, int Ws, int dt, int dh, int dw,
                              float base, cudaStream_t stream) {
-    const int total = T * (dt / 2) + Hs * (dh / 2) + Ws * (dw / 2);
-    if (total == 0) return cudaSuccess;
+    const int pt = dt / 2, ph = dh / 2, pw = dw / 2;
+    const int axes = T * pt + Hs * ph + Ws * pw;
+    const int tokens = T * Hs * Ws * (pt + ph + pw);
     const int threads = 256;
-    int blocks = (total + threads - 1) / threads;
-    if (blocks > 1024) blocks = 1024;
-    rope_fill_kernel<<<blocks, threads, 0, stream>>>(reinterpret_cast<float2*>(table), T, Hs,
-                                                      Ws, dt / 2, dh / 2, dw / 2, (double)base);
+    if (axes > 0)
+        rope_axes_kernel<<<grid_for(axes, threads), threads, 0, stream>>>(
+            reinterpret_cast<float2*>(table), T, Hs, Ws, pt, ph, pw, (double)base);
+    if (tokens > 0) {
+        uint32_t* rows = reinterpret_cast<uint32_t*>(table) +
+                         rope_tok_offset_words(T, Hs, Ws, dt, dh, dw);
+        rope_tokens_kernel<<<grid_for(tokens, threads), threads, 0, stream>>>(
+            rows, T, Hs, Ws, pt, ph, pw, (double)base);
+    }
     return cudaGetLastError();
 }
 

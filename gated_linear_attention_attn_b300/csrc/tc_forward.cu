@@ -23,9 +23,9 @@
 //                     phi and RoPE to the Q tile in place and form
 //                     den = phi(q) . z + eps; one thread of warp 1 issues
 //                     num = phi~(Q) S (M = N = K = 128) into one of two TMEM
-//                     accumulators; eight epilogue warps read num from TMEM,
-//                     compute sigmoid(g) * num / den over the G tile in place,
-//                     and one of them stores the tile with TMA.
+//                     accumulators; eight epilogue warps read num from TMEM
+//                     and compute sigmoid(g) * num / den over the G tile in
+//                     place, which a storer warp then writes out with TMA.
 //
 // The apply kernel is launched as a programmatic dependent of the state
 // kernel: it prefetches Q and G (which the state kernel does not write) and
@@ -38,6 +38,8 @@
 
 #include <atomic>
 
+#include <cuda_fp16.h>
+
 #include "launch.h"
 #include "tc_ptx.cuh"
 
@@ -47,38 +49,52 @@ namespace {
 using namespace ptx;
 
 constexpr int kRowBytes = kHeadDim * 2;                          // one bf16 token row: 256 B
-// A partial slot: S^T [128][128] fp32, then z as one 128-float part per
-// transform warp of the state kernel.
-constexpr int kStXWarps = 8;                                     // transform warps
-constexpr int kPartialFloats = kHeadDim * kHeadDim + kStXWarps * kHeadDim;
+// A partial slot: S^T [128][128] fp32, then z [128] fp32.
+constexpr int kPartialFloats = kHeadDim * kHeadDim + kHeadDim;
 constexpr int kStateSBytes = kHeadDim * kHeadDim * 2;            // S^T bf16: 32 KB
 constexpr int kStateBytes = kStateSBytes + kHeadDim * 4;         // + z fp32: 33280 B
 constexpr int kStateHalf = kStateSBytes / 2;                     // one 64-column half
 
 // ---- state kernel geometry
 constexpr int kStTok = 64;                        // tokens per tile
-constexpr int kStStages = 6;
 constexpr int kStHalf = kStTok * 128;             // one 64-column box: 8 KB
 constexpr int kStTile = 2 * kStHalf;              // one tensor tile: 16 KB
-constexpr int kStStage = 2 * kStTile;             // K + V: 32 KB
+constexpr int kStRing = 6 * 2 * kStTile;          // the stage ring: 192 KB
+constexpr int kStXWarps = 8;                      // transform warps
+constexpr int kStFWarps = 4;                      // flush + merge warps
 constexpr int kStXThreads = 32 * kStXWarps;
-constexpr int kStThreads = 64 + kStXThreads;      // TMA warp, MMA warp, transform warps
+constexpr int kStThreads = 32 * (2 + kStXWarps + kStFWarps);   // + TMA warp, MMA warp
 constexpr int kStTmemCols = 256;                  // two 128-column accumulators
 constexpr int kStRowsPerThread = kStTok * 16 / kStXThreads;   // 4
 
 // ---- apply kernel geometry
 constexpr int kApTok = 128;
-constexpr int kApStages = 3;
 constexpr int kApHalf = kApTok * 128;             // 16 KB
 constexpr int kApTile = 2 * kApHalf;              // 32 KB
-constexpr int kApStage = 2 * kApTile;             // Q + G: 64 KB
+constexpr int kApRing = 3 * 2 * kApTile;          // the stage ring: 192 KB
+
+// A state stage holds one tile of K and of V and, with RoPE, the tile's rows
+// of the per-token RoPE table (256 bytes per token, the size of a tensor
+// row); the ring has the same size either way, so RoPE trades stages for the
+// table rows.  An apply stage holds Q and G; its transform warps read their
+// RoPE rows straight from global memory (L2), one tile ahead.
+template <bool ROPE>
+struct StGeo {
+    static constexpr int kStage = (ROPE ? 3 : 2) * kStTile;
+    static constexpr int kStages = kStRing / kStage;       // 4 or 6
+};
+template <bool ROPE>
+struct ApGeo {
+    static constexpr int kStage = 2 * kApTile;
+    static constexpr int kStages = kApRing / kStage;       // 3
+};
 constexpr int kApXWarps = 8;
 constexpr int kApEWarps = 8;
 constexpr int kApXThreads = 32 * kApXWarps;
-constexpr int kApThreads = 64 + 32 * (kApXWarps + kApEWarps);
+constexpr int kApStorerWarp = 2 + kApXWarps + kApEWarps;       // issues the output stores
+constexpr int kApThreads = 32 * (kApStorerWarp + 1);
 constexpr int kApTmemCols = 256;
 constexpr int kApRowsPerThread = kApTok * 16 / kApXThreads;   // 8
-constexpr int kApFirstEpilogue = 64 + kApXThreads;            // thread index of the storer
 
 static_assert(kStRowsPerThread == 4 && kApRowsPerThread == 8, "thread/tile split");
 
@@ -129,58 +145,24 @@ __device__ __forceinline__ void unpack8(const uint4& x, float (&f)[8]) {
     }
 }
 
-// Grid coordinates of token n: n = (t*Hs + h)*Ws + w.
-__device__ __forceinline__ void grid_pos(const RopeView& r, int n, int& t, int& h, int& w) {
-    const int hw = fast_div(n, r.div_ws);
-    w = n - hw * r.Ws;
-    t = fast_div(hw, r.div_hs);
-    h = hw - t * r.Hs;
+// The four (cos, sin) pairs of one 16-byte chunk, stored as fp16 pairs.
+__device__ __forceinline__ void unpack_cs(const uint4& w, float2 (&cs)[4]) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) cs[i] = __half22float2(*reinterpret_cast<const __half2*>(&u[i]));
 }
 
-// RoPE of the four pairs of one 16-byte chunk (dims 8c..8c+7).  Pair p's
-// (cos, sin) sits in the table of its band at the row given by the token's
-// coordinate on that band's axis; the band of each pair is fixed per chunk,
-// so it is resolved once and the per-token lookup has no branches.
-struct ChunkRope {
-    const float2* base[4];   // band table + pair index inside the band
-    int stride[4];           // pairs per row of that band
-    int axis[4];             // 0 = t, 1 = h, 2 = w
-
-    __device__ __forceinline__ void init(const RopeView& r, int c) {
+// Rotates the pairs of f (phi of one chunk) and returns them packed as bf16.
+__device__ __forceinline__ uint4 rotate_chunk(const float (&f)[8], const float2 (&cs)[4]) {
+    uint32_t o[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int p = 4 * c + i;
-            if (p < r.pt) {
-                axis[i] = 0;
-                base[i] = r.tab_t + p;
-                stride[i] = r.pt;
-            } else if (p < r.pt + r.ph) {
-                axis[i] = 1;
-                base[i] = r.tab_h + (p - r.pt);
-                stride[i] = r.ph;
-            } else {
-                axis[i] = 2;
-                base[i] = r.tab_w + (p - r.pt - r.ph);
-                stride[i] = r.pw;
-            }
-        }
+    for (int i = 0; i < 4; ++i) {
+        const float a = f[2 * i] * cs[i].x - f[2 * i + 1] * cs[i].y;
+        const float b = f[2 * i] * cs[i].y + f[2 * i + 1] * cs[i].x;
+        o[i] = f2_to_bf2(a, b);
     }
-
-    // Rotates the pairs of f (phi of one chunk) for the token at (t, h, w)
-    // and returns them packed as bf16.
-    __device__ __forceinline__ uint4 rotate(const float (&f)[8], int t, int h, int w) const {
-        uint32_t o[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int coord = axis[i] == 0 ? t : (axis[i] == 1 ? h : w);
-            const float2 cs = __ldg(base[i] + coord * stride[i]);
-            const float a = f[2 * i] * cs.x - f[2 * i + 1] * cs.y;
-            const float b = f[2 * i] * cs.y + f[2 * i + 1] * cs.x;
-            o[i] = f2_to_bf2(a, b);
-        }
-        return make_uint4(o[0], o[1], o[2], o[3]);
-    }
-};
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
 
 // A wait taken by all 32 lanes of a warp: the warp proceeds only if every
 // lane saw the phase complete, so the lanes never split on an abort.
@@ -218,16 +200,23 @@ __device__ uint32_t count_contributor(unsigned long long* ctr, uint32_t epoch, u
 template <bool ROPE>
 __global__ void __launch_bounds__(kStThreads, 1)
 tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                StateParams p) {
+                const __grid_constant__ CUtensorMap tm_t, StateParams p) {
+    constexpr int kStStages = StGeo<ROPE>::kStages;
+    constexpr int kStStage = StGeo<ROPE>::kStage;
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStStages * kStStage);
+    float* zred = reinterpret_cast<float*>(smem + kStRing);   // [2][8 warps][128]
+    uint64_t* full = reinterpret_cast<uint64_t*>(zred + 2 * kStXWarps * kHeadDim);
     uint64_t* kready = full + kStStages;
     uint64_t* empty = kready + kStStages;
     uint64_t* accfull = empty + kStStages;        // [2]
     uint64_t* accempty = accfull + 2;             // [2]
-    uint64_t* slotdone = accempty + 2;            // a segment's slot is written
+    uint64_t* zready = accempty + 2;              // [2] the transform warps' z is in zred
+    uint64_t* zfree = zready + 2;                 // [2] zred read by the flush warps
+    uint64_t* slotdone = zfree + 2;               // a segment's slot is written
     uint64_t* lastknown = slotdone + 1;           // the head's last contributor is known
-    uint64_t* mma_done = lastknown + 1;
+    uint64_t* mfull = lastknown + 1;              // merge: slots landed in the idle ring
+    uint64_t* mfree = mfull + 1;                  // merge: slots read, ring reusable
+    uint64_t* mma_done = mfree + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* last_flag = abort_flag + 1;
@@ -245,16 +234,21 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&accfull[a], 1);
-            mbar_init(&accempty[a], kStXWarps);
+            mbar_init(&accempty[a], kStFWarps);
+            mbar_init(&zready[a], kStXWarps);
+            mbar_init(&zfree[a], kStFWarps);
         }
-        mbar_init(slotdone, kStXWarps);
+        mbar_init(slotdone, kStFWarps);
         mbar_init(lastknown, 1);
+        mbar_init(mfull, 1);
+        mbar_init(mfree, kStFWarps);
         mbar_init(mma_done, 1);
         *abort_flag = (smem0 & 1023u) ? 1 : 0;    // the swizzled tiles need 1 KB alignment
         if (smem0 & 1023u) raise_status(p.status, kStatusLayout);
         fence_mbar_init();
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
+        if (ROPE) prefetch_tmap(&tm_t);
         griddep_launch_dependents();
     }
     if (warp == 1) {
@@ -270,6 +264,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         // ------------------------------------------------ TMA producer
         if (lane == 0 && !*abort_flag) {
             const uint64_t policy = policy_evict_first();
+            const uint64_t keep = policy_evict_last();   // the RoPE rows serve every head
             long long it = 0;
             for (long long u = u0; u < u1; ++u, ++it) {
                 const int h = (int)(u / p.Tk), tile = (int)(u % p.Tk);
@@ -283,6 +278,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 tma_load_3d(st + kStTile, &tm_v, &full[s], 0, tile * kStTok, h, policy);
                 tma_load_3d(st + kStTile + kStHalf, &tm_v, &full[s], 64, tile * kStTok, h,
                             policy);
+                if (ROPE) tma_load_2d(st + 2 * kStTile, &tm_t, &full[s], 0, tile * kStTok, keep);
             }
             // every load issued has landed before the CTA may exit
             const long long first = it > kStStages ? it - kStStages : 0;
@@ -331,130 +327,43 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             mma_commit(mma_done);
             mbar_wait_drain(mma_done, 0);
         }
-    } else {
-        // ------------------------------------------------ transform + flush + merge
+    } else if (warp < 2 + kStXWarps) {
+        // ------------------------------------------------ transform: phi, RoPE, z
         const int tt = threadIdx.x - 64;           // 0..255
         const int c = tt & 15, rl = tt >> 4;        // chunk (dims 8c..8c+7), row lane 0..15
         const int xw = warp - 2;                    // transform warp 0..7
         float zacc[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) zacc[j] = 0.f;
-        ChunkRope cr;
-        if (ROPE) cr.init(p.rope, c);
-        long long it = 0;
-        int seg = -1, cur_h = -1;
-        bool ok = !*abort_flag;
 
-        // The head's state from its partial slots, summed in slot order.
-        auto merge = [&](int hh) {
-            const int lo = p.split.owner((long long)hh * p.Tk);
-            const int hi = p.split.owner((long long)(hh + 1) * p.Tk - 1);
-            uint8_t* dst = p.state + (size_t)hh * kStateBytes;
-            float4 acc[8][2];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                acc[i][0] = acc[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int cc = lo; cc <= hi; ++cc) {
-                const float* src = p.partial + (size_t)(cc + hh) * kPartialFloats + c * 8;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float4* s4 = reinterpret_cast<const float4*>(src + (rl + 16 * i) * 128);
-                    const float4 a = __ldcg(s4), b = __ldcg(s4 + 1);
-                    acc[i][0].x += a.x; acc[i][0].y += a.y; acc[i][0].z += a.z; acc[i][0].w += a.w;
-                    acc[i][1].x += b.x; acc[i][1].y += b.y; acc[i][1].z += b.z; acc[i][1].w += b.w;
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int n = rl + 16 * i;
-                uint4 w;
-                w.x = f2_to_bf2(acc[i][0].x, acc[i][0].y);
-                w.y = f2_to_bf2(acc[i][0].z, acc[i][0].w);
-                w.z = f2_to_bf2(acc[i][1].x, acc[i][1].y);
-                w.w = f2_to_bf2(acc[i][1].z, acc[i][1].w);
-                *reinterpret_cast<uint4*>(dst + sw128_off(n, c, kStateHalf)) = w;
-            }
-            if (tt < kHeadDim) {
-                float zs = 0.f;
-                for (int cc = lo; cc <= hi; ++cc) {
-                    const float* zp = p.partial + (size_t)(cc + hh) * kPartialFloats +
-                                      kHeadDim * kHeadDim + tt;
-#pragma unroll
-                    for (int w8 = 0; w8 < kStXWarps; ++w8) zs += __ldcg(zp + w8 * kHeadDim);
-                }
-                reinterpret_cast<float*>(dst + kStateSBytes)[tt] = zs;
-            }
-        };
-
-        // S^T and z of this CTA's share of head hh -> slot (cta + hh); the
-        // head's last contributor then merges.  The warps meet only on
-        // mbarriers with bounded waits, so a warp that gives up cannot strand
-        // the others.
-        auto flush = [&](int sg, int hh) -> bool {
-            const bool got = warp_wait(&accfull[sg & 1], (sg >> 1) & 1, abort_flag, p.status);
-            float* slot = p.partial + (size_t)(cta + hh) * kPartialFloats;
-            if (got) {
-                tc_fence_after();
-                const int quad = warp & 3, hf = xw >> 2;   // TMEM lanes 32*quad.., columns 64*hf..
-                const int m = 32 * quad + lane;
-#pragma unroll 1
-                for (int ch = 0; ch < 2; ++ch) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(sg & 1) * 128 +
-                                  hf * 64 + ch * 32,
-                              r);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        slot[(size_t)(hf * 64 + ch * 32 + j) * kHeadDim + m] =
-                            __uint_as_float(r[j]);
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&accempty[sg & 1]);
-            }
-            // this warp's z: lanes l and l^16 hold the same dims for neighbouring rows
+        // Hands this warp's z of segment sg to the flush warps through zred.
+        auto hand_z = [&](int sg) -> bool {
+            const int b = sg & 1;
+            if (sg >= 2 && !warp_wait(&zfree[b], ((sg >> 1) - 1) & 1, abort_flag, p.status))
+                return false;
+            // lanes l and l^16 hold the same dims for neighbouring rows
 #pragma unroll
             for (int j = 0; j < 8; ++j) zacc[j] += __shfl_xor_sync(0xffffffffu, zacc[j], 16);
             if (lane < 16) {
-                float4* zp = reinterpret_cast<float4*>(slot + kHeadDim * kHeadDim +
-                                                       xw * kHeadDim + c * 8);
+                float4* zp = reinterpret_cast<float4*>(zred + (b * kStXWarps + xw) * kHeadDim +
+                                                       c * 8);
                 zp[0] = make_float4(zacc[0], zacc[1], zacc[2], zacc[3]);
                 zp[1] = make_float4(zacc[4], zacc[5], zacc[6], zacc[7]);
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j) zacc[j] = 0.f;
-            __threadfence();
             __syncwarp();
-            if (!got) return false;
-            if (lane == 0) mbar_arrive(slotdone);
-            if (tt == 0) {
-                // every warp's share of the slot is written: count this CTA in
-                const bool done = mbar_wait(slotdone, sg & 1, abort_flag, p.status);
-                int last = 0;
-                if (done) {
-                    __threadfence();
-                    const int lo = p.split.owner((long long)hh * p.Tk);
-                    const int hi = p.split.owner((long long)(hh + 1) * p.Tk - 1);
-                    const uint32_t n = count_contributor(p.counters + hh, p.epoch, p.status);
-                    last = n == (uint32_t)(hi - lo + 1) ? 1 : 0;
-                    __threadfence();
-                }
-                *last_flag = last;
-                mbar_arrive(lastknown);
-            }
-            if (!warp_wait(lastknown, sg & 1, abort_flag, p.status)) return false;
-            if (*last_flag) {
-                __threadfence();
-                merge(hh);
-            }
+            if (lane == 0) mbar_arrive(&zready[b]);
             return true;
         };
 
+        long long it = 0;
+        int seg = -1, cur_h = -1;
+        bool ok = !*abort_flag;
         for (long long u = u0; ok && u < u1; ++u, ++it) {
-            const int h = (int)(u / p.Tk), tile = (int)(u % p.Tk);
+            const int h = (int)(u / p.Tk);
             if (h != cur_h) {
-                if (seg >= 0 && !(ok = flush(seg, cur_h))) break;
+                if (seg >= 0 && !(ok = hand_z(seg))) break;
                 ++seg;
                 cur_h = h;
             }
@@ -462,33 +371,206 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             const uint32_t round = (uint32_t)(it / kStStages);
             if (!(ok = warp_wait(&full[s], round & 1, abort_flag, p.status))) break;
             const uint32_t kb = smem0 + s * kStStage;
-            const int n0 = tile * kStTok;
+            // all loads of the tile first, so their latencies overlap
+            uint32_t addr[kStRowsPerThread];
+            uint4 x[kStRowsPerThread];
 #pragma unroll
             for (int i = 0; i < kStRowsPerThread; ++i) {
-                const int r = rl + 16 * i;
-                const uint32_t addr = kb + sw128_off(r, c, kStHalf);
-                uint4 x = lds128(addr);
-                x.x = relu_bf2(x.x);
-                x.y = relu_bf2(x.y);
-                x.z = relu_bf2(x.z);
-                x.w = relu_bf2(x.w);
+                addr[i] = kb + sw128_off(rl + 16 * i, c, kStHalf);
+                x[i] = lds128(addr[i]);
+            }
+            float2 cs[kStRowsPerThread][4];
+            if (ROPE) {
+                // this chunk's (cos, sin) in each row's 256-byte RoPE row
+#pragma unroll
+                for (int i = 0; i < kStRowsPerThread; ++i)
+                    unpack_cs(lds128(kb + 2 * kStTile + (rl + 16 * i) * 256 + c * 16), cs[i]);
+            }
+#pragma unroll
+            for (int i = 0; i < kStRowsPerThread; ++i) {
+                x[i].x = relu_bf2(x[i].x);
+                x[i].y = relu_bf2(x[i].y);
+                x[i].z = relu_bf2(x[i].z);
+                x[i].w = relu_bf2(x[i].w);
                 float f[8];
-                unpack8(x, f);
+                unpack8(x[i], f);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) zacc[j] += f[j];
-                if (ROPE) {
-                    // rows past N are zero (TMA fill): any in-range position will do
-                    int t, hh, w;
-                    grid_pos(p.rope, min(n0 + r, p.N - 1), t, hh, w);
-                    x = cr.rotate(f, t, hh, w);
-                }
-                sts128(addr, x);
+                if (ROPE) x[i] = rotate_chunk(f, cs[i]);
             }
+#pragma unroll
+            for (int i = 0; i < kStRowsPerThread; ++i) sts128(addr[i], x[i]);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&kready[s]);
         }
-        if (ok && seg >= 0) flush(seg, cur_h);
+        if (ok && seg >= 0) hand_z(seg);
+    } else {
+        // ------------------------------------------------ flush + merge
+        // For every head segment of the CTA's range: S^T from TMEM and z from
+        // zred into slot (cta + head), then the count; the head's last
+        // contributor merges the head's slots.  The transform warps never wait
+        // for any of this.
+        const int ft = threadIdx.x - 32 * (2 + kStXWarps);   // 0..127
+        const int quad = warp & 3;                           // TMEM lanes 32*quad..
+        const int c = ft & 15, rq = ft >> 4;                 // merge: chunk, row lane 0..7
+        const int h_first = (int)(u0 / p.Tk), h_last = (int)((u1 - 1) / p.Tk);
+        int mbatch = 0;                                      // bulk merge batches issued
+
+        // Writes the merged S^T rows [64*half, 64*half + 64) handled by this
+        // thread (rows 64*half + rq + 8i, chunk c) from acc, as bf16.
+        auto write_half = [&](uint8_t* dst, int half, const float4 (&acc)[8][2]) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int n = 64 * half + rq + 8 * i;
+                uint4 w;
+                w.x = f2_to_bf2(acc[i][0].x, acc[i][0].y);
+                w.y = f2_to_bf2(acc[i][0].z, acc[i][0].w);
+                w.z = f2_to_bf2(acc[i][1].x, acc[i][1].y);
+                w.w = f2_to_bf2(acc[i][1].z, acc[i][1].w);
+                *reinterpret_cast<uint4*>(dst + sw128_off(n, c, kStateHalf)) = w;
+            }
+        };
+        auto add4 = [](float4& a, const float4& b) {
+            a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+        };
+        auto merge_z = [&](uint8_t* dst, int hh, int lo, int hi) {
+            float zs = 0.f;
+            for (int cc = lo; cc <= hi; ++cc)
+                zs += __ldcg(p.partial + (size_t)(cc + hh) * kPartialFloats +
+                             kHeadDim * kHeadDim + ft);
+            reinterpret_cast<float*>(dst + kStateSBytes)[ft] = zs;
+        };
+
+        // The head's state from its partial slots, summed in slot order, read
+        // from L2 (the ring is still in use).
+        auto merge = [&](int hh, int lo, int hi) {
+            uint8_t* dst = p.state + (size_t)hh * kStateBytes;
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                float4 acc[8][2];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    acc[i][0] = acc[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int cc = lo; cc <= hi; ++cc) {
+                    const float* src = p.partial + (size_t)(cc + hh) * kPartialFloats + c * 8;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float4* s4 = reinterpret_cast<const float4*>(
+                            src + (64 * half + rq + 8 * i) * kHeadDim);
+                        add4(acc[i][0], __ldcg(s4));
+                        add4(acc[i][1], __ldcg(s4 + 1));
+                    }
+                }
+                write_half(dst, half, acc);
+            }
+            merge_z(dst, hh, lo, hi);
+        };
+
+        // The same merge once the CTA's stage ring is idle: half-slots (32 KB,
+        // 64 rows) come in by bulk copies, six at a time, and are summed from
+        // shared memory in the same order.
+        auto merge_bulk = [&](int hh, int lo, int hi) -> bool {
+            constexpr int kHalfBytes = 64 * kHeadDim * 4;
+            constexpr int kPerBatch = kStRing / kHalfBytes;   // 6
+            uint8_t* dst = p.state + (size_t)hh * kStateBytes;
+            bool ok2 = true;
+#pragma unroll 1
+            for (int half = 0; ok2 && half < 2; ++half) {
+                float4 acc[8][2];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    acc[i][0] = acc[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int b0 = lo; ok2 && b0 <= hi; b0 += kPerBatch) {
+                    const int cnt = min(kPerBatch, hi - b0 + 1);
+                    if (ft == 0) {
+                        if (mbatch == 0 ||
+                            mbar_wait(mfree, (mbatch - 1) & 1, abort_flag, p.status)) {
+                            mbar_arrive_expect_tx(mfull, cnt * kHalfBytes);
+                            for (int j = 0; j < cnt; ++j)
+                                bulk_load(smem + j * kHalfBytes,
+                                          p.partial + (size_t)(b0 + j + hh) * kPartialFloats +
+                                              64 * half * kHeadDim,
+                                          kHalfBytes, mfull);
+                        }
+                    }
+                    const int bi = mbatch++;
+                    if (!(ok2 = warp_wait(mfull, bi & 1, abort_flag, p.status))) break;
+                    for (int j = 0; j < cnt; ++j) {
+                        const float* sl = reinterpret_cast<const float*>(smem + j * kHalfBytes);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float4* s4 = reinterpret_cast<const float4*>(
+                                sl + (rq + 8 * i) * kHeadDim + c * 8);
+                            add4(acc[i][0], s4[0]);
+                            add4(acc[i][1], s4[1]);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(mfree);
+                }
+                if (ok2) write_half(dst, half, acc);
+            }
+            if (ok2) merge_z(dst, hh, lo, hi);
+            return ok2;
+        };
+
+        bool ok = !*abort_flag;
+        for (int sg = 0; ok && sg <= h_last - h_first; ++sg) {
+            const int hh = h_first + sg, b = sg & 1;
+            if (!(ok = warp_wait(&accfull[b], (sg >> 1) & 1, abort_flag, p.status))) break;
+            tc_fence_after();
+            float* slot = p.partial + (size_t)(cta + hh) * kPartialFloats;
+            const int m = 32 * quad + lane;
+#pragma unroll 1
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t r[32];
+                tmem_ld32(tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)b * 128 + ch * 32, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    slot[(size_t)(ch * 32 + j) * kHeadDim + m] = __uint_as_float(r[j]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&accempty[b]);
+            if (!(ok = warp_wait(&zready[b], (sg >> 1) & 1, abort_flag, p.status))) break;
+            float zsum = 0.f;
+#pragma unroll
+            for (int w8 = 0; w8 < kStXWarps; ++w8) zsum += zred[(b * kStXWarps + w8) * kHeadDim + ft];
+            slot[kHeadDim * kHeadDim + ft] = zsum;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&zfree[b]);
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(slotdone);
+            const int lo = p.split.owner((long long)hh * p.Tk);
+            const int hi = p.split.owner((long long)(hh + 1) * p.Tk - 1);
+            if (ft == 0) {
+                // every flush warp's share of the slot is written: count this CTA in
+                const bool done = mbar_wait(slotdone, sg & 1, abort_flag, p.status);
+                int last = 0;
+                if (done) {
+                    __threadfence();
+                    const uint32_t n = count_contributor(p.counters + hh, p.epoch, p.status);
+                    last = n == (uint32_t)(hi - lo + 1) ? 1 : 0;
+                    __threadfence();
+                }
+                *last_flag = last;
+                mbar_arrive(lastknown);
+            }
+            if (!(ok = warp_wait(lastknown, sg & 1, abort_flag, p.status))) break;
+            if (*last_flag) {
+                __threadfence();
+                // after the last segment every tile has been consumed: the ring is idle
+                if (hh == h_last)
+                    ok = merge_bulk(hh, lo, hi);
+                else
+                    merge(hh, lo, hi);
+            }
+        }
+        // no bulk copy of ours may still be landing when the CTA exits
+        if (ft == 0 && mbatch > 0) mbar_wait_drain(mfull, (mbatch - 1) & 1);
     }
 
     tc_fence_before();
@@ -506,6 +588,8 @@ template <bool ROPE>
 __global__ void __launch_bounds__(kApThreads, 1)
 tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_g,
                 const __grid_constant__ CUtensorMap tm_o, ApplyParams p) {
+    constexpr int kApStages = ApGeo<ROPE>::kStages;
+    constexpr int kApStage = ApGeo<ROPE>::kStage;
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t* sbuf = smem + kApStages * kApStage;               // S^T bf16 (B operand), then z
     float* zs = reinterpret_cast<float*>(sbuf + kStateSBytes);  // [128]
@@ -576,6 +660,35 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 load_state(first_h);
                 first_pending = false;
             };
+            // A later head's state may load only once the previous state is free
+            // (sfree); that load stays pending while tiles keep streaming, and is
+            // issued from inside the waits for free stages.
+            int pending = -1;
+            uint32_t pend_parity = 0;
+            auto resolve_pending = [&]() -> bool {
+                if (pending < 0) return true;
+                if (!mbar_wait(sfree, pend_parity, abort_flag, p.status)) return false;
+                load_state(pending);
+                pending = -1;
+                return true;
+            };
+            auto wait_stage = [&](int s, uint32_t parity) -> bool {
+                if (pending < 0) return mbar_wait(&empty[s], parity, abort_flag, p.status);
+                const uint64_t t0 = global_ns();
+                for (uint32_t k = 0;; ++k) {
+                    if (pending >= 0 && mbar_try_wait(sfree, pend_parity)) {
+                        load_state(pending);
+                        pending = -1;
+                    }
+                    if (mbar_try_wait_sleep(&empty[s], parity, 2000)) return true;
+                    if (*abort_flag) return false;
+                    if ((k & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) {
+                        raise_status(p.status, kStatusTimeout);
+                        *abort_flag = 1;
+                        return false;
+                    }
+                }
+            };
             long long it = 0;
             int heads = 0, cur_h = -1;
             bool ok = true;
@@ -586,9 +699,9 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         first_h = h;
                     } else {
                         if (first_pending) load_first();
-                        if (!(ok = mbar_wait(sfree, (heads - 1) & 1, abort_flag, p.status)))
-                            break;
-                        load_state(h);
+                        if (!(ok = resolve_pending())) break;
+                        pending = h;
+                        pend_parity = (uint32_t)(heads - 1) & 1;
                     }
                     ++heads;
                     cur_h = h;
@@ -596,7 +709,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (first_pending && it == kApStages) load_first();
                 const int s = (int)(it % kApStages);
                 const uint32_t round = (uint32_t)(it / kApStages);
-                if (!(ok = mbar_wait(&empty[s], (round & 1) ^ 1, abort_flag, p.status))) break;
+                if (!(ok = wait_stage(s, (round & 1) ^ 1))) break;
                 uint8_t* st = smem + s * kApStage;
                 mbar_arrive_expect_tx(&full[s], kApStage);
                 tma_load_3d(st, &tm_q, &full[s], 0, tile * kApTok, h, policy);
@@ -606,6 +719,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             policy);
             }
             if (ok && first_pending && first_h >= 0) load_first();
+            if (ok) resolve_pending();
             // every copy issued has landed before the CTA may exit
             const long long first = it > kApStages ? it - kApStages : 0;
             for (long long j = first; j < it; ++j)
@@ -656,14 +770,27 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // ------------------------------------------------ transform: phi, RoPE, den
         const int tt = threadIdx.x - 64;            // 0..255
         const int c = tt & 15, rl = tt >> 4;         // chunk, row lane 0..15
-        ChunkRope cr;
-        if (ROPE) cr.init(p.rope, c);
         float zc[8];
+        // This thread's 16 bytes of the RoPE rows of its 8 rows in the next
+        // tile, loaded while the current tile is transformed.
+        uint4 trow[kApRowsPerThread];
+        auto fetch_rows = [&](int tile, int i0) {
+#pragma unroll
+            for (int i = i0; i < i0 + 4; ++i) {
+                const int n = min(tile * kApTok + rl + 16 * i, p.N - 1);   // rows past N are zero
+                trow[i] = ldg_nc_na128(p.rope.tok + (size_t)n * kPairs + c * 4);
+            }
+        };
+        if (ROPE && u0 < u1) {
+            fetch_rows((int)(u0 % p.Tq), 0);
+            fetch_rows((int)(u0 % p.Tq), 4);
+        }
         long long it = 0;
         int heads = 0, cur_h = -1;
         bool ok = !*abort_flag;
         for (long long u = u0; ok && u < u1; ++u, ++it) {
-            const int h = (int)(u / p.Tq), tile = (int)(u % p.Tq);
+            const int h = (int)(u / p.Tq);
+            const int next_tile = u + 1 < u1 ? (int)((u + 1) % p.Tq) : -1;
             if (h != cur_h) {
                 if (!(ok = warp_wait(sready, heads & 1, abort_flag, p.status))) break;
                 const float4 za = *reinterpret_cast<const float4*>(zs + 8 * c);
@@ -679,68 +806,90 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const uint32_t round = (uint32_t)(it / kApStages);
             if (!(ok = warp_wait(&full[s], round & 1, abort_flag, p.status))) break;
             const uint32_t qb = smem0 + s * kApStage;
-            const int n0 = tile * kApTok;
-            float den[kApRowsPerThread];
+            // two batches of four rows; in each, all loads first
 #pragma unroll
-            for (int i = 0; i < kApRowsPerThread; ++i) {
-                const int r = rl + 16 * i;
-                const uint32_t addr = qb + sw128_off(r, c, kApHalf);
-                uint4 x = lds128(addr);
-                x.x = relu_bf2(x.x);
-                x.y = relu_bf2(x.y);
-                x.z = relu_bf2(x.z);
-                x.w = relu_bf2(x.w);
-                float f[8];
-                unpack8(x, f);
-                float d = 0.f;
+            for (int b4 = 0; b4 < kApRowsPerThread; b4 += 4) {
+                float den[4];
+                uint32_t addr[4];
+                uint4 x[4];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) d = fmaf(f[j], zc[j], d);
-                den[i] = d;
-                if (ROPE) {
-                    int t, hh, w;
-                    grid_pos(p.rope, min(n0 + r, p.N - 1), t, hh, w);
-                    x = cr.rotate(f, t, hh, w);
+                for (int i = 0; i < 4; ++i) {
+                    addr[i] = qb + sw128_off(rl + 16 * (b4 + i), c, kApHalf);
+                    x[i] = lds128(addr[i]);
                 }
-                sts128(addr, x);
-            }
-            // Sum den over the 16 chunk lanes of each row: each step halves the
-            // rows a lane holds, so lane c ends with row rl + 16*(c >> 1).
-            {
-                const bool b3 = (c >> 3) & 1, b2 = (c >> 2) & 1, b1 = (c >> 1) & 1;
+
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float send = b3 ? den[k] : den[k + 4];
-                    const float keep = b3 ? den[k + 4] : den[k];
-                    den[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+                for (int i = 0; i < 4; ++i) {
+                    x[i].x = relu_bf2(x[i].x);
+                    x[i].y = relu_bf2(x[i].y);
+                    x[i].z = relu_bf2(x[i].z);
+                    x[i].w = relu_bf2(x[i].w);
+                    float f[8];
+                    unpack8(x[i], f);
+                    float d = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) d = fmaf(f[j], zc[j], d);
+                    den[i] = d;
+                    if (ROPE) {
+                        float2 cs[4];
+                        unpack_cs(trow[b4 + i], cs);
+                        x[i] = rotate_chunk(f, cs);
+                    }
                 }
+                // these rows of the RoPE table are used: load the next tile's
+                if (ROPE && next_tile >= 0) fetch_rows(next_tile, b4);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sts128(addr[i], x[i]);
+                // Sum den over the 16 chunk lanes of each row: each step halves the
+                // rows a lane holds, so lane c ends with row b4 + ((c >> 2) & 3).
+                const bool b3 = (c >> 3) & 1, b2 = (c >> 2) & 1;
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
-                    const float send = b2 ? den[k] : den[k + 2];
-                    const float keep = b2 ? den[k + 2] : den[k];
-                    den[k] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+                    const float send = b3 ? den[k] : den[k + 2];
+                    const float keep = b3 ? den[k + 2] : den[k];
+                    den[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
                 }
                 {
-                    const float send = b1 ? den[0] : den[1];
-                    const float keep = b1 ? den[1] : den[0];
-                    den[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+                    const float send = b2 ? den[0] : den[1];
+                    const float keep = b2 ? den[1] : den[0];
+                    den[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
                 }
+                den[0] += __shfl_xor_sync(0xffffffffu, den[0], 2);
                 den[0] += __shfl_xor_sync(0xffffffffu, den[0], 1);
-                if ((c & 1) == 0) dens[s * kApTok + rl + 16 * (c >> 1)] = den[0] + p.eps;
+                if ((c & 3) == 0) dens[s * kApTok + rl + 16 * (b4 + ((c >> 2) & 3))] = den[0] + p.eps;
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&qready[s]);
         }
+    } else if (warp == kApStorerWarp) {
+        // ------------------------------------------------ output stores
+        if (lane == 0) {
+            long long it = 0;
+            bool ok = !*abort_flag;
+            for (long long u = u0; ok && u < u1; ++u, ++it) {
+                const int h = (int)(u / p.Tq), tile = (int)(u % p.Tq);
+                const int s = (int)(it % kApStages);
+                const uint32_t round = (uint32_t)(it / kApStages);
+                // the eight epilogue warps have written the tile of o over G
+                if (!(ok = mbar_wait(&ogather[s], round & 1, abort_flag, p.status))) break;
+                const uint8_t* ot = smem + s * kApStage + kApTile;
+                tma_store_3d(&tm_o, ot, 0, tile * kApTok, h);
+                tma_store_3d(&tm_o, ot + kApHalf, 64, tile * kApTok, h);
+                bulk_commit();
+                bulk_wait_read_all();          // the stage may be refilled after this
+                mbar_arrive(&empty[s]);
+            }
+            bulk_wait_all();
+        }
     } else {
-        // ------------------------------------------------ epilogue: gate, divide, store
+        // ------------------------------------------------ epilogue: gate, divide
         const int ew = warp - 2 - kApXWarps;        // 0..7
         const int quad = warp & 3, hf = ew >> 2;     // TMEM lanes 32*quad.., columns 64*hf..
         const int r = 32 * quad + lane;              // TMEM lane = token row of the tile
-        const bool storer = threadIdx.x == kApFirstEpilogue;
         long long it = 0;
         bool ok = !*abort_flag;
         for (long long u = u0; ok && u < u1; ++u, ++it) {
-            const int h = (int)(u / p.Tq), tile = (int)(u % p.Tq);
             const int s = (int)(it % kApStages);
             const uint32_t round = (uint32_t)(it / kApStages);
             const int a = (int)(it & 1);
@@ -754,6 +903,13 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const uint32_t gb = smem0 + s * kApStage + kApTile;
 #pragma unroll 1
             for (int ch = 0; ch < 2; ++ch) {
+                uint32_t addr[4];
+                uint4 gv[4];
+#pragma unroll
+                for (int sub = 0; sub < 4; ++sub) {
+                    addr[sub] = gb + sw128_off(r, hf * 8 + ch * 4 + sub, kApHalf);
+                    gv[sub] = lds128(addr[sub]);
+                }
                 uint32_t v[32];
                 tmem_ld32(tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)a * 128 + hf * 64 +
                               ch * 32,
@@ -761,10 +917,8 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tmem_ld_wait();
 #pragma unroll
                 for (int sub = 0; sub < 4; ++sub) {
-                    const uint32_t addr = gb + sw128_off(r, hf * 8 + ch * 4 + sub, kApHalf);
-                    const uint4 gv = lds128(addr);
                     float gf[8];
-                    unpack8(gv, gf);
+                    unpack8(gv[sub], gf);
                     uint32_t ow[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -774,8 +928,10 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                                     1.f + __expf(-gf[2 * e + 1]));
                         ow[e] = f2_to_bf2(o0, o1);
                     }
-                    sts128(addr, make_uint4(ow[0], ow[1], ow[2], ow[3]));
+                    gv[sub] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
                 }
+#pragma unroll
+                for (int sub = 0; sub < 4; ++sub) sts128(addr[sub], gv[sub]);
             }
             tc_fence_before();
             fence_proxy_async_smem();
@@ -784,21 +940,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 mbar_arrive(&accempty[a]);
                 mbar_arrive(&ogather[s]);
             }
-            bool stored = true;
-            if (storer) {
-                stored = mbar_wait(&ogather[s], round & 1, abort_flag, p.status);
-                if (stored) {
-                    const uint8_t* ot = smem + s * kApStage + kApTile;
-                    tma_store_3d(&tm_o, ot, 0, tile * kApTok, h);
-                    tma_store_3d(&tm_o, ot + kApHalf, 64, tile * kApTok, h);
-                    bulk_commit();
-                    bulk_wait_read_all();          // the stage may be refilled after this
-                    mbar_arrive(&empty[s]);
-                }
-            }
-            if (!(ok = __all_sync(0xffffffffu, stored))) break;
         }
-        if (storer) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -841,11 +983,36 @@ bool make_map(CUtensorMap* m, const void* base, int N, int BH, int rows) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr size_t kStSmem = (size_t)kStStages * kStStage + 256;
-constexpr size_t kApSmem = (size_t)kApStages * kApStage + kStateBytes +
-                           kApStages * kApTok * sizeof(float) + 256;
-static_assert(kStSmem <= 232448, "state kernel exceeds the shared-memory limit");
-static_assert(kApSmem <= 232448, "apply kernel exceeds the shared-memory limit");
+// The per-token RoPE rows, [N][64] 4-byte (cos, sin) fp16 pairs, 256 bytes per
+// token, boxes of `rows` tokens; rows past N read as zero.
+bool make_rope_map(CUtensorMap* m, const uint32_t* base, int N, int rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)kPairs, (cuuint64_t)N};
+    cuuint64_t strides[1] = {(cuuint64_t)kPairs * 4};
+    cuuint32_t box[2] = {(cuuint32_t)kPairs, (cuuint32_t)rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(base), dims, strides,
+              box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Barriers and flags follow the buffers: state 3*stages + 13 mbarriers plus
+// three words, apply 4*stages + 7 mbarriers plus two words.
+template <bool ROPE>
+constexpr size_t st_smem() {
+    return (size_t)kStRing + 2 * kStXWarps * kHeadDim * sizeof(float) +
+           (3 * StGeo<ROPE>::kStages + 13) * 8 + 16;
+}
+template <bool ROPE>
+constexpr size_t ap_smem() {
+    return (size_t)ApGeo<ROPE>::kStages * ApGeo<ROPE>::kStage + kStateBytes +
+           ApGeo<ROPE>::kStages * kApTok * sizeof(float) + (4 * ApGeo<ROPE>::kStages + 7) * 8 +
+           16;
+}
+static_assert(st_smem<true>() <= 232448 && st_smem<false>() <= 232448, "state kernel smem");
+static_assert(ap_smem<true>() <= 232448 && ap_smem<false>() <= 232448, "apply kernel smem");
 
 struct Plan {
     int Tk, Tq;
@@ -889,10 +1056,10 @@ cudaError_t configure(int dev) {
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (done[dev]) return cudaSuccess;
     cudaError_t e;
-    if ((e = set_smem(tc_state_kernel<false>, kStSmem)) != cudaSuccess) return e;
-    if ((e = set_smem(tc_state_kernel<true>, kStSmem)) != cudaSuccess) return e;
-    if ((e = set_smem(tc_apply_kernel<false>, kApSmem)) != cudaSuccess) return e;
-    if ((e = set_smem(tc_apply_kernel<true>, kApSmem)) != cudaSuccess) return e;
+    if ((e = set_smem(tc_state_kernel<false>, st_smem<false>())) != cudaSuccess) return e;
+    if ((e = set_smem(tc_state_kernel<true>, st_smem<true>())) != cudaSuccess) return e;
+    if ((e = set_smem(tc_apply_kernel<false>, ap_smem<false>())) != cudaSuccess) return e;
+    if ((e = set_smem(tc_apply_kernel<true>, ap_smem<true>())) != cudaSuccess) return e;
     done[dev] = true;
     return cudaSuccess;
 }
@@ -914,10 +1081,14 @@ cudaError_t launch_state(const void* k, const void* v, int BH, int N, const Rope
     sp.epoch = next_epoch();
     sp.status = status;
     if (rope) {
+        CUtensorMap mt;
+        if (!make_rope_map(&mt, rope->tok, N, kStTok)) return cudaErrorInvalidValue;
         sp.rope = *rope;
-        tc_state_kernel<true><<<pl.st.G, kStThreads, kStSmem, stream>>>(mk, mv, sp);
+        tc_state_kernel<true><<<pl.st.G, kStThreads, st_smem<true>(), stream>>>(mk, mv, mt, sp);
     } else {
-        tc_state_kernel<false><<<pl.st.G, kStThreads, kStSmem, stream>>>(mk, mv, sp);
+        // no RoPE: the table map is never read; K's map fills the parameter
+        tc_state_kernel<false><<<pl.st.G, kStThreads, st_smem<false>(), stream>>>(mk, mv, mk,
+                                                                                 sp);
     }
     return cudaGetLastError();
 }
@@ -941,7 +1112,7 @@ cudaError_t launch_apply(const void* q, const void* g, const uint8_t* state, voi
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(pl.ap.G);
     cfg.blockDim = dim3(kApThreads);
-    cfg.dynamicSmemBytes = kApSmem;
+    cfg.dynamicSmemBytes = rope ? ap_smem<true>() : ap_smem<false>();
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

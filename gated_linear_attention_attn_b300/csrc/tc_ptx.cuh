@@ -49,6 +49,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The same test, but a thread whose phase is not complete is suspended in
+// hardware until the phase completes or about `hint_ns` nanoseconds pass,
+// instead of returning at once: a waiting warp then takes no issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Suspension granted to one wait attempt (each attempt ends early when the
+// phase completes).
+constexpr uint32_t kWaitSleepNs = 20000;
+
 // Waits for the phase of `bar` with the given parity to complete.  Gives up
 // when *abort is set by another role, or after kWaitLimitNs; on a timeout it
 // raises the status word and sets *abort.  Returns true when the phase
@@ -57,10 +77,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           volatile int* abort, unsigned* status) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
         if (*abort) return false;
-        if ((it & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) {
+        if (global_ns() - t0 > kWaitLimitNs) {
             raise_status(status, kStatusTimeout);
             *abort = 1;
             return false;
@@ -72,9 +92,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
 // ignores the abort flag.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
     const uint64_t t0 = global_ns();
-    for (uint32_t it = 0;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
     }
 }
 
@@ -92,6 +112,16 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
         ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
         "l"(policy)
+        : "memory");
+}
+
+// 2D tiled load global -> shared, completion counted on `bar` in bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar,
+                                            int c0, int c1, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
 
@@ -126,6 +156,12 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
 }
 
 __device__ __forceinline__ uint64_t policy_evict_first() {
@@ -266,6 +302,16 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "r"(addr)
                  : "memory");
+    return v;
+}
+
+// 16-byte read-only global load that does not allocate in L1 (data read once
+// per SM, kept in L2).
+__device__ __forceinline__ uint4 ldg_nc_na128(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(reinterpret_cast<uint64_t>(p)));
     return v;
 }
 

@@ -88,7 +88,8 @@ class RopeTable:
     """A filled 3D RoPE table on one device, plus its grid and band split.
 
     The table holds, for each axis, the (cos, sin) of every coordinate value
-    times every frequency of that axis's band (see ``sla_rope_table_t``).
+    times every frequency of that axis's band in fp32, and for every token its
+    d/2 (cos, sin) pairs in fp16 (see ``sla_rope_table_t``).
     """
 
     def __init__(self, grid: Sequence[int], split: Sequence[int] = (44, 42, 42),
@@ -113,6 +114,16 @@ class RopeTable:
 
     def c_struct(self) -> RopeTableC:
         return RopeTableC(self.table.data_ptr(), *self.grid, *self.split)
+
+    def token_rows(self):
+        """The per-token rows as an [N, d/2, 2] float16 tensor of (cos, sin)."""
+        T, Hs, Ws = self.grid
+        dt, dh, dw = self.split
+        sep = T * dt + Hs * dh + Ws * dw
+        off = (sep + 63) // 64 * 64
+        n = T * Hs * Ws
+        p = (dt + dh + dw) // 2
+        return self.table[off:off + n * p].view(torch.float16).view(n, p, 2)
 
     def axis_tables(self):
         """The (cos, sin) rows of each axis as [extent, pairs, 2] float tensors."""

@@ -25,7 +25,7 @@
  *
  * Ownership.  The caller owns every buffer passed in.  The library owns a
  * workspace per (device, stream) for the split-N partial states and the
- * heads' states (about 68 KB per SM of the device plus 101 KB per head),
+ * heads' states (about 66 KB per SM of the device plus 99 KB per head),
  * allocated with cudaMalloc on the first call that needs it (or more of it)
  * and kept until the process exits.  A call that has to grow the workspace synchronises the
  * device; make the first call of the largest shape outside stream capture.
@@ -53,7 +53,7 @@ typedef enum sla_status {
     SLA_OK = 0,
     SLA_ERR_INVALID_ARG = 1,    /* null pointer, size < 1, bad eps, aliasing, bad RoPE grid */
     SLA_ERR_UNSUPPORTED = 2,    /* a shape the kernels do not implement (d != 128) */
-    SLA_ERR_ALIGNMENT = 3,      /* a tensor not 16-byte aligned (a RoPE table not 8-byte aligned) */
+    SLA_ERR_ALIGNMENT = 3,      /* a tensor not 16-byte aligned (a RoPE table not 256-byte aligned) */
     SLA_ERR_CUDA = 4,           /* a CUDA runtime call failed (launch, allocation, no device) */
     SLA_ERR_DEVICE_TIMEOUT = 5  /* a kernel gave up a wait and returned early */
 } sla_status_t;
@@ -67,26 +67,31 @@ typedef enum sla_status {
  * a band of width W, pair j = (x_{2p}, x_{2p+1}) turns by pos * base^(-2j/W)
  * radians (complex multiplication of x_{2p} + i x_{2p+1}).
  *
- * `table` is a device buffer of sla_rope_table_floats(...) floats written by
- * sla_rope_table_fill: (cos, sin) pairs for t in [0,T) x j in [0,dt/2), then
- * for h in [0,Hs) x j in [0,dh/2), then for w in [0,Ws) x j in [0,dw/2).
- * The angles are separable by axis, so the table holds
- * T*dt + Hs*dh + Ws*dw floats rather than one row per token.
+ * `table` is a device buffer of sla_rope_table_floats(...) 4-byte words
+ * written by sla_rope_table_fill, in two parts.  First the angles separated
+ * by axis, as fp32 (cos, sin) pairs: for t in [0,T) x j in [0,dt/2), then for
+ * h in [0,Hs) x j in [0,dh/2), then for w in [0,Ws) x j in [0,dw/2)
+ * (T*dt + Hs*dh + Ws*dw words; the fp32 kernels read these).  Then, from the
+ * next multiple of 64 words, one row per token n of its d/2 pairs, each pair
+ * one word holding fp16 cos (low half) and fp16 sin (high half): 256 bytes
+ * per token for d = 128, streamed by the bf16 kernels next to the token's
+ * row of q or k.
  */
 typedef struct sla_rope_table {
-    const float* table;   /* device pointer, 8-byte aligned */
+    const float* table;   /* device pointer, 256-byte aligned */
     int T, Hs, Ws;        /* latent grid; N must equal T*Hs*Ws */
     int dt, dh, dw;       /* even band widths, dt + dh + dw == d */
 } sla_rope_table_t;
 
-/* Number of floats of the RoPE table for this grid and split (0 if invalid). */
+/* Number of 4-byte words of the RoPE table for this grid and split (0 if invalid). */
 size_t sla_rope_table_floats(int T, int Hs, int Ws, int dt, int dh, int dw);
 
 /*
  * Writes the RoPE table (layout above) for base `base` (10000 for the Wan
- * embedding) into `table` (device, sla_rope_table_floats(...) floats).  The
- * angles are formed and the cosine and sine taken in double precision, then
- * rounded to float.  Asynchronous on `stream`.
+ * embedding) into `table` (device, sla_rope_table_floats(...) words, 256-byte
+ * aligned).  The angles are formed and the cosine and sine taken in double
+ * precision, then rounded to fp32 (first part) and fp16 (second part).
+ * Asynchronous on `stream`.
  */
 sla_status_t sla_rope_table_fill(float* table, int T, int Hs, int Ws, int dt, int dh,
                                  int dw, float base, sla_stream_t stream);
@@ -170,7 +175,7 @@ sla_status_t sla_linattn_apply(const void* q, const void* g, const void* state, 
  *
  * Size limit: a shape whose scratch does not fit in the 24 MiB array returns
  * SLA_ERR_UNSUPPORTED before anything is launched.  The scratch is about
- * 68 KB x (number of SMs + B*H) + 33 KB x B*H, so B*H up to about 140 heads
+ * 66 KB x (number of SMs + B*H) + 33 KB x B*H, so B*H up to about 150 heads
  * fits on a 148-SM B300.
  *
  * The first call on a device looks up the array's device address (once per

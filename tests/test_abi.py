@@ -97,8 +97,10 @@ def test_forward_rejects_bad_rope():
 
 def test_rope_table_sizes():
     f = sla.raw_lib().sla_rope_table_floats
-    assert f(25, 22, 40, 44, 42, 42) == 25 * 44 + 22 * 42 + 40 * 42
-    assert f(181, 22, 40, 44, 42, 42) == 10568
+    # fp32 axis rows (rounded up to 64 words), then 64 fp16 pairs per token
+    assert f(25, 22, 40, 44, 42, 42) == 3712 + 22000 * 64
+    assert f(181, 22, 40, 44, 42, 42) == 10624 + 159280 * 64
+    assert f(1, 1, 1, 2, 2, 2) == 64 + 3
     assert f(0, 1, 1, 2, 2, 2) == 0
     assert f(1, 1, 1, 3, 2, 2) == 0
     fill = sla.raw_lib().sla_rope_table_fill

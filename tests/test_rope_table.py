@@ -22,3 +22,8 @@ def test_table_matches_oracle_angles(grid, split, cuda_device):
     assert cs.shape == ang.shape + (2,)
     assert np.max(np.abs(cs[..., 0] - np.cos(ang))) <= 1e-6
     assert np.max(np.abs(cs[..., 1] - np.sin(ang))) <= 1e-6
+    # the per-token fp16 rows: every pair of every token, rounded to fp16
+    tok = rt.token_rows().double().cpu().numpy()              # [N, 64, 2]
+    assert tok.shape == ang.shape + (2,)
+    assert np.max(np.abs(tok[..., 0] - np.cos(ang))) <= 2.5e-4
+    assert np.max(np.abs(tok[..., 1] - np.sin(ang))) <= 2.5e-4
