@@ -23,9 +23,9 @@
 //                     phi and RoPE to the Q tile in place and form
 //                     den = phi(q) . z + eps; one thread of warp 1 issues
 //                     num = phi~(Q) S (M = N = K = 128) into one of two TMEM
-//                     accumulators; eight epilogue warps read num from TMEM
-//                     and compute sigmoid(g) * num / den over the G tile in
-//                     place, which a storer warp then writes out with TMA.
+//                     accumulators; eight epilogue warps read num from TMEM,
+//                     compute sigmoid(g) * num / den over the G tile in place
+//                     and each stores its 32 x 64 block of o with TMA.
 //
 // The apply kernel is launched as a programmatic dependent of the state
 // kernel: it prefetches Q and G (which the state kernel does not write) and
@@ -91,8 +91,8 @@ struct ApGeo {
 constexpr int kApXWarps = 8;
 constexpr int kApEWarps = 8;
 constexpr int kApXThreads = 32 * kApXWarps;
-constexpr int kApStorerWarp = 2 + kApXWarps + kApEWarps;       // issues the output stores
-constexpr int kApThreads = 32 * (kApStorerWarp + 1);
+constexpr int kApThreads = 32 * (2 + kApXWarps + kApEWarps);
+constexpr int kApORows = 32;                      // rows of o one epilogue warp stores
 constexpr int kApTmemCols = 256;
 constexpr int kApRowsPerThread = kApTok * 16 / kApXThreads;   // 8
 
@@ -587,7 +587,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 template <bool ROPE>
 __global__ void __launch_bounds__(kApThreads, 1)
 tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_g,
-                const __grid_constant__ CUtensorMap tm_o, ApplyParams p) {
+                const __grid_constant__ CUtensorMap tm_o32, ApplyParams p) {
     constexpr int kApStages = ApGeo<ROPE>::kStages;
     constexpr int kApStage = ApGeo<ROPE>::kStage;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -597,8 +597,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint64_t* full = reinterpret_cast<uint64_t*>(dens + kApStages * kApTok);
     uint64_t* qready = full + kApStages;
     uint64_t* empty = qready + kApStages;
-    uint64_t* ogather = empty + kApStages;
-    uint64_t* accfull = ogather + kApStages;    // [2]
+    uint64_t* accfull = empty + kApStages;      // [2]
     uint64_t* accempty = accfull + 2;           // [2]
     uint64_t* sready = accempty + 2;
     uint64_t* sfree = sready + 1;
@@ -615,8 +614,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int s = 0; s < kApStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&qready[s], kApXWarps);
-            mbar_init(&empty[s], 1);
-            mbar_init(&ogather[s], kApEWarps);
+            mbar_init(&empty[s], kApEWarps);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&accfull[a], 1);
@@ -630,7 +628,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         fence_mbar_init();
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_g);
-        prefetch_tmap(&tm_o);
+        prefetch_tmap(&tm_o32);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, kApTmemCols);
@@ -836,8 +834,10 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         x[i] = rotate_chunk(f, cs);
                     }
                 }
-                // these rows of the RoPE table are used: load the next tile's
-                if (ROPE && next_tile >= 0) fetch_rows(next_tile, b4);
+                // rows 0-3 of the RoPE table are used: load the next tile's.  The
+                // fence below waits for this thread's loads in flight, so rows 4-7
+                // are loaded only after it.
+                if (ROPE && next_tile >= 0 && b4 == 0) fetch_rows(next_tile, 0);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) sts128(addr[i], x[i]);
                 // Sum den over the 16 chunk lanes of each row: each step halves the
@@ -861,35 +861,17 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&qready[s]);
-        }
-    } else if (warp == kApStorerWarp) {
-        // ------------------------------------------------ output stores
-        if (lane == 0) {
-            long long it = 0;
-            bool ok = !*abort_flag;
-            for (long long u = u0; ok && u < u1; ++u, ++it) {
-                const int h = (int)(u / p.Tq), tile = (int)(u % p.Tq);
-                const int s = (int)(it % kApStages);
-                const uint32_t round = (uint32_t)(it / kApStages);
-                // the eight epilogue warps have written the tile of o over G
-                if (!(ok = mbar_wait(&ogather[s], round & 1, abort_flag, p.status))) break;
-                const uint8_t* ot = smem + s * kApStage + kApTile;
-                tma_store_3d(&tm_o, ot, 0, tile * kApTok, h);
-                tma_store_3d(&tm_o, ot + kApHalf, 64, tile * kApTok, h);
-                bulk_commit();
-                bulk_wait_read_all();          // the stage may be refilled after this
-                mbar_arrive(&empty[s]);
-            }
-            bulk_wait_all();
+            if (ROPE && next_tile >= 0) fetch_rows(next_tile, 4);
         }
     } else {
-        // ------------------------------------------------ epilogue: gate, divide
+        // ------------------------------------------------ epilogue: gate, divide, store
         const int ew = warp - 2 - kApXWarps;        // 0..7
         const int quad = warp & 3, hf = ew >> 2;     // TMEM lanes 32*quad.., columns 64*hf..
         const int r = 32 * quad + lane;              // TMEM lane = token row of the tile
         long long it = 0;
         bool ok = !*abort_flag;
         for (long long u = u0; ok && u < u1; ++u, ++it) {
+            const int h = (int)(u / p.Tq), tile = (int)(u % p.Tq);
             const int s = (int)(it % kApStages);
             const uint32_t round = (uint32_t)(it / kApStages);
             const int a = (int)(it & 1);
@@ -899,7 +881,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                  warp_wait(&full[s], round & 1, abort_flag, p.status);
             if (!ok) break;
             tc_fence_after();
-            const float rden = 1.f / dens[s * kApTok + r];
+            const float den = dens[s * kApTok + r];
             const uint32_t gb = smem0 + s * kApStage + kApTile;
 #pragma unroll 1
             for (int ch = 0; ch < 2; ++ch) {
@@ -920,12 +902,13 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     float gf[8];
                     unpack8(gv[sub], gf);
                     uint32_t ow[4];
+                    // o = num / (den * (1 + exp(-g))), the product formed by one fma
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float o0 = __fdividef(__uint_as_float(v[sub * 8 + 2 * e]) * rden,
-                                                    1.f + __expf(-gf[2 * e]));
-                        const float o1 = __fdividef(__uint_as_float(v[sub * 8 + 2 * e + 1]) * rden,
-                                                    1.f + __expf(-gf[2 * e + 1]));
+                        const float d0 = fmaf(den, __expf(-gf[2 * e]), den);
+                        const float d1 = fmaf(den, __expf(-gf[2 * e + 1]), den);
+                        const float o0 = __fdividef(__uint_as_float(v[sub * 8 + 2 * e]), d0);
+                        const float o1 = __fdividef(__uint_as_float(v[sub * 8 + 2 * e + 1]), d1);
                         ow[e] = f2_to_bf2(o0, o1);
                     }
                     gv[sub] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
@@ -938,9 +921,16 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&accempty[a]);
-                mbar_arrive(&ogather[s]);
+                // this warp's rows 32*quad.. of column half hf, 4 KB of the tile
+                tma_store_3d(&tm_o32, smem + s * kApStage + kApTile + hf * kApHalf +
+                                          quad * kApORows * 128,
+                             64 * hf, tile * kApTok + quad * kApORows, h);
+                bulk_commit();
+                bulk_wait_read_all();          // the stage may be refilled after this
+                mbar_arrive(&empty[s]);
             }
         }
+        if (lane == 0) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -999,7 +989,7 @@ bool make_rope_map(CUtensorMap* m, const uint32_t* base, int N, int rows) {
 }
 
 // Barriers and flags follow the buffers: state 3*stages + 13 mbarriers plus
-// three words, apply 4*stages + 7 mbarriers plus two words.
+// three words, apply 3*stages + 7 mbarriers plus two words.
 template <bool ROPE>
 constexpr size_t st_smem() {
     return (size_t)kStRing + 2 * kStXWarps * kHeadDim * sizeof(float) +
@@ -1008,7 +998,7 @@ constexpr size_t st_smem() {
 template <bool ROPE>
 constexpr size_t ap_smem() {
     return (size_t)ApGeo<ROPE>::kStages * ApGeo<ROPE>::kStage + kStateBytes +
-           ApGeo<ROPE>::kStages * kApTok * sizeof(float) + (4 * ApGeo<ROPE>::kStages + 7) * 8 +
+           ApGeo<ROPE>::kStages * kApTok * sizeof(float) + (3 * ApGeo<ROPE>::kStages + 7) * 8 +
            16;
 }
 static_assert(st_smem<true>() <= 232448 && st_smem<false>() <= 232448, "state kernel smem");
@@ -1099,7 +1089,7 @@ cudaError_t launch_apply(const void* q, const void* g, const uint8_t* state, voi
     const Plan pl = make_plan(BH, N, num_sms);
     CUtensorMap mq, mg, mo;
     if (!make_map(&mq, q, N, BH, kApTok) || !make_map(&mg, g, N, BH, kApTok) ||
-        !make_map(&mo, out, N, BH, kApTok))
+        !make_map(&mo, out, N, BH, kApORows))
         return cudaErrorInvalidValue;
     ApplyParams ap{};
     ap.N = N;
