@@ -141,12 +141,16 @@ class ClockSampler:
                 "reasons": sorted(self.reasons)}
 
 
+# The sources the tensor-core kernels are built from.
+KERNEL_SOURCES = ("tc_forward.cu", "tc_ptx.cuh", "common.cuh", "launch.h")
+
+
 def source_hash():
-    """Hash of the CUDA sources, to tell whether a stored ncu traffic figure is current."""
+    """Hash of the kernels' sources, to tell whether a stored ncu traffic figure is current."""
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "gated_linear_attention_attn_b300", "csrc", "*"))):
-        with open(p, "rb") as fh:
-            h.update(os.path.basename(p).encode())
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "gated_linear_attention_attn_b300", "csrc", name), "rb") as fh:
+            h.update(name.encode())
             h.update(fh.read())
     return h.hexdigest()[:16]
 

@@ -5,9 +5,9 @@
 // head dimension by the token's frame, row and column index.  The angles of a
 // band depend on one coordinate only, so the first part of the table holds
 // one short fp32 row per coordinate value (read by the fp32 kernels); the
-// second part holds, for every token, all d/2 pairs as fp16 (cos, sin), so
-// that the tensor-core kernels stream a token's rotation with its row of q or
-// k instead of gathering it pair by pair.
+// second part holds, for every token, all d/2 pairs as fp16 (cos, sin) copied
+// from those rows, so that the tensor-core kernels stream a token's rotation
+// with its row of q or k instead of gathering it pair by pair.
 #include <cuda_fp16.h>
 
 #include "launch.h"
@@ -47,27 +47,28 @@ __global__ void rope_axes_kernel(float2* __restrict__ table, int T, int Hs, int 
     }
 }
 
-// Entry (n, p): pair p of token n = (t*Hs + h)*Ws + w.
-__global__ void rope_tokens_kernel(uint32_t* __restrict__ rows, int T, int Hs, int Ws, int pt,
-                                   int ph, int pw, double base) {
+// Entry (n, p): pair p of token n = (t*Hs + h)*Ws + w, copied from the axis
+// rows (written just before on the same stream) and rounded to fp16.
+__global__ void rope_tokens_kernel(uint32_t* __restrict__ rows, const float2* __restrict__ axes,
+                                   int T, int Hs, int Ws, int pt, int ph, int pw) {
     const int P = pt + ph + pw;
     const int total = T * Hs * Ws * P;
+    const float2* tab_h = axes + T * pt;
+    const float2* tab_w = tab_h + Hs * ph;
     for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < total;
          e += gridDim.x * blockDim.x) {
         const int n = e / P, p = e - n * P;
         const int hw = n / Ws, w = n - hw * Ws;
         const int t = hw / Hs, h = hw - t * Hs;
-        double ang;
+        float2 cs;
         if (p < pt)
-            ang = band_angle(base, t, p, pt);
+            cs = axes[t * pt + p];
         else if (p < pt + ph)
-            ang = band_angle(base, h, p - pt, ph);
+            cs = tab_h[h * ph + (p - pt)];
         else
-            ang = band_angle(base, w, p - pt - ph, pw);
-        double s, c;
-        sincos(ang, &s, &c);
-        const __half2 cs = __floats2half2_rn((float)c, (float)s);
-        rows[e] = *reinterpret_cast<const uint32_t*>(&cs);
+            cs = tab_w[w * pw + (p - pt - ph)];
+        const __half2 v = __floats2half2_rn(cs.x, cs.y);
+        rows[e] = *reinterpret_cast<const uint32_t*>(&v);
     }
 }
 
@@ -91,7 +92,7 @@ cudaError_t launch_rope_fill(float* table, int T, int Hs, int Ws, int dt, int dh
         uint32_t* rows = reinterpret_cast<uint32_t*>(table) +
                          rope_tok_offset_words(T, Hs, Ws, dt, dh, dw);
         rope_tokens_kernel<<<grid_for(tokens, threads), threads, 0, stream>>>(
-            rows, T, Hs, Ws, pt, ph, pw, (double)base);
+            rows, reinterpret_cast<const float2*>(table), T, Hs, Ws, pt, ph, pw);
     }
     return cudaGetLastError();
 }

@@ -90,7 +90,8 @@ size_t sla_rope_table_floats(int T, int Hs, int Ws, int dt, int dh, int dw);
  * Writes the RoPE table (layout above) for base `base` (10000 for the Wan
  * embedding) into `table` (device, sla_rope_table_floats(...) words, 256-byte
  * aligned).  The angles are formed and the cosine and sine taken in double
- * precision, then rounded to fp32 (first part) and fp16 (second part).
+ * precision and rounded to fp32 (first part); the second part holds the same
+ * values rounded from fp32 to fp16.
  * Asynchronous on `stream`.
  */
 sla_status_t sla_rope_table_fill(float* table, int T, int Hs, int Ws, int dt, int dh,
