@@ -13,13 +13,16 @@
 //                     K = 64 tokens, both operands MN-major).  When a CTA
 //                     leaves a head it writes its partial (S^T, z) in fp32 to
 //                     workspace slot (cta + head) and counts itself in the
-//                     head's counter; the last contributor of a head sums the
-//                     head's slots in a fixed order and writes the head's
+//                     head's counter; the CTAs whose ranges end in the head
+//                     wait for all its counts and each sums a block of rows
+//                     of the head's slots, in a fixed order, into the head's
 //                     state: S^T in bf16, already in the tensor-core layout of
-//                     the apply kernel's B operand, and z in fp32.
-//   tc_apply_kernel   units = (head, 128-token tile).  Warp 0 streams Q and G
-//                     tiles into a 3-stage ring and, once per head, the head's
-//                     state with one bulk copy.  Eight transform warps apply
+//                     the apply kernel's B operand, and z in fp32.  (The
+//                     launch is cooperative, so those CTAs are resident.)
+//   tc_apply_kernel   units = (head, 128-token tile).  Warp 0 streams Q tiles
+//                     (and, once per head, the head's state with one bulk
+//                     copy) and a last warp streams G tiles, each into its own
+//                     3-slot ring.  Eight transform warps apply
 //                     phi and RoPE to the Q tile in place and form
 //                     den = phi(q) . z + eps; one thread of warp 1 issues
 //                     num = phi~(Q) S (M = N = K = 128) into one of two TMEM
@@ -71,27 +74,26 @@ constexpr int kStRowsPerThread = kStTok * 16 / kStXThreads;   // 4
 constexpr int kApTok = 128;
 constexpr int kApHalf = kApTok * 128;             // 16 KB
 constexpr int kApTile = 2 * kApHalf;              // 32 KB
-constexpr int kApRing = 3 * 2 * kApTile;          // the stage ring: 192 KB
+constexpr int kApQStages = 3;                     // Q ring: a slot is free once the MMA read it
+constexpr int kApGStages = 3;                     // G ring: a slot is free once o is stored
+constexpr int kApDSlots = 4;                      // den of the tiles between transform and epilogue
 
 // A state stage holds one tile of K and of V and, with RoPE, the tile's rows
 // of the per-token RoPE table (256 bytes per token, the size of a tensor
 // row); the ring has the same size either way, so RoPE trades stages for the
-// table rows.  An apply stage holds Q and G; its transform warps read their
+// table rows.  The apply kernel streams Q and G in separate rings, so a Q slot
+// turns over as soon as the MMA has read it; its transform warps read their
 // RoPE rows straight from global memory (L2), one tile ahead.
 template <bool ROPE>
 struct StGeo {
     static constexpr int kStage = (ROPE ? 3 : 2) * kStTile;
     static constexpr int kStages = kStRing / kStage;       // 4 or 6
 };
-template <bool ROPE>
-struct ApGeo {
-    static constexpr int kStage = 2 * kApTile;
-    static constexpr int kStages = kApRing / kStage;       // 3
-};
+
 constexpr int kApXWarps = 8;
 constexpr int kApEWarps = 8;
 constexpr int kApXThreads = 32 * kApXWarps;
-constexpr int kApThreads = 32 * (2 + kApXWarps + kApEWarps);
+constexpr int kApThreads = 32 * (3 + kApXWarps + kApEWarps);   // + the G producer warp
 constexpr int kApORows = 32;                      // rows of o one epilogue warp stores
 constexpr int kApTmemCols = 256;
 constexpr int kApRowsPerThread = kApTok * 16 / kApXThreads;   // 8
@@ -193,6 +195,27 @@ __device__ uint32_t count_contributor(unsigned long long* ctr, uint32_t epoch, u
     }
     raise_status(status, kStatusTimeout);
     return 0;
+}
+
+// Waits until the head's counter shows k contributors for launch `epoch`.
+// Every contributor is resident (the state kernel is a cooperative launch) and
+// counts itself without waiting for anyone, so the wait ends; it still gives
+// up after kWaitLimitNs.
+__device__ bool wait_count(const unsigned long long* ctr, uint32_t epoch, uint32_t k,
+                           volatile int* abort, unsigned* status) {
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        unsigned long long v;
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
+        if ((uint32_t)(v >> 32) == epoch && (uint32_t)v >= k) return true;
+        if (*abort) return false;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            raise_status(status, kStatusTimeout);
+            *abort = 1;
+            return false;
+        }
+        __nanosleep(100);
+    }
 }
 
 // =================================================================== state ==
@@ -515,6 +538,47 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             return ok2;
         };
 
+        // Rows [r0, r1) of the head's state from all its slots, in slot order;
+        // with_z also sums z.  Several CTAs each merge a block of rows.
+        auto merge_rows = [&](int hh, int lo, int hi, int r0, int r1, bool with_z) {
+            uint8_t* dst = p.state + (size_t)hh * kStateBytes;
+            const int tasks = (r1 - r0) * 16;                 // (row, 8-column chunk)
+#pragma unroll 1
+            for (int t0 = 0; t0 < tasks; t0 += 4 * 128) {
+                float4 acc[4][2];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    acc[i][0] = acc[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int cc = lo; cc <= hi; ++cc) {
+                    const float* src = p.partial + (size_t)(cc + hh) * kPartialFloats;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int t = t0 + i * 128 + ft;
+                        if (t < tasks) {
+                            const float4* s4 = reinterpret_cast<const float4*>(
+                                src + (r0 + (t >> 4)) * kHeadDim + (t & 15) * 8);
+                            add4(acc[i][0], __ldcg(s4));
+                            add4(acc[i][1], __ldcg(s4 + 1));
+                        }
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int t = t0 + i * 128 + ft;
+                    if (t < tasks) {
+                        uint4 w;
+                        w.x = f2_to_bf2(acc[i][0].x, acc[i][0].y);
+                        w.y = f2_to_bf2(acc[i][0].z, acc[i][0].w);
+                        w.z = f2_to_bf2(acc[i][1].x, acc[i][1].y);
+                        w.w = f2_to_bf2(acc[i][1].z, acc[i][1].w);
+                        *reinterpret_cast<uint4*>(dst + sw128_off(r0 + (t >> 4), t & 15,
+                                                                  kStateHalf)) = w;
+                    }
+                }
+            }
+            if (with_z) merge_z(dst, hh, lo, hi);
+        };
+
         bool ok = !*abort_flag;
         for (int sg = 0; ok && sg <= h_last - h_first; ++sg) {
             const int hh = h_first + sg, b = sg & 1;
@@ -544,29 +608,44 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             __threadfence();
             __syncwarp();
             if (lane == 0) mbar_arrive(slotdone);
+            // The head's contributors are CTAs lo..hi; those whose ranges end
+            // in the head (lo..e_hi, at least lo when there are two or more)
+            // finish together at the end of the kernel and share its merge.
             const int lo = p.split.owner((long long)hh * p.Tk);
             const int hi = p.split.owner((long long)(hh + 1) * p.Tk - 1);
+            const int k = hi - lo + 1;
+            const int e_hi = (p.split.start(hi + 1) - 1) / p.Tk == hh ? hi : hi - 1;
+            const bool last_seg = hh == h_last;
             if (ft == 0) {
                 // every flush warp's share of the slot is written: count this CTA in
                 const bool done = mbar_wait(slotdone, sg & 1, abort_flag, p.status);
-                int last = 0;
+                int action = 0;                      // 0 none, 1 whole merge, 2 a block of rows
                 if (done) {
                     __threadfence();
-                    const uint32_t n = count_contributor(p.counters + hh, p.epoch, p.status);
-                    last = n == (uint32_t)(hi - lo + 1) ? 1 : 0;
+                    count_contributor(p.counters + hh, p.epoch, p.status);
+                    if (k == 1)
+                        action = 1;
+                    else if (last_seg && wait_count(p.counters + hh, p.epoch, (uint32_t)k,
+                                                    abort_flag, p.status))
+                        action = 2;
                     __threadfence();
                 }
-                *last_flag = last;
+                *last_flag = action;
                 mbar_arrive(lastknown);
             }
             if (!(ok = warp_wait(lastknown, sg & 1, abort_flag, p.status))) break;
-            if (*last_flag) {
+            const int action = *last_flag;
+            if (action == 1) {
                 __threadfence();
                 // after the last segment every tile has been consumed: the ring is idle
-                if (hh == h_last)
+                if (last_seg)
                     ok = merge_bulk(hh, lo, hi);
                 else
                     merge(hh, lo, hi);
+            } else if (action == 2) {
+                __threadfence();
+                const int m = e_hi - lo + 1, j = cta - lo;
+                merge_rows(hh, lo, hi, j * kHeadDim / m, (j + 1) * kHeadDim / m, j == 0);
             }
         }
         // no bulk copy of ours may still be landing when the CTA exits
@@ -588,17 +667,21 @@ template <bool ROPE>
 __global__ void __launch_bounds__(kApThreads, 1)
 tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_g,
                 const __grid_constant__ CUtensorMap tm_o32, ApplyParams p) {
-    constexpr int kApStages = ApGeo<ROPE>::kStages;
-    constexpr int kApStage = ApGeo<ROPE>::kStage;
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint8_t* sbuf = smem + kApStages * kApStage;               // S^T bf16 (B operand), then z
+    uint8_t* qring = smem;                                      // [kApQStages][32 KB]
+    uint8_t* gring = smem + kApQStages * kApTile;               // [kApGStages][32 KB]
+    uint8_t* sbuf = gring + kApGStages * kApTile;               // S^T bf16 (B operand), then z
     float* zs = reinterpret_cast<float*>(sbuf + kStateSBytes);  // [128]
-    float* dens = zs + kHeadDim;                                // [stages][128]
-    uint64_t* full = reinterpret_cast<uint64_t*>(dens + kApStages * kApTok);
-    uint64_t* qready = full + kApStages;
-    uint64_t* empty = qready + kApStages;
-    uint64_t* accfull = empty + kApStages;      // [2]
-    uint64_t* accempty = accfull + 2;           // [2]
+    float* dens = zs + kHeadDim;                                // [kApDSlots][128]
+    uint64_t* qfull = reinterpret_cast<uint64_t*>(dens + kApDSlots * kApTok);
+    uint64_t* qready = qfull + kApQStages;       // Q tile transformed (MMA may read it)
+    uint64_t* qempty = qready + kApQStages;      // Q tile read by the MMA
+    uint64_t* gfull = qempty + kApQStages;
+    uint64_t* gempty = gfull + kApGStages;       // o stored from the G slot
+    uint64_t* dready = gempty + kApGStages;      // [kApDSlots] den of a tile written
+    uint64_t* dfree = dready + kApDSlots;        // [kApDSlots] den of a tile read
+    uint64_t* accfull = dfree + kApDSlots;       // [2]
+    uint64_t* accempty = accfull + 2;            // [2]
     uint64_t* sready = accempty + 2;
     uint64_t* sfree = sready + 1;
     uint64_t* mma_done = sfree + 1;
@@ -611,10 +694,18 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t smem0 = smem_u32(smem);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kApStages; ++s) {
-            mbar_init(&full[s], 1);
+        for (int s = 0; s < kApQStages; ++s) {
+            mbar_init(&qfull[s], 1);
             mbar_init(&qready[s], kApXWarps);
-            mbar_init(&empty[s], kApEWarps);
+            mbar_init(&qempty[s], 1);
+        }
+        for (int s = 0; s < kApGStages; ++s) {
+            mbar_init(&gfull[s], 1);
+            mbar_init(&gempty[s], kApEWarps);
+        }
+        for (int s = 0; s < kApDSlots; ++s) {
+            mbar_init(&dready[s], kApXWarps);
+            mbar_init(&dfree[s], kApEWarps);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&accfull[a], 1);
@@ -640,11 +731,11 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer
+        // ------------------------------------------------ Q producer (+ the heads' states)
         if (lane == 0 && !*abort_flag) {
             const uint64_t policy = policy_evict_first();
             // The first head's state is written by the preceding launch: its load
-            // waits for that launch to complete, after the first Q/G tiles are in
+            // waits for that launch to complete, after the first Q tiles are in
             // flight.  Later heads wait until the previous state is no longer read.
             int first_h = -1, loads = 0;
             bool first_pending = true;
@@ -671,14 +762,14 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 return true;
             };
             auto wait_stage = [&](int s, uint32_t parity) -> bool {
-                if (pending < 0) return mbar_wait(&empty[s], parity, abort_flag, p.status);
+                if (pending < 0) return mbar_wait(&qempty[s], parity, abort_flag, p.status);
                 const uint64_t t0 = global_ns();
                 for (uint32_t k = 0;; ++k) {
                     if (pending >= 0 && mbar_try_wait(sfree, pend_parity)) {
                         load_state(pending);
                         pending = -1;
                     }
-                    if (mbar_try_wait_sleep(&empty[s], parity, 2000)) return true;
+                    if (mbar_try_wait_sleep(&qempty[s], parity, 2000)) return true;
                     if (*abort_flag) return false;
                     if ((k & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) {
                         raise_status(p.status, kStatusTimeout);
@@ -704,24 +795,21 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     ++heads;
                     cur_h = h;
                 }
-                if (first_pending && it == kApStages) load_first();
-                const int s = (int)(it % kApStages);
-                const uint32_t round = (uint32_t)(it / kApStages);
+                if (first_pending && it == kApQStages) load_first();
+                const int s = (int)(it % kApQStages);
+                const uint32_t round = (uint32_t)(it / kApQStages);
                 if (!(ok = wait_stage(s, (round & 1) ^ 1))) break;
-                uint8_t* st = smem + s * kApStage;
-                mbar_arrive_expect_tx(&full[s], kApStage);
-                tma_load_3d(st, &tm_q, &full[s], 0, tile * kApTok, h, policy);
-                tma_load_3d(st + kApHalf, &tm_q, &full[s], 64, tile * kApTok, h, policy);
-                tma_load_3d(st + kApTile, &tm_g, &full[s], 0, tile * kApTok, h, policy);
-                tma_load_3d(st + kApTile + kApHalf, &tm_g, &full[s], 64, tile * kApTok, h,
-                            policy);
+                uint8_t* st = qring + s * kApTile;
+                mbar_arrive_expect_tx(&qfull[s], kApTile);
+                tma_load_3d(st, &tm_q, &qfull[s], 0, tile * kApTok, h, policy);
+                tma_load_3d(st + kApHalf, &tm_q, &qfull[s], 64, tile * kApTok, h, policy);
             }
             if (ok && first_pending && first_h >= 0) load_first();
             if (ok) resolve_pending();
             // every copy issued has landed before the CTA may exit
-            const long long first = it > kApStages ? it - kApStages : 0;
+            const long long first = it > kApQStages ? it - kApQStages : 0;
             for (long long j = first; j < it; ++j)
-                mbar_wait_drain(&full[j % kApStages], (uint32_t)((j / kApStages) & 1));
+                mbar_wait_drain(&qfull[j % kApQStages], (uint32_t)((j / kApQStages) & 1));
             if (loads > 0) mbar_wait_drain(sready, (loads - 1) & 1);
         }
     } else if (warp == 1) {
@@ -741,16 +829,16 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     ++heads;
                     cur_h = h;
                 }
-                const int s = (int)(it % kApStages);
-                const uint32_t round = (uint32_t)(it / kApStages);
+                const int s = (int)(it % kApQStages);
+                const uint32_t round = (uint32_t)(it / kApQStages);
                 const int a = (int)(it & 1);
                 const uint32_t around = (uint32_t)(it >> 1);
                 ok = mbar_wait(&accempty[a], (around & 1) ^ 1, abort_flag, p.status) &&
                      mbar_wait(&qready[s], round & 1, abort_flag, p.status) &&
-                     mbar_wait(&full[s], round & 1, abort_flag, p.status);
+                     mbar_wait(&qfull[s], round & 1, abort_flag, p.status);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t qb = smem0 + s * kApStage;
+                const uint32_t qb = smem0 + s * kApTile;
 #pragma unroll
                 for (int ks = 0; ks < kHeadDim / 16; ++ks) {
                     // K-major, 128-byte swizzle: 16 k-values = 32 bytes inside a row
@@ -760,6 +848,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     mma_bf16(tmem + (uint32_t)a * 128, ad, bd, idesc, ks > 0 ? 1u : 0u);
                 }
                 mma_commit(&accfull[a]);
+                mma_commit(&qempty[s]);                   // the Q slot may be refilled
             }
             mma_commit(mma_done);
             mbar_wait_drain(mma_done, 0);
@@ -800,10 +889,15 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 ++heads;
                 cur_h = h;
             }
-            const int s = (int)(it % kApStages);
-            const uint32_t round = (uint32_t)(it / kApStages);
-            if (!(ok = warp_wait(&full[s], round & 1, abort_flag, p.status))) break;
-            const uint32_t qb = smem0 + s * kApStage;
+            const int s = (int)(it % kApQStages);
+            const uint32_t round = (uint32_t)(it / kApQStages);
+            const int ds = (int)(it % kApDSlots);
+            const uint32_t dround = (uint32_t)(it / kApDSlots);
+            if (!(ok = warp_wait(&qfull[s], round & 1, abort_flag, p.status))) break;
+            // the epilogue has read the den slot's previous tile
+            if (dround > 0 && !(ok = warp_wait(&dfree[ds], (dround - 1) & 1, abort_flag, p.status)))
+                break;
+            const uint32_t qb = smem0 + s * kApTile;
             // two batches of four rows; in each, all loads first
 #pragma unroll
             for (int b4 = 0; b4 < kApRowsPerThread; b4 += 4) {
@@ -815,7 +909,6 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     addr[i] = qb + sw128_off(rl + 16 * (b4 + i), c, kApHalf);
                     x[i] = lds128(addr[i]);
                 }
-
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     x[i].x = relu_bf2(x[i].x);
@@ -856,14 +949,18 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
                 den[0] += __shfl_xor_sync(0xffffffffu, den[0], 2);
                 den[0] += __shfl_xor_sync(0xffffffffu, den[0], 1);
-                if ((c & 3) == 0) dens[s * kApTok + rl + 16 * (b4 + ((c >> 2) & 3))] = den[0] + p.eps;
+                if ((c & 3) == 0)
+                    dens[ds * kApTok + rl + 16 * (b4 + ((c >> 2) & 3))] = den[0] + p.eps;
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&qready[s]);
+            if (lane == 0) {
+                mbar_arrive(&qready[s]);
+                mbar_arrive(&dready[ds]);
+            }
             if (ROPE && next_tile >= 0) fetch_rows(next_tile, 4);
         }
-    } else {
+    } else if (warp < 2 + kApXWarps + kApEWarps) {
         // ------------------------------------------------ epilogue: gate, divide, store
         const int ew = warp - 2 - kApXWarps;        // 0..7
         const int quad = warp & 3, hf = ew >> 2;     // TMEM lanes 32*quad.., columns 64*hf..
@@ -872,17 +969,20 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         bool ok = !*abort_flag;
         for (long long u = u0; ok && u < u1; ++u, ++it) {
             const int h = (int)(u / p.Tq), tile = (int)(u % p.Tq);
-            const int s = (int)(it % kApStages);
-            const uint32_t round = (uint32_t)(it / kApStages);
+            const int gs = (int)(it % kApGStages);
+            const uint32_t ground = (uint32_t)(it / kApGStages);
+            const int ds = (int)(it % kApDSlots);
             const int a = (int)(it & 1);
             const uint32_t around = (uint32_t)(it >> 1);
             ok = warp_wait(&accfull[a], around & 1, abort_flag, p.status) &&
-                 warp_wait(&qready[s], round & 1, abort_flag, p.status) &&
-                 warp_wait(&full[s], round & 1, abort_flag, p.status);
+                 warp_wait(&dready[ds], (uint32_t)(it / kApDSlots) & 1, abort_flag, p.status) &&
+                 warp_wait(&gfull[gs], ground & 1, abort_flag, p.status);
             if (!ok) break;
             tc_fence_after();
-            const float den = dens[s * kApTok + r];
-            const uint32_t gb = smem0 + s * kApStage + kApTile;
+            const float den = dens[ds * kApTok + r];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&dfree[ds]);
+            const uint32_t gb = smem0 + kApQStages * kApTile + gs * kApTile;
 #pragma unroll 1
             for (int ch = 0; ch < 2; ++ch) {
                 uint32_t addr[4];
@@ -922,15 +1022,34 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (lane == 0) {
                 mbar_arrive(&accempty[a]);
                 // this warp's rows 32*quad.. of column half hf, 4 KB of the tile
-                tma_store_3d(&tm_o32, smem + s * kApStage + kApTile + hf * kApHalf +
+                tma_store_3d(&tm_o32, gring + gs * kApTile + hf * kApHalf +
                                           quad * kApORows * 128,
                              64 * hf, tile * kApTok + quad * kApORows, h);
                 bulk_commit();
-                bulk_wait_read_all();          // the stage may be refilled after this
-                mbar_arrive(&empty[s]);
+                bulk_wait_read_all();          // the G slot may be refilled after this
+                mbar_arrive(&gempty[gs]);
             }
         }
         if (lane == 0) bulk_wait_all();
+    } else {
+        // ------------------------------------------------ G producer
+        if (lane == 0 && !*abort_flag) {
+            const uint64_t policy = policy_evict_first();
+            long long it = 0;
+            for (long long u = u0; u < u1; ++u, ++it) {
+                const int h = (int)(u / p.Tq), tile = (int)(u % p.Tq);
+                const int s = (int)(it % kApGStages);
+                const uint32_t round = (uint32_t)(it / kApGStages);
+                if (!mbar_wait(&gempty[s], (round & 1) ^ 1, abort_flag, p.status)) break;
+                uint8_t* st = gring + s * kApTile;
+                mbar_arrive_expect_tx(&gfull[s], kApTile);
+                tma_load_3d(st, &tm_g, &gfull[s], 0, tile * kApTok, h, policy);
+                tma_load_3d(st + kApHalf, &tm_g, &gfull[s], 64, tile * kApTok, h, policy);
+            }
+            const long long first = it > kApGStages ? it - kApGStages : 0;
+            for (long long j = first; j < it; ++j)
+                mbar_wait_drain(&gfull[j % kApGStages], (uint32_t)((j / kApGStages) & 1));
+        }
     }
 
     tc_fence_before();
@@ -989,7 +1108,8 @@ bool make_rope_map(CUtensorMap* m, const uint32_t* base, int N, int rows) {
 }
 
 // Barriers and flags follow the buffers: state 3*stages + 13 mbarriers plus
-// three words, apply 3*stages + 7 mbarriers plus two words.
+// three words, apply 3*Q stages + 2*G stages + 2*den slots + 7 mbarriers plus
+// two words.
 template <bool ROPE>
 constexpr size_t st_smem() {
     return (size_t)kStRing + 2 * kStXWarps * kHeadDim * sizeof(float) +
@@ -997,9 +1117,9 @@ constexpr size_t st_smem() {
 }
 template <bool ROPE>
 constexpr size_t ap_smem() {
-    return (size_t)ApGeo<ROPE>::kStages * ApGeo<ROPE>::kStage + kStateBytes +
-           ApGeo<ROPE>::kStages * kApTok * sizeof(float) + (3 * ApGeo<ROPE>::kStages + 7) * 8 +
-           16;
+    return (size_t)(kApQStages + kApGStages) * kApTile + kStateBytes +
+           kApDSlots * kApTok * sizeof(float) +
+           (3 * kApQStages + 2 * kApGStages + 2 * kApDSlots + 7) * 8 + 16;
 }
 static_assert(st_smem<true>() <= 232448 && st_smem<false>() <= 232448, "state kernel smem");
 static_assert(ap_smem<true>() <= 232448 && ap_smem<false>() <= 232448, "apply kernel smem");
@@ -1070,17 +1190,23 @@ cudaError_t launch_state(const void* k, const void* v, int BH, int N, const Rope
     sp.state = state;
     sp.epoch = next_epoch();
     sp.status = status;
-    if (rope) {
-        CUtensorMap mt;
-        if (!make_rope_map(&mt, rope->tok, N, kStTok)) return cudaErrorInvalidValue;
-        sp.rope = *rope;
-        tc_state_kernel<true><<<pl.st.G, kStThreads, st_smem<true>(), stream>>>(mk, mv, mt, sp);
-    } else {
-        // no RoPE: the table map is never read; K's map fills the parameter
-        tc_state_kernel<false><<<pl.st.G, kStThreads, st_smem<false>(), stream>>>(mk, mv, mk,
-                                                                                 sp);
-    }
-    return cudaGetLastError();
+    CUtensorMap mt = mk;   // without RoPE the table map is never read
+    if (rope && !make_rope_map(&mt, rope->tok, N, kStTok)) return cudaErrorInvalidValue;
+    if (rope) sp.rope = *rope;
+    // Cooperative: all CTAs are resident together, which the shared merge of a
+    // head's state relies on (its CTAs wait for each other's counts).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(pl.st.G);
+    cfg.blockDim = dim3(kStThreads);
+    cfg.dynamicSmemBytes = rope ? st_smem<true>() : st_smem<false>();
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (rope) return cudaLaunchKernelEx(&cfg, tc_state_kernel<true>, mk, mv, mt, sp);
+    return cudaLaunchKernelEx(&cfg, tc_state_kernel<false>, mk, mv, mt, sp);
 }
 
 cudaError_t launch_apply(const void* q, const void* g, const uint8_t* state, void* out, int BH,
