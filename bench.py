@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip timing the oracle on the host")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    ap.add_argument("--forward-kernel", default="auto", choices=["auto", "fused", "split"],
+                    help="launch plan of the bf16 forward (SLA_FORWARD_KERNEL)")
     return ap.parse_args()
 
 
@@ -239,7 +241,7 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def _config(wl, world, note=""):
+def _config(wl, world, note="", plan=None):
     cfg = {"workload": wl.name, "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d,
            "grid": list(wl.grid), "rope": wl.rope,
            "rope_split": list(wl.split) if wl.rope else None, "eps": wl.eps,
@@ -249,6 +251,8 @@ def _config(wl, world, note=""):
                   % (wl.algorithmic_bytes / 1e6) if wl.algorithmic_bytes >= 4 * L2_BYTES
                   else "L2 flushed between steps (a 252 MB buffer written outside the "
                        "timed events)")}
+    if plan:
+        cfg["launch_plan"] = plan
     if note:
         cfg["note"] = note
     return cfg
@@ -315,6 +319,9 @@ def run_sla(args, rank, world, local):
         def scrub():
             scrub_buf.fill_(1)
 
+    os.environ["SLA_FORWARD_KERNEL"] = args.forward_kernel
+    cluster = sla.forward_cluster(wl.B, wl.H, wl.N, wl.rope, device=dev) if bf16 else 0
+
     def step():
         sla.linattn_forward(q, k, v, g, out=out, rope=rope, eps=wl.eps, stream=stream)
 
@@ -340,8 +347,23 @@ def run_sla(args, rank, world, local):
     per_step = secs / args.steps
     value = world * wl.token_heads / per_step
 
-    # -------- each kernel on its own (the two phases of the forward), for the roofline
+    # -------- each kernel on its own, for the roofline: the fused kernel is the
+    # whole forward; the two-launch plan is timed phase by phase
     kernels = {}
+    plans = {}
+    if bf16 and cluster > 0:
+        kernels["tc_fused_kernel"] = {"us": 1e6 * per_step,
+                                      "algorithmic_bytes": wl.algorithmic_bytes,
+                                      "gbs": wl.algorithmic_bytes / per_step / 1e9,
+                                      "cluster": cluster}
+        plans["fused"] = {"us": 1e6 * per_step, "cluster": cluster}
+        with sla.forward_kernel("split"):
+            for _ in range(3):
+                step()
+            plans["split"] = {"us": 1e6 * _time_steps(step, args.steps, stream, scrub)
+                              / args.steps}
+    elif bf16:
+        plans["split"] = {"us": 1e6 * per_step}
     if bf16:
         state = sla.linattn_state(k, v, rope=rope, stream=stream)
 
@@ -352,14 +374,19 @@ def run_sla(args, rank, world, local):
             sla.linattn_apply(q, g, state, out=out, rope=rope, eps=wl.eps, stream=stream)
 
         per_tok = wl.d * wl.elem_size
+        phases = {}
         for name, fn, unit_bytes in (("tc_state_kernel", k_state, 2 * per_tok),
                                      ("tc_apply_kernel", k_apply, 3 * per_tok)):
             for _ in range(3):
                 fn()
             ksecs = _time_steps(fn, args.steps, stream, scrub) / args.steps
             alg = unit_bytes * wl.B * wl.H * wl.N
-            kernels[name] = {"us": 1e6 * ksecs, "algorithmic_bytes": alg,
-                             "gbs": alg / ksecs / 1e9}
+            phases[name] = {"us": 1e6 * ksecs, "algorithmic_bytes": alg,
+                            "gbs": alg / ksecs / 1e9}
+        if cluster > 0:
+            plans["split"]["kernels"] = phases
+        else:
+            kernels.update(phases)
         status = sla.last_device_status(stream, dev)
         if status != sla.OK:
             raise RuntimeError(f"device status after kernel timing: {sla.status_string(status)}")
@@ -404,7 +431,7 @@ def run_sla(args, rank, world, local):
                     "traffic": stored_traffic(dom, wl.name),
                     "forward": {"achieved": wl.algorithmic_bytes / per_step / 1e9,
                                 "frac": wl.algorithmic_bytes / per_step / 1e9 / peak},
-                    "kernels": kernels}
+                    "kernels": kernels, "plans": plans}
     else:
         achieved = wl.algorithmic_bytes / per_step / 1e9
         roofline = {"bound": "hbm", "kernel": "simt forward (both launches)",
@@ -417,10 +444,11 @@ def run_sla(args, rank, world, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if bf16 else "f32",
         "data": "synthetic (seeded N(0,1) q,k,v,g on the latent token grid)",
-        "config": _config(wl, world),
+        "config": _config(wl, world, plan=("fused, clusters of %d CTAs per head" % cluster
+                                           if cluster > 0 else "state + apply launches")),
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": sla.launches_per_forward(wl.dtype) * args.steps,
+        "gpu_launches": (1 if cluster > 0 else 2) * args.steps,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline:

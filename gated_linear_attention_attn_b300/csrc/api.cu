@@ -199,11 +199,13 @@ static sla_status_t forward(const void* q, const void* k, const void* v, const v
         if ((st = workspace(dev, s, simt_workspace_bytes(BH, C), &ws)) != SLA_OK) return st;
         err = launch_simt_f32((const float*)q, (const float*)k, (const float*)v,
                               (const float*)g, (float*)out, B, H, N, rp, eps, (float*)ws, C, s);
+    } else if (const int C = tc_forward_cluster(dev, BH, N, rp != nullptr, ds->num_sms)) {
+        err = launch_tc_fused(q, k, v, g, out, B, H, N, C, rp, eps, ds->status, s);
     } else {
         if ((st = workspace(dev, s, tc_workspace_bytes(BH, N, ds->num_sms), &ws)) != SLA_OK)
             return st;
-        err = launch_tc_bf16(q, k, v, g, out, B, H, N, rp, eps, (float*)ws, ds->status,
-                             ds->num_sms, s);
+        err = launch_tc_two_phase(q, k, v, g, out, B, H, N, rp, eps, (float*)ws, ds->status,
+                                  ds->num_sms, s);
     }
     if (err != cudaSuccess) {
         cudaGetLastError();
@@ -224,6 +226,19 @@ sla_status_t sla_linattn_forward_f32(const float* q, const float* k, const float
                                      const sla_rope_table_t* rope_table, float eps,
                                      sla_stream_t stream) {
     return forward(q, k, v, g, out, B, H, N, d, rope_table, eps, stream, true);
+}
+
+int sla_linattn_forward_cluster(int B, int H, int N, int d, int rope) {
+    if (check_dims(B, H, N, d) != SLA_OK) return -1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* ds = nullptr;
+    if (device_state(dev, &ds) != SLA_OK) return -1;
+    return tc_forward_cluster(dev, B * H, N, rope != 0, ds->num_sms);
 }
 
 size_t sla_linattn_state_bytes(int B, int H, int d) {

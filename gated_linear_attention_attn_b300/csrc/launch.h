@@ -31,9 +31,18 @@ cudaError_t launch_simt_bf16(const void* q, const void* k, const void* v, const 
 size_t tc_workspace_bytes(int BH, int N, int num_sms);
 size_t tc_state_workspace_bytes(int BH, int N, int num_sms);
 size_t tc_state_bytes(int BH);
-cudaError_t launch_tc_bf16(const void* q, const void* k, const void* v, const void* g, void* out,
-                           int B, int H, int N, const RopeView* rope, float eps, float* workspace,
-                           unsigned* status, int num_sms, cudaStream_t stream);
+// The forward runs either as one fused launch (one cluster of C CTAs per
+// head, no workspace) or as the state and apply launches.
+// tc_forward_cluster gives C for the shape on device `dev`, 0 for the two
+// launches.
+int tc_forward_cluster(int dev, int BH, int N, bool rope, int num_sms);
+cudaError_t launch_tc_fused(const void* q, const void* k, const void* v, const void* g, void* out,
+                            int B, int H, int N, int C, const RopeView* rope, float eps,
+                            unsigned* status, cudaStream_t stream);
+cudaError_t launch_tc_two_phase(const void* q, const void* k, const void* v, const void* g,
+                                void* out, int B, int H, int N, const RopeView* rope, float eps,
+                                float* workspace, unsigned* status, int num_sms,
+                                cudaStream_t stream);
 cudaError_t launch_tc_state(const void* k, const void* v, void* state, int B, int H, int N,
                             const RopeView* rope, void* workspace, unsigned* status, int num_sms,
                             cudaStream_t stream);

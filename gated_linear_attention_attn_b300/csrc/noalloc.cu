@@ -77,12 +77,19 @@ extern "C" sla_status_t sla_linattn_forward_noalloc(const void* q, const void* k
     NoAllocDevice* nd = nullptr;
     if ((st = noalloc_device(dev, &nd)) != SLA_OK) return st;
     const int BH = B * H;
-    // the whole scratch this shape needs must fit in the fixed array
-    if (tc_workspace_bytes(BH, N, nd->num_sms) > kScratchBytes) return SLA_ERR_UNSUPPORTED;
-    const cudaError_t err =
-        launch_tc_bf16(q, k, v, g, out, B, H, N, rope_table ? &rv : nullptr, eps,
-                       reinterpret_cast<float*>(nd->scratch), device_status, nd->num_sms,
-                       reinterpret_cast<cudaStream_t>(stream));
+    const RopeView* rp = rope_table ? &rv : nullptr;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t err;
+    if (const int C = tc_forward_cluster(dev, BH, N, rp != nullptr, nd->num_sms)) {
+        // the fused kernel needs no scratch
+        err = launch_tc_fused(q, k, v, g, out, B, H, N, C, rp, eps, device_status, s);
+    } else {
+        // the whole scratch this shape needs must fit in the fixed array
+        if (tc_workspace_bytes(BH, N, nd->num_sms) > kScratchBytes) return SLA_ERR_UNSUPPORTED;
+        err = launch_tc_two_phase(q, k, v, g, out, B, H, N, rp, eps,
+                                  reinterpret_cast<float*>(nd->scratch), device_status,
+                                  nd->num_sms, s);
+    }
     if (err != cudaSuccess) {
         cudaGetLastError();
         return SLA_ERR_CUDA;

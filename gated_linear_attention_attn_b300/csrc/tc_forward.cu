@@ -40,6 +40,9 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
 
 #include <cuda_fp16.h>
 
@@ -171,6 +174,13 @@ __device__ __forceinline__ uint4 rotate_chunk(const float (&f)[8], const float2 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           unsigned* status) {
     const bool ok = mbar_wait(bar, parity, abort, status);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// warp_wait for phases completed by arrivals from other CTAs of the cluster.
+__device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort, unsigned* status) {
+    const bool ok = mbar_wait_cluster(bar, parity, abort, status);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -1061,6 +1071,554 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
 }
 
+// =================================================================== fused ==
+//
+// One cluster of C CTAs per head does the whole forward of that head in one
+// launch (for shapes with few heads per SM, where the two-launch path pays
+// its fixed costs: launch, ramp, merge tail).  Phase 1: CTA r of the cluster
+// streams its share of the head's K and V tiles as the state kernel does,
+// accumulating its partial S^T in TMEM and its z in registers, and writes
+// both to its own shared memory.  Reduction: CTA r sums rows
+// [r*128/C, (r+1)*128/C) of the C partials through distributed shared memory
+// and writes them, as bf16 in the MMA layout, into every CTA's state buffer;
+// each CTA sums z itself.  Phase 2: CTA r applies the state to its share of
+// the head's Q and G tiles as the apply kernel does.  The cluster meets only
+// on mbarriers with bounded waits, and on one cluster barrier just before
+// exit, which every thread reaches after bounded work.
+
+constexpr int kFuThreads = kApThreads;            // the apply kernel's 19 warps
+constexpr int kFuTmemCols = 512;                  // phase 2 at 0 and 128, phase 1 at 256
+constexpr int kFuMaxCluster = 8;
+constexpr int kFuAutoMaxTiles = 36;               // longest head the shape rule fuses
+constexpr int kFuPartial = kApQStages * kApTile;  // partial S^T, then z parts: at the G ring
+constexpr int kFuPartialBytes = (kHeadDim * kHeadDim + kStXWarps * kHeadDim) * 4;
+static_assert(kFuPartial + kFuPartialBytes <= kStRing, "the partial fits in the idle ring");
+
+struct FusedParams {
+    int N, Tk, Tq, C;           // tokens, 64-token and 128-token tiles per head, cluster size
+    RopeView rope;
+    float eps;
+    unsigned* status;
+};
+
+template <bool ROPE>
+__global__ void __launch_bounds__(kFuThreads, 1)
+tc_fused_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                const __grid_constant__ CUtensorMap tm_t, const __grid_constant__ CUtensorMap tm_q,
+                const __grid_constant__ CUtensorMap tm_g,
+                const __grid_constant__ CUtensorMap tm_o32, FusedParams p) {
+    constexpr int kS1 = StGeo<ROPE>::kStages;   // phase-1 ring
+    constexpr int kS1Stage = StGeo<ROPE>::kStage;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint8_t* qring = smem;                                      // phase 2
+    uint8_t* gring = smem + kApQStages * kApTile;               // phase 2
+    float* partial = reinterpret_cast<float*>(smem + kFuPartial);   // S^T [128][128], z [8][128]
+    uint8_t* sbuf = smem + kStRing;                             // S^T bf16, then z
+    float* zs = reinterpret_cast<float*>(sbuf + kStateSBytes);
+    float* dens = zs + kHeadDim;                                // [kApDSlots][128]
+    uint64_t* full = reinterpret_cast<uint64_t*>(dens + kApDSlots * kApTok);
+    uint64_t* kready = full + kS1;
+    uint64_t* empty = kready + kS1;
+    uint64_t* s1full = empty + kS1;          // phase-1 MMAs done: TMEM partial final, ring idle
+    uint64_t* flushdone = s1full + 1;        // partial S^T and z parts written (12 warps)
+    uint64_t* pready = flushdone + 1;        // every CTA's partial written (C arrivals)
+    uint64_t* reddone = pready + 1;          // this CTA's rows written everywhere (8 warps)
+    uint64_t* sready = reddone + 1;          // the state is complete here (C arrivals)
+    uint64_t* qfull = sready + 1;
+    uint64_t* qready = qfull + kApQStages;
+    uint64_t* qempty = qready + kApQStages;
+    uint64_t* gfull = qempty + kApQStages;
+    uint64_t* gempty = gfull + kApGStages;
+    uint64_t* dready = gempty + kApGStages;
+    uint64_t* dfree = dready + kApDSlots;
+    uint64_t* accfull = dfree + kApDSlots;   // [2]
+    uint64_t* accempty = accfull + 2;        // [2]
+    uint64_t* mma_done = accempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int C = p.C;
+    const uint32_t rank = cluster_ctarank();
+    const int h = blockIdx.x / C;                               // the head of this cluster
+    const int k0 = (int)((long long)rank * p.Tk / C), k1 = (int)((long long)(rank + 1) * p.Tk / C);
+    const int q0 = (int)((long long)rank * p.Tq / C), q1 = (int)((long long)(rank + 1) * p.Tq / C);
+    const uint32_t smem0 = smem_u32(smem);
+    const uint32_t tmem_acc1 = 256;          // phase-1 accumulator column
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kS1; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&kready[s], kStXWarps);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(s1full, 1);
+        mbar_init(flushdone, kStXWarps + kStFWarps);
+        mbar_init(pready, C);
+        mbar_init(reddone, kApEWarps);
+        mbar_init(sready, C);
+        for (int s = 0; s < kApQStages; ++s) {
+            mbar_init(&qfull[s], 1);
+            mbar_init(&qready[s], kApXWarps);
+            mbar_init(&qempty[s], 1);
+        }
+        for (int s = 0; s < kApGStages; ++s) {
+            mbar_init(&gfull[s], 1);
+            mbar_init(&gempty[s], kApEWarps);
+        }
+        for (int s = 0; s < kApDSlots; ++s) {
+            mbar_init(&dready[s], kApXWarps);
+            mbar_init(&dfree[s], kApEWarps);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&accfull[a], 1);
+            mbar_init(&accempty[a], kApEWarps);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = (smem0 & 1023u) ? 1 : 0;
+        if (smem0 & 1023u) raise_status(p.status, kStatusLayout);
+        fence_mbar_init();
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        if (ROPE) prefetch_tmap(&tm_t);
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_g);
+        prefetch_tmap(&tm_o32);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kFuTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    // the other CTAs' barriers are initialised before anyone arrives on them
+    cluster_arrive();
+    cluster_wait();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ producer: K, V, then Q
+        if (lane == 0 && !*abort_flag) {
+            const uint64_t policy = policy_evict_first();
+            const uint64_t keep = policy_evict_last();
+            int it = 0;
+            bool ok = true;
+            for (int t = k0; t < k1; ++t, ++it) {
+                const int s = it % kS1;
+                const uint32_t round = (uint32_t)(it / kS1);
+                if (!(ok = mbar_wait(&empty[s], (round & 1) ^ 1, abort_flag, p.status))) break;
+                uint8_t* st = smem + s * kS1Stage;
+                mbar_arrive_expect_tx(&full[s], kS1Stage);
+                tma_load_3d(st, &tm_k, &full[s], 0, t * kStTok, h, policy);
+                tma_load_3d(st + kStHalf, &tm_k, &full[s], 64, t * kStTok, h, policy);
+                tma_load_3d(st + kStTile, &tm_v, &full[s], 0, t * kStTok, h, policy);
+                tma_load_3d(st + kStTile + kStHalf, &tm_v, &full[s], 64, t * kStTok, h, policy);
+                if (ROPE) tma_load_2d(st + 2 * kStTile, &tm_t, &full[s], 0, t * kStTok, keep);
+            }
+            // the Q ring reuses the phase-1 ring once every phase-1 tile is consumed
+            if (ok) ok = mbar_wait(s1full, 0, abort_flag, p.status);
+            int jt = 0;
+            for (int t = q0; ok && t < q1; ++t, ++jt) {
+                const int s = jt % kApQStages;
+                const uint32_t round = (uint32_t)(jt / kApQStages);
+                if (!(ok = mbar_wait(&qempty[s], (round & 1) ^ 1, abort_flag, p.status))) break;
+                uint8_t* st = qring + s * kApTile;
+                mbar_arrive_expect_tx(&qfull[s], kApTile);
+                tma_load_3d(st, &tm_q, &qfull[s], 0, t * kApTok, h, policy);
+                tma_load_3d(st + kApHalf, &tm_q, &qfull[s], 64, t * kApTok, h, policy);
+            }
+            // every copy issued has landed before the CTA may exit
+            if (jt == 0) {
+                const int first = it > kS1 ? it - kS1 : 0;
+                for (int j = first; j < it; ++j)
+                    mbar_wait_drain(&full[j % kS1], (uint32_t)((j / kS1) & 1));
+            }
+            const int first = jt > kApQStages ? jt - kApQStages : 0;
+            for (int j = first; j < jt; ++j)
+                mbar_wait_drain(&qfull[j % kApQStages], (uint32_t)((j / kApQStages) & 1));
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            bool ok = !*abort_flag;
+            {
+                constexpr uint32_t idesc = idesc_bf16(128, 128, true, true);
+                int it = 0;
+                for (int t = k0; ok && t < k1; ++t, ++it) {
+                    const int s = it % kS1;
+                    const uint32_t round = (uint32_t)(it / kS1);
+                    ok = mbar_wait(&kready[s], round & 1, abort_flag, p.status) &&
+                         mbar_wait(&full[s], round & 1, abort_flag, p.status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t kb = smem0 + s * kS1Stage, vb = kb + kStTile;
+#pragma unroll
+                    for (int ks = 0; ks < kStTok / 16; ++ks) {
+                        const uint64_t a = smem_desc_sw128(kb + ks * 2048, kStHalf, 1024);
+                        const uint64_t b = smem_desc_sw128(vb + ks * 2048, kStHalf, 1024);
+                        mma_bf16(tmem + tmem_acc1, a, b, idesc, (it > 0 || ks > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&empty[s]);
+                }
+                if (ok) mma_commit(s1full);
+            }
+            if (ok) ok = mbar_wait_cluster(sready, 0, abort_flag, p.status);
+            if (ok) {
+                fence_proxy_async_all();
+                tc_fence_after();
+                constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
+                const uint32_t sb = smem_u32(sbuf);
+                int it = 0;
+                for (int t = q0; ok && t < q1; ++t, ++it) {
+                    const int s = it % kApQStages;
+                    const uint32_t round = (uint32_t)(it / kApQStages);
+                    const int a = it & 1;
+                    const uint32_t around = (uint32_t)(it >> 1);
+                    ok = mbar_wait(&accempty[a], (around & 1) ^ 1, abort_flag, p.status) &&
+                         mbar_wait(&qready[s], round & 1, abort_flag, p.status) &&
+                         mbar_wait(&qfull[s], round & 1, abort_flag, p.status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t qb = smem0 + s * kApTile;
+#pragma unroll
+                    for (int ks = 0; ks < kHeadDim / 16; ++ks) {
+                        const uint32_t off = (ks >> 2) * kApHalf + (ks & 3) * 32;
+                        const uint64_t ad = smem_desc_sw128(qb + off, 16, 1024);
+                        const uint64_t bd = smem_desc_sw128(sb + off, 16, 1024);
+                        mma_bf16(tmem + (uint32_t)a * 128, ad, bd, idesc, ks > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&accfull[a]);
+                    mma_commit(&qempty[s]);
+                }
+            }
+            mma_commit(mma_done);
+            mbar_wait_drain(mma_done, 0);
+        }
+    } else if (warp < 2 + kApXWarps) {
+        // ------------------------------------------------ transform: K (z, RoPE), then Q
+        const int tt = threadIdx.x - 64;            // 0..255
+        const int c = tt & 15, rl = tt >> 4;
+        const int xw = warp - 2;
+        bool ok = !*abort_flag;
+        {
+            float zacc[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) zacc[j] = 0.f;
+            int it = 0;
+            for (int t = k0; ok && t < k1; ++t, ++it) {
+                const int s = it % kS1;
+                const uint32_t round = (uint32_t)(it / kS1);
+                if (!(ok = warp_wait(&full[s], round & 1, abort_flag, p.status))) break;
+                const uint32_t kb = smem0 + s * kS1Stage;
+                uint32_t addr[kStRowsPerThread];
+                uint4 x[kStRowsPerThread];
+#pragma unroll
+                for (int i = 0; i < kStRowsPerThread; ++i) {
+                    addr[i] = kb + sw128_off(rl + 16 * i, c, kStHalf);
+                    x[i] = lds128(addr[i]);
+                }
+                float2 cs[kStRowsPerThread][4];
+                if (ROPE) {
+#pragma unroll
+                    for (int i = 0; i < kStRowsPerThread; ++i)
+                        unpack_cs(lds128(kb + 2 * kStTile + (rl + 16 * i) * 256 + c * 16), cs[i]);
+                }
+#pragma unroll
+                for (int i = 0; i < kStRowsPerThread; ++i) {
+                    x[i].x = relu_bf2(x[i].x);
+                    x[i].y = relu_bf2(x[i].y);
+                    x[i].z = relu_bf2(x[i].z);
+                    x[i].w = relu_bf2(x[i].w);
+                    float f[8];
+                    unpack8(x[i], f);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) zacc[j] += f[j];
+                    if (ROPE) x[i] = rotate_chunk(f, cs[i]);
+                }
+#pragma unroll
+                for (int i = 0; i < kStRowsPerThread; ++i) sts128(addr[i], x[i]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&kready[s]);
+            }
+            // this warp's z into the partial (the ring is idle once the MMAs are done)
+            if (ok) ok = warp_wait(s1full, 0, abort_flag, p.status);
+            if (ok) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) zacc[j] += __shfl_xor_sync(0xffffffffu, zacc[j], 16);
+                if (lane < 16) {
+                    float4* zp = reinterpret_cast<float4*>(partial + kHeadDim * kHeadDim +
+                                                           xw * kHeadDim + c * 8);
+                    zp[0] = make_float4(zacc[0], zacc[1], zacc[2], zacc[3]);
+                    zp[1] = make_float4(zacc[4], zacc[5], zacc[6], zacc[7]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(flushdone);
+            }
+        }
+        // phase 2
+        if (ok) ok = warp_wait_cluster(sready, 0, abort_flag, p.status);
+        float zc[8];
+        if (ok) {
+            const float4 za = *reinterpret_cast<const float4*>(zs + 8 * c);
+            const float4 zb = *reinterpret_cast<const float4*>(zs + 8 * c + 4);
+            zc[0] = za.x; zc[1] = za.y; zc[2] = za.z; zc[3] = za.w;
+            zc[4] = zb.x; zc[5] = zb.y; zc[6] = zb.z; zc[7] = zb.w;
+        }
+        uint4 trow[kApRowsPerThread];
+        auto fetch_rows = [&](int tile, int i0) {
+#pragma unroll
+            for (int i = i0; i < i0 + 4; ++i) {
+                const int n = min(tile * kApTok + rl + 16 * i, p.N - 1);
+                trow[i] = ldg_nc_na128(p.rope.tok + (size_t)n * kPairs + c * 4);
+            }
+        };
+        if (ROPE && ok && q0 < q1) {
+            fetch_rows(q0, 0);
+            fetch_rows(q0, 4);
+        }
+        int it = 0;
+        for (int t = q0; ok && t < q1; ++t, ++it) {
+            const int next_tile = t + 1 < q1 ? t + 1 : -1;
+            const int s = it % kApQStages;
+            const uint32_t round = (uint32_t)(it / kApQStages);
+            const int ds = it % kApDSlots;
+            const uint32_t dround = (uint32_t)(it / kApDSlots);
+            if (!(ok = warp_wait(&qfull[s], round & 1, abort_flag, p.status))) break;
+            if (dround > 0 && !(ok = warp_wait(&dfree[ds], (dround - 1) & 1, abort_flag, p.status)))
+                break;
+            const uint32_t qb = smem0 + s * kApTile;
+#pragma unroll
+            for (int b4 = 0; b4 < kApRowsPerThread; b4 += 4) {
+                float den[4];
+                uint32_t addr[4];
+                uint4 x[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    addr[i] = qb + sw128_off(rl + 16 * (b4 + i), c, kApHalf);
+                    x[i] = lds128(addr[i]);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    x[i].x = relu_bf2(x[i].x);
+                    x[i].y = relu_bf2(x[i].y);
+                    x[i].z = relu_bf2(x[i].z);
+                    x[i].w = relu_bf2(x[i].w);
+                    float f[8];
+                    unpack8(x[i], f);
+                    float d = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) d = fmaf(f[j], zc[j], d);
+                    den[i] = d;
+                    if (ROPE) {
+                        float2 cs[4];
+                        unpack_cs(trow[b4 + i], cs);
+                        x[i] = rotate_chunk(f, cs);
+                    }
+                }
+                if (ROPE && next_tile >= 0 && b4 == 0) fetch_rows(next_tile, 0);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sts128(addr[i], x[i]);
+                const bool b3 = (c >> 3) & 1, b2 = (c >> 2) & 1;
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const float send = b3 ? den[k] : den[k + 2];
+                    const float keep = b3 ? den[k + 2] : den[k];
+                    den[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+                }
+                {
+                    const float send = b2 ? den[0] : den[1];
+                    const float keep = b2 ? den[1] : den[0];
+                    den[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+                }
+                den[0] += __shfl_xor_sync(0xffffffffu, den[0], 2);
+                den[0] += __shfl_xor_sync(0xffffffffu, den[0], 1);
+                if ((c & 3) == 0)
+                    dens[ds * kApTok + rl + 16 * (b4 + ((c >> 2) & 3))] = den[0] + p.eps;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&qready[s]);
+                mbar_arrive(&dready[ds]);
+            }
+            if (ROPE && next_tile >= 0) fetch_rows(next_tile, 4);
+        }
+    } else if (warp < 2 + kApXWarps + kApEWarps) {
+        // ------------------------------------------------ flush, reduction, epilogue
+        const int ew = warp - 2 - kApXWarps;        // 0..7
+        const int quad = warp & 3, hf = ew >> 2;
+        const int rt = threadIdx.x - 32 * (2 + kApXWarps);   // 0..255
+        bool ok = !*abort_flag;
+        // phase 1 (four of the warps): the partial S^T from TMEM into shared memory
+        if (ew < kStFWarps) {
+            if (ok) ok = warp_wait(s1full, 0, abort_flag, p.status);
+            if (ok) {
+                tc_fence_after();
+                const int m = 32 * quad + lane;
+#pragma unroll 1
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + ((uint32_t)(32 * quad) << 16) + tmem_acc1 + ch * 32, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        partial[(ch * 32 + j) * kHeadDim + m] = __uint_as_float(r[j]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(flushdone);
+            }
+        }
+        // every warp of this CTA has written its share: tell the cluster
+        if (rt == 0) {
+            bool done = ok && mbar_wait(flushdone, 0, abort_flag, p.status);
+            if (done) {
+                fence_acq_rel_cluster();
+                for (int q = 0; q < C; ++q) mbar_arrive_cluster(mapa_shared(smem_u32(pready), q));
+            }
+        }
+        // reduction: rows [rank*128/C, (rank+1)*128/C) of every CTA's partial
+        if (ok) ok = warp_wait_cluster(pready, 0, abort_flag, p.status);
+        if (ok) {
+            const int r0 = (int)rank * kHeadDim / C, r1 = ((int)rank + 1) * kHeadDim / C;
+            const uint32_t pbase = smem_u32(partial), sbase = smem_u32(sbuf);
+            const int tasks = (r1 - r0) * 16;
+            for (int t = rt; t < tasks; t += 32 * kApEWarps) {
+                const int n = r0 + (t >> 4), cc = t & 15;
+                float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+                const uint32_t off = (uint32_t)((n * kHeadDim + cc * 8) * 4);
+                for (int q = 0; q < C; ++q) {
+                    const uint32_t src = mapa_shared(pbase + off, q);
+                    const float4 b0 = ld_cluster_f4(src), b1 = ld_cluster_f4(src + 16);
+                    a0.x += b0.x; a0.y += b0.y; a0.z += b0.z; a0.w += b0.w;
+                    a1.x += b1.x; a1.y += b1.y; a1.z += b1.z; a1.w += b1.w;
+                }
+                uint4 w;
+                w.x = f2_to_bf2(a0.x, a0.y);
+                w.y = f2_to_bf2(a0.z, a0.w);
+                w.z = f2_to_bf2(a1.x, a1.y);
+                w.w = f2_to_bf2(a1.z, a1.w);
+                const uint32_t dst = sbase + sw128_off(n, cc, kStateHalf);
+                for (int q = 0; q < C; ++q) st_cluster_u4(mapa_shared(dst, q), w);
+            }
+            if (rt < kHeadDim) {
+                // z in full here: the sum of every CTA's eight warp parts
+                float zsum = 0.f;
+                for (int q = 0; q < C; ++q) {
+                    const uint32_t zb = mapa_shared(pbase + (uint32_t)((kHeadDim * kHeadDim + rt) * 4), q);
+#pragma unroll
+                    for (int w8 = 0; w8 < kStXWarps; ++w8) zsum += ld_cluster_f32(zb + w8 * kHeadDim * 4);
+                }
+                zs[rt] = zsum;
+            }
+            fence_proxy_async_all();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(reddone);
+            if (rt == 0 && mbar_wait(reddone, 0, abort_flag, p.status)) {
+                fence_acq_rel_cluster();
+                for (int q = 0; q < C; ++q) mbar_arrive_cluster(mapa_shared(smem_u32(sready), q));
+            }
+        }
+        // phase 2: the epilogue of the apply kernel
+        if (ok) ok = warp_wait_cluster(sready, 0, abort_flag, p.status);
+        const int r = 32 * quad + lane;
+        int it = 0;
+        for (int t = q0; ok && t < q1; ++t, ++it) {
+            const int gs = it % kApGStages;
+            const uint32_t ground = (uint32_t)(it / kApGStages);
+            const int ds = it % kApDSlots;
+            const int a = it & 1;
+            const uint32_t around = (uint32_t)(it >> 1);
+            ok = warp_wait(&accfull[a], around & 1, abort_flag, p.status) &&
+                 warp_wait(&dready[ds], (uint32_t)(it / kApDSlots) & 1, abort_flag, p.status) &&
+                 warp_wait(&gfull[gs], ground & 1, abort_flag, p.status);
+            if (!ok) break;
+            tc_fence_after();
+            const float den = dens[ds * kApTok + r];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&dfree[ds]);
+            const uint32_t gb = smem0 + kApQStages * kApTile + gs * kApTile;
+#pragma unroll 1
+            for (int ch = 0; ch < 2; ++ch) {
+                uint32_t addr[4];
+                uint4 gv[4];
+#pragma unroll
+                for (int sub = 0; sub < 4; ++sub) {
+                    addr[sub] = gb + sw128_off(r, hf * 8 + ch * 4 + sub, kApHalf);
+                    gv[sub] = lds128(addr[sub]);
+                }
+                uint32_t v[32];
+                tmem_ld32(tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)a * 128 + hf * 64 +
+                              ch * 32,
+                          v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int sub = 0; sub < 4; ++sub) {
+                    float gf[8];
+                    unpack8(gv[sub], gf);
+                    uint32_t ow[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float d0 = fmaf(den, __expf(-gf[2 * e]), den);
+                        const float d1 = fmaf(den, __expf(-gf[2 * e + 1]), den);
+                        const float o0 = __fdividef(__uint_as_float(v[sub * 8 + 2 * e]), d0);
+                        const float o1 = __fdividef(__uint_as_float(v[sub * 8 + 2 * e + 1]), d1);
+                        ow[e] = f2_to_bf2(o0, o1);
+                    }
+                    gv[sub] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                }
+#pragma unroll
+                for (int sub = 0; sub < 4; ++sub) sts128(addr[sub], gv[sub]);
+            }
+            tc_fence_before();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&accempty[a]);
+                tma_store_3d(&tm_o32, gring + gs * kApTile + hf * kApHalf + quad * kApORows * 128,
+                             64 * hf, t * kApTok + quad * kApORows, h);
+                bulk_commit();
+                bulk_wait_read_all();
+                mbar_arrive(&gempty[gs]);
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+    } else {
+        // ------------------------------------------------ G producer (after the reduction)
+        if (lane == 0 && !*abort_flag) {
+            const uint64_t policy = policy_evict_first();
+            // the G ring overlays this CTA's partial, which the cluster reads
+            // until every CTA has arrived on sready
+            bool ok = mbar_wait_cluster(sready, 0, abort_flag, p.status);
+            int it = 0;
+            for (int t = q0; ok && t < q1; ++t, ++it) {
+                const int s = it % kApGStages;
+                const uint32_t round = (uint32_t)(it / kApGStages);
+                if (!(ok = mbar_wait(&gempty[s], (round & 1) ^ 1, abort_flag, p.status))) break;
+                uint8_t* st = gring + s * kApTile;
+                mbar_arrive_expect_tx(&gfull[s], kApTile);
+                tma_load_3d(st, &tm_g, &gfull[s], 0, t * kApTok, h, policy);
+                tma_load_3d(st + kApHalf, &tm_g, &gfull[s], 64, t * kApTok, h, policy);
+            }
+            const int first = it > kApGStages ? it - kApGStages : 0;
+            for (int j = first; j < it; ++j)
+                mbar_wait_drain(&gfull[j % kApGStages], (uint32_t)((j / kApGStages) & 1));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    // no CTA leaves while another may still read or write its shared memory
+    cluster_arrive();
+    cluster_wait();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem, kFuTmemCols);
+    }
+}
+
 // ==================================================================== host ==
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1121,6 +1679,16 @@ constexpr size_t ap_smem() {
            kApDSlots * kApTok * sizeof(float) +
            (3 * kApQStages + 2 * kApGStages + 2 * kApDSlots + 7) * 8 + 16;
 }
+// fused: the ring, the state, the denominators, then 3*stages + 5 phase-1 and
+// cluster mbarriers, the apply kernel's 3*Q + 2*G + 2*den + 5 and two words.
+template <bool ROPE>
+constexpr size_t fu_smem() {
+    return (size_t)kStRing + kStateBytes + kApDSlots * kApTok * sizeof(float) +
+           (3 * StGeo<ROPE>::kStages + 5 + 3 * kApQStages + 2 * kApGStages + 2 * kApDSlots + 5) *
+               8 +
+           16;
+}
+static_assert(fu_smem<true>() <= 232448 && fu_smem<false>() <= 232448, "fused kernel smem");
 static_assert(st_smem<true>() <= 232448 && st_smem<false>() <= 232448, "state kernel smem");
 static_assert(ap_smem<true>() <= 232448 && ap_smem<false>() <= 232448, "apply kernel smem");
 
@@ -1170,6 +1738,8 @@ cudaError_t configure(int dev) {
     if ((e = set_smem(tc_state_kernel<true>, st_smem<true>())) != cudaSuccess) return e;
     if ((e = set_smem(tc_apply_kernel<false>, ap_smem<false>())) != cudaSuccess) return e;
     if ((e = set_smem(tc_apply_kernel<true>, ap_smem<true>())) != cudaSuccess) return e;
+    if ((e = set_smem(tc_fused_kernel<false>, fu_smem<false>())) != cudaSuccess) return e;
+    if ((e = set_smem(tc_fused_kernel<true>, fu_smem<true>())) != cudaSuccess) return e;
     done[dev] = true;
     return cudaSuccess;
 }
@@ -1241,6 +1811,113 @@ cudaError_t launch_apply(const void* q, const void* g, const uint8_t* state, voi
     return cudaLaunchKernelEx(&cfg, tc_apply_kernel<false>, mq, mg, mo, ap);
 }
 
+template <bool ROPE>
+cudaLaunchConfig_t fused_config(int BH, int C, cudaStream_t stream, cudaLaunchAttribute* attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(BH * C);
+    cfg.blockDim = dim3(kFuThreads);
+    cfg.dynamicSmemBytes = fu_smem<ROPE>();
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+// How many clusters of C fused CTAs the device holds at once (cached per
+// device, variant and C; 0 if the query fails).
+int fused_capacity(int dev, bool rope, int C) {
+    static int cache[64][2][kFuMaxCluster + 1];
+    static bool known[64][2][kFuMaxCluster + 1];
+    static std::mutex mu;
+    if (dev < 0 || dev >= 64 || C < 2 || C > kFuMaxCluster) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!known[dev][rope][C]) {
+        cudaLaunchAttribute attr[1];
+        int n = 0;
+        cudaError_t e;
+        if (rope) {
+            cudaLaunchConfig_t cfg = fused_config<true>(1, C, nullptr, attr);
+            e = cudaOccupancyMaxActiveClusters(&n, tc_fused_kernel<true>, &cfg);
+        } else {
+            cudaLaunchConfig_t cfg = fused_config<false>(1, C, nullptr, attr);
+            e = cudaOccupancyMaxActiveClusters(&n, tc_fused_kernel<false>, &cfg);
+        }
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+        cache[dev][rope][C] = n;
+        known[dev][rope][C] = true;
+    }
+    return cache[dev][rope][C];
+}
+
+// The forward's kernels: SLA_FORWARD_KERNEL = "fused" or "split" forces one
+// (fused only where it applies), anything else lets the shape decide.
+enum class Path { kAuto, kFused, kSplit };
+
+Path forced_path() {
+    const char* v = std::getenv("SLA_FORWARD_KERNEL");
+    if (!v) return Path::kAuto;
+    if (!std::strcmp(v, "fused")) return Path::kFused;
+    if (!std::strcmp(v, "split")) return Path::kSplit;
+    return Path::kAuto;
+}
+
+// The cluster size of the fused kernel for this shape, or 0 for the two
+// launches.  Every head needs its own cluster resident at once (the cluster's
+// CTAs wait for each other), so C is the largest size, at most 8 and at most
+// the head's 128-token tiles (every CTA then has at least one tile of each
+// phase), for which all B*H clusters fit on the device together.
+int fused_cluster(int dev, int BH, int N, bool rope, int num_sms) {
+    const Path path = forced_path();
+    if (path == Path::kSplit) return 0;
+    const int Tq = (N + kApTok - 1) / kApTok;
+    // Measured on B300: the fused launch saves the second launch and the
+    // merge (a few microseconds), but leaves SMs idle when B*H does not
+    // divide their number and runs its two phases back to back in each CTA,
+    // so the two launches stream faster once a head has more than about 36
+    // tiles of 128 queries.
+    if (path == Path::kAuto && Tq > kFuAutoMaxTiles) return 0;
+    int cmax = num_sms / BH;
+    if (cmax > kFuMaxCluster) cmax = kFuMaxCluster;
+    if (cmax > Tq) cmax = Tq;
+    for (int C = cmax; C >= 2; --C)
+        if (fused_capacity(dev, rope, C) >= BH) return C;
+    return 0;
+}
+
+cudaError_t launch_fused(const void* q, const void* k, const void* v, const void* g, void* out,
+                         int BH, int N, int C, const RopeView* rope, float eps, unsigned* status,
+                         cudaStream_t stream) {
+    CUtensorMap mk, mv, mq, mg, mo;
+    if (!make_map(&mk, k, N, BH, kStTok) || !make_map(&mv, v, N, BH, kStTok) ||
+        !make_map(&mq, q, N, BH, kApTok) || !make_map(&mg, g, N, BH, kApTok) ||
+        !make_map(&mo, out, N, BH, kApORows))
+        return cudaErrorInvalidValue;
+    CUtensorMap mt = mk;   // without RoPE the table map is never read
+    if (rope && !make_rope_map(&mt, rope->tok, N, kStTok)) return cudaErrorInvalidValue;
+    FusedParams fp{};
+    fp.N = N;
+    fp.Tk = (N + kStTok - 1) / kStTok;
+    fp.Tq = (N + kApTok - 1) / kApTok;
+    fp.C = C;
+    if (rope) fp.rope = *rope;
+    fp.eps = eps;
+    fp.status = status;
+    cudaLaunchAttribute attr[1];
+    if (rope) {
+        cudaLaunchConfig_t cfg = fused_config<true>(BH, C, stream, attr);
+        return cudaLaunchKernelEx(&cfg, tc_fused_kernel<true>, mk, mv, mt, mq, mg, mo, fp);
+    }
+    cudaLaunchConfig_t cfg = fused_config<false>(BH, C, stream, attr);
+    return cudaLaunchKernelEx(&cfg, tc_fused_kernel<false>, mk, mv, mt, mq, mg, mo, fp);
+}
+
 int current_device() {
     int dev = 0;
     cudaGetDevice(&dev);
@@ -1277,9 +1954,26 @@ cudaError_t launch_tc_apply(const void* q, const void* g, const void* state, voi
                         status, num_sms, false, stream);
 }
 
-cudaError_t launch_tc_bf16(const void* q, const void* k, const void* v, const void* g, void* out,
-                           int B, int H, int N, const RopeView* rope, float eps, float* workspace,
-                           unsigned* status, int num_sms, cudaStream_t stream) {
+int tc_forward_cluster(int dev, int BH, int N, bool rope, int num_sms) {
+    if (configure(dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return fused_cluster(dev, BH, N, rope, num_sms);
+}
+
+cudaError_t launch_tc_fused(const void* q, const void* k, const void* v, const void* g, void* out,
+                            int B, int H, int N, int C, const RopeView* rope, float eps,
+                            unsigned* status, cudaStream_t stream) {
+    cudaError_t e = configure(current_device());
+    if (e != cudaSuccess) return e;
+    return launch_fused(q, k, v, g, out, B * H, N, C, rope, eps, status, stream);
+}
+
+cudaError_t launch_tc_two_phase(const void* q, const void* k, const void* v, const void* g,
+                                void* out, int B, int H, int N, const RopeView* rope, float eps,
+                                float* workspace, unsigned* status, int num_sms,
+                                cudaStream_t stream) {
     const int BH = B * H;
     cudaError_t e = configure(current_device());
     if (e != cudaSuccess) return e;

@@ -52,6 +52,8 @@ _lib.sla_linattn_apply.argtypes = [_vp] * 4 + [_int] * 4 + [ctypes.POINTER(RopeT
 _lib.sla_linattn_apply.restype = _int
 _lib.sla_linattn_forward_noalloc.argtypes = _FWD_ARGS[:-1] + [_vp, _vp]
 _lib.sla_linattn_forward_noalloc.restype = _int
+_lib.sla_linattn_forward_cluster.argtypes = [_int] * 5
+_lib.sla_linattn_forward_cluster.restype = _int
 _lib.sla_status_string.argtypes = [_int]
 _lib.sla_status_string.restype = ctypes.c_char_p
 _lib.sla_last_device_status.argtypes = [_vp]
@@ -59,8 +61,8 @@ _lib.sla_last_device_status.restype = _int
 
 EXPORTED = ("sla_rope_table_floats", "sla_rope_table_fill", "sla_linattn_forward",
             "sla_linattn_forward_f32", "sla_linattn_state_bytes", "sla_linattn_state",
-            "sla_linattn_apply", "sla_linattn_forward_noalloc", "sla_status_string",
-            "sla_last_device_status")
+            "sla_linattn_apply", "sla_linattn_forward_noalloc", "sla_linattn_forward_cluster",
+            "sla_status_string", "sla_last_device_status")
 
 
 class SlaError(RuntimeError):
@@ -242,8 +244,46 @@ def last_device_status(stream: Optional[torch.cuda.Stream] = None, device="cuda"
         return _lib.sla_last_device_status(_stream_handle(stream, dev))
 
 
-def launches_per_forward(dtype: torch.dtype) -> int:
-    """Kernels one forward call launches (the state reduction and the apply)."""
+def forward_cluster(B: int, H: int, N: int, rope: bool, d: int = HEAD_DIM,
+                    device=None) -> int:
+    """Cluster size of the fused one-launch forward for this shape, 0 for the
+    state and apply launches (``sla_linattn_forward_cluster``)."""
+    dev = torch.device(device) if device is not None else torch.device("cuda")
+    with torch.cuda.device(dev):
+        c = int(_lib.sla_linattn_forward_cluster(B, H, N, d, 1 if rope else 0))
+    if c < 0:
+        raise SlaError(INVALID_ARG, "sla_linattn_forward_cluster")
+    return c
+
+
+class forward_kernel:
+    """Context manager that sets SLA_FORWARD_KERNEL ("fused", "split" or
+    "auto") for the calls made inside it."""
+
+    def __init__(self, path: str):
+        if path not in ("fused", "split", "auto"):
+            raise ValueError(f"forward kernel {path!r}: expected fused, split or auto")
+        self.path = path
+
+    def __enter__(self):
+        self._old = os.environ.get("SLA_FORWARD_KERNEL")
+        os.environ["SLA_FORWARD_KERNEL"] = self.path
+        return self
+
+    def __exit__(self, *exc):
+        if self._old is None:
+            os.environ.pop("SLA_FORWARD_KERNEL", None)
+        else:
+            os.environ["SLA_FORWARD_KERNEL"] = self._old
+        return False
+
+
+def launches_per_forward(dtype: torch.dtype, B: int = 1, H: int = 1, N: int = 1,
+                         rope: bool = False, device=None) -> int:
+    """Kernels one forward call launches: the fused kernel alone, or the state
+    reduction and the apply (the fp32 path: the state and apply kernels)."""
+    if dtype == torch.bfloat16 and forward_cluster(B, H, N, rope, device=device) > 0:
+        return 1
     return 2
 
 

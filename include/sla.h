@@ -25,7 +25,8 @@
  *
  * Ownership.  The caller owns every buffer passed in.  The library owns a
  * workspace per (device, stream) for the split-N partial states and the
- * heads' states (about 66 KB per SM of the device plus 99 KB per head),
+ * heads' states of the two-launch plan (about 66 KB per SM of the device plus
+ * 99 KB per head; the fused plan needs none),
  * allocated with cudaMalloc on the first call that needs it (or more of it)
  * and kept until the process exits.  A call that has to grow the workspace synchronises the
  * device; make the first call of the largest shape outside stream capture.
@@ -120,11 +121,34 @@ sla_status_t sla_linattn_forward_f32(const float* q, const float* k, const float
                                      sla_stream_t stream);
 
 /*
+ * How sla_linattn_forward runs a shape on the current device.  The bf16
+ * forward has two launch plans.  One fused launch gives every head a cluster
+ * of C CTAs (2 <= C <= 8): each CTA sums its share of the head's keys and
+ * values, the cluster adds the partial states through distributed shared
+ * memory, and each CTA applies the state to its share of the queries.  This
+ * needs no workspace.  It applies when every head's cluster can be resident
+ * at once (B*H clusters of C CTAs on the device's SMs) and the head has at
+ * least C tiles of 128 queries, and it is taken when it applies and N is at
+ * most 36 * 128 = 4608 tokens (beyond that the two launches measured faster
+ * on B300).  Otherwise the forward launches the state kernel and then the
+ * apply kernel (sla_linattn_state, sla_linattn_apply).
+ *
+ * Returns C for the fused launch, 0 for the two launches, -1 for an invalid
+ * shape (rope: nonzero when a RoPE table will be passed).  The environment
+ * variable SLA_FORWARD_KERNEL, read on every call, overrides the choice:
+ * "split" always takes the two launches, "fused" the fused launch wherever it
+ * applies (the same rule as without it).
+ */
+int sla_linattn_forward_cluster(int B, int H, int N, int d, int rope);
+
+/*
  * The two phases of sla_linattn_forward, for callers that reuse a state
  * (several query sets against one set of keys and values) or time the phases.
- * sla_linattn_forward is exactly sla_linattn_state followed by
- * sla_linattn_apply, except that it keeps the state in the library's
- * workspace and lets the apply kernel start while the state kernel finishes.
+ * When sla_linattn_forward_cluster returns 0, sla_linattn_forward is exactly
+ * sla_linattn_state followed by sla_linattn_apply, except that it keeps the
+ * state in the library's workspace and lets the apply kernel start while the
+ * state kernel finishes (the fused launch sums the partial states in another
+ * order, so its output may differ in the last bits).
  *
  * The state of one head is sla_linattn_state_bytes(1, 1, 128) = 33280 bytes:
  * S^T (row n = output dim, column m = key dim) as bf16 in the layout the
@@ -174,10 +198,11 @@ sla_status_t sla_linattn_apply(const void* q, const void* g, const void* state, 
  * waits gives up (the word is never cleared by the library).  With NULL,
  * such an early return is not reported.
  *
- * Size limit: a shape whose scratch does not fit in the 24 MiB array returns
- * SLA_ERR_UNSUPPORTED before anything is launched.  The scratch is about
- * 66 KB x (number of SMs + B*H) + 33 KB x B*H, so B*H up to about 150 heads
- * fits on a 148-SM B300.
+ * Size limit: the fused launch (see sla_linattn_forward_cluster) needs no
+ * scratch.  For the two launches, a shape whose scratch does not fit in the
+ * 24 MiB array returns SLA_ERR_UNSUPPORTED before anything is launched.  That
+ * scratch is about 66 KB x (number of SMs + B*H) + 33 KB x B*H, so B*H up to
+ * about 150 heads fits on a 148-SM B300.
  *
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream

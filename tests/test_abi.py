@@ -157,3 +157,10 @@ def test_phase_entry_points_reject_bad_arguments():
     assert ap(Q, 0, S, O, 1, 2, 256, 128, None, 1e-6, None) == sla.INVALID_ARG
     r = ctypes.byref(_rope(T=5))
     assert ap(Q, G, S, O, 1, 2, 256, 128, r, 1e-6, None) == sla.INVALID_ARG
+
+
+def test_forward_cluster_rejects_bad_shapes_before_cuda():
+    lib = sla.raw_lib()
+    assert lib.sla_linattn_forward_cluster(0, 1, 256, 128, 0) == -1
+    assert lib.sla_linattn_forward_cluster(1, 1, 0, 128, 1) == -1
+    assert lib.sla_linattn_forward_cluster(1, 1, 256, 64, 0) == -1

@@ -39,9 +39,10 @@ def _rope_table(wl: Workload, device):
     return _sla().RopeTable(wl.grid, wl.split, wl.base, device=device) if wl.rope else None
 
 
-def _run(wl, tensors, device):
+def _run(wl, tensors, device, path="auto"):
     q, k, v, g = (t.to(device) for t in tensors)
-    out = _sla().linattn_forward(q, k, v, g, rope=_rope_table(wl, device), eps=wl.eps)
+    with _sla().forward_kernel(path):
+        out = _sla().linattn_forward(q, k, v, g, rope=_rope_table(wl, device), eps=wl.eps)
     assert _sla().last_device_status(device=device) == 0
     return out
 
@@ -63,15 +64,64 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("path", ["fused", "split"])
 @pytest.mark.parametrize("B,H,grid,dtype,rope", SMALL,
                          ids=[f"B{b}H{h}N{g[0]*g[1]*g[2]}-{str(dt)[6:]}-{'rope' if r else 'norope'}"
                               for b, h, g, dt, r in SMALL])
-def test_small_shapes_elementwise(B, H, grid, dtype, rope, cuda_device):
+def test_small_shapes_elementwise(B, H, grid, dtype, rope, path, cuda_device):
+    """Both launch plans of the bf16 forward ("fused" falls back to the two
+    launches where one head has a single 128-token tile)."""
     wl = Workload("small", B=B, H=H, grid=grid, dtype=dtype, rope=rope)
     tensors = make_inputs(wl, seed=7)
-    out = _run(wl, tensors, cuda_device)
+    out = _run(wl, tensors, cuda_device, path)
     ref = ol.linattn_forward(*tensors, eps=wl.eps, rope=_spec(wl))
     assert _rel(_np64(out), ref) <= TOL[dtype]
+
+
+# Shapes whose fused plan takes each cluster size C = min(8, SMs // heads,
+# 128-token tiles), lowered by the device where that many clusters do not fit
+# at once; ragged tails in both tile sizes.
+FUSED = [
+    # (B, H, grid, rope, C expected on a 148-SM device)
+    (2, 1, (1, 22, 50), True, 8),
+    (1, 2, (1, 1, 891), False, 7),
+    (1, 3, (7, 10, 10), True, 6),
+    (1, 1, (1, 20, 30), False, 5),
+    (2, 1, (5, 10, 10), True, 4),
+    (3, 1, (1, 1, 300), False, 3),
+    (1, 5, (2, 10, 10), True, 2),
+    (1, 60, (1, 3, 100), True, 2),
+]
+
+
+@pytest.mark.parametrize("B,H,grid,rope,C", FUSED,
+                         ids=[f"B{b}H{h}N{g[0]*g[1]*g[2]}-C{c}-{'rope' if r else 'norope'}"
+                              for b, h, g, r, c in FUSED])
+def test_fused_cluster_sizes_elementwise(B, H, grid, rope, C, cuda_device):
+    sla = _sla()
+    wl = Workload("fused", B=B, H=H, grid=grid, rope=rope)
+    with sla.forward_kernel("fused"):
+        got_c = sla.forward_cluster(B, H, wl.N, rope, device=cuda_device)
+    sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
+    assert 2 <= got_c <= min(8, sms // (B * H), (wl.N + 127) // 128)
+    if sms == 148:
+        assert got_c <= C
+    tensors = make_inputs(wl, seed=17)
+    out = _run(wl, tensors, cuda_device, "fused")
+    ref = ol.linattn_forward(*tensors, eps=wl.eps, rope=_spec(wl))
+    assert _rel(_np64(out), ref) <= TOL[torch.bfloat16]
+    split = _run(wl, tensors, cuda_device, "split")
+    assert _rel(_np64(out), _np64(split)) <= TOL[torch.bfloat16]
+
+
+def test_plan_choice_follows_the_override(cuda_device):
+    sla = _sla()
+    with sla.forward_kernel("split"):
+        assert sla.forward_cluster(2, 20, 4290, False, device=cuda_device) == 0
+    with sla.forward_kernel("fused"):
+        assert sla.forward_cluster(1, 1, 128, False, device=cuda_device) == 0   # one tile
+        assert sla.forward_cluster(1, 200, 4096, False, device=cuda_device) == 0  # too many heads
+        assert sla.forward_cluster(2, 20, 4290, False, device=cuda_device) >= 2
 
 
 def test_tiny_fp32_workload_elementwise(cuda_device):
@@ -82,19 +132,34 @@ def test_tiny_fp32_workload_elementwise(cuda_device):
     assert _rel(_np64(out), ref) <= 1e-5
 
 
+_FULL_CACHE = {}
+
+
+def _full_size_case(name):
+    """Inputs, sampled rows, heads and the oracle's rows for a workload (kept
+    for the other launch plan)."""
+    if name not in _FULL_CACHE:
+        wl = WORKLOADS[name]
+        tensors = make_inputs(wl, seed=0)
+        rows = sample_rows(wl.N, 48)
+        heads = [(b, h) for b in range(wl.B) for h in range(wl.H)]
+        if wl.N > 50000:          # the longest clip: first, last and two more heads
+            heads = [heads[0], heads[7], heads[13], heads[-1]]
+        q, k, v, g = tensors
+        ref = ol.linattn_forward_rows(q, k, v, g, rows, eps=wl.eps, rope=_spec(wl), heads=heads)
+        _FULL_CACHE.clear()
+        _FULL_CACHE[name] = (tensors, rows, heads, np.stack([ref[bh] for bh in heads]))
+    return _FULL_CACHE[name]
+
+
+@pytest.mark.parametrize("path", ["auto", "split"])
 @pytest.mark.parametrize("name", ["5b_480p", "5b_720p", "14b_480p", "5b_720p_60s"])
-def test_full_size_sampled_rows(name, cuda_device):
+def test_full_size_sampled_rows(name, path, cuda_device):
+    """"auto" is the plan the benchmark times."""
     wl = WORKLOADS[name]
-    tensors = make_inputs(wl, seed=0)
-    out = _run(wl, tensors, cuda_device)
-    rows = sample_rows(wl.N, 48)
-    heads = [(b, h) for b in range(wl.B) for h in range(wl.H)]
-    if wl.N > 50000:          # the longest clip: first, last and two more heads
-        heads = [heads[0], heads[7], heads[13], heads[-1]]
-    q, k, v, g = tensors
-    ref = ol.linattn_forward_rows(q, k, v, g, rows, eps=wl.eps, rope=_spec(wl), heads=heads)
+    tensors, rows, heads, want = _full_size_case(name)
+    out = _run(wl, tensors, cuda_device, path)
     got = np.stack([_np64(out[b, h][rows]) for b, h in heads])
-    want = np.stack([ref[bh] for bh in heads])
     assert _rel(got, want) <= wl.tol
     assert np.all(np.isfinite(_np64(out[0, 0])))
 
@@ -145,13 +210,15 @@ def test_repeatable_and_stream_independent(cuda_device):
 
 
 def test_phases_equal_forward(cuda_device):
-    """sla_linattn_state + sla_linattn_apply give the forward's output bit for bit."""
+    """sla_linattn_state + sla_linattn_apply give the two-launch forward's
+    output bit for bit."""
     sla = _sla()
     for rope_on in (False, True):
         wl = Workload("phases", B=2, H=3, grid=(3, 7, 11), rope=rope_on)
         q, k, v, g = (t.to(cuda_device) for t in make_inputs(wl, seed=8))
         rope = _rope_table(wl, cuda_device)
-        fwd = sla.linattn_forward(q, k, v, g, rope=rope)
+        with sla.forward_kernel("split"):
+            fwd = sla.linattn_forward(q, k, v, g, rope=rope)
         state = sla.linattn_state(k, v, rope=rope)
         out = sla.linattn_apply(q, g, state, rope=rope)
         assert sla.last_device_status(device=cuda_device) == 0

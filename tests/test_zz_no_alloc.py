@@ -39,11 +39,14 @@ def _rel(a, b):
     return float(np.max(np.abs(a - b)) / np.max(np.abs(b)))
 
 
+@pytest.mark.parametrize("path", ["auto", "split"])
 @pytest.mark.parametrize("wl,seeds", [
     (Workload("na_rope", B=2, H=3, grid=(4, 11, 13), rope=True), (11, 12)),
     (Workload("na_norope", B=1, H=4, grid=(1, 1, 300), rope=False), (13, 14)),
 ])
-def test_noalloc_matches_forward_on_two_calls(wl, seeds, cuda_device):
+def test_noalloc_matches_forward_on_two_calls(wl, seeds, path, cuda_device, monkeypatch):
+    """Both launch plans: the fused one needs no scratch, the two launches use the array."""
+    monkeypatch.setenv("SLA_FORWARD_KERNEL", path)
     sla = _sla()
     lib = sla.raw_lib()
     stream = torch.cuda.current_stream(cuda_device)
