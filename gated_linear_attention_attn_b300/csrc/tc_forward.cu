@@ -177,6 +177,30 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, ok);
 }
 
+// Eight outputs o = num / (den * (1 + exp(-g))) = sigmoid(g) * num / den of
+// one 16-byte chunk of g, with den = phi(q) . z + eps of the row and num the
+// eight fp32 numerators.  exp(-g) = 2^(-g log2 e); a gate far below zero
+// gives exp(-g) = +inf and o = 0, far above zero exp(-g) = 0 and o = num / den.
+__device__ __forceinline__ uint4 gate_chunk(uint4 g8, const uint32_t* num, float den) {
+    constexpr float kLog2e = 1.4426950408889634f;
+    const float2 dd = make_float2(den, den);
+    const float2 kl = make_float2(-kLog2e, -kLog2e);
+    const uint32_t w[4] = {g8.x, g8.y, g8.z, g8.w};
+    uint32_t ow[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 gp = make_float2(__uint_as_float(w[e] << 16),
+                                      __uint_as_float(w[e] & 0xffff0000u));
+        const float2 t = mul2(gp, kl);
+        const float2 d = fma2(dd, make_float2(ex2_approx(t.x), ex2_approx(t.y)), dd);
+        const float2 o = mul2(make_float2(__uint_as_float(num[2 * e]),
+                                          __uint_as_float(num[2 * e + 1])),
+                              make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+        ow[e] = f2_to_bf2(o.x, o.y);
+    }
+    return make_uint4(ow[0], ow[1], ow[2], ow[3]);
+}
+
 // warp_wait for phases completed by arrivals from other CTAs of the cluster.
 __device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity,
                                                   volatile int* abort, unsigned* status) {
@@ -682,7 +706,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint8_t* gring = smem + kApQStages * kApTile;               // [kApGStages][32 KB]
     uint8_t* sbuf = gring + kApGStages * kApTile;               // S^T bf16 (B operand), then z
     float* zs = reinterpret_cast<float*>(sbuf + kStateSBytes);  // [128]
-    float* dens = zs + kHeadDim;                                // [kApDSlots][128]
+    float* dens = zs + kHeadDim;                // [kApDSlots][128] phi(q) . z + eps
     uint64_t* qfull = reinterpret_cast<uint64_t*>(dens + kApDSlots * kApTok);
     uint64_t* qready = qfull + kApQStages;       // Q tile transformed (MMA may read it)
     uint64_t* qempty = qready + kApQStages;      // Q tile read by the MMA
@@ -927,10 +951,11 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     x[i].w = relu_bf2(x[i].w);
                     float f[8];
                     unpack8(x[i], f);
-                    float d = 0.f;
+                    float2 d2 = mul2(make_float2(f[0], f[1]), make_float2(zc[0], zc[1]));
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) d = fmaf(f[j], zc[j], d);
-                    den[i] = d;
+                    for (int j = 2; j < 8; j += 2)
+                        d2 = fma2(make_float2(f[j], f[j + 1]), make_float2(zc[j], zc[j + 1]), d2);
+                    den[i] = d2.x + d2.y;
                     if (ROPE) {
                         float2 cs[4];
                         unpack_cs(trow[b4 + i], cs);
@@ -1008,21 +1033,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                           v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int sub = 0; sub < 4; ++sub) {
-                    float gf[8];
-                    unpack8(gv[sub], gf);
-                    uint32_t ow[4];
-                    // o = num / (den * (1 + exp(-g))), the product formed by one fma
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float d0 = fmaf(den, __expf(-gf[2 * e]), den);
-                        const float d1 = fmaf(den, __expf(-gf[2 * e + 1]), den);
-                        const float o0 = __fdividef(__uint_as_float(v[sub * 8 + 2 * e]), d0);
-                        const float o1 = __fdividef(__uint_as_float(v[sub * 8 + 2 * e + 1]), d1);
-                        ow[e] = f2_to_bf2(o0, o1);
-                    }
-                    gv[sub] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-                }
+                for (int sub = 0; sub < 4; ++sub) gv[sub] = gate_chunk(gv[sub], v + 8 * sub, den);
 #pragma unroll
                 for (int sub = 0; sub < 4; ++sub) sts128(addr[sub], gv[sub]);
             }
@@ -1036,8 +1047,9 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                           quad * kApORows * 128,
                              64 * hf, tile * kApTok + quad * kApORows, h);
                 bulk_commit();
-                bulk_wait_read_all();          // the G slot may be refilled after this
-                mbar_arrive(&gempty[gs]);
+                // the previous tile's store has read its G slot, which may be refilled
+                bulk_wait_read_one();
+                if (it > 0) mbar_arrive(&gempty[(it - 1) % kApGStages]);
             }
         }
         if (lane == 0) bulk_wait_all();
@@ -1078,21 +1090,28 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 // its fixed costs: launch, ramp, merge tail).  Phase 1: CTA r of the cluster
 // streams its share of the head's K and V tiles as the state kernel does,
 // accumulating its partial S^T in TMEM and its z in registers, and writes
-// both to its own shared memory.  Reduction: CTA r sums rows
-// [r*128/C, (r+1)*128/C) of the C partials through distributed shared memory
-// and writes them, as bf16 in the MMA layout, into every CTA's state buffer;
-// each CTA sums z itself.  Phase 2: CTA r applies the state to its share of
+// both to its own shared memory.  Reduction: every CTA sums the C partial z
+// itself, which lets its transform warps start on its first Q tile, while
+// CTA r sums rows [r*128/C, (r+1)*128/C) of the C partial S^T through
+// distributed shared memory and writes them, as bf16 in the MMA layout, into
+// every CTA's state buffer.  Phase 2: CTA r applies the state to its share of
 // the head's Q and G tiles as the apply kernel does.  The cluster meets only
 // on mbarriers with bounded waits, and on one cluster barrier just before
 // exit, which every thread reaches after bounded work.
+//
+// Shared memory in phase 2: the Q ring's first stage and the G ring's first
+// two stages are loaded as soon as phase 1 ends; the partial S^T sits in Q
+// stages 1-2 and the partial z in G stage 2, which are loaded only once every
+// CTA of the cluster has read them.
 
 constexpr int kFuThreads = kApThreads;            // the apply kernel's 19 warps
 constexpr int kFuTmemCols = 512;                  // phase 2 at 0 and 128, phase 1 at 256
 constexpr int kFuMaxCluster = 8;
 constexpr int kFuAutoMaxTiles = 36;               // longest head the shape rule fuses
-constexpr int kFuPartial = kApQStages * kApTile;  // partial S^T, then z parts: at the G ring
-constexpr int kFuPartialBytes = (kHeadDim * kHeadDim + kStXWarps * kHeadDim) * 4;
-static_assert(kFuPartial + kFuPartialBytes <= kStRing, "the partial fits in the idle ring");
+constexpr int kFuPartial = kApTile;               // partial S^T fp32 [128][128]: Q stages 1-2
+constexpr int kFuZLocal = kApQStages * kApTile + 2 * kApTile;   // partial z: G stage 2
+static_assert(kFuPartial + kHeadDim * kHeadDim * 4 == kApQStages * kApTile, "Q stages 1-2");
+static_assert(kStXWarps * kHeadDim * 4 <= kStateSBytes, "z parts fit in the state buffer");
 
 struct FusedParams {
     int N, Tk, Tq, C;           // tokens, 64-token and 128-token tiles per head, cluster size
@@ -1112,17 +1131,21 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t* qring = smem;                                      // phase 2
     uint8_t* gring = smem + kApQStages * kApTile;               // phase 2
-    float* partial = reinterpret_cast<float*>(smem + kFuPartial);   // S^T [128][128], z [8][128]
+    float* partial = reinterpret_cast<float*>(smem + kFuPartial);   // S^T [128][128]
+    float* zloc = reinterpret_cast<float*>(smem + kFuZLocal);       // z of this CTA [128]
     uint8_t* sbuf = smem + kStRing;                             // S^T bf16, then z
+    float* zparts = reinterpret_cast<float*>(sbuf);             // [8 warps][128] before the merge
     float* zs = reinterpret_cast<float*>(sbuf + kStateSBytes);
-    float* dens = zs + kHeadDim;                                // [kApDSlots][128]
+    float* dens = zs + kHeadDim;                // [kApDSlots][128] phi(q) . z + eps
     uint64_t* full = reinterpret_cast<uint64_t*>(dens + kApDSlots * kApTok);
     uint64_t* kready = full + kS1;
     uint64_t* empty = kready + kS1;
     uint64_t* s1full = empty + kS1;          // phase-1 MMAs done: TMEM partial final, ring idle
-    uint64_t* flushdone = s1full + 1;        // partial S^T and z parts written (12 warps)
+    uint64_t* zpdone = s1full + 1;           // the transform warps' z parts written (8 warps)
+    uint64_t* flushdone = zpdone + 1;        // partial S^T and z written (4 warps)
     uint64_t* pready = flushdone + 1;        // every CTA's partial written (C arrivals)
-    uint64_t* reddone = pready + 1;          // this CTA's rows written everywhere (8 warps)
+    uint64_t* zready = pready + 1;           // z of the head in zs (4 warps)
+    uint64_t* reddone = zready + 1;          // this CTA's rows written everywhere (8 warps)
     uint64_t* sready = reddone + 1;          // the state is complete here (C arrivals)
     uint64_t* qfull = sready + 1;
     uint64_t* qready = qfull + kApQStages;
@@ -1153,8 +1176,10 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             mbar_init(&empty[s], 1);
         }
         mbar_init(s1full, 1);
-        mbar_init(flushdone, kStXWarps + kStFWarps);
+        mbar_init(zpdone, kStXWarps);
+        mbar_init(flushdone, kStFWarps);
         mbar_init(pready, C);
+        mbar_init(zready, kStFWarps);
         mbar_init(reddone, kApEWarps);
         mbar_init(sready, C);
         for (int s = 0; s < kApQStages; ++s) {
@@ -1215,12 +1240,15 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 tma_load_3d(st + kStTile + kStHalf, &tm_v, &full[s], 64, t * kStTok, h, policy);
                 if (ROPE) tma_load_2d(st + 2 * kStTile, &tm_t, &full[s], 0, t * kStTok, keep);
             }
-            // the Q ring reuses the phase-1 ring once every phase-1 tile is consumed
+            // Q stage 0 reuses the phase-1 ring once every phase-1 tile is
+            // consumed; stages 1-2 hold the partial S^T until the cluster has
+            // read it
             if (ok) ok = mbar_wait(s1full, 0, abort_flag, p.status);
             int jt = 0;
             for (int t = q0; ok && t < q1; ++t, ++jt) {
                 const int s = jt % kApQStages;
                 const uint32_t round = (uint32_t)(jt / kApQStages);
+                if (jt == 1 && !(ok = mbar_wait_cluster(sready, 0, abort_flag, p.status))) break;
                 if (!(ok = mbar_wait(&qempty[s], (round & 1) ^ 1, abort_flag, p.status))) break;
                 uint8_t* st = qring + s * kApTile;
                 mbar_arrive_expect_tx(&qfull[s], kApTile);
@@ -1341,23 +1369,22 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&kready[s]);
             }
-            // this warp's z into the partial (the ring is idle once the MMAs are done)
-            if (ok) ok = warp_wait(s1full, 0, abort_flag, p.status);
+            // this warp's z into the z parts (the state buffer is idle until
+            // the cluster has published its partials)
             if (ok) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) zacc[j] += __shfl_xor_sync(0xffffffffu, zacc[j], 16);
                 if (lane < 16) {
-                    float4* zp = reinterpret_cast<float4*>(partial + kHeadDim * kHeadDim +
-                                                           xw * kHeadDim + c * 8);
+                    float4* zp = reinterpret_cast<float4*>(zparts + xw * kHeadDim + c * 8);
                     zp[0] = make_float4(zacc[0], zacc[1], zacc[2], zacc[3]);
                     zp[1] = make_float4(zacc[4], zacc[5], zacc[6], zacc[7]);
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(flushdone);
+                if (lane == 0) mbar_arrive(zpdone);
             }
         }
-        // phase 2
-        if (ok) ok = warp_wait_cluster(sready, 0, abort_flag, p.status);
+        // phase 2 starts as soon as z of the head is known
+        if (ok) ok = warp_wait(zready, 0, abort_flag, p.status);
         float zc[8];
         if (ok) {
             const float4 za = *reinterpret_cast<const float4*>(zs + 8 * c);
@@ -1406,10 +1433,11 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                     x[i].w = relu_bf2(x[i].w);
                     float f[8];
                     unpack8(x[i], f);
-                    float d = 0.f;
+                    float2 d2 = mul2(make_float2(f[0], f[1]), make_float2(zc[0], zc[1]));
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) d = fmaf(f[j], zc[j], d);
-                    den[i] = d;
+                    for (int j = 2; j < 8; j += 2)
+                        d2 = fma2(make_float2(f[j], f[j + 1]), make_float2(zc[j], zc[j + 1]), d2);
+                    den[i] = d2.x + d2.y;
                     if (ROPE) {
                         float2 cs[4];
                         unpack_cs(trow[b4 + i], cs);
@@ -1450,7 +1478,9 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         const int quad = warp & 3, hf = ew >> 2;
         const int rt = threadIdx.x - 32 * (2 + kApXWarps);   // 0..255
         bool ok = !*abort_flag;
-        // phase 1 (four of the warps): the partial S^T from TMEM into shared memory
+        const uint32_t pbase = smem_u32(partial), zbase = smem_u32(zloc), sbase = smem_u32(sbuf);
+        // phase 1 (four of the warps): the partial S^T from TMEM, and the sum
+        // of the eight z parts, into shared memory
         if (ew < kStFWarps) {
             if (ok) ok = warp_wait(s1full, 0, abort_flag, p.status);
             if (ok) {
@@ -1466,33 +1496,65 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                         partial[(ch * 32 + j) * kHeadDim + m] = __uint_as_float(r[j]);
                 }
                 tc_fence_before();
+            }
+            if (ok) ok = warp_wait(zpdone, 0, abort_flag, p.status);
+            if (ok) {
+                float z = 0.f;
+#pragma unroll
+                for (int w8 = 0; w8 < kStXWarps; ++w8) z += zparts[w8 * kHeadDim + rt];
+                zloc[rt] = z;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(flushdone);
             }
         }
         // every warp of this CTA has written its share: tell the cluster
-        if (rt == 0) {
-            bool done = ok && mbar_wait(flushdone, 0, abort_flag, p.status);
-            if (done) {
-                fence_acq_rel_cluster();
-                for (int q = 0; q < C; ++q) mbar_arrive_cluster(mapa_shared(smem_u32(pready), q));
-            }
+        if (rt == 0 && ok && mbar_wait(flushdone, 0, abort_flag, p.status)) {
+            fence_acq_rel_cluster();
+            for (int q = 0; q < C; ++q) mbar_arrive_cluster(mapa_shared(smem_u32(pready), q));
         }
-        // reduction: rows [rank*128/C, (rank+1)*128/C) of every CTA's partial
         if (ok) ok = warp_wait_cluster(pready, 0, abort_flag, p.status);
+        // z of the head first (the transform warps wait for it), every CTA's
+        // part loaded before any is added, added in rank order
+        if (ok && ew < kStFWarps) {
+            float zq[kFuMaxCluster];
+#pragma unroll
+            for (int q = 0; q < kFuMaxCluster; ++q)
+                if (q < C) zq[q] = ld_cluster_f32(mapa_shared(zbase + rt * 4, q));
+            float z = 0.f;
+#pragma unroll
+            for (int q = 0; q < kFuMaxCluster; ++q)
+                if (q < C) z += zq[q];
+            zs[rt] = z;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(zready);
+        }
+        // rows [rank*128/C, (rank+1)*128/C) of S^T, summed in rank order from
+        // every CTA's partial (four CTAs' loads in flight at a time) and written
+        // as bf16 into every CTA's state buffer
         if (ok) {
             const int r0 = (int)rank * kHeadDim / C, r1 = ((int)rank + 1) * kHeadDim / C;
-            const uint32_t pbase = smem_u32(partial), sbase = smem_u32(sbuf);
             const int tasks = (r1 - r0) * 16;
             for (int t = rt; t < tasks; t += 32 * kApEWarps) {
                 const int n = r0 + (t >> 4), cc = t & 15;
-                float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
                 const uint32_t off = (uint32_t)((n * kHeadDim + cc * 8) * 4);
-                for (int q = 0; q < C; ++q) {
-                    const uint32_t src = mapa_shared(pbase + off, q);
-                    const float4 b0 = ld_cluster_f4(src), b1 = ld_cluster_f4(src + 16);
-                    a0.x += b0.x; a0.y += b0.y; a0.z += b0.z; a0.w += b0.w;
-                    a1.x += b1.x; a1.y += b1.y; a1.z += b1.z; a1.w += b1.w;
+                float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+                for (int qb = 0; qb < C; qb += 4) {
+                    float4 b0[4], b1[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if (qb + j < C) {
+                            const uint32_t src = mapa_shared(pbase + off, qb + j);
+                            b0[j] = ld_cluster_f4(src);
+                            b1[j] = ld_cluster_f4(src + 16);
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if (qb + j < C) {
+                            a0.x += b0[j].x; a0.y += b0[j].y; a0.z += b0[j].z; a0.w += b0[j].w;
+                            a1.x += b1[j].x; a1.y += b1[j].y; a1.z += b1[j].z; a1.w += b1[j].w;
+                        }
+                    }
                 }
                 uint4 w;
                 w.x = f2_to_bf2(a0.x, a0.y);
@@ -1501,16 +1563,6 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 w.w = f2_to_bf2(a1.z, a1.w);
                 const uint32_t dst = sbase + sw128_off(n, cc, kStateHalf);
                 for (int q = 0; q < C; ++q) st_cluster_u4(mapa_shared(dst, q), w);
-            }
-            if (rt < kHeadDim) {
-                // z in full here: the sum of every CTA's eight warp parts
-                float zsum = 0.f;
-                for (int q = 0; q < C; ++q) {
-                    const uint32_t zb = mapa_shared(pbase + (uint32_t)((kHeadDim * kHeadDim + rt) * 4), q);
-#pragma unroll
-                    for (int w8 = 0; w8 < kStXWarps; ++w8) zsum += ld_cluster_f32(zb + w8 * kHeadDim * 4);
-                }
-                zs[rt] = zsum;
             }
             fence_proxy_async_all();
             __syncwarp();
@@ -1554,20 +1606,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                           v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int sub = 0; sub < 4; ++sub) {
-                    float gf[8];
-                    unpack8(gv[sub], gf);
-                    uint32_t ow[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float d0 = fmaf(den, __expf(-gf[2 * e]), den);
-                        const float d1 = fmaf(den, __expf(-gf[2 * e + 1]), den);
-                        const float o0 = __fdividef(__uint_as_float(v[sub * 8 + 2 * e]), d0);
-                        const float o1 = __fdividef(__uint_as_float(v[sub * 8 + 2 * e + 1]), d1);
-                        ow[e] = f2_to_bf2(o0, o1);
-                    }
-                    gv[sub] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-                }
+                for (int sub = 0; sub < 4; ++sub) gv[sub] = gate_chunk(gv[sub], v + 8 * sub, den);
 #pragma unroll
                 for (int sub = 0; sub < 4; ++sub) sts128(addr[sub], gv[sub]);
             }
@@ -1579,22 +1618,23 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 tma_store_3d(&tm_o32, gring + gs * kApTile + hf * kApHalf + quad * kApORows * 128,
                              64 * hf, t * kApTok + quad * kApORows, h);
                 bulk_commit();
-                bulk_wait_read_all();
-                mbar_arrive(&gempty[gs]);
+                bulk_wait_read_one();
+                if (it > 0) mbar_arrive(&gempty[(it - 1) % kApGStages]);
             }
         }
         if (lane == 0) bulk_wait_all();
     } else {
-        // ------------------------------------------------ G producer (after the reduction)
+        // ------------------------------------------------ G producer
         if (lane == 0 && !*abort_flag) {
             const uint64_t policy = policy_evict_first();
-            // the G ring overlays this CTA's partial, which the cluster reads
-            // until every CTA has arrived on sready
-            bool ok = mbar_wait_cluster(sready, 0, abort_flag, p.status);
+            // stages 0-1 are free once phase 1 is done; stage 2 holds this
+            // CTA's partial z until the cluster has read it
+            bool ok = mbar_wait(s1full, 0, abort_flag, p.status);
             int it = 0;
             for (int t = q0; ok && t < q1; ++t, ++it) {
                 const int s = it % kApGStages;
                 const uint32_t round = (uint32_t)(it / kApGStages);
+                if (it == 2 && !(ok = mbar_wait_cluster(sready, 0, abort_flag, p.status))) break;
                 if (!(ok = mbar_wait(&gempty[s], (round & 1) ^ 1, abort_flag, p.status))) break;
                 uint8_t* st = gring + s * kApTile;
                 mbar_arrive_expect_tx(&gfull[s], kApTile);
@@ -1679,12 +1719,12 @@ constexpr size_t ap_smem() {
            kApDSlots * kApTok * sizeof(float) +
            (3 * kApQStages + 2 * kApGStages + 2 * kApDSlots + 7) * 8 + 16;
 }
-// fused: the ring, the state, the denominators, then 3*stages + 5 phase-1 and
+// fused: the ring, the state, the denominators, then 3*stages + 7 phase-1 and
 // cluster mbarriers, the apply kernel's 3*Q + 2*G + 2*den + 5 and two words.
 template <bool ROPE>
 constexpr size_t fu_smem() {
     return (size_t)kStRing + kStateBytes + kApDSlots * kApTok * sizeof(float) +
-           (3 * StGeo<ROPE>::kStages + 5 + 3 * kApQStages + 2 * kApGStages + 2 * kApDSlots + 5) *
+           (3 * StGeo<ROPE>::kStages + 7 + 3 * kApQStages + 2 * kApGStages + 2 * kApDSlots + 5) *
                8 +
            16;
 }
