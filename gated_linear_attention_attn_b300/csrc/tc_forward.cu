@@ -1107,7 +1107,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 constexpr int kFuThreads = kApThreads;            // the apply kernel's 19 warps
 constexpr int kFuTmemCols = 512;                  // phase 2 at 0 and 128, phase 1 at 256
 constexpr int kFuMaxCluster = 8;
-constexpr int kFuAutoMaxTiles = 36;               // longest head the shape rule fuses
+constexpr int kFuAutoMaxTiles = 64;               // heads the shape rule always fuses
 constexpr int kFuPartial = kApTile;               // partial S^T fp32 [128][128]: Q stages 1-2
 constexpr int kFuZLocal = kApQStages * kApTile + 2 * kApTile;   // partial z: G stage 2
 static_assert(kFuPartial + kHeadDim * kHeadDim * 4 == kApQStages * kApTile, "Q stages 1-2");
@@ -1917,18 +1917,19 @@ int fused_cluster(int dev, int BH, int N, bool rope, int num_sms) {
     const Path path = forced_path();
     if (path == Path::kSplit) return 0;
     const int Tq = (N + kApTok - 1) / kApTok;
-    // Measured on B300: the fused launch saves the second launch and the
-    // merge (a few microseconds), but leaves SMs idle when B*H does not
-    // divide their number and runs its two phases back to back in each CTA,
-    // so the two launches stream faster once a head has more than about 36
-    // tiles of 128 queries.
-    if (path == Path::kAuto && Tq > kFuAutoMaxTiles) return 0;
     int cmax = num_sms / BH;
     if (cmax > kFuMaxCluster) cmax = kFuMaxCluster;
     if (cmax > Tq) cmax = Tq;
-    for (int C = cmax; C >= 2; --C)
-        if (fused_capacity(dev, rope, C) >= BH) return C;
-    return 0;
+    int C = cmax;
+    while (C >= 2 && fused_capacity(dev, rope, C) < BH) --C;
+    if (C < 2) return 0;
+    // Measured on B300: the fused launch saves the second launch, the merge
+    // through global memory and the hand-over between the launches, but it
+    // leaves SMs idle when B*H does not divide their number.  It wins for
+    // heads of up to 64 query tiles, and for longer heads only when its
+    // clusters cover at least 85% of the SMs.
+    if (path == Path::kAuto && Tq > kFuAutoMaxTiles && 100 * BH * C < 85 * num_sms) return 0;
+    return C;
 }
 
 cudaError_t launch_fused(const void* q, const void* k, const void* v, const void* g, void* out,

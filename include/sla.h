@@ -128,10 +128,11 @@ sla_status_t sla_linattn_forward_f32(const float* q, const float* k, const float
  * memory, and each CTA applies the state to its share of the queries.  This
  * needs no workspace.  It applies when every head's cluster can be resident
  * at once (B*H clusters of C CTAs on the device's SMs) and the head has at
- * least C tiles of 128 queries, and it is taken when it applies and N is at
- * most 36 * 128 = 4608 tokens (beyond that the two launches measured faster
- * on B300).  Otherwise the forward launches the state kernel and then the
- * apply kernel (sla_linattn_state, sla_linattn_apply).
+ * least C tiles of 128 queries.  It is taken when it applies and either N is
+ * at most 64 * 128 = 8192 tokens or its B*H*C CTAs cover at least 85% of the
+ * SMs (otherwise the two launches measured faster on B300).  Otherwise the
+ * forward launches the state kernel and then the apply kernel
+ * (sla_linattn_state, sla_linattn_apply).
  *
  * Returns C for the fused launch, 0 for the two launches, -1 for an invalid
  * shape (rope: nonzero when a RoPE table will be passed).  The environment
