@@ -107,11 +107,24 @@ simt_apply_kernel(const T* __restrict__ q, const T* __restrict__ g,
     const int cnt = min(kSimtTile, N - base);
     const size_t head = (size_t)bh * N * kHeadDim;
 
+    // The head's state: the C partials summed in chunk order, four elements per
+    // thread at a time so that four loads are in flight.
     const float* src = partial + (size_t)bh * C * kPartialFloats;
-    for (int e = tid; e < kPartialFloats; e += blockDim.x) {
-        float s = 0.f;
-        for (int cc = 0; cc < C; ++cc) s += src[(size_t)cc * kPartialFloats + e];
-        smem[e] = s;
+    for (int e0 = tid; e0 < kPartialFloats; e0 += 4 * blockDim.x) {
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int cc = 0; cc < C; ++cc) {
+            float x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int e = e0 + u * blockDim.x;
+                x[u] = e < kPartialFloats ? src[(size_t)cc * kPartialFloats + e] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) s[u] += x[u];
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (e0 + u * blockDim.x < kPartialFloats) smem[e0 + u * blockDim.x] = s[u];
     }
     for (int e = tid; e < kSimtTile * kHeadDim; e += blockDim.x) {
         const int r = e / kHeadDim, col = e % kHeadDim;
@@ -180,7 +193,9 @@ size_t simt_workspace_bytes(int BH, int C) {
 int simt_chunks(int BH, int N, int num_sms) {
     const int tiles = (N + kSimtTile - 1) / kSimtTile;
     int C = (2 * num_sms + BH - 1) / BH;
-    if (C > tiles) C = tiles;
+    // every apply block sums all C partials of its head: keep at least four
+    // tiles per chunk so that this sum stays short
+    if (C > (tiles + 3) / 4) C = (tiles + 3) / 4;
     if (C < 1) C = 1;
     return C;
 }

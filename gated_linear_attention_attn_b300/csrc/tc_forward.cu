@@ -491,11 +491,21 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         auto add4 = [](float4& a, const float4& b) {
             a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
         };
+        // z of the head: the slots' z summed in slot order, eight slots' loads
+        // in flight at a time.
         auto merge_z = [&](uint8_t* dst, int hh, int lo, int hi) {
             float zs = 0.f;
-            for (int cc = lo; cc <= hi; ++cc)
-                zs += __ldcg(p.partial + (size_t)(cc + hh) * kPartialFloats +
-                             kHeadDim * kHeadDim + ft);
+            for (int c0 = lo; c0 <= hi; c0 += 8) {
+                float zq[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    zq[j] = c0 + j <= hi ? __ldcg(p.partial + (size_t)(c0 + j + hh) * kPartialFloats +
+                                                  kHeadDim * kHeadDim + ft)
+                                         : 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (c0 + j <= hi) zs += zq[j];
+            }
             reinterpret_cast<float*>(dst + kStateSBytes)[ft] = zs;
         };
 
@@ -613,6 +623,54 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             if (with_z) merge_z(dst, hh, lo, hi);
         };
 
+        // merge_rows once the CTA's ring is idle: the rows [r0, r1) of every
+        // slot come in by one batch of bulk copies and are summed from shared
+        // memory in slot order (the same sums as merge_rows).
+        auto merge_rows_bulk = [&](int hh, int lo, int hi, int r0, int r1, bool with_z) -> bool {
+            const int k = hi - lo + 1;
+            const int slot_bytes = (r1 - r0) * kHeadDim * 4;
+            if (k * slot_bytes > kStRing) {        // not reached: m >= k - 1 mergers share rows
+                merge_rows(hh, lo, hi, r0, r1, with_z);
+                return true;
+            }
+            if (ft == 0) {
+                if (mbatch == 0 || mbar_wait(mfree, (mbatch - 1) & 1, abort_flag, p.status)) {
+                    mbar_arrive_expect_tx(mfull, k * slot_bytes);
+                    for (int j = 0; j < k; ++j)
+                        bulk_load(smem + j * slot_bytes,
+                                  p.partial + (size_t)(lo + j + hh) * kPartialFloats +
+                                      (size_t)r0 * kHeadDim,
+                                  slot_bytes, mfull);
+                }
+            }
+            const int bi = mbatch++;
+            if (!warp_wait(mfull, bi & 1, abort_flag, p.status)) return false;
+            uint8_t* dst = p.state + (size_t)hh * kStateBytes;
+            const int tasks = (r1 - r0) * 16;                 // (row, 8-column chunk)
+            for (int t = ft; t < tasks; t += 128) {
+                float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+                const uint32_t off = smem0 + (uint32_t)((t >> 4) * kHeadDim * 4 + (t & 15) * 32);
+                for (int j = 0; j < k; ++j) {
+                    const uint4 x0 = lds128(off + j * slot_bytes);
+                    const uint4 x1 = lds128(off + j * slot_bytes + 16);
+                    add4(a0, make_float4(__uint_as_float(x0.x), __uint_as_float(x0.y),
+                                         __uint_as_float(x0.z), __uint_as_float(x0.w)));
+                    add4(a1, make_float4(__uint_as_float(x1.x), __uint_as_float(x1.y),
+                                         __uint_as_float(x1.z), __uint_as_float(x1.w)));
+                }
+                uint4 w;
+                w.x = f2_to_bf2(a0.x, a0.y);
+                w.y = f2_to_bf2(a0.z, a0.w);
+                w.z = f2_to_bf2(a1.x, a1.y);
+                w.w = f2_to_bf2(a1.z, a1.w);
+                *reinterpret_cast<uint4*>(dst + sw128_off(r0 + (t >> 4), t & 15, kStateHalf)) = w;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(mfree);
+            if (with_z) merge_z(dst, hh, lo, hi);
+            return true;
+        };
+
         bool ok = !*abort_flag;
         for (int sg = 0; ok && sg <= h_last - h_first; ++sg) {
             const int hh = h_first + sg, b = sg & 1;
@@ -679,7 +737,8 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             } else if (action == 2) {
                 __threadfence();
                 const int m = e_hi - lo + 1, j = cta - lo;
-                merge_rows(hh, lo, hi, j * kHeadDim / m, (j + 1) * kHeadDim / m, j == 0);
+                // a shared merge happens only at the CTA's last segment: the ring is idle
+                ok = merge_rows_bulk(hh, lo, hi, j * kHeadDim / m, (j + 1) * kHeadDim / m, j == 0);
             }
         }
         // no bulk copy of ours may still be landing when the CTA exits
