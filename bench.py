@@ -188,14 +188,19 @@ def _blas_threads():
 
 def oracle_heads(wl, tensors, heads):
     """Run the fp64 oracle on the given (b, h) heads at full N; returns elapsed seconds."""
-    import oracle.linattn as ol   # the CPU baseline is the one place bench.py runs the oracle
+    import oracle.block_causal as bc   # the CPU baseline is the one place bench.py runs the oracle
+    import oracle.linattn as ol
     spec = ol.RopeSpec(*wl.grid, *wl.split, base=wl.base) if wl.rope else None
     q, k, v, g = tensors
     t0 = time.perf_counter()
     for b, h in heads:
         ang = ol.rope3d_angles(spec) if spec is not None else None
-        ol.linattn_head(q[b, h].double().numpy(), k[b, h].double().numpy(),
-                        v[b, h].double().numpy(), g[b, h].double().numpy(), wl.eps, ang)
+        args = (q[b, h].double().numpy(), k[b, h].double().numpy(), v[b, h].double().numpy(),
+                g[b, h].double().numpy())
+        if wl.block_frames:
+            bc.linattn_block_causal_head(*args, wl.block_tokens, wl.eps, ang)
+        else:
+            ol.linattn_head(*args, wl.eps, ang)
     return time.perf_counter() - t0
 
 
@@ -251,6 +256,9 @@ def _config(wl, world, note="", plan=None):
                   % (wl.algorithmic_bytes / 1e6) if wl.algorithmic_bytes >= 4 * L2_BYTES
                   else "L2 flushed between steps (a 252 MB buffer written outside the "
                        "timed events)")}
+    if wl.block_frames:
+        cfg["block_frames"] = wl.block_frames
+        cfg["block_tokens"] = wl.block_tokens
     if plan:
         cfg["launch_plan"] = plan
     if note:
@@ -320,10 +328,20 @@ def run_sla(args, rank, world, local):
             scrub_buf.fill_(1)
 
     os.environ["SLA_FORWARD_KERNEL"] = args.forward_kernel
-    cluster = sla.forward_cluster(wl.B, wl.H, wl.N, wl.rope, device=dev) if bf16 else 0
+    blocks = wl.block_frames > 0
+    cluster = sla.forward_cluster(wl.B, wl.H, wl.N, wl.rope, device=dev) \
+        if bf16 and not blocks else 0
+    carried = torch.zeros(wl.B, wl.H, sla.CARRIED_FLOATS, dtype=torch.float32, device=dev) \
+        if blocks else None
 
     def step():
-        sla.linattn_forward(q, k, v, g, out=out, rope=rope, eps=wl.eps, stream=stream)
+        if blocks:
+            # one stretch of a stream: the carried state comes in and goes out in place
+            sla.linattn_forward_block_causal(q, k, v, g, wl.block_tokens, out=out, rope=rope,
+                                             eps=wl.eps, state_in=carried, state_out=carried,
+                                             stream=stream)
+        else:
+            sla.linattn_forward(q, k, v, g, out=out, rope=rope, eps=wl.eps, stream=stream)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -351,7 +369,11 @@ def run_sla(args, rank, world, local):
     # whole forward; the two-launch plan is timed phase by phase
     kernels = {}
     plans = {}
-    if bf16 and cluster > 0:
+    if blocks:
+        kernels["block-causal forward (state, scan, apply)"] = {
+            "us": 1e6 * per_step, "algorithmic_bytes": wl.algorithmic_bytes,
+            "gbs": wl.algorithmic_bytes / per_step / 1e9}
+    elif bf16 and cluster > 0:
         kernels["tc_fused_kernel"] = {"us": 1e6 * per_step,
                                       "algorithmic_bytes": wl.algorithmic_bytes,
                                       "gbs": wl.algorithmic_bytes / per_step / 1e9,
@@ -364,7 +386,7 @@ def run_sla(args, rank, world, local):
                               / args.steps}
     elif bf16:
         plans["split"] = {"us": 1e6 * per_step}
-    if bf16:
+    if bf16 and not blocks:
         state = sla.linattn_state(k, v, rope=rope, stream=stream)
 
         def k_state():
@@ -444,11 +466,14 @@ def run_sla(args, rank, world, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if bf16 else "f32",
         "data": "synthetic (seeded N(0,1) q,k,v,g on the latent token grid)",
-        "config": _config(wl, world, plan=("fused, clusters of %d CTAs per head" % cluster
-                                           if cluster > 0 else "state + apply launches")),
+        "config": _config(wl, world, plan=(
+            "block-causal: state, block scan and apply launches, %d blocks of %d tokens, carried "
+            "state updated in place" % (wl.N // wl.block_tokens, wl.block_tokens) if blocks else
+            "fused, clusters of %d CTAs per head" % cluster if cluster > 0 else
+            "state + apply launches")),
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": (1 if cluster > 0 else 2) * args.steps,
+        "gpu_launches": (3 if blocks else 1 if cluster > 0 else 2) * args.steps,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline:

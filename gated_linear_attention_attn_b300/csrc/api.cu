@@ -87,15 +87,19 @@ static sla_status_t check_dims(int B, int H, int N, int d) {
 
 static bool bad_eps(float eps) { return !std::isfinite(eps) || eps < 0.f; }
 
-// The RoPE grid must have N tokens and bands that sum to d; fills *rv.
-static sla_status_t check_rope(const sla_rope_table_t* rope, int N, int d, RopeView* rv) {
+// The RoPE grid must cover tokens [offset, offset + N) (exactly N tokens when
+// exact) and have bands that sum to d; fills *rv.
+static sla_status_t check_rope_range(const sla_rope_table_t* rope, int N, int d, long long offset,
+                                     bool exact, RopeView* rv) {
     if (!rope) return SLA_OK;
     if (!rope->table) return SLA_ERR_INVALID_ARG;
     if (rope->T < 1 || rope->Hs < 1 || rope->Ws < 1) return SLA_ERR_INVALID_ARG;
     if (rope->dt < 0 || rope->dh < 0 || rope->dw < 0) return SLA_ERR_INVALID_ARG;
     if ((rope->dt | rope->dh | rope->dw) & 1) return SLA_ERR_INVALID_ARG;
     if (rope->dt + rope->dh + rope->dw != d) return SLA_ERR_INVALID_ARG;
-    if ((long long)rope->T * rope->Hs * rope->Ws != N) return SLA_ERR_INVALID_ARG;
+    const long long grid = (long long)rope->T * rope->Hs * rope->Ws;
+    if (exact ? grid != N : (offset < 0 || offset + N > grid)) return SLA_ERR_INVALID_ARG;
+    if (grid > 0x7fffffffLL) return SLA_ERR_UNSUPPORTED;
     if (misaligned(rope->table, 256)) return SLA_ERR_ALIGNMENT;
     const float2* base = reinterpret_cast<const float2*>(rope->table);
     rv->pt = rope->dt / 2;
@@ -110,6 +114,10 @@ static sla_status_t check_rope(const sla_rope_table_t* rope, int N, int d, RopeV
     rv->tok = reinterpret_cast<const uint32_t*>(rope->table) +
               rope_tok_offset_words(rope->T, rope->Hs, rope->Ws, rope->dt, rope->dh, rope->dw);
     return SLA_OK;
+}
+
+static sla_status_t check_rope(const sla_rope_table_t* rope, int N, int d, RopeView* rv) {
+    return check_rope_range(rope, N, d, 0, true, rv);
 }
 
 // Buffers: none null, all 16-byte aligned, the output overlapping no input.
@@ -226,6 +234,74 @@ sla_status_t sla_linattn_forward_f32(const float* q, const float* k, const float
                                      const sla_rope_table_t* rope_table, float eps,
                                      sla_stream_t stream) {
     return forward(q, k, v, g, out, B, H, N, d, rope_table, eps, stream, true);
+}
+
+size_t sla_linattn_carried_state_bytes(int B, int H, int d) {
+    if (B < 1 || H < 1 || d != kHeadDim) return 0;
+    return (size_t)B * H * (kHeadDim * kHeadDim + kHeadDim) * sizeof(float);
+}
+
+sla_status_t sla_linattn_forward_block_causal(const void* q, const void* k, const void* v,
+                                              const void* g, void* out, int B, int H, int N,
+                                              int d, int block_tokens,
+                                              const sla_rope_table_t* rope_table,
+                                              int rope_offset, float eps, const float* state_in,
+                                              float* state_out, sla_stream_t stream) {
+    if (!q || !k || !v || !g || !out) return SLA_ERR_INVALID_ARG;
+    sla_status_t st = check_dims(B, H, N, d);
+    if (st == SLA_ERR_INVALID_ARG) return st;
+    if (bad_eps(eps)) return SLA_ERR_INVALID_ARG;
+    if (st != SLA_OK) return st;
+    if (block_tokens < 1 || N % block_tokens != 0) return SLA_ERR_INVALID_ARG;
+    const size_t bytes = (size_t)B * H * N * d * 2;
+    const size_t sbytes = sla_linattn_carried_state_bytes(B, H, d);
+    const void* ins[4] = {q, k, v, g};
+    const size_t sizes[4] = {bytes, bytes, bytes, bytes};
+    if ((st = check_buffers(ins, sizes, 4, out, bytes)) != SLA_OK) return st;
+    if (state_in && misaligned(state_in, 16)) return SLA_ERR_ALIGNMENT;
+    if (state_out) {
+        // the outgoing state overlaps no tensor and no incoming state but itself
+        if (misaligned(state_out, 16)) return SLA_ERR_ALIGNMENT;
+        const void* others[6] = {q, k, v, g, out, state_in};
+        const size_t osizes[6] = {bytes, bytes, bytes, bytes, bytes, sbytes};
+        for (int i = 0; i < 6; ++i) {
+            if (!others[i] || (i == 5 && others[i] == state_out)) continue;
+            const uintptr_t x = reinterpret_cast<uintptr_t>(state_out);
+            const uintptr_t y = reinterpret_cast<uintptr_t>(others[i]);
+            if (x < y + osizes[i] && y < x + sbytes) return SLA_ERR_INVALID_ARG;
+        }
+    }
+    if (state_in) {
+        // out is written while the incoming state may still be read
+        const uintptr_t x = reinterpret_cast<uintptr_t>(state_in);
+        const uintptr_t y = reinterpret_cast<uintptr_t>(out);
+        if (x < y + bytes && y < x + sbytes) return SLA_ERR_INVALID_ARG;
+    }
+    RopeView rv{};
+    if ((st = check_rope_range(rope_table, N, d, rope_offset, false, &rv)) != SLA_OK) return st;
+    if (!rope_table && rope_offset != 0) return SLA_ERR_INVALID_ARG;
+    const int nb = N / block_tokens;
+    if ((long long)B * H * nb > 0x7fffffffLL / 2) return SLA_ERR_UNSUPPORTED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SLA_ERR_CUDA;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* ds = nullptr;
+    if ((st = device_state(dev, &ds)) != SLA_OK) return st;
+    void* ws = nullptr;
+    if ((st = workspace(dev, s, tc_workspace_bytes(B * H * nb, block_tokens, ds->num_sms), &ws)) !=
+        SLA_OK)
+        return st;
+    if (launch_tc_block_causal(q, k, v, g, out, B, H, N, block_tokens,
+                               rope_table ? &rv : nullptr, rope_offset, eps, state_in, state_out,
+                               (float*)ws, ds->status, ds->num_sms, s) != cudaSuccess) {
+        cudaGetLastError();
+        return SLA_ERR_CUDA;
+    }
+    return SLA_OK;
 }
 
 int sla_linattn_forward_cluster(int B, int H, int N, int d, int rope) {

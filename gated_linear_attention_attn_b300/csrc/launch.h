@@ -43,6 +43,15 @@ cudaError_t launch_tc_two_phase(const void* q, const void* k, const void* v, con
                                 void* out, int B, int H, int N, const RopeView* rope, float eps,
                                 float* workspace, unsigned* status, int num_sms,
                                 cudaStream_t stream);
+// Block-causal form (tc_forward.cu): N = nb * block_tokens tokens per head,
+// the RoPE rows of tokens [rope_offset, rope_offset + N) of the grid, carried
+// states in and out (null for none).  Workspace: tc_workspace_bytes(B*H*nb,
+// block_tokens, num_sms).
+cudaError_t launch_tc_block_causal(const void* q, const void* k, const void* v, const void* g,
+                                   void* out, int B, int H, int N, int block_tokens,
+                                   const RopeView* rope, int rope_offset, float eps,
+                                   const float* state_in, float* state_out, float* workspace,
+                                   unsigned* status, int num_sms, cudaStream_t stream);
 cudaError_t launch_tc_state(const void* k, const void* v, void* state, int B, int H, int N,
                             const RopeView* rope, void* workspace, unsigned* status, int num_sms,
                             cudaStream_t stream);

@@ -123,6 +123,10 @@ struct StateParams {
     uint8_t* state;                 // per head: kStateBytes
     uint32_t epoch;                 // distinct for every launch
     unsigned* status;
+    // A "head" of this launch may be one block of a head's tokens: head hh
+    // covers tokens [(hh % nb) * N + tok0, ...) of the RoPE grid.  merge = 0
+    // leaves the partial slots unmerged (the block scan sums them).
+    int nb, tok0, merge;
 };
 
 struct ApplyParams {
@@ -132,6 +136,7 @@ struct ApplyParams {
     const uint8_t* state;
     float eps;
     unsigned* status;
+    int nb, tok0;                   // as in StateParams
 };
 
 __device__ __forceinline__ uint32_t relu_bf2(uint32_t x) {
@@ -323,8 +328,11 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             const uint64_t policy = policy_evict_first();
             const uint64_t keep = policy_evict_last();   // the RoPE rows serve every head
             long long it = 0;
-            for (long long u = u0; u < u1; ++u, ++it) {
-                const int h = (int)(u / p.Tk), tile = (int)(u % p.Tk);
+            int rope_h = -1, rope_base = 0;
+            // (head uh, tile ut) of unit u, advanced without divisions
+            int uh = (int)(u0 / p.Tk), ut = (int)(u0 % p.Tk);
+            for (long long u = u0; u < u1; ++u, ++it, ut = ut + 1 == p.Tk ? 0 : ut + 1, uh += ut == 0) {
+                const int h = uh, tile = ut;
                 const int s = (int)(it % kStStages);
                 const uint32_t round = (uint32_t)(it / kStStages);
                 if (!mbar_wait(&empty[s], (round & 1) ^ 1, abort_flag, p.status)) break;
@@ -335,7 +343,14 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 tma_load_3d(st + kStTile, &tm_v, &full[s], 0, tile * kStTok, h, policy);
                 tma_load_3d(st + kStTile + kStHalf, &tm_v, &full[s], 64, tile * kStTok, h,
                             policy);
-                if (ROPE) tma_load_2d(st + 2 * kStTile, &tm_t, &full[s], 0, tile * kStTok, keep);
+                if (ROPE) {
+                    if (h != rope_h) {                   // this head's first RoPE grid token
+                        rope_h = h;
+                        rope_base = (p.nb == 1 ? 0 : (h % p.nb) * p.N) + p.tok0;
+                    }
+                    tma_load_2d(st + 2 * kStTile, &tm_t, &full[s], 0, rope_base + tile * kStTok,
+                                keep);
+                }
             }
             // every load issued has landed before the CTA may exit
             const long long first = it > kStStages ? it - kStStages : 0;
@@ -349,8 +364,10 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             long long it = 0;
             int seg = -1, cur_h = -1;
             bool ok = !*abort_flag, first = false;
-            for (long long u = u0; ok && u < u1; ++u, ++it) {
-                const int h = (int)(u / p.Tk);
+            // (head uh, tile ut) of unit u, advanced without divisions
+            int uh = (int)(u0 / p.Tk), ut = (int)(u0 % p.Tk);
+            for (long long u = u0; ok && u < u1; ++u, ++it, ut = ut + 1 == p.Tk ? 0 : ut + 1, uh += ut == 0) {
+                const int h = uh;
                 const int s = (int)(it % kStStages);
                 const uint32_t round = (uint32_t)(it / kStStages);
                 if (h != cur_h) {
@@ -417,8 +434,10 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         long long it = 0;
         int seg = -1, cur_h = -1;
         bool ok = !*abort_flag;
-        for (long long u = u0; ok && u < u1; ++u, ++it) {
-            const int h = (int)(u / p.Tk);
+        // (head uh, tile ut) of unit u, advanced without divisions
+        int uh = (int)(u0 / p.Tk), ut = (int)(u0 % p.Tk);
+        for (long long u = u0; ok && u < u1; ++u, ++it, ut = ut + 1 == p.Tk ? 0 : ut + 1, uh += ut == 0) {
+            const int h = uh;
             if (h != cur_h) {
                 if (seg >= 0 && !(ok = hand_z(seg))) break;
                 ++seg;
@@ -712,7 +731,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 // every flush warp's share of the slot is written: count this CTA in
                 const bool done = mbar_wait(slotdone, sg & 1, abort_flag, p.status);
                 int action = 0;                      // 0 none, 1 whole merge, 2 a block of rows
-                if (done) {
+                if (done && p.merge) {
                     __threadfence();
                     count_contributor(p.counters + hh, p.epoch, p.status);
                     if (k == 1)
@@ -954,16 +973,19 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // This thread's 16 bytes of the RoPE rows of its 8 rows in the next
         // tile, loaded while the current tile is transformed.
         uint4 trow[kApRowsPerThread];
-        auto fetch_rows = [&](int tile, int i0) {
+        // (tile `tile` of head hh; head hh is block hh % nb of its head's
+        // tokens, which start at RoPE grid token (hh % nb) * N + tok0)
+        auto fetch_rows = [&](int hh, int tile, int i0) {
+            const int base = (p.nb == 1 ? 0 : (hh % p.nb) * p.N) + p.tok0;
 #pragma unroll
             for (int i = i0; i < i0 + 4; ++i) {
                 const int n = min(tile * kApTok + rl + 16 * i, p.N - 1);   // rows past N are zero
-                trow[i] = ldg_nc_na128(p.rope.tok + (size_t)n * kPairs + c * 4);
+                trow[i] = ldg_nc_na128(p.rope.tok + (size_t)(base + n) * kPairs + c * 4);
             }
         };
         if (ROPE && u0 < u1) {
-            fetch_rows((int)(u0 % p.Tq), 0);
-            fetch_rows((int)(u0 % p.Tq), 4);
+            fetch_rows((int)(u0 / p.Tq), (int)(u0 % p.Tq), 0);
+            fetch_rows((int)(u0 / p.Tq), (int)(u0 % p.Tq), 4);
         }
         long long it = 0;
         int heads = 0, cur_h = -1;
@@ -1024,7 +1046,9 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 // rows 0-3 of the RoPE table are used: load the next tile's.  The
                 // fence below waits for this thread's loads in flight, so rows 4-7
                 // are loaded only after it.
-                if (ROPE && next_tile >= 0 && b4 == 0) fetch_rows(next_tile, 0);
+                // the next unit is tile 0 of the next head, or the next tile of this one
+                if (ROPE && next_tile >= 0 && b4 == 0)
+                    fetch_rows(next_tile == 0 ? h + 1 : h, next_tile, 0);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) sts128(addr[i], x[i]);
                 // Sum den over the 16 chunk lanes of each row: each step halves the
@@ -1052,7 +1076,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 mbar_arrive(&qready[s]);
                 mbar_arrive(&dready[ds]);
             }
-            if (ROPE && next_tile >= 0) fetch_rows(next_tile, 4);
+            if (ROPE && next_tile >= 0) fetch_rows(next_tile == 0 ? h + 1 : h, next_tile, 4);
         }
     } else if (warp < 2 + kApXWarps + kApEWarps) {
         // ------------------------------------------------ epilogue: gate, divide, store
@@ -1718,6 +1742,92 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     }
 }
 
+// ========================================================== block scan ==
+//
+// Block-causal form: the state kernel runs over (head, block) segments and
+// leaves each segment's partial slots unmerged; this kernel turns them into
+// running states.  For head h it starts from the incoming carried state (or
+// zero), adds block b's slots in slot order and writes the running sum as the
+// bf16 state of segment (h, b) for the apply kernel, for b = 0, 1, ...; the
+// final sum is the outgoing carried state.  The running sum stays in fp32.
+//
+// CTA (h, r) owns rows [16 r, 16 r + 16) of S^T (value dims); thread t adds
+// row 16 r + t/16, key dims 8 (t % 16) .. +7.  CTA (h, 0) also carries z.
+
+constexpr int kScanRows = 16;
+constexpr int kScanThreads = kScanRows * 16;      // one thread per (row, 8 key dims)
+
+struct ScanParams {
+    const float* partial;       // the state kernel's slots (cta + segment)
+    Split split;                // the state kernel's split over segments
+    int Tk, nb;                 // 64-token tiles per segment, blocks per head
+    const float* state_in;      // [heads][128*128 + 128]: S[m][n], then z; or null
+    float* state_out;           // same layout, or null (may equal state_in)
+    uint8_t* states;            // [heads*nb][kStateBytes]
+};
+
+__global__ void __launch_bounds__(kScanThreads)
+block_scan_kernel(ScanParams p) {
+    griddep_wait();                       // the slots are complete
+    griddep_launch_dependents();          // the apply kernel may start its prologue
+    const int head = blockIdx.x, rg = blockIdx.y, t = threadIdx.x;
+    const int n = kScanRows * rg + (t >> 4), cc = t & 15;
+    const bool with_z = rg == 0 && t < kHeadDim;
+    constexpr int kCarried = kHeadDim * kHeadDim + kHeadDim;
+    float acc[8], z = 0.f;
+    if (p.state_in) {
+        const float* sin = p.state_in + (size_t)head * kCarried;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = sin[(cc * 8 + j) * kHeadDim + n];
+        if (with_z) z = sin[kHeadDim * kHeadDim + t];
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+    }
+    for (int b = 0; b < p.nb; ++b) {
+        const int sh = head * p.nb + b;
+        const int lo = p.split.owner((long long)sh * p.Tk);
+        const int hi = p.split.owner((long long)(sh + 1) * p.Tk - 1);
+        // the block's slots, four loaded before any is added, added in order
+        for (int c0 = lo; c0 <= hi; c0 += 4) {
+            float4 x0[4], x1[4];
+            float zx[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (c0 + j <= hi) {
+                    const float* slot = p.partial + (size_t)(c0 + j + sh) * kPartialFloats;
+                    const float4* src = reinterpret_cast<const float4*>(slot + n * kHeadDim + cc * 8);
+                    x0[j] = __ldcg(src);
+                    x1[j] = __ldcg(src + 1);
+                    zx[j] = with_z ? __ldcg(slot + kHeadDim * kHeadDim + t) : 0.f;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (c0 + j <= hi) {
+                    acc[0] += x0[j].x; acc[1] += x0[j].y; acc[2] += x0[j].z; acc[3] += x0[j].w;
+                    acc[4] += x1[j].x; acc[5] += x1[j].y; acc[6] += x1[j].z; acc[7] += x1[j].w;
+                    z += zx[j];
+                }
+            }
+        }
+        uint8_t* dst = p.states + (size_t)sh * kStateBytes;
+        uint4 w;
+        w.x = f2_to_bf2(acc[0], acc[1]);
+        w.y = f2_to_bf2(acc[2], acc[3]);
+        w.z = f2_to_bf2(acc[4], acc[5]);
+        w.w = f2_to_bf2(acc[6], acc[7]);
+        *reinterpret_cast<uint4*>(dst + sw128_off(n, cc, kStateHalf)) = w;
+        if (with_z) reinterpret_cast<float*>(dst + kStateSBytes)[t] = z;
+    }
+    if (p.state_out) {
+        float* sout = p.state_out + (size_t)head * kCarried;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) sout[(cc * 8 + j) * kHeadDim + n] = acc[j];
+        if (with_z) sout[kHeadDim * kHeadDim + t] = z;
+    }
+}
+
 // ==================================================================== host ==
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1843,9 +1953,11 @@ cudaError_t configure(int dev) {
     return cudaSuccess;
 }
 
+// BH "heads" of N tokens; in the block-causal form each is one block of nb
+// per head, starting at token tok0 of the RoPE grid, and merge is 0.
 cudaError_t launch_state(const void* k, const void* v, int BH, int N, const RopeView* rope,
                          void* workspace, uint8_t* state, unsigned* status, int num_sms,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, int nb = 1, int tok0 = 0, bool merge = true) {
     const Plan pl = make_plan(BH, N, num_sms);
     CUtensorMap mk, mv;
     if (!make_map(&mk, k, N, BH, kStTok) || !make_map(&mv, v, N, BH, kStTok))
@@ -1859,8 +1971,12 @@ cudaError_t launch_state(const void* k, const void* v, int BH, int N, const Rope
     sp.state = state;
     sp.epoch = next_epoch();
     sp.status = status;
+    sp.nb = nb;
+    sp.tok0 = tok0;
+    sp.merge = merge ? 1 : 0;
     CUtensorMap mt = mk;   // without RoPE the table map is never read
-    if (rope && !make_rope_map(&mt, rope->tok, N, kStTok)) return cudaErrorInvalidValue;
+    if (rope && !make_rope_map(&mt, rope->tok, rope->T * rope->Hs * rope->Ws, kStTok))
+        return cudaErrorInvalidValue;
     if (rope) sp.rope = *rope;
     // Cooperative: all CTAs are resident together, which the shared merge of a
     // head's state relies on (its CTAs wait for each other's counts).
@@ -1880,7 +1996,7 @@ cudaError_t launch_state(const void* k, const void* v, int BH, int N, const Rope
 
 cudaError_t launch_apply(const void* q, const void* g, const uint8_t* state, void* out, int BH,
                          int N, const RopeView* rope, float eps, unsigned* status, int num_sms,
-                         bool after_state, cudaStream_t stream) {
+                         bool after_state, cudaStream_t stream, int nb = 1, int tok0 = 0) {
     const Plan pl = make_plan(BH, N, num_sms);
     CUtensorMap mq, mg, mo;
     if (!make_map(&mq, q, N, BH, kApTok) || !make_map(&mg, g, N, BH, kApTok) ||
@@ -1893,6 +2009,8 @@ cudaError_t launch_apply(const void* q, const void* g, const uint8_t* state, voi
     ap.state = state;
     ap.eps = eps;
     ap.status = status;
+    ap.nb = nb;
+    ap.tok0 = tok0;
     if (rope) ap.rope = *rope;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(pl.ap.G);
@@ -1902,8 +2020,8 @@ cudaError_t launch_apply(const void* q, const void* g, const uint8_t* state, voi
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    // Only right after our own state kernel: Q and G are then complete before
-    // this grid starts, whatever wrote them.
+    // Only right after our own state (or block scan) kernel: Q and G are then
+    // complete before this grid starts, whatever wrote them.
     cfg.attrs = attr;
     cfg.numAttrs = after_state ? 1 : 0;
     if (rope) return cudaLaunchKernelEx(&cfg, tc_apply_kernel<true>, mq, mg, mo, ap);
@@ -2068,6 +2186,44 @@ cudaError_t launch_tc_fused(const void* q, const void* k, const void* v, const v
     cudaError_t e = configure(current_device());
     if (e != cudaSuccess) return e;
     return launch_fused(q, k, v, g, out, B * H, N, C, rope, eps, status, stream);
+}
+
+cudaError_t launch_tc_block_causal(const void* q, const void* k, const void* v, const void* g,
+                                   void* out, int B, int H, int N, int block_tokens,
+                                   const RopeView* rope, int rope_offset, float eps,
+                                   const float* state_in, float* state_out, float* workspace,
+                                   unsigned* status, int num_sms, cudaStream_t stream) {
+    const int BH = B * H, nb = N / block_tokens, BHs = BH * nb;
+    cudaError_t e = configure(current_device());
+    if (e != cudaSuccess) return e;
+    uint8_t* states = reinterpret_cast<uint8_t*>(workspace) +
+                      tc_state_workspace_bytes(BHs, block_tokens, num_sms);
+    // the (head, block) segments' partial slots, left unmerged
+    if ((e = launch_state(k, v, BHs, block_tokens, rope, workspace, nullptr, status, num_sms,
+                          stream, nb, rope_offset, false)) != cudaSuccess)
+        return e;
+    const Plan pl = make_plan(BHs, block_tokens, num_sms);
+    ScanParams sp{};
+    sp.partial = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(workspace) +
+                                          counters_bytes(BHs));
+    sp.split = pl.st;
+    sp.Tk = pl.Tk;
+    sp.nb = nb;
+    sp.state_in = state_in;
+    sp.state_out = state_out;
+    sp.states = states;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(BH, kHeadDim / kScanRows);
+    cfg.blockDim = dim3(kScanThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((e = cudaLaunchKernelEx(&cfg, block_scan_kernel, sp)) != cudaSuccess) return e;
+    return launch_apply(q, g, states, out, BHs, block_tokens, rope, eps, status, num_sms, true,
+                        stream, nb, rope_offset);
 }
 
 cudaError_t launch_tc_two_phase(const void* q, const void* k, const void* v, const void* g,

@@ -52,6 +52,12 @@ _lib.sla_linattn_apply.argtypes = [_vp] * 4 + [_int] * 4 + [ctypes.POINTER(RopeT
 _lib.sla_linattn_apply.restype = _int
 _lib.sla_linattn_forward_noalloc.argtypes = _FWD_ARGS[:-1] + [_vp, _vp]
 _lib.sla_linattn_forward_noalloc.restype = _int
+_lib.sla_linattn_carried_state_bytes.argtypes = [_int] * 3
+_lib.sla_linattn_carried_state_bytes.restype = ctypes.c_size_t
+_lib.sla_linattn_forward_block_causal.argtypes = ([_vp] * 5 + [_int] * 5 +
+                                                  [ctypes.POINTER(RopeTableC), _int, _flt,
+                                                   _vp, _vp, _vp])
+_lib.sla_linattn_forward_block_causal.restype = _int
 _lib.sla_linattn_forward_cluster.argtypes = [_int] * 5
 _lib.sla_linattn_forward_cluster.restype = _int
 _lib.sla_status_string.argtypes = [_int]
@@ -62,6 +68,7 @@ _lib.sla_last_device_status.restype = _int
 EXPORTED = ("sla_rope_table_floats", "sla_rope_table_fill", "sla_linattn_forward",
             "sla_linattn_forward_f32", "sla_linattn_state_bytes", "sla_linattn_state",
             "sla_linattn_apply", "sla_linattn_forward_noalloc", "sla_linattn_forward_cluster",
+            "sla_linattn_carried_state_bytes", "sla_linattn_forward_block_causal",
             "sla_status_string", "sla_last_device_status")
 
 
@@ -242,6 +249,57 @@ def last_device_status(stream: Optional[torch.cuda.Stream] = None, device="cuda"
     dev = torch.device(device)
     with torch.cuda.device(dev):
         return _lib.sla_last_device_status(_stream_handle(stream, dev))
+
+
+CARRIED_FLOATS = HEAD_DIM * HEAD_DIM + HEAD_DIM
+
+
+def carried_state_bytes(B: int, H: int, d: int = HEAD_DIM) -> int:
+    """Bytes of a carried (S, z) state for B*H heads (``sla_linattn_carried_state_bytes``)."""
+    return int(_lib.sla_linattn_carried_state_bytes(B, H, d))
+
+
+def carried_state_parts(state: torch.Tensor):
+    """Views (S [B, H, 128, 128], z [B, H, 128]) of a [B, H, 128*128 + 128] carried state."""
+    B, H = state.shape[:2]
+    S = state[..., :HEAD_DIM * HEAD_DIM].view(B, H, HEAD_DIM, HEAD_DIM)
+    return S, state[..., HEAD_DIM * HEAD_DIM:]
+
+
+def linattn_forward_block_causal(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                                 g: torch.Tensor, block_tokens: int,
+                                 out: Optional[torch.Tensor] = None,
+                                 rope: Optional[RopeTable] = None, rope_offset: int = 0,
+                                 eps: float = 1e-6, state_in: Optional[torch.Tensor] = None,
+                                 state_out=True, stream: Optional[torch.cuda.Stream] = None):
+    """Block-causal forward with a carried state (bf16; ``sla_linattn_forward_block_causal``).
+
+    state_in: None or a float32 [B, H, 128*128 + 128] tensor (S row-major,
+    then z).  state_out: True to allocate one, a tensor to fill (may be
+    state_in), or None for none.  Returns (out, state_out).
+    """
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g)):
+        _check_bf16(name, t, like=q if name != "q" else None)
+    B, H, N, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _check_bf16("out", out, like=q)
+    if state_out is True:
+        state_out = torch.empty(B, H, CARRIED_FLOATS, dtype=torch.float32, device=q.device)
+    for name, t in (("state_in", state_in), ("state_out", state_out)):
+        if t is not None and (t.dtype != torch.float32 or t.device != q.device
+                              or not t.is_contiguous() or t.numel() != B * H * CARRIED_FLOATS):
+            raise SlaError(INVALID_ARG, f"{name} must be a contiguous float32 [B, H, "
+                                        f"{CARRIED_FLOATS}] tensor on q's device")
+    rope_c = ctypes.byref(rope.c_struct()) if rope is not None else None
+    with torch.cuda.device(q.device):
+        _check(_lib.sla_linattn_forward_block_causal(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(), out.data_ptr(),
+            B, H, N, d, int(block_tokens), rope_c, int(rope_offset), float(eps),
+            state_in.data_ptr() if state_in is not None else None,
+            state_out.data_ptr() if state_out is not None else None,
+            _stream_handle(stream, q.device)), "sla_linattn_forward_block_causal")
+    return out, state_out
 
 
 def forward_cluster(B: int, H: int, N: int, rope: bool, d: int = HEAD_DIM,

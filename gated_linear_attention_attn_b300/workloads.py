@@ -38,11 +38,18 @@ class Workload:
     k_scale: float = 1.0
     tol: float = 1e-2                   # max|err| / max|ref| bound for parity
     description: str = ""
+    block_frames: int = 0               # > 0: block-causal form, blocks of this many frames
 
     @property
     def N(self) -> int:
         T, Hs, Ws = self.grid
         return T * Hs * Ws
+
+    @property
+    def block_tokens(self) -> int:
+        """Tokens per block of the block-causal form (0 for the bidirectional layer)."""
+        T, Hs, Ws = self.grid
+        return self.block_frames * Hs * Ws
 
     @property
     def token_heads(self) -> int:
@@ -84,6 +91,10 @@ WORKLOADS = {
     "5b_720p_60s": Workload(
         "5b_720p_60s", B=1, H=20, grid=(181, 22, 40), rope=True, k_scale=0.5,
         description="long clip, 720p/60 s: B=1 H=20 N=159280 (181x22x40) bf16, 3D RoPE, k x 0.5"),
+    "5b_720p_block5": Workload(
+        "5b_720p_block5", B=2, H=20, grid=(25, 22, 40), rope=True, block_frames=5,
+        description="block-causal form of the 720p shape: 5 blocks of 5 latent frames "
+                    "(4400 tokens), carried state in and out"),
 }
 
 # The workload the throughput metric is quoted on (5B shape at 720p).

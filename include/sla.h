@@ -181,6 +181,46 @@ sla_status_t sla_linattn_apply(const void* q, const void* g, const void* state, 
                                sla_stream_t stream);
 
 /*
+ * Block-causal form with a carried state ("SANA-Video" model card, "Constant-
+ * Memory KV Cache for Block Linear Attention": block-wise autoregressive
+ * generation that keeps global context in the cumulative state of linear
+ * attention at a fixed memory cost).  The N tokens of each head form N /
+ * block_tokens consecutive blocks (whole latent frames, so block_tokens =
+ * frames per block * Hs * Ws).  A token of block b attends to its own block in
+ * both directions and to every earlier block through the running state:
+ *
+ *     S_b = S_in + sum_{j in blocks 0..b} R_j phi(k_j) v_j^T
+ *     z_b = z_in + sum_{j in blocks 0..b} phi(k_j)
+ *     o_i = sigmoid(g_i) * (R_i phi(q_i))^T S_b / (phi(q_i) . z_b + eps)
+ *
+ * and the outgoing state is (S_last, z_last).  With block_tokens = N and no
+ * incoming state this is sla_linattn_forward.  Calls on consecutive
+ * stretches of a sequence, each passing the previous call's state_out as its
+ * state_in, give the same result as one call on the whole sequence.
+ *
+ * Arguments as for sla_linattn_forward (bf16 q, k, v, g, out), plus:
+ * block_tokens: >= 1, dividing N.  rope_table: NULL or a table whose grid
+ * covers tokens [rope_offset, rope_offset + N): this call's token n is token
+ * rope_offset + n of the grid (absolute positions, so a later stretch of a
+ * video passes its first token's index); rope_offset must be 0 without RoPE.
+ * state_in, state_out: NULL (a zero incoming state; no outgoing state) or
+ * device buffers of sla_linattn_carried_state_bytes(B, H, d) bytes, 16-byte
+ * aligned: per head (b-major) S as 128 x 128 fp32 row-major (row m = key
+ * dim, column n = value dim), then z as 128 fp32.  The running sums are kept
+ * in fp32; state_out may equal state_in (updated in place) but must not
+ * overlap anything else, and state_in must not overlap out.  Uses the
+ * library's per-stream workspace (about 66 KB per SM plus 99 KB per block of
+ * every head).
+ */
+size_t sla_linattn_carried_state_bytes(int B, int H, int d);   /* 0 if the shape is invalid */
+sla_status_t sla_linattn_forward_block_causal(const void* q, const void* k, const void* v,
+                                              const void* g, void* out, int B, int H, int N,
+                                              int d, int block_tokens,
+                                              const sla_rope_table_t* rope_table,
+                                              int rope_offset, float eps, const float* state_in,
+                                              float* state_out, sla_stream_t stream);
+
+/*
  * The bf16 forward of sla_linattn_forward for callers that cannot allocate
  * device memory.  No page has a counterpart: this entry point exists for
  * library users, not for the method.  Some callers must not see a library

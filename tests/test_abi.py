@@ -164,3 +164,35 @@ def test_forward_cluster_rejects_bad_shapes_before_cuda():
     assert lib.sla_linattn_forward_cluster(0, 1, 256, 128, 0) == -1
     assert lib.sla_linattn_forward_cluster(1, 1, 0, 128, 1) == -1
     assert lib.sla_linattn_forward_cluster(1, 1, 256, 64, 0) == -1
+
+
+def _bc(q=A, k=A + STEP, v=A + 2 * STEP, g=A + 3 * STEP, out=A + 4 * STEP, B=1, H=2, N=256,
+        d=128, bt=64, rope=None, off=0, eps=1e-6, sin=None, sout=None):
+    r = ctypes.byref(rope) if rope is not None else None
+    return sla.raw_lib().sla_linattn_forward_block_causal(q, k, v, g, out, B, H, N, d, bt, r, off,
+                                                          eps, sin, sout, None)
+
+
+def test_block_causal_rejects_bad_arguments_before_cuda():
+    S = A + 6 * STEP                                  # a carried-state buffer
+    assert sla.carried_state_bytes(1, 2) == 2 * (128 * 128 + 128) * 4
+    assert sla.carried_state_bytes(0, 2) == 0
+    bad = [
+        (dict(q=0), sla.INVALID_ARG),
+        (dict(bt=0), sla.INVALID_ARG),
+        (dict(bt=100), sla.INVALID_ARG),              # 256 tokens are not whole blocks of 100
+        (dict(eps=-1.0), sla.INVALID_ARG),
+        (dict(d=64), sla.UNSUPPORTED),
+        (dict(off=64), sla.INVALID_ARG),              # an offset without a RoPE table
+        (dict(rope=_rope(T=4), off=1), sla.INVALID_ARG),    # tokens 1..256 of a 256-token grid
+        (dict(rope=_rope(T=3)), sla.INVALID_ARG),     # a 192-token grid
+        (dict(rope=_rope(T=5), off=-1), sla.INVALID_ARG),
+        (dict(sin=S + 4), sla.ALIGNMENT),
+        (dict(sout=S + 8), sla.ALIGNMENT),
+        (dict(sout=A + 4 * STEP + 1024), sla.INVALID_ARG),  # state out inside out
+        (dict(sout=A + 1024), sla.INVALID_ARG),             # state out inside q
+        (dict(sin=A + 4 * STEP), sla.INVALID_ARG),          # state in is out
+        (dict(sin=S, sout=S + 1024), sla.INVALID_ARG),      # partial overlap of the states
+    ]
+    for kw, want in bad:
+        assert _bc(**kw) == want, kw
