@@ -1,0 +1,100 @@
+"""The bf16 entry points inside a captured CUDA graph.
+
+A serving loop replays a captured graph instead of launching each call.  The
+library's workspace is allocated on the first call of a shape, so one call
+runs before capture; the captured replay must then give the call's result bit
+for bit, for each launch plan and for the block-causal form.  The allocation-
+free entry point only needs its first call on the device (which looks up its
+scratch array) before capture.
+"""
+import ctypes
+
+import pytest
+import torch
+
+from gated_linear_attention_attn_b300.workloads import Workload, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _sla():
+    from gated_linear_attention_attn_b300 import sla
+    return sla
+
+
+@pytest.mark.parametrize("path", ["fused", "split"])
+def test_forward_replays_in_a_graph(path, cuda_device, monkeypatch):
+    sla = _sla()
+    monkeypatch.setenv("SLA_FORWARD_KERNEL", path)
+    wl = Workload("graph", B=2, H=4, grid=(3, 10, 20), rope=True)
+    q, k, v, g = (t.to(cuda_device) for t in make_inputs(wl, seed=31))
+    rope = sla.RopeTable(wl.grid, wl.split, wl.base, device=cuda_device)
+    ref = sla.linattn_forward(q, k, v, g, rope=rope)        # allocates the workspace
+    out = torch.full_like(q, float("nan"))
+    stream = torch.cuda.Stream(cuda_device)
+    stream.wait_stream(torch.cuda.current_stream(cuda_device))
+    with torch.cuda.stream(stream):
+        sla.linattn_forward(q, k, v, g, out=out, rope=rope, stream=stream)   # this stream's workspace
+    stream.synchronize()
+    out.fill_(float("nan"))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        sla.linattn_forward(q, k, v, g, out=out, rope=rope, stream=stream)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize(cuda_device)
+    assert sla.last_device_status(device=cuda_device) == 0
+    assert torch.equal(out, ref)
+
+
+def test_block_causal_replays_in_a_graph(cuda_device):
+    sla = _sla()
+    wl = Workload("graphbc", B=1, H=3, grid=(4, 8, 10), rope=True, block_frames=2)
+    q, k, v, g = (t.to(cuda_device) for t in make_inputs(wl, seed=32))
+    rope = sla.RopeTable(wl.grid, wl.split, wl.base, device=cuda_device)
+    stream = torch.cuda.Stream(cuda_device)
+    stream.wait_stream(torch.cuda.current_stream(cuda_device))
+    with torch.cuda.stream(stream):
+        ref, st_ref = sla.linattn_forward_block_causal(q, k, v, g, wl.block_tokens, rope=rope,
+                                                       stream=stream)
+    stream.synchronize()
+    out = torch.full_like(q, float("nan"))
+    st = torch.full_like(st_ref, float("nan"))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        sla.linattn_forward_block_causal(q, k, v, g, wl.block_tokens, out=out, rope=rope,
+                                         state_out=st, stream=stream)
+    graph.replay()
+    torch.cuda.synchronize(cuda_device)
+    assert sla.last_device_status(device=cuda_device) == 0
+    assert torch.equal(out, ref) and torch.equal(st, st_ref)
+
+
+def test_noalloc_replays_in_a_graph(cuda_device):
+    sla = _sla()
+    lib = sla.raw_lib()
+    wl = Workload("graphna", B=1, H=2, grid=(2, 9, 11), rope=False)
+    q, k, v, g = (t.to(cuda_device) for t in make_inputs(wl, seed=33))
+    ref = sla.linattn_forward(q, k, v, g)
+    out = torch.full_like(q, float("nan"))
+    status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    B, H, N, d = q.shape
+    stream = torch.cuda.Stream(cuda_device)
+    # the device address of the scratch array is looked up once per device, outside capture
+    with torch.cuda.device(cuda_device):
+        rc = lib.sla_linattn_forward_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                             g.data_ptr(), out.data_ptr(), B, H, N, d, None,
+                                             1e-6, status.data_ptr(), stream.cuda_stream)
+    assert rc == sla.OK
+    stream.synchronize()
+    out.fill_(float("nan"))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        rc = lib.sla_linattn_forward_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                             g.data_ptr(), out.data_ptr(), B, H, N, d, None,
+                                             1e-6, status.data_ptr(), stream.cuda_stream)
+    assert rc == sla.OK
+    graph.replay()
+    torch.cuda.synchronize(cuda_device)
+    assert int(status.item()) == 0
+    assert torch.equal(out, ref)
