@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip timing the oracle on the host")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "backward"],
+                    help="time the layer's forward (the headline) or its backward")
     ap.add_argument("--forward-kernel", default="auto", choices=["auto", "fused", "split"],
                     help="launch plan of the bf16 forward (SLA_FORWARD_KERNEL)")
     return ap.parse_args()
@@ -481,13 +483,126 @@ def run_sla(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+BWD_METRIC = "linear-attn bwd token-heads/s; HBM GB/s as % of B300 peak"
+
+
+def oracle_backward_heads(wl, tensors, heads):
+    """The fp64 backward oracle on the given heads at full N; returns elapsed seconds."""
+    import oracle.backward as ob   # the CPU baseline of the backward line
+    import oracle.linattn as ol
+    spec = ol.RopeSpec(*wl.grid, *wl.split, base=wl.base) if wl.rope else None
+    t0 = time.perf_counter()
+    for b, h in heads:
+        ang = ol.rope3d_angles(spec) if spec is not None else None
+        ob.linattn_head_backward(*(x[b, h].double().numpy() for x in tensors), wl.eps, ang)
+    return time.perf_counter() - t0
+
+
+def run_backward(args, rank, world, local):
+    """The layer's backward: dq, dk, dv, dg from q, k, v, g and the upstream gradient."""
+    from gated_linear_attention_attn_b300 import sla
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    wl = WORKLOADS[args.workload]
+    if wl.block_frames:
+        raise SystemExit("the backward is timed on the bidirectional workloads")
+    host = make_inputs(wl, seed=0)
+    gen = torch.Generator().manual_seed(1000)
+    host = host + (torch.randn(host[0].shape, generator=gen).to(wl.dtype),)
+    q, k, v, g, dout = (t.to(dev) for t in host)
+    rope = sla.RopeTable(wl.grid, wl.split, wl.base, device=dev) if wl.rope else None
+    grads = tuple(torch.empty_like(q) for _ in range(4))
+    stream = torch.cuda.current_stream(dev)
+    alg = 9 * wl.B * wl.H * wl.N * wl.d * wl.elem_size      # 5 tensors read, 4 written
+    scrub = None
+    if alg < 4 * L2_BYTES:
+        scrub_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+
+        def scrub():
+            scrub_buf.fill_(1)
+
+    def step():
+        sla.linattn_backward(q, k, v, g, dout, rope=rope, eps=wl.eps, grads=grads, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    if sla.last_device_status(stream, dev) != sla.OK:
+        raise RuntimeError("device status after warm-up")
+    _barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(dev)
+    sampler.start()
+    secs = _time_steps(step, args.steps, stream, scrub)
+    clocks = sampler.stop()
+    torch.cuda.synchronize(dev)
+    _barrier(world)
+    secs = _max_over_ranks(secs, world, dev)
+    per_step = secs / args.steps
+    e2e = None
+    if not args.no_e2e:
+        hin = tuple(t.pin_memory() for t in host)
+        hout = tuple(torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in range(4))
+
+        def e2e_step():
+            for dst, src in zip((q, k, v, g, dout), hin):
+                dst.copy_(src, non_blocking=True)
+            step()
+            for dst, src in zip(hout, grads):
+                dst.copy_(src, non_blocking=True)
+
+        e2e_step()
+        ke = max(3, min(args.steps, 10))
+        esecs = _max_over_ranks(_time_steps(e2e_step, ke, stream), world, dev)
+        e2e = {"value": world * wl.token_heads * ke / esecs, "unit": UNIT,
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout),
+               "steps": ke, "ms_per_step": 1e3 * esecs / ke}
+    if rank != 0:
+        return
+    peak, peak_src = measured_peaks()
+    achieved = alg / per_step / 1e9
+    line = {
+        "metric": BWD_METRIC, "value": world * wl.token_heads / per_step, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": 1e3 * per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if wl.dtype == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded N(0,1) q,k,v,g and upstream gradient on the latent token grid)",
+        "config": _config(wl, world, plan="backward: state partials, query pass, key pass (fp32 "
+                                          "FMA kernels)"),
+        "roofline": {"bound": "hbm", "kernel": "backward (3 launches)", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_src} copy bandwidth",
+                     "algorithmic_bytes_per_launch": alg, "traffic": None},
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        heads = [(b, h) for b in range(wl.B) for h in range(wl.H)]
+        done, elapsed = 0, 0.0
+        while elapsed < 10.0 and done < 4 * len(heads):
+            elapsed += oracle_backward_heads(wl, host, [heads[done % len(heads)]])
+            done += 1
+        line["cpu_baseline"] = {"value": done * wl.N / elapsed, "unit": UNIT,
+                                "cores": _blas_threads(), "kind": "oracle",
+                                "sample": f"{done} heads of {wl.name} at full N (fp64 numpy "
+                                          f"backward, {elapsed:.1f} s)"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
-    run_sla(args, rank, world, local)
+    if args.pass_ == "backward":
+        run_backward(args, rank, world, local)
+    else:
+        run_sla(args, rank, world, local)
     if world > 1:
         torch.distributed.destroy_process_group()
 

@@ -236,6 +236,79 @@ sla_status_t sla_linattn_forward_f32(const float* q, const float* k, const float
     return forward(q, k, v, g, out, B, H, N, d, rope_table, eps, stream, true);
 }
 
+// Shared body of both backward entry points.
+static sla_status_t backward(const void* q, const void* k, const void* v, const void* g,
+                             const void* dout, void* dq, void* dk, void* dv, void* dg, int B,
+                             int H, int N, int d, const sla_rope_table_t* rope, float eps,
+                             sla_stream_t stream, bool is_f32) {
+    if (!q || !k || !v || !g || !dout || !dq || !dk || !dv || !dg) return SLA_ERR_INVALID_ARG;
+    sla_status_t st = check_dims(B, H, N, d);
+    if (st == SLA_ERR_INVALID_ARG) return st;
+    if (bad_eps(eps)) return SLA_ERR_INVALID_ARG;
+    if (st != SLA_OK) return st;
+    const size_t bytes = (size_t)B * H * N * d * (is_f32 ? 4 : 2);
+    const void* ins[5] = {q, k, v, g, dout};
+    const size_t sizes[5] = {bytes, bytes, bytes, bytes, bytes};
+    void* outs[4] = {dq, dk, dv, dg};
+    for (int i = 0; i < 4; ++i)
+        if ((st = check_buffers(ins, sizes, 5, outs[i], bytes)) != SLA_OK) return st;
+    for (int i = 0; i < 4; ++i)                      // the gradients overlap one another neither
+        for (int j = i + 1; j < 4; ++j) {
+            const uintptr_t x = reinterpret_cast<uintptr_t>(outs[i]);
+            const uintptr_t y = reinterpret_cast<uintptr_t>(outs[j]);
+            if (x < y + bytes && y < x + bytes) return SLA_ERR_INVALID_ARG;
+        }
+    RopeView rv{};
+    if ((st = check_rope(rope, N, d, &rv)) != SLA_OK) return st;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SLA_ERR_CUDA;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* ds = nullptr;
+    if ((st = device_state(dev, &ds)) != SLA_OK) return st;
+    // one CTA per SM (a CTA holds S and S^T): chunks for whole waves of two CTAs
+    // per SM at most, at least four 32-token tiles each
+    const int tiles = (N + 31) / 32;
+    int C = 2 * ds->num_sms / (B * H);
+    if (C > (tiles + 3) / 4) C = (tiles + 3) / 4;
+    if (C < 1) C = 1;
+    void* ws = nullptr;
+    const size_t ws_bytes = is_f32 ? backward_workspace_bytes(B * H, C)
+                                   : backward_bf16_workspace_bytes(B * H, N, C, ds->num_sms);
+    if ((st = workspace(dev, s, ws_bytes, &ws)) != SLA_OK) return st;
+    const RopeView* rp = rope ? &rv : nullptr;
+    const cudaError_t err =
+        is_f32 ? launch_backward_f32((const float*)q, (const float*)k, (const float*)v,
+                                     (const float*)g, (const float*)dout, (float*)dq, (float*)dk,
+                                     (float*)dv, (float*)dg, B, H, N, rp, eps, (float*)ws, C, s)
+               : launch_backward_bf16(q, k, v, g, dout, dq, dk, dv, dg, B, H, N, rp, eps,
+                                      (float*)ws, C, ds->num_sms, ds->status, s);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return SLA_ERR_CUDA;
+    }
+    return SLA_OK;
+}
+
+sla_status_t sla_linattn_backward(const void* q, const void* k, const void* v, const void* g,
+                                  const void* dout, void* dq, void* dk, void* dv, void* dg,
+                                  int B, int H, int N, int d,
+                                  const sla_rope_table_t* rope_table, float eps,
+                                  sla_stream_t stream) {
+    return backward(q, k, v, g, dout, dq, dk, dv, dg, B, H, N, d, rope_table, eps, stream, false);
+}
+
+sla_status_t sla_linattn_backward_f32(const float* q, const float* k, const float* v,
+                                      const float* g, const float* dout, float* dq, float* dk,
+                                      float* dv, float* dg, int B, int H, int N, int d,
+                                      const sla_rope_table_t* rope_table, float eps,
+                                      sla_stream_t stream) {
+    return backward(q, k, v, g, dout, dq, dk, dv, dg, B, H, N, d, rope_table, eps, stream, true);
+}
+
 size_t sla_linattn_carried_state_bytes(int B, int H, int d) {
     if (B < 1 || H < 1 || d != kHeadDim) return 0;
     return (size_t)B * H * (kHeadDim * kHeadDim + kHeadDim) * sizeof(float);

@@ -24,6 +24,30 @@ cudaError_t launch_simt_bf16(const void* q, const void* k, const void* v, const 
                              void* out, int B, int H, int N, const RopeView* rope, float eps,
                              float* workspace, int C, cudaStream_t stream);
 
+// The fp32 SIMT state partials (S_c in [m][n] order, then z_c) of C chunks
+// per head, as simt_state_kernel writes them (simt.cu).
+cudaError_t launch_simt_state_partials(const float* k, const float* v, int B, int H, int N,
+                                       const RopeView* rope, float* partial, int C,
+                                       cudaStream_t stream);
+cudaError_t launch_simt_state_partials(const __nv_bfloat16* k, const __nv_bfloat16* v, int B,
+                                       int H, int N, const RopeView* rope, float* partial, int C,
+                                       cudaStream_t stream);
+
+// Backward (backward.cu): dq, dk, dv, dg of L = sum(dout * o), in three
+// launches over C chunks per head; workspace backward_workspace_bytes(BH, C).
+// The bf16 backward takes the state from the tensor-core state kernel and
+// needs backward_bf16_workspace_bytes.
+size_t backward_workspace_bytes(int BH, int C);
+size_t backward_bf16_workspace_bytes(int BH, int N, int C, int num_sms);
+cudaError_t launch_backward_bf16(const void* q, const void* k, const void* v, const void* g,
+                                 const void* dout, void* dq, void* dk, void* dv, void* dg, int B,
+                                 int H, int N, const RopeView* rope, float eps, float* workspace,
+                                 int C, int num_sms, unsigned* status, cudaStream_t stream);
+cudaError_t launch_backward_f32(const float* q, const float* k, const float* v, const float* g,
+                                const float* dout, float* dq, float* dk, float* dv, float* dg,
+                                int B, int H, int N, const RopeView* rope, float eps,
+                                float* workspace, int C, cudaStream_t stream);
+
 // bf16 path on tcgen05 (tc_forward.cu).  The whole forward needs
 // tc_workspace_bytes of workspace (counters, partial states, the heads'
 // states); the state phase alone needs tc_state_workspace_bytes and writes

@@ -227,6 +227,33 @@ static cudaError_t launch_simt(const T* q, const T* k, const T* v, const T* g, T
     return cudaGetLastError();
 }
 
+template <typename T>
+static cudaError_t launch_state_partials(const T* k, const T* v, int B, int H, int N,
+                                         const RopeView* rope, float* partial, int C,
+                                         cudaStream_t stream) {
+    const int tiles = (N + kSimtTile - 1) / kSimtTile;
+    const int chunk = ((tiles + C - 1) / C) * kSimtTile;
+    const RopeView rv = rope ? *rope : RopeView{};
+    const dim3 gs(C, B * H);
+    if (rope)
+        simt_state_kernel<T, true><<<gs, 256, 0, stream>>>(k, v, N, C, chunk, rv, partial);
+    else
+        simt_state_kernel<T, false><<<gs, 256, 0, stream>>>(k, v, N, C, chunk, rv, partial);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_simt_state_partials(const float* k, const float* v, int B, int H, int N,
+                                       const RopeView* rope, float* partial, int C,
+                                       cudaStream_t stream) {
+    return launch_state_partials<float>(k, v, B, H, N, rope, partial, C, stream);
+}
+
+cudaError_t launch_simt_state_partials(const __nv_bfloat16* k, const __nv_bfloat16* v, int B,
+                                       int H, int N, const RopeView* rope, float* partial, int C,
+                                       cudaStream_t stream) {
+    return launch_state_partials<__nv_bfloat16>(k, v, B, H, N, rope, partial, C, stream);
+}
+
 cudaError_t launch_simt_f32(const float* q, const float* k, const float* v, const float* g,
                             float* out, int B, int H, int N, const RopeView* rope, float eps,
                             float* workspace, int C, cudaStream_t stream) {

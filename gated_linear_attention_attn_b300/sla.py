@@ -58,6 +58,10 @@ _lib.sla_linattn_forward_block_causal.argtypes = ([_vp] * 5 + [_int] * 5 +
                                                   [ctypes.POINTER(RopeTableC), _int, _flt,
                                                    _vp, _vp, _vp])
 _lib.sla_linattn_forward_block_causal.restype = _int
+_BWD_ARGS = [_vp] * 9 + [_int] * 4 + [ctypes.POINTER(RopeTableC), _flt, _vp]
+for _name in ("sla_linattn_backward", "sla_linattn_backward_f32"):
+    getattr(_lib, _name).argtypes = _BWD_ARGS
+    getattr(_lib, _name).restype = _int
 _lib.sla_linattn_forward_cluster.argtypes = [_int] * 5
 _lib.sla_linattn_forward_cluster.restype = _int
 _lib.sla_status_string.argtypes = [_int]
@@ -69,6 +73,7 @@ EXPORTED = ("sla_rope_table_floats", "sla_rope_table_fill", "sla_linattn_forward
             "sla_linattn_forward_f32", "sla_linattn_state_bytes", "sla_linattn_state",
             "sla_linattn_apply", "sla_linattn_forward_noalloc", "sla_linattn_forward_cluster",
             "sla_linattn_carried_state_bytes", "sla_linattn_forward_block_causal",
+            "sla_linattn_backward", "sla_linattn_backward_f32",
             "sla_status_string", "sla_last_device_status")
 
 
@@ -249,6 +254,41 @@ def last_device_status(stream: Optional[torch.cuda.Stream] = None, device="cuda"
     dev = torch.device(device)
     with torch.cuda.device(dev):
         return _lib.sla_last_device_status(_stream_handle(stream, dev))
+
+
+def linattn_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                     dout: torch.Tensor, rope: Optional[RopeTable] = None, eps: float = 1e-6,
+                     grads: Optional[Sequence[torch.Tensor]] = None,
+                     stream: Optional[torch.cuda.Stream] = None):
+    """(dq, dk, dv, dg) of sum(dout * o) for [B, H, N, d] CUDA tensors (bf16 or fp32;
+    ``sla_linattn_backward`` / ``sla_linattn_backward_f32``).  grads: four output
+    tensors to fill, else new ones."""
+    for name, t in (("k", k), ("v", v), ("g", g), ("dout", dout)):
+        if t.shape != q.shape or t.dtype != q.dtype or t.device != q.device \
+                or not t.is_contiguous():
+            raise SlaError(INVALID_ARG, f"linattn_backward: {name} differs from q")
+    if q.dim() != 4 or not q.is_contiguous() or q.device.type != "cuda":
+        raise SlaError(INVALID_ARG, "linattn_backward: q must be a contiguous [B, H, N, d] "
+                                    "CUDA tensor")
+    if q.dtype == torch.bfloat16:
+        fn = _lib.sla_linattn_backward
+    elif q.dtype == torch.float32:
+        fn = _lib.sla_linattn_backward_f32
+    else:
+        raise SlaError(UNSUPPORTED, f"linattn_backward: dtype {q.dtype}")
+    if grads is None:
+        grads = tuple(torch.empty_like(q) for _ in range(4))
+    for t in grads:
+        if t.shape != q.shape or t.dtype != q.dtype or t.device != q.device \
+                or not t.is_contiguous():
+            raise SlaError(INVALID_ARG, "linattn_backward: gradient tensors must match q")
+    B, H, N, d = q.shape
+    rope_c = ctypes.byref(rope.c_struct()) if rope is not None else None
+    with torch.cuda.device(q.device):
+        _check(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(), dout.data_ptr(),
+                  *(t.data_ptr() for t in grads), B, H, N, d, rope_c, float(eps),
+                  _stream_handle(stream, q.device)), fn.__name__)
+    return tuple(grads)
 
 
 CARRIED_FLOATS = HEAD_DIM * HEAD_DIM + HEAD_DIM

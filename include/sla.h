@@ -221,6 +221,40 @@ sla_status_t sla_linattn_forward_block_causal(const void* q, const void* k, cons
                                               float* state_out, sla_stream_t stream);
 
 /*
+ * Backward of the layer: the gradients of L = sum(dout * o) for the o of
+ * sla_linattn_forward (bf16, fp32 arithmetic) or sla_linattn_forward_f32
+ * (fp32), as the models of "SANA-Video 2.0" (NVlabs/Sana
+ * docs/sana_video2.md, section "Training") are trained through the layer.
+ * With num_i = (R_i phi(q_i))^T S, den_i = phi(q_i) . z + eps,
+ * s_i = sigmoid(g_i):
+ *
+ *     a_i    = dout_i * s_i / den_i,    dg_i = dout_i * num_i / den_i * s_i (1 - s_i)
+ *     dden_i = -(a_i . num_i) / den_i
+ *     dS = sum_i (R_i phi(q_i)) a_i^T,  dz = sum_i dden_i phi(q_i)
+ *     dq_i = [q_i > 0] (R_i^T (S a_i) + dden_i z)
+ *     dk_j = [k_j > 0] (R_j^T (dS v_j) + dz),   dv_j = dS^T R_j phi(k_j)
+ *
+ * (the ReLU derivative at 0 is 0).  q, k, v, g, dout: inputs as for the
+ * forward; dq, dk, dv, dg: outputs of the same shape, layout and type, none
+ * overlapping an input or another output.  rope_table and eps as for the
+ * forward.  The state S, z is recomputed from k and v: on the tensor cores
+ * for bf16 (S rounded to bf16, as the forward uses it), in fp32 for fp32;
+ * everything else runs on the fp32 FMA units.  Uses the library's
+ * per-stream workspace (2 * 66 KB per chunk of every head, plus the state
+ * kernel's for bf16).
+ */
+sla_status_t sla_linattn_backward(const void* q, const void* k, const void* v, const void* g,
+                                  const void* dout, void* dq, void* dk, void* dv, void* dg,
+                                  int B, int H, int N, int d,
+                                  const sla_rope_table_t* rope_table, float eps,
+                                  sla_stream_t stream);
+sla_status_t sla_linattn_backward_f32(const float* q, const float* k, const float* v,
+                                      const float* g, const float* dout, float* dq, float* dk,
+                                      float* dv, float* dg, int B, int H, int N, int d,
+                                      const sla_rope_table_t* rope_table, float eps,
+                                      sla_stream_t stream);
+
+/*
  * The bf16 forward of sla_linattn_forward for callers that cannot allocate
  * device memory.  No page has a counterpart: this entry point exists for
  * library users, not for the method.  Some callers must not see a library

@@ -196,3 +196,27 @@ def test_block_causal_rejects_bad_arguments_before_cuda():
     ]
     for kw, want in bad:
         assert _bc(**kw) == want, kw
+
+
+def test_backward_rejects_bad_arguments_before_cuda():
+    lib = sla.raw_lib()
+
+    def bwd(q=A, k=A + STEP, v=A + 2 * STEP, g=A + 3 * STEP, do=A + 4 * STEP, dq=A + 5 * STEP,
+            dk=A + 6 * STEP, dv=A + 7 * STEP, dg=A + 8 * STEP, N=256, d=128, eps=1e-6, f32=False):
+        fn = lib.sla_linattn_backward_f32 if f32 else lib.sla_linattn_backward
+        return fn(q, k, v, g, do, dq, dk, dv, dg, 1, 2, N, d, None, eps, None)
+
+    bad = [
+        (dict(do=0), sla.INVALID_ARG),
+        (dict(dg=0), sla.INVALID_ARG),
+        (dict(N=0), sla.INVALID_ARG),
+        (dict(eps=-1.0), sla.INVALID_ARG),
+        (dict(d=64), sla.UNSUPPORTED),
+        (dict(dk=A + 6 * STEP + 4), sla.ALIGNMENT),
+        (dict(dq=A + 2 * STEP), sla.INVALID_ARG),             # dq is v
+        (dict(dv=A + 5 * STEP + 4096), sla.INVALID_ARG),      # dv overlaps dq
+        (dict(dg=A + 4 * STEP + 64), sla.INVALID_ARG),        # dg overlaps dout
+    ]
+    for f32 in (False, True):
+        for kw, want in bad:
+            assert bwd(f32=f32, **kw) == want, (f32, kw)
