@@ -165,16 +165,6 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
     return d;
 }
 
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
-    float2 d;
-    asm("{\n\t.reg .b64 pa, pb, pd;\n\t"
-        "mov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
-        "add.rn.f32x2 pd, pa, pb;\n\tmov.b64 {%0, %1}, pd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
-
 // ------------------------------------------------------------------ TMA ----
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
@@ -225,10 +215,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-__device__ __forceinline__ void bulk_wait_read_all() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 // Waits until at most one committed bulk group still reads shared memory.
@@ -423,21 +409,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
            | ((b_mn_major ? 1u : 0u) << 16)     // B major-ness
            | ((uint32_t)(N >> 3) << 17)         // N / 8
            | ((uint32_t)(M >> 4) << 24);        // M / 16
-}
-
-__device__ __forceinline__ uint32_t elect_one_sync() {
-    uint32_t pred = 0;
-    asm volatile(
-        "{\n\t.reg .b32 rx;\n\t.reg .pred px;\n\t"
-        "elect.sync rx|px, %1;\n\t"
-        "selp.b32 %0, 1, 0, px;\n\t}"
-        : "=r"(pred)
-        : "r"(0xffffffffu));
-    return pred;
-}
-
-__device__ __forceinline__ void named_bar_sync(int id, int threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
