@@ -58,6 +58,9 @@ SMALL = [
     (2, 2, (10, 10, 10), torch.bfloat16, True),
     (1, 2, (11, 15, 26), torch.bfloat16, False),
     (4, 16, (1, 1, 3), torch.bfloat16, True),
+    (8, 32, (1, 1, 40), torch.bfloat16, False),     # 256 heads: more heads than SMs
+    (2, 3, (1, 1, 1), torch.bfloat16, True),         # one token per head
+    (1, 1, (2, 33, 31), torch.bfloat16, True),       # one head, 16 tiles and a ragged tail
     (1, 1, (5, 7, 9), torch.float32, True),
     (2, 3, (1, 1, 129), torch.float32, False),
     (1, 2, (4, 8, 8), torch.float32, True),
