@@ -564,20 +564,27 @@ def run_backward(args, rank, world, local):
         return
     peak, peak_src = measured_peaks()
     achieved = alg / per_step / 1e9
+    if wl.dtype == torch.bfloat16:
+        launches = 9
+        plan = ("backward: state(k, v), apply raw(q), terms, state(q, a; dden), apply(a; S), "
+                "dq, apply(v; dS), dk, apply(k; dS) (tcgen05 state/apply kernels + elementwise)")
+    else:
+        launches = 3
+        plan = "backward: state partials, query pass, key pass (fp32 FMA kernels)"
     line = {
         "metric": BWD_METRIC, "value": world * wl.token_heads / per_step, "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
         "ms_per_step": 1e3 * per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if wl.dtype == torch.bfloat16 else "f32",
         "data": "synthetic (seeded N(0,1) q,k,v,g and upstream gradient on the latent token grid)",
-        "config": _config(wl, world, plan="backward: state partials, query pass, key pass (fp32 "
-                                          "FMA kernels)"),
-        "roofline": {"bound": "hbm", "kernel": "backward (3 launches)", "achieved": achieved,
+        "config": _config(wl, world, plan=plan),
+        "roofline": {"bound": "hbm", "kernel": f"backward ({launches} launches)",
+                     "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_src} copy bandwidth",
                      "algorithmic_bytes_per_launch": alg, "traffic": None},
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": launches * args.steps,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline:

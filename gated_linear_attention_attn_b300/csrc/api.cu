@@ -269,15 +269,15 @@ static sla_status_t backward(const void* q, const void* k, const void* v, const 
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceState* ds = nullptr;
     if ((st = device_state(dev, &ds)) != SLA_OK) return st;
-    // one CTA per SM (a CTA holds S and S^T): chunks for whole waves of two CTAs
-    // per SM at most, at least four 32-token tiles each
+    // fp32: one CTA per SM (a CTA holds S and S^T): chunks for whole waves of
+    // two CTAs per SM at most, at least four 32-token tiles each
     const int tiles = (N + 31) / 32;
     int C = 2 * ds->num_sms / (B * H);
     if (C > (tiles + 3) / 4) C = (tiles + 3) / 4;
     if (C < 1) C = 1;
     void* ws = nullptr;
     const size_t ws_bytes = is_f32 ? backward_workspace_bytes(B * H, C)
-                                   : backward_bf16_workspace_bytes(B * H, N, C, ds->num_sms);
+                                   : backward_bf16_workspace_bytes(B * H, N, ds->num_sms);
     if ((st = workspace(dev, s, ws_bytes, &ws)) != SLA_OK) return st;
     const RopeView* rp = rope ? &rv : nullptr;
     const cudaError_t err =
@@ -285,7 +285,7 @@ static sla_status_t backward(const void* q, const void* k, const void* v, const 
                                      (const float*)g, (const float*)dout, (float*)dq, (float*)dk,
                                      (float*)dv, (float*)dg, B, H, N, rp, eps, (float*)ws, C, s)
                : launch_backward_bf16(q, k, v, g, dout, dq, dk, dv, dg, B, H, N, rp, eps,
-                                      (float*)ws, C, ds->num_sms, ds->status, s);
+                                      (float*)ws, ds->num_sms, ds->status, s);
     if (err != cudaSuccess) {
         cudaGetLastError();
         return SLA_ERR_CUDA;

@@ -1,4 +1,4 @@
-// Backward of the gated linear-attention layer: plain SIMT FFMA kernels.
+// Backward of the gated linear-attention layer.
 //
 // For one head, with num_i = qr_i^T S, den_i = phi(q_i) . z + eps and
 // s_i = sigmoid(g_i), the gradients of L = sum(dO * o) are
@@ -9,14 +9,22 @@
 //     dq_i   = [q_i > 0] (R_i^T (S a_i) + dden_i z)
 //     dk_j   = [k_j > 0] (R_j^T (dS v_j) + dz)    dv_j = dS^T kr_j
 //
-// in three launches, each over (chunk of tokens, head):
-//   1. the heads' S, z: the tensor-core state kernel for bf16 inputs, the fp32
-//      partials S_c, z_c of simt_state_kernel for fp32 inputs;
-//   2. bwd_query_kernel: sums the head's S, z; per 32-token tile of queries
-//      forms num, a, dg, dden, dq and adds the tile to the chunk's dS, dz;
-//   3. bwd_key_kernel: sums the head's dS, dz; per 32-token tile of keys
-//      forms dk and dv.
-// The arithmetic is fp32 throughout (inputs bf16 or fp32).
+// bf16 inputs: the contractions run on the tensor cores through the state and
+// apply kernels, glued by three elementwise kernels:
+//   1. state(k, v)                  S (bf16, as the forward uses it), z
+//   2. apply, raw(q; S)             num
+//   3. bwd_terms_kernel             a, dg, dden
+//   4. state(q, a; weights dden)    dS, dz
+//   5. apply, raw MN(a; S)          S a
+//   6. bwd_grad_kernel              dq
+//   7. apply, raw MN(v; dS)         dS v
+//   8. bwd_grad_kernel              dk
+//   9. apply, raw(k; dS)            dv = dS^T kr
+// fp32 inputs: fp32 FMA kernels in three launches, each over (chunk of tokens,
+// head): the state partials (simt_state_kernel); bwd_query_kernel (num, a, dg,
+// dden, dq and the chunk's dS, dz); bwd_key_kernel (dk, dv).
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -26,17 +34,12 @@ namespace {
 constexpr int kBTile = 32;                          // tokens per tile
 constexpr int kBThreads = 256;
 constexpr int kBPartial = kHeadDim * kHeadDim + kHeadDim;
-constexpr int kTcStateBytes = kHeadDim * kHeadDim * 2 + kHeadDim * 4;   // bf16 S^T, then z
 // S, S^T, z, then three [32][128] tiles and two [32] vectors
 constexpr size_t kBSmem =
     (2 * kHeadDim * kHeadDim + kHeadDim + 3 * kBTile * kHeadDim + 2 * kBTile) * sizeof(float);
 
 __device__ __forceinline__ float ld_elem(const float* p) { return __ldg(p); }
-__device__ __forceinline__ float ld_elem(const __nv_bfloat16* p) {
-    return __bfloat162float(__ldg(p));
-}
 __device__ __forceinline__ void st_elem(float* p, float x) { *p = x; }
-__device__ __forceinline__ void st_elem(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 
 // Sums the C partials (chunk order) of a head into M ([m][n]), Mt ([n][m])
 // and the vector part into vec, four elements per thread at a time so that
@@ -65,30 +68,6 @@ __device__ void sum_partials(const float* src, int C, float* M, float* Mt, float
             }
         }
     }
-}
-
-// A head's state as the tensor-core state kernel writes it (S^T in bf16,
-// two 64-column halves of 128 rows of 128 bytes, 16-byte chunk c of row n at
-// chunk position (c mod 8) xor (n mod 8); then z in fp32), into M = S
-// ([m][n]), Mt = S^T and vec = z.
-__device__ void load_tc_state(const uint8_t* st, float* M, float* Mt, float* vec) {
-    for (int t = threadIdx.x; t < kHeadDim * 16; t += blockDim.x) {
-        const int n = t >> 4, c = t & 15;
-        const uint4 w = *reinterpret_cast<const uint4*>(
-            st + (c >> 3) * (kHeadDim * 64 * 2) + n * 128 + (((c & 7) ^ (n & 7)) << 4));
-        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = bf2_to_f2(u[i]);
-            const int m = 8 * c + 2 * i;
-            Mt[n * kHeadDim + m] = f.x;
-            Mt[n * kHeadDim + m + 1] = f.y;
-            M[m * kHeadDim + n] = f.x;
-            M[(m + 1) * kHeadDim + n] = f.y;
-        }
-    }
-    for (int m = threadIdx.x; m < kHeadDim; m += blockDim.x)
-        vec[m] = reinterpret_cast<const float*>(st + kHeadDim * kHeadDim * 2)[m];
 }
 
 // Loads rows [base, base + cnt) of a head into fp (ReLU) and fr (ReLU, then
@@ -163,8 +142,8 @@ template <typename T, bool ROPE>
 __global__ void __launch_bounds__(kBThreads)
 bwd_query_kernel(const T* __restrict__ q, const T* __restrict__ g, const T* __restrict__ dout,
                  T* __restrict__ dq, T* __restrict__ dg, int N, int C, int chunk,
-                 const float* __restrict__ state_partial, const uint8_t* __restrict__ tc_state,
-                 float* __restrict__ grad_partial, float eps, RopeView rope) {
+                 const float* __restrict__ state_partial, float* __restrict__ grad_partial,
+                 float eps, RopeView rope) {
     extern __shared__ float sm[];
     float* S = sm;                                   // [m][n]
     float* St = S + kHeadDim * kHeadDim;             // [n][m]
@@ -177,12 +156,8 @@ bwd_query_kernel(const T* __restrict__ q, const T* __restrict__ g, const T* __re
     const int bh = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
     const int ty = tid / 16, tx = tid % 16;
     const size_t head = (size_t)bh * N * kHeadDim;
-    // the head's S, z: from the tensor-core state kernel (bf16 inputs), else
-    // summed from the fp32 partials
-    if (tc_state)
-        load_tc_state(tc_state + (size_t)bh * kTcStateBytes, S, St, z);
-    else
-        sum_partials(state_partial + (size_t)bh * C * kBPartial, C, S, St, z);
+    // the head's S, z, summed from the fp32 partials
+    sum_partials(state_partial + (size_t)bh * C * kBPartial, C, S, St, z);
 
     float acc[8][8];                          // dS rows 8 ty.., columns col_of(tx, ..)
 #pragma unroll
@@ -332,13 +307,116 @@ bwd_key_kernel(const T* __restrict__ k, const T* __restrict__ v, T* __restrict__
     }
 }
 
-// tc_state: the heads' states written by the tensor-core state kernel (bf16
-// inputs), or null to sum fp32 SIMT partials from workspace (fp32 inputs).
+// ------------------------------------------------ bf16, on the tensor cores
+
+constexpr int kStateBytesB = kHeadDim * kHeadDim * 2 + kHeadDim * 4;   // bf16 S^T, then z
+constexpr int kRowsPerBlock = 16;                 // 16 threads (8 dims each) per row
+
+__device__ __forceinline__ void bf8_to_f8(uint4 u, float (&f)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 t = bf2_to_f2(w[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
+__device__ __forceinline__ uint4 f8_to_bf8(const float (&f)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[i] = f2_to_bf2(f[2 * i], f[2 * i + 1]);
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Sum over the 16 lanes of a row (lanes 16 (lane / 16) .. + 15 of the warp).
+__device__ __forceinline__ float row_sum16(float x) {
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
+// a = dO s / den, dg = dO num / den s (1 - s), dden = -(a . num) / den, with
+// den = phi(q) . z + eps and z from the head's state; thread (row, c) holds
+// dims 8c .. 8c + 7 of one row.
+__global__ void __launch_bounds__(256)
+bwd_terms_kernel(const uint4* __restrict__ q, const uint4* __restrict__ g,
+                 const uint4* __restrict__ dout, const uint4* __restrict__ num,
+                 const uint8_t* __restrict__ states, int N, long long rows, float eps,
+                 uint4* __restrict__ a, uint4* __restrict__ dg, float* __restrict__ dden) {
+    const long long row = (long long)blockIdx.x * kRowsPerBlock + threadIdx.x / 16;
+    const int c = threadIdx.x % 16;
+    const bool live = row < rows;
+    const size_t at = (size_t)(live ? row : 0) * 16 + c;
+    float qf[8], gf[8], df[8], nf[8], zf[8];
+    bf8_to_f8(q[at], qf);
+    bf8_to_f8(g[at], gf);
+    bf8_to_f8(dout[at], df);
+    bf8_to_f8(num[at], nf);
+    const float* z = reinterpret_cast<const float*>(
+        states + (size_t)((live ? row : 0) / N) * kStateBytesB + kHeadDim * kHeadDim * 2);
+    const float4 z0 = *reinterpret_cast<const float4*>(z + 8 * c);
+    const float4 z1 = *reinterpret_cast<const float4*>(z + 8 * c + 4);
+    zf[0] = z0.x; zf[1] = z0.y; zf[2] = z0.z; zf[3] = z0.w;
+    zf[4] = z1.x; zf[5] = z1.y; zf[6] = z1.z; zf[7] = z1.w;
+    float d = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) d = fmaf(fmaxf(qf[j], 0.f), zf[j], d);
+    const float den = row_sum16(d) + eps, inv = 1.f / den;
+    float af[8], gg[8], part = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float s = 1.f / (1.f + expf(-gf[j]));
+        af[j] = df[j] * s * inv;
+        gg[j] = df[j] * nf[j] * inv * s * (1.f - s);
+        part = fmaf(af[j], nf[j], part);
+    }
+    const float dd = -row_sum16(part) * inv;
+    if (live) {
+        a[at] = f8_to_bf8(af);
+        dg[at] = f8_to_bf8(gg);
+        if (c == 0) dden[row] = dd;
+    }
+}
+
+// out = [x > 0] (R^T y + w z) per row, with w = weight[row] (1 without
+// weights) and z from the head's state: dq from S a, dk from dS v.
+template <bool ROPE>
+__global__ void __launch_bounds__(256)
+bwd_grad_kernel(const uint4* __restrict__ x, const uint4* __restrict__ y,
+                const float* __restrict__ weight, const uint8_t* __restrict__ states, int N,
+                long long rows, RopeView rope, uint4* __restrict__ out) {
+    const long long row = (long long)blockIdx.x * kRowsPerBlock + threadIdx.x / 16;
+    const int c = threadIdx.x % 16;
+    if (row >= rows) return;
+    const size_t at = (size_t)row * 16 + c;
+    float xf[8], yf[8];
+    bf8_to_f8(x[at], xf);
+    bf8_to_f8(y[at], yf);
+    const int n = (int)(row % N);
+    if (ROPE) {
+        // pairs 4c .. 4c + 3 of the token's fp16 (cos, sin) row, turned back
+        const uint4 t = __ldg(reinterpret_cast<const uint4*>(rope.tok + (size_t)n * kPairs) + c);
+        const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const float2 cs = __half22float2(*reinterpret_cast<const __half2*>(&w[p]));
+            rotate_pair(yf[2 * p], yf[2 * p + 1], make_float2(cs.x, -cs.y));
+        }
+    }
+    const float wr = weight ? weight[row] : 1.f;
+    const float* z = reinterpret_cast<const float*>(states + (size_t)(row / N) * kStateBytesB +
+                                                    kHeadDim * kHeadDim * 2) + 8 * c;
+    float of[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) of[j] = xf[j] > 0.f ? fmaf(wr, z[j], yf[j]) : 0.f;
+    out[at] = f8_to_bf8(of);
+}
+
 template <typename T>
 cudaError_t launch_backward(const T* q, const T* k, const T* v, const T* g, const T* dout, T* dq,
                             T* dk, T* dv, T* dg, int B, int H, int N, const RopeView* rope,
-                            float eps, float* workspace, const uint8_t* tc_state, int C,
-                            cudaStream_t stream) {
+                            float eps, float* workspace, int C, cudaStream_t stream) {
     const int BH = B * H;
     const int tiles = (N + kBTile - 1) / kBTile;
     const int chunk = ((tiles + C - 1) / C) * kBTile;
@@ -346,9 +424,8 @@ cudaError_t launch_backward(const T* q, const T* k, const T* v, const T* g, cons
     float* state_partial = workspace;
     float* grad_partial = workspace + (size_t)BH * C * kBPartial;
     cudaError_t e = cudaSuccess;
-    if (!tc_state &&
-        (e = launch_simt_state_partials(k, v, B, H, N, rope, state_partial, C, stream)) !=
-            cudaSuccess)
+    if ((e = launch_simt_state_partials(k, v, B, H, N, rope, state_partial, C, stream)) !=
+        cudaSuccess)
         return e;
     const dim3 grid(C, BH);
     if (rope) {
@@ -357,7 +434,7 @@ cudaError_t launch_backward(const T* q, const T* k, const T* v, const T* g, cons
         cudaFuncSetAttribute(bwd_key_kernel<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kBSmem);
         bwd_query_kernel<T, true><<<grid, kBThreads, kBSmem, stream>>>(
-            q, g, dout, dq, dg, N, C, chunk, state_partial, tc_state, grad_partial, eps, rv);
+            q, g, dout, dq, dg, N, C, chunk, state_partial, grad_partial, eps, rv);
         bwd_key_kernel<T, true><<<grid, kBThreads, kBSmem, stream>>>(k, v, dk, dv, N, C, chunk,
                                                                      grad_partial, rv);
     } else {
@@ -366,7 +443,7 @@ cudaError_t launch_backward(const T* q, const T* k, const T* v, const T* g, cons
         cudaFuncSetAttribute(bwd_key_kernel<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kBSmem);
         bwd_query_kernel<T, false><<<grid, kBThreads, kBSmem, stream>>>(
-            q, g, dout, dq, dg, N, C, chunk, state_partial, tc_state, grad_partial, eps, rv);
+            q, g, dout, dq, dg, N, C, chunk, state_partial, grad_partial, eps, rv);
         bwd_key_kernel<T, false><<<grid, kBThreads, kBSmem, stream>>>(k, v, dk, dv, N, C, chunk,
                                                                       grad_partial, rv);
     }
@@ -379,23 +456,63 @@ size_t backward_workspace_bytes(int BH, int C) {
     return 2 * (size_t)BH * C * kBPartial * sizeof(float);
 }
 
-size_t backward_bf16_workspace_bytes(int BH, int N, int C, int num_sms) {
-    return backward_workspace_bytes(BH, C) + tc_workspace_bytes(BH, N, num_sms);
+size_t backward_bf16_workspace_bytes(int BH, int N, int num_sms) {
+    const size_t tensor = (size_t)BH * N * kHeadDim * 2;
+    return tc_state_workspace_bytes(BH, N, num_sms) + 2 * (size_t)BH * kStateBytesB +
+           2 * tensor + (size_t)BH * N * sizeof(float) + 1024;
 }
 
 cudaError_t launch_backward_bf16(const void* q, const void* k, const void* v, const void* g,
                                  const void* dout, void* dq, void* dk, void* dv, void* dg, int B,
                                  int H, int N, const RopeView* rope, float eps, float* workspace,
-                                 int C, int num_sms, unsigned* status, cudaStream_t stream) {
-    using bf = __nv_bfloat16;
-    // the state on the tensor cores, after the gradient partials in the workspace
-    uint8_t* tail = reinterpret_cast<uint8_t*>(workspace) + backward_workspace_bytes(B * H, C);
-    uint8_t* states = tail + tc_state_workspace_bytes(B * H, N, num_sms);
-    cudaError_t e = launch_tc_state(k, v, states, B, H, N, rope, tail, status, num_sms, stream);
-    if (e != cudaSuccess) return e;
-    return launch_backward<bf>((const bf*)q, (const bf*)k, (const bf*)v, (const bf*)g,
-                               (const bf*)dout, (bf*)dq, (bf*)dk, (bf*)dv, (bf*)dg, B, H, N, rope,
-                               eps, workspace, states, C, stream);
+                                 int num_sms, unsigned* status, cudaStream_t stream) {
+    const int BH = B * H;
+    const long long rows = (long long)BH * N;
+    const size_t tensor = (size_t)rows * kHeadDim * 2;
+    // workspace: the state kernel's, the two states, two [rows][128] bf16
+    // tensors (X: num, then S a, then dS v; A: a), then dden
+    uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+    uint8_t* S = ws + tc_state_workspace_bytes(BH, N, num_sms);
+    uint8_t* dS = S + (size_t)BH * kStateBytesB;
+    uint8_t* X = dS + (size_t)BH * kStateBytesB;
+    uint8_t* A = X + tensor;
+    float* dden = reinterpret_cast<float*>(A + tensor);
+    const unsigned blocks = (unsigned)((rows + kRowsPerBlock - 1) / kRowsPerBlock);
+    const RopeView rv = rope ? *rope : RopeView{};
+    cudaError_t e;
+    if ((e = launch_tc_state(k, v, S, B, H, N, rope, ws, status, num_sms, stream)) != cudaSuccess)
+        return e;
+    if ((e = launch_tc_apply(q, q, S, X, B, H, N, rope, eps, status, num_sms, stream,
+                             kApplyRaw)) != cudaSuccess)
+        return e;
+    bwd_terms_kernel<<<blocks, 256, 0, stream>>>(
+        (const uint4*)q, (const uint4*)g, (const uint4*)dout, (const uint4*)X, S, N, rows, eps,
+        (uint4*)A, (uint4*)dg, dden);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_tc_state(q, A, dS, B, H, N, rope, ws, status, num_sms, stream, dden)) !=
+        cudaSuccess)
+        return e;
+    if ((e = launch_tc_apply(A, A, S, X, B, H, N, nullptr, eps, status, num_sms, stream,
+                             kApplyRawMN)) != cudaSuccess)
+        return e;
+    if (rope)
+        bwd_grad_kernel<true><<<blocks, 256, 0, stream>>>((const uint4*)q, (const uint4*)X, dden,
+                                                          S, N, rows, rv, (uint4*)dq);
+    else
+        bwd_grad_kernel<false><<<blocks, 256, 0, stream>>>((const uint4*)q, (const uint4*)X, dden,
+                                                           S, N, rows, rv, (uint4*)dq);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_tc_apply(v, v, dS, X, B, H, N, nullptr, eps, status, num_sms, stream,
+                             kApplyRawMN)) != cudaSuccess)
+        return e;
+    if (rope)
+        bwd_grad_kernel<true><<<blocks, 256, 0, stream>>>((const uint4*)k, (const uint4*)X,
+                                                          nullptr, dS, N, rows, rv, (uint4*)dk);
+    else
+        bwd_grad_kernel<false><<<blocks, 256, 0, stream>>>((const uint4*)k, (const uint4*)X,
+                                                           nullptr, dS, N, rows, rv, (uint4*)dk);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return launch_tc_apply(k, k, dS, dv, B, H, N, rope, eps, status, num_sms, stream, kApplyRaw);
 }
 
 cudaError_t launch_backward_f32(const float* q, const float* k, const float* v, const float* g,
@@ -403,7 +520,7 @@ cudaError_t launch_backward_f32(const float* q, const float* k, const float* v, 
                                 int B, int H, int N, const RopeView* rope, float eps,
                                 float* workspace, int C, cudaStream_t stream) {
     return launch_backward<float>(q, k, v, g, dout, dq, dk, dv, dg, B, H, N, rope, eps, workspace,
-                                  nullptr, C, stream);
+                                  C, stream);
 }
 
 }  // namespace sla

@@ -33,16 +33,16 @@ cudaError_t launch_simt_state_partials(const __nv_bfloat16* k, const __nv_bfloat
                                        int H, int N, const RopeView* rope, float* partial, int C,
                                        cudaStream_t stream);
 
-// Backward (backward.cu): dq, dk, dv, dg of L = sum(dout * o), in three
-// launches over C chunks per head; workspace backward_workspace_bytes(BH, C).
-// The bf16 backward takes the state from the tensor-core state kernel and
-// needs backward_bf16_workspace_bytes.
+// Backward (backward.cu): dq, dk, dv, dg of L = sum(dout * o).  bf16: nine
+// launches on the tensor-core state and apply kernels plus three elementwise
+// kernels, workspace backward_bf16_workspace_bytes(BH, N, num_sms).  fp32:
+// three launches over C chunks per head, workspace backward_workspace_bytes(BH, C).
 size_t backward_workspace_bytes(int BH, int C);
-size_t backward_bf16_workspace_bytes(int BH, int N, int C, int num_sms);
+size_t backward_bf16_workspace_bytes(int BH, int N, int num_sms);
 cudaError_t launch_backward_bf16(const void* q, const void* k, const void* v, const void* g,
                                  const void* dout, void* dq, void* dk, void* dv, void* dg, int B,
                                  int H, int N, const RopeView* rope, float eps, float* workspace,
-                                 int C, int num_sms, unsigned* status, cudaStream_t stream);
+                                 int num_sms, unsigned* status, cudaStream_t stream);
 cudaError_t launch_backward_f32(const float* q, const float* k, const float* v, const float* g,
                                 const float* dout, float* dq, float* dk, float* dv, float* dg,
                                 int B, int H, int N, const RopeView* rope, float eps,
@@ -76,12 +76,15 @@ cudaError_t launch_tc_block_causal(const void* q, const void* k, const void* v, 
                                    const RopeView* rope, int rope_offset, float eps,
                                    const float* state_in, float* state_out, float* workspace,
                                    unsigned* status, int num_sms, cudaStream_t stream);
+// zweight: null, or a weight per token ([B*H][N] fp32) for z = sum_j w_j phi(k_j).
 cudaError_t launch_tc_state(const void* k, const void* v, void* state, int B, int H, int N,
                             const RopeView* rope, void* workspace, unsigned* status, int num_sms,
-                            cudaStream_t stream);
+                            cudaStream_t stream, const float* zweight = nullptr);
+// mode: 0 the gated apply; 1 out = (R phi(q))^T S; 2 out = S q (q as it is, g unread).
+constexpr int kApplyGate = 0, kApplyRaw = 1, kApplyRawMN = 2;
 cudaError_t launch_tc_apply(const void* q, const void* g, const void* state, void* out, int B,
                             int H, int N, const RopeView* rope, float eps, unsigned* status,
-                            int num_sms, cudaStream_t stream);
+                            int num_sms, cudaStream_t stream, int mode = kApplyGate);
 
 // RoPE table (rope_table.cu).
 cudaError_t launch_rope_fill(float* table, int T, int Hs, int Ws, int dt, int dh, int dw,

@@ -99,6 +99,10 @@ constexpr int kApXThreads = 32 * kApXWarps;
 constexpr int kApThreads = 32 * (3 + kApXWarps + kApEWarps);   // + the G producer warp
 constexpr int kApORows = 32;                      // rows of o one epilogue warp stores
 constexpr int kApTmemCols = 256;
+// tc_apply_kernel modes: the gated apply, and two raw products for the backward
+constexpr int kApGate = 0, kApRaw = 1, kApRawMN = 2;
+static_assert(kApGate == kApplyGate && kApRaw == kApplyRaw && kApRawMN == kApplyRawMN,
+              "apply modes of the launcher");
 constexpr int kApRowsPerThread = kApTok * 16 / kApXThreads;   // 8
 
 static_assert(kStRowsPerThread == 4 && kApRowsPerThread == 8, "thread/tile split");
@@ -127,6 +131,8 @@ struct StateParams {
     // covers tokens [(hh % nb) * N + tok0, ...) of the RoPE grid.  merge = 0
     // leaves the partial slots unmerged (the block scan sums them).
     int nb, tok0, merge;
+    // null, or a weight per token ([heads][N] fp32): z = sum_j w_j phi(k_j)
+    const float* zweight;
 };
 
 struct ApplyParams {
@@ -445,6 +451,15 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             }
             const int s = (int)(it % kStStages);
             const uint32_t round = (uint32_t)(it / kStStages);
+            // the rows' weights of z, loaded while the tile lands
+            float zw[kStRowsPerThread];
+            if (p.zweight) {
+#pragma unroll
+                for (int i = 0; i < kStRowsPerThread; ++i) {
+                    const int tok = ut * kStTok + rl + 16 * i;
+                    zw[i] = tok < p.N ? __ldg(p.zweight + (size_t)h * p.N + tok) : 0.f;
+                }
+            }
             if (!(ok = warp_wait(&full[s], round & 1, abort_flag, p.status))) break;
             const uint32_t kb = smem0 + s * kStStage;
             // all loads of the tile first, so their latencies overlap
@@ -470,8 +485,13 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 x[i].w = relu_bf2(x[i].w);
                 float f[8];
                 unpack8(x[i], f);
+                if (p.zweight) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) zacc[j] += f[j];
+                    for (int j = 0; j < 8; ++j) zacc[j] = fmaf(zw[i], f[j], zacc[j]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) zacc[j] += f[j];
+                }
                 if (ROPE) x[i] = rotate_chunk(f, cs[i]);
             }
 #pragma unroll
@@ -775,7 +795,14 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 
 // =================================================================== apply ==
 
-template <bool ROPE>
+// MODE kApGate is the layer's apply.  The backward reuses the kernel for plain
+// products of a [N][128] bf16 tensor x with a head's state buffer, which
+// holds some 128 x 128 matrix S as S^T rows (g is not read, nothing is gated):
+//   kApRaw    out_i = (R_i phi(x_i))^T S, the forward's numerator;
+//   kApRawMN  out_i[m] = sum_n x_i[n] S[m][n] = S x_i, x taken as it is (no
+//             feature map, no rotation) and the buffer read as an MN-major
+//             B operand.
+template <bool ROPE, int MODE>
 __global__ void __launch_bounds__(kApThreads, 1)
 tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_g,
                 const __grid_constant__ CUtensorMap tm_o32, ApplyParams p) {
@@ -927,7 +954,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
+            constexpr uint32_t idesc = idesc_bf16(128, 128, false, MODE == kApRawMN);
             const uint32_t sb = smem_u32(sbuf);
             long long it = 0;
             int heads = 0, cur_h = -1;
@@ -956,7 +983,11 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     // K-major, 128-byte swizzle: 16 k-values = 32 bytes inside a row
                     const uint32_t off = (ks >> 2) * kApHalf + (ks & 3) * 32;
                     const uint64_t ad = smem_desc_sw128(qb + off, 16, 1024);
-                    const uint64_t bd = smem_desc_sw128(sb + off, 16, 1024);
+                    // K-major: the buffer's rows are N; MN-major: its rows are K
+                    // (16 rows = 2048 bytes a step, the two N halves kStateHalf apart)
+                    const uint64_t bd = MODE == kApRawMN
+                                            ? smem_desc_sw128(sb + ks * 2048, kStateHalf, 1024)
+                                            : smem_desc_sw128(sb + off, 16, 1024);
                     mma_bf16(tmem + (uint32_t)a * 128, ad, bd, idesc, ks > 0 ? 1u : 0u);
                 }
                 mma_commit(&accfull[a]);
@@ -1013,6 +1044,8 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (dround > 0 && !(ok = warp_wait(&dfree[ds], (dround - 1) & 1, abort_flag, p.status)))
                 break;
             const uint32_t qb = smem0 + s * kApTile;
+            // (kApRawMN multiplies the tile as it is: nothing to transform)
+            if constexpr (MODE != kApRawMN) {
             // two batches of four rows; in each, all loads first
 #pragma unroll
             for (int b4 = 0; b4 < kApRowsPerThread; b4 += 4) {
@@ -1071,6 +1104,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     dens[ds * kApTok + rl + 16 * (b4 + ((c >> 2) & 3))] = den[0] + p.eps;
             }
             fence_proxy_async_smem();
+            }
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&qready[s]);
@@ -1108,15 +1142,27 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                 for (int sub = 0; sub < 4; ++sub) {
                     addr[sub] = gb + sw128_off(r, hf * 8 + ch * 4 + sub, kApHalf);
-                    gv[sub] = lds128(addr[sub]);
+                    if (MODE == kApGate) gv[sub] = lds128(addr[sub]);
                 }
                 uint32_t v[32];
                 tmem_ld32(tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)a * 128 + hf * 64 +
                               ch * 32,
                           v);
                 tmem_ld_wait();
+                if constexpr (MODE == kApGate) {
 #pragma unroll
-                for (int sub = 0; sub < 4; ++sub) gv[sub] = gate_chunk(gv[sub], v + 8 * sub, den);
+                    for (int sub = 0; sub < 4; ++sub) gv[sub] = gate_chunk(gv[sub], v + 8 * sub, den);
+                } else {
+#pragma unroll
+                    for (int sub = 0; sub < 4; ++sub) {
+                        const uint32_t* n8 = v + 8 * sub;
+                        gv[sub] = make_uint4(
+                            f2_to_bf2(__uint_as_float(n8[0]), __uint_as_float(n8[1])),
+                            f2_to_bf2(__uint_as_float(n8[2]), __uint_as_float(n8[3])),
+                            f2_to_bf2(__uint_as_float(n8[4]), __uint_as_float(n8[5])),
+                            f2_to_bf2(__uint_as_float(n8[6]), __uint_as_float(n8[7])));
+                    }
+                }
 #pragma unroll
                 for (int sub = 0; sub < 4; ++sub) sts128(addr[sub], gv[sub]);
             }
@@ -1146,6 +1192,10 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const int s = (int)(it % kApGStages);
                 const uint32_t round = (uint32_t)(it / kApGStages);
                 if (!mbar_wait(&gempty[s], (round & 1) ^ 1, abort_flag, p.status)) break;
+                if constexpr (MODE != kApGate) {
+                    mbar_arrive(&gfull[s]);         // the slot only stages the output
+                    continue;
+                }
                 uint8_t* st = gring + s * kApTile;
                 mbar_arrive_expect_tx(&gfull[s], kApTile);
                 tma_load_3d(st, &tm_g, &gfull[s], 0, tile * kApTok, h, policy);
@@ -1945,8 +1995,12 @@ cudaError_t configure(int dev) {
     cudaError_t e;
     if ((e = set_smem(tc_state_kernel<false>, st_smem<false>())) != cudaSuccess) return e;
     if ((e = set_smem(tc_state_kernel<true>, st_smem<true>())) != cudaSuccess) return e;
-    if ((e = set_smem(tc_apply_kernel<false>, ap_smem<false>())) != cudaSuccess) return e;
-    if ((e = set_smem(tc_apply_kernel<true>, ap_smem<true>())) != cudaSuccess) return e;
+    if ((e = set_smem(tc_apply_kernel<false, kApGate>, ap_smem<false>())) != cudaSuccess) return e;
+    if ((e = set_smem(tc_apply_kernel<true, kApGate>, ap_smem<true>())) != cudaSuccess) return e;
+    if ((e = set_smem(tc_apply_kernel<false, kApRaw>, ap_smem<false>())) != cudaSuccess) return e;
+    if ((e = set_smem(tc_apply_kernel<true, kApRaw>, ap_smem<true>())) != cudaSuccess) return e;
+    if ((e = set_smem(tc_apply_kernel<false, kApRawMN>, ap_smem<false>())) != cudaSuccess)
+        return e;
     if ((e = set_smem(tc_fused_kernel<false>, fu_smem<false>())) != cudaSuccess) return e;
     if ((e = set_smem(tc_fused_kernel<true>, fu_smem<true>())) != cudaSuccess) return e;
     done[dev] = true;
@@ -1957,7 +2011,8 @@ cudaError_t configure(int dev) {
 // per head, starting at token tok0 of the RoPE grid, and merge is 0.
 cudaError_t launch_state(const void* k, const void* v, int BH, int N, const RopeView* rope,
                          void* workspace, uint8_t* state, unsigned* status, int num_sms,
-                         cudaStream_t stream, int nb = 1, int tok0 = 0, bool merge = true) {
+                         cudaStream_t stream, int nb = 1, int tok0 = 0, bool merge = true,
+                         const float* zweight = nullptr) {
     const Plan pl = make_plan(BH, N, num_sms);
     CUtensorMap mk, mv;
     if (!make_map(&mk, k, N, BH, kStTok) || !make_map(&mv, v, N, BH, kStTok))
@@ -1974,6 +2029,7 @@ cudaError_t launch_state(const void* k, const void* v, int BH, int N, const Rope
     sp.nb = nb;
     sp.tok0 = tok0;
     sp.merge = merge ? 1 : 0;
+    sp.zweight = zweight;
     CUtensorMap mt = mk;   // without RoPE the table map is never read
     if (rope && !make_rope_map(&mt, rope->tok, rope->T * rope->Hs * rope->Ws, kStTok))
         return cudaErrorInvalidValue;
@@ -1996,7 +2052,8 @@ cudaError_t launch_state(const void* k, const void* v, int BH, int N, const Rope
 
 cudaError_t launch_apply(const void* q, const void* g, const uint8_t* state, void* out, int BH,
                          int N, const RopeView* rope, float eps, unsigned* status, int num_sms,
-                         bool after_state, cudaStream_t stream, int nb = 1, int tok0 = 0) {
+                         bool after_state, cudaStream_t stream, int nb = 1, int tok0 = 0,
+                         int mode = kApGate) {
     const Plan pl = make_plan(BH, N, num_sms);
     CUtensorMap mq, mg, mo;
     if (!make_map(&mq, q, N, BH, kApTok) || !make_map(&mg, g, N, BH, kApTok) ||
@@ -2024,8 +2081,14 @@ cudaError_t launch_apply(const void* q, const void* g, const uint8_t* state, voi
     // complete before this grid starts, whatever wrote them.
     cfg.attrs = attr;
     cfg.numAttrs = after_state ? 1 : 0;
-    if (rope) return cudaLaunchKernelEx(&cfg, tc_apply_kernel<true>, mq, mg, mo, ap);
-    return cudaLaunchKernelEx(&cfg, tc_apply_kernel<false>, mq, mg, mo, ap);
+    if (mode == kApRawMN)
+        return cudaLaunchKernelEx(&cfg, tc_apply_kernel<false, kApRawMN>, mq, mg, mo, ap);
+    if (mode == kApRaw) {
+        if (rope) return cudaLaunchKernelEx(&cfg, tc_apply_kernel<true, kApRaw>, mq, mg, mo, ap);
+        return cudaLaunchKernelEx(&cfg, tc_apply_kernel<false, kApRaw>, mq, mg, mo, ap);
+    }
+    if (rope) return cudaLaunchKernelEx(&cfg, tc_apply_kernel<true, kApGate>, mq, mg, mo, ap);
+    return cudaLaunchKernelEx(&cfg, tc_apply_kernel<false, kApGate>, mq, mg, mo, ap);
 }
 
 template <bool ROPE>
@@ -2156,20 +2219,20 @@ size_t tc_state_bytes(int BH) { return (size_t)BH * kStateBytes; }
 
 cudaError_t launch_tc_state(const void* k, const void* v, void* state, int B, int H, int N,
                             const RopeView* rope, void* workspace, unsigned* status, int num_sms,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, const float* zweight) {
     cudaError_t e = configure(current_device());
     if (e != cudaSuccess) return e;
     return launch_state(k, v, B * H, N, rope, workspace, static_cast<uint8_t*>(state), status,
-                        num_sms, stream);
+                        num_sms, stream, 1, 0, true, zweight);
 }
 
 cudaError_t launch_tc_apply(const void* q, const void* g, const void* state, void* out, int B,
                             int H, int N, const RopeView* rope, float eps, unsigned* status,
-                            int num_sms, cudaStream_t stream) {
+                            int num_sms, cudaStream_t stream, int mode) {
     cudaError_t e = configure(current_device());
     if (e != cudaSuccess) return e;
     return launch_apply(q, g, static_cast<const uint8_t*>(state), out, B * H, N, rope, eps,
-                        status, num_sms, false, stream);
+                        status, num_sms, false, stream, 1, 0, mode);
 }
 
 int tc_forward_cluster(int dev, int BH, int N, bool rope, int num_sms) {

@@ -237,11 +237,13 @@ sla_status_t sla_linattn_forward_block_causal(const void* q, const void* k, cons
  * (the ReLU derivative at 0 is 0).  q, k, v, g, dout: inputs as for the
  * forward; dq, dk, dv, dg: outputs of the same shape, layout and type, none
  * overlapping an input or another output.  rope_table and eps as for the
- * forward.  The state S, z is recomputed from k and v: on the tensor cores
- * for bf16 (S rounded to bf16, as the forward uses it), in fp32 for fp32;
- * everything else runs on the fp32 FMA units.  Uses the library's
- * per-stream workspace (2 * 66 KB per chunk of every head, plus the state
- * kernel's for bf16).
+ * forward.  The state S, z is recomputed from k and v.  bf16: the six
+ * contractions (S, num, dS, S a, dS v, dS^T kr) run on the tensor cores with
+ * bf16 operands and fp32 accumulation, S and dS rounded to bf16, the
+ * elementwise terms in fp32; the per-stream workspace holds the state
+ * kernel's partials, the two states, two [B*H*N][128] bf16 scratch tensors
+ * and B*H*N floats.  fp32: everything on the fp32 FMA units, with a
+ * workspace of 2 * 66 KB per chunk of every head.
  */
 sla_status_t sla_linattn_backward(const void* q, const void* k, const void* v, const void* g,
                                   const void* dout, void* dq, void* dk, void* dv, void* dg,

@@ -53,6 +53,8 @@ CASES = [
     (1, 2, (1, 8, 16), torch.bfloat16, True),
     (2, 3, (1, 1, 129), torch.bfloat16, False),
     (1, 2, (3, 10, 10), torch.bfloat16, True),
+    (2, 4, (2, 9, 17), torch.bfloat16, True),
+    (3, 1, (1, 1, 1000), torch.bfloat16, False),
     (1, 2, (4, 8, 8), torch.float32, True),
     (2, 1, (1, 1, 300), torch.float32, False),
 ]
@@ -71,7 +73,7 @@ def test_backward_elementwise(B, H, grid, dtype, rope, cuda_device):
         assert _rel(_np64(a), b) <= TOL[dtype], name
 
 
-@pytest.mark.parametrize("name", ["5b_480p", "14b_480p"])
+@pytest.mark.parametrize("name", ["5b_480p", "14b_480p", "5b_720p"])
 def test_backward_full_size_sampled_rows(name, cuda_device):
     wl = WORKLOADS[name]
     tensors = _inputs(wl, seed=0)
