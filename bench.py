@@ -600,13 +600,192 @@ def run_backward(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+ANCHOR_METRIC = "softmax-anchor fwd token-heads/s; bf16 TFLOP/s as % of B300 peak"
+FALLBACK_BF16_TFLOPS = (1800.0, 1400.0)
+ANCHOR_ROWS = 256          # query rows of one head per oracle call (all N keys each)
+
+
+def measured_tensor_peaks():
+    """(burst, sustained) dense bf16 TFLOP/s and where they come from."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            data = json.load(fh)
+        return float(data["bf16_tflops"]), float(data["bf16_tflops_sustained"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return (*FALLBACK_BF16_TFLOPS, "fallback")
+
+
+def oracle_anchor_rows(wl, tensors, head, rows):
+    """The fp64 anchor oracle on some query rows of one head (all N keys); elapsed seconds."""
+    import oracle.linattn as ol
+    import oracle.softmax_anchor as oa   # the CPU baseline of the anchor line
+    spec = ol.RopeSpec(*wl.grid, *wl.split, base=wl.base) if wl.rope else None
+    t0 = time.perf_counter()
+    oa.anchor_forward_rows(*tensors, rows, rope=spec, heads=[head])
+    return time.perf_counter() - t0
+
+
+def _anchor_row_sample(wl, i):
+    """The i-th oracle sample: ANCHOR_ROWS consecutive query rows of one head."""
+    heads = [(b, h) for b in range(wl.B) for h in range(wl.H)]
+    n = min(ANCHOR_ROWS, wl.N)
+    start = (i * 7919 * n) % max(wl.N - n + 1, 1)
+    return heads[i % len(heads)], list(range(start, start + n))
+
+
+def anchor_cpu_baseline(wl, tensors, budget_s=10.0):
+    done, elapsed, rows = 0, 0.0, 0
+    while elapsed < budget_s and done < 64:
+        head, sel = _anchor_row_sample(wl, done)
+        elapsed += oracle_anchor_rows(wl, tensors, head, sel)
+        rows += len(sel)
+        done += 1
+    return {"value": rows / elapsed, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"{done} samples of {min(ANCHOR_ROWS, wl.N)} query rows of one head of "
+                      f"{wl.name}, each against all N={wl.N} keys (fp64 numpy, "
+                      f"{elapsed:.1f} s); token-heads = query rows"}
+
+
+def run_anchor(args, rank, world, local):
+    """The gated-softmax anchor forward: rotated q, k (RoPE pre-pass) and the attention kernel."""
+    from gated_linear_attention_attn_b300 import sla
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    wl = WORKLOADS[args.workload]
+    host = make_inputs(wl, seed=0)
+    q, k, v, g = (t.to(dev) for t in host)
+    rope = sla.RopeTable(wl.grid, wl.split, wl.base, device=dev) if wl.rope else None
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+    flops = wl.algorithmic_flops
+    scrub = None
+    if wl.algorithmic_bytes < 4 * L2_BYTES:
+        scrub_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+
+        def scrub():
+            scrub_buf.fill_(1)
+
+    def step():
+        sla.anchor_forward(q, k, v, g, out=out, rope=rope, stream=stream)
+
+    def attn_only():          # the same attention kernel without the RoPE pre-pass
+        sla.anchor_forward(q, k, v, g, out=out, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    if sla.last_device_status(stream, dev) != sla.OK:
+        raise RuntimeError("device status after warm-up")
+    _barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(dev)
+    sampler.start()
+    secs = _time_steps(step, args.steps, stream, scrub)
+    clocks = sampler.stop()
+    torch.cuda.synchronize(dev)
+    _barrier(world)
+    secs = _max_over_ranks(secs, world, dev)
+    per_step = secs / args.steps
+    for _ in range(3):
+        attn_only()
+    attn = _time_steps(attn_only, args.steps, stream, scrub) / args.steps
+    if sla.last_device_status(stream, dev) != sla.OK:
+        raise RuntimeError("device status after timing")
+    e2e = None
+    if not args.no_e2e:
+        hin = tuple(t.pin_memory() for t in host)
+        hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+
+        def e2e_step():
+            for dst, src in zip((q, k, v, g), hin):
+                dst.copy_(src, non_blocking=True)
+            step()
+            hout.copy_(out, non_blocking=True)
+
+        e2e_step()
+        ke = max(3, min(args.steps, 10))
+        esecs = _max_over_ranks(_time_steps(e2e_step, ke, stream), world, dev)
+        e2e = {"value": world * wl.token_heads * ke / esecs, "unit": UNIT,
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin),
+               "d2h_bytes_per_step": hout.numel() * hout.element_size(),
+               "steps": ke, "ms_per_step": 1e3 * esecs / ke}
+    if rank != 0:
+        return
+    burst, sustained, src = measured_tensor_peaks()
+    achieved = flops / attn / 1e12
+    line = {
+        "metric": ANCHOR_METRIC, "value": world * wl.token_heads / per_step, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": 1e3 * per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q,k,v,g on the latent token grid)",
+        "config": _config(wl, world, plan=(
+            "RoPE pre-pass (rotated q, k) + anchor_attn_kernel (tcgen05, 128 queries x 64-key "
+            "tiles per CTA)" if wl.rope else "anchor_attn_kernel"),
+            note="compute-bound: K and V of a head are re-read from L2 by every CTA"),
+        "roofline": {"bound": "tensor", "kernel": "anchor_attn_kernel", "achieved": achieved,
+                     "peak": sustained, "unit": "TFLOP/s", "frac": achieved / sustained,
+                     "peak_source": f"{src} cuBLAS bf16, sustained (bf16_tflops_sustained)",
+                     "frac_of_burst_peak": achieved / burst,
+                     "algorithmic_flops_per_launch": flops, "launch_us": 1e6 * attn,
+                     "step_tflops": flops / per_step / 1e12, "traffic": None},
+        "e2e": e2e,
+        "gpu_launches": (2 if wl.rope else 1) * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = anchor_cpu_baseline(wl, host)
+    print(json.dumps(line), flush=True)
+
+
+def run_anchor_reference(args, rank, world):
+    """Reference arm of an anchor workload: the fp64 oracle, ANCHOR_ROWS query rows per step."""
+    if rank != 0:
+        return
+    wl = WORKLOADS[args.workload]
+    tensors = make_inputs(wl, seed=0)
+    for i in range(args.warmup):
+        oracle_anchor_rows(wl, tensors, *_anchor_row_sample(wl, i))
+    total, rows = 0.0, 0
+    for i in range(args.steps):
+        head, sel = _anchor_row_sample(wl, args.warmup + i)
+        total += oracle_anchor_rows(wl, tensors, head, sel)
+        rows += len(sel)
+    value = rows / total
+    line = {
+        "impl": "reference", "metric": ANCHOR_METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(wl, world, note=f"{min(ANCHOR_ROWS, wl.N)} query rows of one head "
+                                          "(all N keys) per step on the host cores"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": _blas_threads(),
+                         "kind": "oracle",
+                         "sample": f"{args.steps} samples of {min(ANCHOR_ROWS, wl.N)} query "
+                                   f"rows of {wl.name}, one per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_env()
+    anchor = WORKLOADS[args.workload].layer == "anchor"
     if args.impl == "reference":
-        run_reference(args, rank, world)
+        if anchor:
+            run_anchor_reference(args, rank, world)
+        else:
+            run_reference(args, rank, world)
         return
-    if args.pass_ == "backward":
+    if anchor:
+        if args.pass_ == "backward":
+            raise SystemExit("the anchor layer has a forward only")
+        run_anchor(args, rank, world, local)
+    elif args.pass_ == "backward":
         run_backward(args, rank, world, local)
     else:
         run_sla(args, rank, world, local)

@@ -309,6 +309,42 @@ sla_status_t sla_linattn_backward_f32(const float* q, const float* k, const floa
     return backward(q, k, v, g, dout, dq, dk, dv, dg, B, H, N, d, rope_table, eps, stream, true);
 }
 
+sla_status_t sla_anchor_forward(const void* q, const void* k, const void* v, const void* g,
+                                void* out, int B, int H, int N, int d,
+                                const sla_rope_table_t* rope_table, sla_stream_t stream) {
+    if (!q || !k || !v || !g || !out) return SLA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1 || d < 1) return SLA_ERR_INVALID_ARG;
+    if (d != 256) return SLA_ERR_UNSUPPORTED;
+    if ((long long)B * H > 65535 || (long long)B * H * N > 0x7fffffffLL)
+        return SLA_ERR_UNSUPPORTED;
+    const size_t bytes = (size_t)B * H * N * d * 2;
+    const void* ins[4] = {q, k, v, g};
+    const size_t sizes[4] = {bytes, bytes, bytes, bytes};
+    sla_status_t st = check_buffers(ins, sizes, 4, out, bytes);
+    if (st != SLA_OK) return st;
+    RopeView rv{};
+    if ((st = check_rope(rope_table, N, d, &rv)) != SLA_OK) return st;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SLA_ERR_CUDA;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* ds = nullptr;
+    if ((st = device_state(dev, &ds)) != SLA_OK) return st;
+    void* ws = nullptr;
+    if (rope_table &&
+        (st = workspace(dev, s, anchor_workspace_bytes(B * H, N, true), &ws)) != SLA_OK)
+        return st;
+    if (launch_anchor(q, k, v, g, out, B, H, N, rope_table ? &rv : nullptr, ws, ds->status, s) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return SLA_ERR_CUDA;
+    }
+    return SLA_OK;
+}
+
 size_t sla_linattn_carried_state_bytes(int B, int H, int d) {
     if (B < 1 || H < 1 || d != kHeadDim) return 0;
     return (size_t)B * H * (kHeadDim * kHeadDim + kHeadDim) * sizeof(float);

@@ -48,6 +48,14 @@ cudaError_t launch_backward_f32(const float* q, const float* k, const float* v, 
                                 int B, int H, int N, const RopeView* rope, float eps,
                                 float* workspace, int C, cudaStream_t stream);
 
+// Gated-softmax anchor forward (anchor.cu), bf16, head dim 256: the RoPE
+// pre-pass (rotated q and k into workspace, anchor_workspace_bytes of it) when
+// rope is given, then one tcgen05 attention launch.
+size_t anchor_workspace_bytes(int BH, int N, bool rope);
+cudaError_t launch_anchor(const void* q, const void* k, const void* v, const void* g, void* out,
+                          int B, int H, int N, const RopeView* rope, void* workspace,
+                          unsigned* status, cudaStream_t stream);
+
 // bf16 path on tcgen05 (tc_forward.cu).  The whole forward needs
 // tc_workspace_bytes of workspace (counters, partial states, the heads'
 // states); the state phase alone needs tc_state_workspace_bytes and writes

@@ -62,6 +62,8 @@ _BWD_ARGS = [_vp] * 9 + [_int] * 4 + [ctypes.POINTER(RopeTableC), _flt, _vp]
 for _name in ("sla_linattn_backward", "sla_linattn_backward_f32"):
     getattr(_lib, _name).argtypes = _BWD_ARGS
     getattr(_lib, _name).restype = _int
+_lib.sla_anchor_forward.argtypes = [_vp] * 5 + [_int] * 4 + [ctypes.POINTER(RopeTableC), _vp]
+_lib.sla_anchor_forward.restype = _int
 _lib.sla_linattn_forward_cluster.argtypes = [_int] * 5
 _lib.sla_linattn_forward_cluster.restype = _int
 _lib.sla_status_string.argtypes = [_int]
@@ -73,7 +75,7 @@ EXPORTED = ("sla_rope_table_floats", "sla_rope_table_fill", "sla_linattn_forward
             "sla_linattn_forward_f32", "sla_linattn_state_bytes", "sla_linattn_state",
             "sla_linattn_apply", "sla_linattn_forward_noalloc", "sla_linattn_forward_cluster",
             "sla_linattn_carried_state_bytes", "sla_linattn_forward_block_causal",
-            "sla_linattn_backward", "sla_linattn_backward_f32",
+            "sla_linattn_backward", "sla_linattn_backward_f32", "sla_anchor_forward",
             "sla_status_string", "sla_last_device_status")
 
 
@@ -188,6 +190,32 @@ def linattn_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.
         _check(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(), out.data_ptr(),
                   B, H, N, d, rope_c, float(eps), _stream_handle(stream, q.device)),
                fn.__name__)
+    return out
+
+
+ANCHOR_HEAD_DIM = 256
+ANCHOR_SPLIT = (88, 84, 84)
+
+
+def anchor_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                   out: Optional[torch.Tensor] = None, rope: Optional[RopeTable] = None,
+                   stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """o = sigmoid(g) * softmax((R q)(R k)^T / sqrt(d)) v for [B, H, N, 256] bf16 CUDA tensors
+    (``sla_anchor_forward``).  Asynchronous on ``stream`` (default: the current stream)."""
+    _check_bf16("q", q)
+    for name, t in (("k", k), ("v", v), ("g", g)):
+        _check_bf16(name, t, like=q)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check_bf16("out", out, like=q)
+    B, H, N, d = q.shape
+    rope_c = ctypes.byref(rope.c_struct()) if rope is not None else None
+    with torch.cuda.device(q.device):
+        _check(_lib.sla_anchor_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(),
+                                       out.data_ptr(), B, H, N, d, rope_c,
+                                       _stream_handle(stream, q.device)),
+               "sla_anchor_forward")
     return out
 
 

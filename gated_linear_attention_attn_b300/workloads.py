@@ -39,6 +39,7 @@ class Workload:
     tol: float = 1e-2                   # max|err| / max|ref| bound for parity
     description: str = ""
     block_frames: int = 0               # > 0: block-causal form, blocks of this many frames
+    layer: str = "linear"               # "linear" or "anchor" (gated-softmax, d = 256)
 
     @property
     def N(self) -> int:
@@ -66,7 +67,10 @@ class Workload:
 
     @property
     def algorithmic_flops(self) -> int:
-        """Two d x d contractions per token: 4 * B*H*N*d^2."""
+        """Linear layer: two d x d contractions per token, 4 * B*H*N*d^2.  Anchor
+        layer: the N x N scores and their product with v, 4 * B*H*N^2*d."""
+        if self.layer == "anchor":
+            return 4 * self.B * self.H * self.N * self.N * self.d
         return 4 * self.B * self.H * self.N * self.d * self.d
 
     def with_(self, **kw) -> "Workload":
@@ -95,6 +99,20 @@ WORKLOADS = {
         "5b_720p_block5", B=2, H=20, grid=(25, 22, 40), rope=True, block_frames=5,
         description="block-causal form of the 720p shape: 5 blocks of 5 latent frames "
                     "(4400 tokens), carried state in and out"),
+    # gated-softmax anchor layers: 10 heads x 256 (5B), 16 heads x 256 (14B),
+    # Wan 3D RoPE with the 88/84/84 split of d = 256
+    "anchor_5b_480p": Workload(
+        "anchor_5b_480p", B=2, H=10, grid=(11, 15, 26), d=256, rope=True, split=(88, 84, 84),
+        layer="anchor",
+        description="5B softmax anchor, 480p/81 frames: B=2 H=10 N=4290 d=256 bf16, 3D RoPE"),
+    "anchor_5b_720p": Workload(
+        "anchor_5b_720p", B=2, H=10, grid=(25, 22, 40), d=256, rope=True, split=(88, 84, 84),
+        layer="anchor",
+        description="5B softmax anchor, 720p/193 frames: B=2 H=10 N=22000 d=256 bf16, 3D RoPE"),
+    "anchor_14b_480p": Workload(
+        "anchor_14b_480p", B=2, H=16, grid=(11, 15, 26), d=256, rope=True, split=(88, 84, 84),
+        layer="anchor",
+        description="14B softmax anchor, 480p/81 frames: B=2 H=16 N=4290 d=256 bf16, 3D RoPE"),
 }
 
 # The workload the throughput metric is quoted on (5B shape at 720p).

@@ -257,6 +257,30 @@ sla_status_t sla_linattn_backward_f32(const float* q, const float* k, const floa
                                       sla_stream_t stream);
 
 /*
+ * Forward of the gated-softmax anchor layer ("SANA-Video 2.0", NVlabs/Sana
+ * docs/sana_video2.md, section "Architecture": one attention layer in four is
+ * a dense softmax layer, 10 heads of 256 in the 5B model, 16 in the 14B
+ * model, with the Wan 3D rotary embedding; the arXiv abstract of 2607.21553
+ * calls them gated-softmax anchors).  Per (batch, head), with
+ * qr_i = R_i q_i and kr_j = R_j k_j (R the identity without RoPE):
+ *
+ *     o_i = sigmoid(g_i) * sum_j softmax_j(qr_i . kr_j / sqrt(d)) v_j
+ *
+ * over all N keys (no mask), the gate elementwise.  q, k, v, g, out: bf16
+ * [B][H][N][d] row-major and contiguous in device memory, 16-byte aligned,
+ * out overlapping no input; d must be 256 (SLA_ERR_UNSUPPORTED otherwise),
+ * B * H <= 65535.  rope_table: NULL, or a filled table whose grid has N
+ * tokens and whose bands sum to 256 (the Wan split is 88/84/84).  Scores and
+ * the output are accumulated in fp32 on the tensor cores; the softmax weights
+ * enter the second product rounded to bf16.  With RoPE the rotated q and k
+ * (bf16) go to the library's per-stream workspace (2 * B*H*N*d*2 bytes).
+ * Asynchronous on `stream`.
+ */
+sla_status_t sla_anchor_forward(const void* q, const void* k, const void* v, const void* g,
+                                void* out, int B, int H, int N, int d,
+                                const sla_rope_table_t* rope_table, sla_stream_t stream);
+
+/*
  * The bf16 forward of sla_linattn_forward for callers that cannot allocate
  * device memory.  No page has a counterpart: this entry point exists for
  * library users, not for the method.  Some callers must not see a library

@@ -220,3 +220,30 @@ def test_backward_rejects_bad_arguments_before_cuda():
     for f32 in (False, True):
         for kw, want in bad:
             assert bwd(f32=f32, **kw) == want, (f32, kw)
+
+
+def test_anchor_rejects_bad_arguments_before_cuda():
+    lib = sla.raw_lib()
+    big = 2 * 256 * 256 * 2                            # one tensor at B=1, H=2, N=256, d=256
+
+    def anchor(q=A, k=A + 2 * STEP, v=A + 4 * STEP, g=A + 6 * STEP, out=A + 8 * STEP,
+               B=1, H=2, N=256, d=256, rope=None):
+        return lib.sla_anchor_forward(q, k, v, g, out, B, H, N, d, rope, None)
+
+    assert 2 * STEP >= big
+    bad = [
+        (dict(q=0), sla.INVALID_ARG),
+        (dict(out=0), sla.INVALID_ARG),
+        (dict(N=0), sla.INVALID_ARG),
+        (dict(B=-1), sla.INVALID_ARG),
+        (dict(d=128), sla.UNSUPPORTED),
+        (dict(B=256, H=256), sla.UNSUPPORTED),             # more than 65535 heads
+        (dict(v=A + 4 * STEP + 4), sla.ALIGNMENT),
+        (dict(out=A + 6 * STEP + 4096), sla.INVALID_ARG),  # out overlaps g
+        (dict(rope=ctypes.byref(sla.RopeTableC(A + 12 * STEP, 4, 8, 8, 44, 42, 42))),
+         sla.INVALID_ARG),                                 # bands sum to 128, not 256
+        (dict(rope=ctypes.byref(sla.RopeTableC(A + 12 * STEP, 4, 8, 4, 88, 84, 84))),
+         sla.INVALID_ARG),                                 # the grid has 128 tokens, not 256
+    ]
+    for kw, want in bad:
+        assert anchor(**kw) == want, kw
