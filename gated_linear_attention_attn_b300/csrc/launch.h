@@ -49,8 +49,8 @@ cudaError_t launch_backward_f32(const float* q, const float* k, const float* v, 
                                 float* workspace, int C, cudaStream_t stream);
 
 // Gated-softmax anchor forward (anchor.cu), bf16, head dim 256: the RoPE
-// pre-pass (rotated q and k into workspace, anchor_workspace_bytes of it) when
-// rope is given, then one tcgen05 attention launch.
+// pre-pass (rotated k into workspace, anchor_workspace_bytes of it) when rope
+// is given, then one tcgen05 attention launch (which rotates q itself).
 size_t anchor_workspace_bytes(int BH, int N, bool rope);
 cudaError_t launch_anchor(const void* q, const void* k, const void* v, const void* g, void* out,
                           int B, int H, int N, const RopeView* rope, void* workspace,

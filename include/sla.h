@@ -271,9 +271,9 @@ sla_status_t sla_linattn_backward_f32(const float* q, const float* k, const floa
  * out overlapping no input; d must be 256 (SLA_ERR_UNSUPPORTED otherwise),
  * B * H <= 65535.  rope_table: NULL, or a filled table whose grid has N
  * tokens and whose bands sum to 256 (the Wan split is 88/84/84).  Scores and
- * the output are accumulated in fp32 on the tensor cores; the softmax weights
- * enter the second product rounded to bf16.  With RoPE the rotated q and k
- * (bf16) go to the library's per-stream workspace (2 * B*H*N*d*2 bytes).
+ * the output are accumulated in fp32 on the tensor cores; the rotated q and k
+ * and the softmax weights enter the products rounded to bf16.  With RoPE the
+ * rotated k goes to the library's per-stream workspace (B*H*N*d*2 bytes).
  * Asynchronous on `stream`.
  */
 sla_status_t sla_anchor_forward(const void* q, const void* k, const void* v, const void* g,
