@@ -771,17 +771,179 @@ def run_anchor_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+ATTNRES_METRIC = "AttnRes aggregation tokens/s; HBM GB/s as % of B300 peak"
+ATTNRES_UNIT = "tokens/s"
+ATTNRES_ROWS = 4096        # tokens per oracle call
+
+
+def _attnres_config(wl, world, note=""):
+    cfg = {"workload": wl.name, "sources": wl.H, "tokens": wl.tokens, "hidden": wl.d,
+           "grid": list(wl.grid), "batch": wl.B, "input_dtype": "bfloat16", "query_dtype": "f32",
+           "eps": 1e-6, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+           "l2": ("inputs larger than L2 (%.0f MB vs 126 MB), steps back to back"
+                  % (wl.algorithmic_bytes / 1e6) if wl.algorithmic_bytes >= 4 * L2_BYTES
+                  else "L2 flushed between steps (a 252 MB buffer written outside the "
+                       "timed events)"),
+           "launch_plan": "attnres_kernel (one warp per token, two passes over the rows)"}
+    if note:
+        cfg["note"] = note
+    return cfg
+
+
+def oracle_attnres_rows(host, rows):
+    import oracle.attnres as oar   # the CPU baseline of the AttnRes line
+    s, w = host
+    t0 = time.perf_counter()
+    oar.attnres_aggregate(s[:, rows].double().numpy(), w.double().numpy(), 1e-6)
+    return time.perf_counter() - t0
+
+
+def _attnres_sample(wl, i):
+    n = min(ATTNRES_ROWS, wl.tokens)
+    start = (i * 7919 * n) % max(wl.tokens - n + 1, 1)
+    return list(range(start, start + n))
+
+
+def run_attnres(args, rank, world, local):
+    """The AttnRes aggregation of a later layer's input over the block summaries."""
+    from gated_linear_attention_attn_b300 import sla
+    from gated_linear_attention_attn_b300.workloads import make_attnres_inputs
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    wl = WORKLOADS[args.workload]
+    host = make_attnres_inputs(wl, seed=0)
+    s, w = (t.to(dev) for t in host)
+    out = torch.empty(s.shape[1:], dtype=torch.bfloat16, device=dev)
+    srcs = list(s.unbind(0))
+    stream = torch.cuda.current_stream(dev)
+    scrub = None
+    if wl.algorithmic_bytes < 4 * L2_BYTES:
+        scrub_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+
+        def scrub():
+            scrub_buf.fill_(1)
+
+    def step():
+        sla.attnres_aggregate(srcs, w, eps=1e-6, out=out, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    _barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(dev)
+    sampler.start()
+    secs = _time_steps(step, args.steps, stream, scrub)
+    clocks = sampler.stop()
+    torch.cuda.synchronize(dev)
+    _barrier(world)
+    secs = _max_over_ranks(secs, world, dev)
+    per_step = secs / args.steps
+    e2e = None
+    if not args.no_e2e:
+        hs, hw = host[0].pin_memory(), host[1].pin_memory()
+        hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+
+        def e2e_step():
+            s.copy_(hs, non_blocking=True)
+            w.copy_(hw, non_blocking=True)
+            step()
+            hout.copy_(out, non_blocking=True)
+
+        e2e_step()
+        ke = max(3, min(args.steps, 10))
+        esecs = _max_over_ranks(_time_steps(e2e_step, ke, stream), world, dev)
+        e2e = {"value": world * wl.tokens * ke / esecs, "unit": ATTNRES_UNIT,
+               "h2d_bytes_per_step": hs.numel() * hs.element_size() + hw.numel() * 4,
+               "d2h_bytes_per_step": hout.numel() * hout.element_size(),
+               "steps": ke, "ms_per_step": 1e3 * esecs / ke}
+    if rank != 0:
+        return
+    peak, peak_src = measured_peaks()
+    achieved = wl.algorithmic_bytes / per_step / 1e9
+    line = {
+        "metric": ATTNRES_METRIC, "value": world * wl.tokens / per_step, "unit": ATTNRES_UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": 1e3 * per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) summaries scaled 1+n, N(0,1)*3/sqrt(C) query)",
+        "config": _attnres_config(wl, world),
+        "roofline": {"bound": "hbm", "kernel": "attnres_kernel", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_src} copy bandwidth",
+                     "algorithmic_bytes_per_launch": wl.algorithmic_bytes,
+                     "launch_us": 1e6 * per_step, "traffic": None},
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        done, elapsed, rows = 0, 0.0, 0
+        while elapsed < 10.0 and done < 64:
+            sel = _attnres_sample(wl, done)
+            elapsed += oracle_attnres_rows(host, sel)
+            rows += len(sel)
+            done += 1
+        line["cpu_baseline"] = {"value": rows / elapsed, "unit": ATTNRES_UNIT,
+                                "cores": _blas_threads(), "kind": "oracle",
+                                "sample": f"{done} samples of {min(ATTNRES_ROWS, wl.tokens)} "
+                                          f"tokens of {wl.name} (fp64 numpy, {elapsed:.1f} s)"}
+    print(json.dumps(line), flush=True)
+
+
+def run_attnres_reference(args, rank, world):
+    """Reference arm of an AttnRes workload: the fp64 oracle, ATTNRES_ROWS tokens per step."""
+    if rank != 0:
+        return
+    from gated_linear_attention_attn_b300.workloads import make_attnres_inputs
+    wl = WORKLOADS[args.workload]
+    host = make_attnres_inputs(wl, seed=0)
+    for i in range(args.warmup):
+        oracle_attnres_rows(host, _attnres_sample(wl, i))
+    total, rows = 0.0, 0
+    for i in range(args.steps):
+        sel = _attnres_sample(wl, args.warmup + i)
+        total += oracle_attnres_rows(host, sel)
+        rows += len(sel)
+    value = rows / total
+    line = {
+        "impl": "reference", "metric": ATTNRES_METRIC, "value": value, "unit": ATTNRES_UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _attnres_config(wl, world, note=f"{min(ATTNRES_ROWS, wl.tokens)} tokens per "
+                                                  "step on the host cores"),
+        "cpu_baseline": {"value": value, "unit": ATTNRES_UNIT, "cores": _blas_threads(),
+                         "kind": "oracle",
+                         "sample": f"{args.steps} samples of {min(ATTNRES_ROWS, wl.tokens)} "
+                                   f"tokens of {wl.name}, one per step"},
+        "e2e": {"value": value, "unit": ATTNRES_UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_env()
-    anchor = WORKLOADS[args.workload].layer == "anchor"
+    layer = WORKLOADS[args.workload].layer
+    anchor = layer == "anchor"
     if args.impl == "reference":
         if anchor:
             run_anchor_reference(args, rank, world)
+        elif layer == "attnres":
+            run_attnres_reference(args, rank, world)
         else:
             run_reference(args, rank, world)
         return
-    if anchor:
+    if layer == "attnres":
+        if args.pass_ == "backward":
+            raise SystemExit("the AttnRes aggregation is timed forward only")
+        run_attnres(args, rank, world, local)
+    elif anchor:
         if args.pass_ == "backward":
             raise SystemExit("the anchor layer has a forward only")
         run_anchor(args, rank, world, local)

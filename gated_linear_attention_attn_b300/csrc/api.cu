@@ -345,6 +345,28 @@ sla_status_t sla_anchor_forward(const void* q, const void* k, const void* v, con
     return SLA_OK;
 }
 
+sla_status_t sla_attnres_aggregate(const void* const* sources, int M, int T, int C,
+                                   const float* w, float eps, void* out, sla_stream_t stream) {
+    if (!sources || !w || !out) return SLA_ERR_INVALID_ARG;
+    if (M < 1 || T < 1 || C < 1 || bad_eps(eps)) return SLA_ERR_INVALID_ARG;
+    if (M > kAttnResMaxSources || C % 256 != 0 || C > 16384) return SLA_ERR_UNSUPPORTED;
+    const size_t bytes = (size_t)T * C * 2;
+    for (int n = 0; n < M; ++n) {
+        if (!sources[n]) return SLA_ERR_INVALID_ARG;
+        if (misaligned(sources[n], 16)) return SLA_ERR_ALIGNMENT;
+        const uintptr_t x = reinterpret_cast<uintptr_t>(out);
+        const uintptr_t y = reinterpret_cast<uintptr_t>(sources[n]);
+        if (x < y + bytes && y < x + bytes) return SLA_ERR_INVALID_ARG;
+    }
+    if (misaligned(out, 16) || misaligned(w, 16)) return SLA_ERR_ALIGNMENT;
+    if (launch_attnres(sources, M, T, C, w, eps, out, reinterpret_cast<cudaStream_t>(stream)) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return SLA_ERR_CUDA;
+    }
+    return SLA_OK;
+}
+
 size_t sla_linattn_carried_state_bytes(int B, int H, int d) {
     if (B < 1 || H < 1 || d != kHeadDim) return 0;
     return (size_t)B * H * (kHeadDim * kHeadDim + kHeadDim) * sizeof(float);

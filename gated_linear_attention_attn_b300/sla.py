@@ -64,6 +64,9 @@ for _name in ("sla_linattn_backward", "sla_linattn_backward_f32"):
     getattr(_lib, _name).restype = _int
 _lib.sla_anchor_forward.argtypes = [_vp] * 5 + [_int] * 4 + [ctypes.POINTER(RopeTableC), _vp]
 _lib.sla_anchor_forward.restype = _int
+_lib.sla_attnres_aggregate.argtypes = [ctypes.POINTER(_vp), _int, _int, _int, _vp, _flt, _vp,
+                                       _vp]
+_lib.sla_attnres_aggregate.restype = _int
 _lib.sla_linattn_forward_cluster.argtypes = [_int] * 5
 _lib.sla_linattn_forward_cluster.restype = _int
 _lib.sla_status_string.argtypes = [_int]
@@ -76,7 +79,7 @@ EXPORTED = ("sla_rope_table_floats", "sla_rope_table_fill", "sla_linattn_forward
             "sla_linattn_apply", "sla_linattn_forward_noalloc", "sla_linattn_forward_cluster",
             "sla_linattn_carried_state_bytes", "sla_linattn_forward_block_causal",
             "sla_linattn_backward", "sla_linattn_backward_f32", "sla_anchor_forward",
-            "sla_status_string", "sla_last_device_status")
+            "sla_attnres_aggregate", "sla_status_string", "sla_last_device_status")
 
 
 class SlaError(RuntimeError):
@@ -216,6 +219,42 @@ def anchor_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.T
                                        out.data_ptr(), B, H, N, d, rope_c,
                                        _stream_handle(stream, q.device)),
                "sla_anchor_forward")
+    return out
+
+
+def attnres_aggregate(sources, w: torch.Tensor, eps: float = 1e-6,
+                      out: Optional[torch.Tensor] = None,
+                      stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """x(t) = sum_n softmax_n(w . rmsnorm(s_n(t))) s_n(t) (``sla_attnres_aggregate``).
+
+    sources: a list of M bf16 [T, C] CUDA tensors, or one [M, T, C] tensor; w: fp32 [C].
+    """
+    if isinstance(sources, torch.Tensor):
+        if sources.dim() != 3:
+            raise SlaError(INVALID_ARG, "attnres_aggregate: a sources tensor must be [M, T, C]")
+        sources = list(sources.unbind(0))
+    if not sources:
+        raise SlaError(INVALID_ARG, "attnres_aggregate: no sources")
+    first = sources[0]
+    for t in sources:
+        if t.dtype != torch.bfloat16 or t.dim() != 2 or t.shape != first.shape \
+                or t.device != first.device or t.device.type != "cuda" or not t.is_contiguous():
+            raise SlaError(INVALID_ARG, "attnres_aggregate: sources must be contiguous bf16 "
+                                        "[T, C] CUDA tensors of one shape")
+    T, C = first.shape
+    if w.dtype != torch.float32 or w.shape != (C,) or w.device != first.device \
+            or not w.is_contiguous():
+        raise SlaError(INVALID_ARG, "attnres_aggregate: w must be a contiguous fp32 [C] tensor")
+    if out is None:
+        out = torch.empty_like(first)
+    elif out.shape != first.shape or out.dtype != torch.bfloat16 or not out.is_contiguous() \
+            or out.device != first.device:
+        raise SlaError(INVALID_ARG, "attnres_aggregate: out must be a bf16 [T, C] tensor")
+    ptrs = (_vp * len(sources))(*[t.data_ptr() for t in sources])
+    with torch.cuda.device(first.device):
+        _check(_lib.sla_attnres_aggregate(ptrs, len(sources), T, C, w.data_ptr(), float(eps),
+                                          out.data_ptr(), _stream_handle(stream, first.device)),
+               "sla_attnres_aggregate")
     return out
 
 

@@ -39,7 +39,8 @@ class Workload:
     tol: float = 1e-2                   # max|err| / max|ref| bound for parity
     description: str = ""
     block_frames: int = 0               # > 0: block-causal form, blocks of this many frames
-    layer: str = "linear"               # "linear" or "anchor" (gated-softmax, d = 256)
+    layer: str = "linear"               # "linear", "anchor" (gated-softmax, d = 256) or
+                                        # "attnres" (H = number of sources, d = hidden size)
 
     @property
     def N(self) -> int:
@@ -61,8 +62,15 @@ class Workload:
         return torch.empty((), dtype=self.dtype).element_size()
 
     @property
+    def tokens(self) -> int:
+        return self.B * self.N
+
+    @property
     def algorithmic_bytes(self) -> int:
-        """Reads of q, k, v, g and the write of o: 5 * B*H*N*d elements."""
+        """Attention layers: reads of q, k, v, g and the write of o, 5 * B*H*N*d
+        elements.  AttnRes: the H source rows read and one row written per token."""
+        if self.layer == "attnres":
+            return (self.H + 1) * self.tokens * self.d * self.elem_size
         return 5 * self.B * self.H * self.N * self.d * self.elem_size
 
     @property
@@ -113,6 +121,15 @@ WORKLOADS = {
         "anchor_14b_480p", B=2, H=16, grid=(11, 15, 26), d=256, rope=True, split=(88, 84, 84),
         layer="anchor",
         description="14B softmax anchor, 480p/81 frames: B=2 H=16 N=4290 d=256 bf16, 3D RoPE"),
+    # AttnRes aggregation: the last block of each model reads every earlier
+    # block's summary plus its own running one (5B: 32 layers in blocks of 8,
+    # 4 sources, hidden 2560; 14B: 40 layers, 5 sources, hidden 4096)
+    "attnres_5b_720p": Workload(
+        "attnres_5b_720p", B=2, H=4, grid=(25, 22, 40), d=2560, layer="attnres",
+        description="AttnRes, 5B at 720p/193 frames: 4 sources of [44000, 2560] bf16"),
+    "attnres_14b_480p": Workload(
+        "attnres_14b_480p", B=2, H=5, grid=(11, 15, 26), d=4096, layer="attnres",
+        description="AttnRes, 14B at 480p/81 frames: 5 sources of [8580, 4096] bf16"),
 }
 
 # The workload the throughput metric is quoted on (5B shape at 720p).
@@ -134,6 +151,23 @@ def make_inputs(wl: Workload, seed: int = 0, device: Optional[str] = None):
             x = x.to(device)
         out.append(x)
     return tuple(out)
+
+
+def make_attnres_inputs(wl: Workload, seed: int = 0, device: Optional[str] = None):
+    """Draw (sources [M, T, C] bf16, w [C] fp32) for an AttnRes workload: one CPU
+    generator seeded with ``seed`` draws the sources as N(0, 1) scaled by 1 + n
+    for source n (summaries of growing magnitude), then w as N(0, 1) * 3 / sqrt(C)
+    (scores of a few units)."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    M, T, C = wl.H, wl.tokens, wl.d
+    s = torch.randn((M, T, C), generator=gen, dtype=torch.float32)
+    s.mul_(torch.arange(1, M + 1, dtype=torch.float32).view(M, 1, 1))
+    w = torch.randn((C,), generator=gen, dtype=torch.float32) * (3.0 / C ** 0.5)
+    s = s.to(torch.bfloat16)
+    if device is not None:
+        s, w = s.to(device), w.to(device)
+    return s, w
 
 
 def sample_rows(N: int, count: int, seed: int = 1):

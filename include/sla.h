@@ -281,6 +281,27 @@ sla_status_t sla_anchor_forward(const void* q, const void* k, const void* v, con
                                 const sla_rope_table_t* rope_table, sla_stream_t stream);
 
 /*
+ * Block Attention Residual (AttnRes) aggregation ("SANA-Video 2.0",
+ * NVlabs/Sana docs/sana_video2.md, section "Architecture": a shared,
+ * timestep-independent Attention Residual aggregation in blocks of eight
+ * layers; the arXiv abstract of 2607.21553: completed block summaries are
+ * routed into later linear layers).  The pages give no formula; this entry
+ * point computes the reading, per token t:
+ *
+ *     k_n(t) = s_n(t) / sqrt(mean_c s_n(t, c)^2 + eps)
+ *     x(t)   = sum_n softmax_n(w . k_n(t)) s_n(t)
+ *
+ * sources: a HOST array of M device pointers, each a bf16 [T][C] row-major
+ * summary (16-byte aligned); 1 <= M <= 8.  C must be a multiple of 256, at
+ * most 16384 (SLA_ERR_UNSUPPORTED otherwise).  w: device, C fp32 values (the shared
+ * query, any RMS-norm gain folded in), 16-byte aligned.  out: device bf16
+ * [T][C], overlapping no source.  eps finite, >= 0.  fp32 arithmetic.
+ * Asynchronous on `stream`; the host array may be freed on return.
+ */
+sla_status_t sla_attnres_aggregate(const void* const* sources, int M, int T, int C,
+                                   const float* w, float eps, void* out, sla_stream_t stream);
+
+/*
  * The bf16 forward of sla_linattn_forward for callers that cannot allocate
  * device memory.  No page has a counterpart: this entry point exists for
  * library users, not for the method.  Some callers must not see a library

@@ -247,3 +247,29 @@ def test_anchor_rejects_bad_arguments_before_cuda():
     ]
     for kw, want in bad:
         assert anchor(**kw) == want, kw
+
+
+def test_attnres_rejects_bad_arguments_before_cuda():
+    lib = sla.raw_lib()
+
+    def agg(srcs=(A, A + STEP), M=None, T=64, C=512, w=A + 4 * STEP, eps=1e-6, out=A + 5 * STEP):
+        arr = (ctypes.c_void_p * max(len(srcs), 1))(*srcs)
+        return lib.sla_attnres_aggregate(arr, len(srcs) if M is None else M, T, C, w, eps, out,
+                                         None)
+
+    bad = [
+        (dict(M=0), sla.INVALID_ARG),
+        (dict(T=0), sla.INVALID_ARG),
+        (dict(eps=-1.0), sla.INVALID_ARG),
+        (dict(w=0), sla.INVALID_ARG),
+        (dict(out=0), sla.INVALID_ARG),
+        (dict(srcs=(A, 0)), sla.INVALID_ARG),
+        (dict(srcs=tuple(A + i * STEP for i in range(9)), out=A + 12 * STEP), sla.UNSUPPORTED),
+        (dict(C=300), sla.UNSUPPORTED),
+        (dict(C=32768), sla.UNSUPPORTED),
+        (dict(srcs=(A, A + STEP + 8)), sla.ALIGNMENT),
+        (dict(w=A + 4 * STEP + 4), sla.ALIGNMENT),
+        (dict(out=A + STEP + 1024), sla.INVALID_ARG),          # out overlaps a source
+    ]
+    for kw, want in bad:
+        assert agg(**kw) == want, kw
