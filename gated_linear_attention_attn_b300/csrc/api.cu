@@ -349,7 +349,7 @@ sla_status_t sla_attnres_aggregate(const void* const* sources, int M, int T, int
                                    const float* w, float eps, void* out, sla_stream_t stream) {
     if (!sources || !w || !out) return SLA_ERR_INVALID_ARG;
     if (M < 1 || T < 1 || C < 1 || bad_eps(eps)) return SLA_ERR_INVALID_ARG;
-    if (M > kAttnResMaxSources || C % 256 != 0 || C > 16384) return SLA_ERR_UNSUPPORTED;
+    if (M > kAttnResMaxSources || C % 256 != 0 || C > 4096) return SLA_ERR_UNSUPPORTED;
     const size_t bytes = (size_t)T * C * 2;
     for (int n = 0; n < M; ++n) {
         if (!sources[n]) return SLA_ERR_INVALID_ARG;
@@ -359,8 +359,19 @@ sla_status_t sla_attnres_aggregate(const void* const* sources, int M, int T, int
         if (x < y + bytes && y < x + bytes) return SLA_ERR_INVALID_ARG;
     }
     if (misaligned(out, 16) || misaligned(w, 16)) return SLA_ERR_ALIGNMENT;
-    if (launch_attnres(sources, M, T, C, w, eps, out, reinterpret_cast<cudaStream_t>(stream)) !=
-        cudaSuccess) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SLA_ERR_CUDA;
+    }
+    DeviceState* ds = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        sla_status_t st = device_state(dev, &ds);
+        if (st != SLA_OK) return st;
+    }
+    if (launch_attnres(sources, M, T, C, w, eps, out, ds->status,
+                       reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return SLA_ERR_CUDA;
     }

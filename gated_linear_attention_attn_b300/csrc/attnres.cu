@@ -12,143 +12,207 @@
 // a reading (the pages print none): one learned query w shared by all tokens,
 // RMS-normalised summaries as keys, the raw summaries as values.
 //
-// HBM-bound: every summary row is read once from HBM and x written once.  One
-// warp per token: the first pass reads the M rows (512 contiguous bytes per
-// warp load) and forms w . s_n and s_n . s_n; after the warp reductions and
-// the softmax, the second pass reads the same rows again, from L2 (the warps
-// in flight hold a few MB), and writes x.
+// HBM-bound: every summary row is read once and x written once.  Each CTA
+// works through its tokens (token blockIdx.x + k * gridDim.x) with a ring of
+// kArStages token slots in shared memory: one thread keeps bulk copies of the
+// next tokens' M rows in flight (cp.async.bulk, completion counted on the
+// slot's mbarrier), so each SM has several hundred KB of reads outstanding
+// without holding them in registers.  Per token, thread i takes the 16-byte
+// piece i of every row, the CTA reduces w . s_n and s_n . s_n (warp shuffles,
+// then shared memory), and every thread forms the softmax and its piece of x.
+// Earlier forms measured slower: re-reading the rows from L2 in a second pass
+// (the rows of the tokens in flight overflow L2 before the second read), and
+// register prefetching one token ahead (too few bytes in flight).
 #include "launch.h"
+#include "tc_ptx.cuh"
 
 namespace sla {
 namespace {
 
-constexpr int kArWarps = 8;                 // tokens per 256-thread block
+using namespace ptx;
+
+constexpr int kArMaxThreads = 512;
+constexpr int kArStages = 4;                // at most; fewer when M rows of C fill the space
+constexpr size_t kArSmemBudget = 200 * 1024;
 
 struct AttnResParams {
     const __nv_bfloat16* src[kAttnResMaxSources];
     int M;
-    int C;                                  // a multiple of 256
+    int C;                                  // a multiple of 256, at most 4096
     long long T;
     float eps;
     const float* w;
     __nv_bfloat16* out;
+    unsigned* status;
+    int stages;                             // token slots in shared memory, 1 .. kArStages
 };
 
-__device__ __forceinline__ void unpack8(uint4 u, float (&x)[8]) {
-    const uint32_t v[4] = {u.x, u.y, u.z, u.w};
+int attnres_stages(int M, int C) {
+    const size_t slot = (size_t)M * C * 2;
+    const size_t fit = kArSmemBudget / slot;
+    return fit >= (size_t)kArStages ? kArStages : (int)fit;
+}
+
+// Sums P values over the 32 lanes of a warp with P - 1 + 5 - log2(P)
+// shuffles instead of 5 P: each round halves the values a lane keeps.  On
+// return v[0] of lane l holds the warp sum of value l >> (5 - log2 P).
+template <int P>
+__device__ __forceinline__ void warp_sum_transposed(float (&v)[P], int lane) {
+    static_assert(P >= 1 && P <= 32 && (P & (P - 1)) == 0, "P a power of two up to 32");
+    int off = 16;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 f = bf2_to_f2(v[i]);
-        x[2 * i] = f.x;
-        x[2 * i + 1] = f.y;
+    for (int width = P; width > 1; width >>= 1, off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < width / 2; ++i) {
+            const float send = upper ? v[i] : v[i + width / 2];
+            const float keep = upper ? v[i + width / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
     }
+#pragma unroll
+    for (; off >= 1; off >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
 }
 
-// 16-byte global load kept in L2 for the second pass, not allocated in L1.
-__device__ __forceinline__ uint4 ld_keep(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(reinterpret_cast<uint64_t>(p)));
-    return v;
-}
+template <int M>
+struct PartCount {                          // 2 M rounded up to a power of two
+    static constexpr int value = M <= 1 ? 2 : M <= 2 ? 4 : M <= 4 ? 8 : 16;
+};
 
-// The second read of a row: its last use, so L2 may evict it first.
-__device__ __forceinline__ uint4 ld_last(const void* p, uint64_t policy) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.b32 {%0, %1, %2, %3}, [%4], %5;"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(reinterpret_cast<uint64_t>(p)), "l"(policy));
-    return v;
-}
-
-__device__ __forceinline__ uint64_t evict_first_policy() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-
-__global__ void __launch_bounds__(kArWarps * 32)
+// blockDim.x * 8 == C: thread i owns columns 8i .. 8i + 7 of every row.
+template <int M>
+__global__ void __launch_bounds__(kArMaxThreads)
 attnres_kernel(AttnResParams p) {
-    extern __shared__ float ws[];           // w, C floats
-    for (int i = threadIdx.x; i < p.C; i += blockDim.x) ws[i] = __ldg(p.w + i);
+    constexpr int P = PartCount<M>::value;
+    constexpr int kShift = P == 2 ? 4 : P == 4 ? 3 : P == 8 ? 2 : 1;   // 5 - log2 P
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ float red[2][kArMaxThreads / 32][P];
+    __shared__ float alpha[2][M];
+    __shared__ uint64_t full[kArStages];
+    __shared__ int abort_flag;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const uint32_t row_bytes = (uint32_t)p.C * 2;
+    const uint32_t slot_bytes = (uint32_t)M * row_bytes;
+    const long long mine = blockIdx.x < p.T ? (p.T - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int S = p.stages;
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
     __syncthreads();
-    const int lane = threadIdx.x & 31;
-    const long long t = (long long)blockIdx.x * kArWarps + (threadIdx.x >> 5);
-    if (t >= p.T) return;
-    const int chunks = p.C >> 8;            // 256 columns: 8 per lane
-    const size_t row = (size_t)t * p.C + (size_t)lane * 8;
-
-    float dot[kAttnResMaxSources], ss[kAttnResMaxSources];
+    auto fetch = [&](long long k) {          // token k of this CTA into slot k % S
+        const int s = (int)(k % S);
+        const size_t off = (size_t)(blockIdx.x + k * gridDim.x) * p.C;
+        mbar_arrive_expect_tx(&full[s], slot_bytes);
 #pragma unroll
-    for (int n = 0; n < kAttnResMaxSources; ++n) {
-        dot[n] = 0.f;
-        ss[n] = 0.f;
-        if (n < p.M) {
-            const __nv_bfloat16* s = p.src[n] + row;
-#pragma unroll 4
-            for (int ch = 0; ch < chunks; ++ch) {
-                float x[8];
-                unpack8(ld_keep(s + ch * 256), x);
-                const float4 w0 = *reinterpret_cast<const float4*>(ws + ch * 256 + lane * 8);
-                const float4 w1 = *reinterpret_cast<const float4*>(ws + ch * 256 + lane * 8 + 4);
-                const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        for (int n = 0; n < M; ++n)
+            bulk_load(smem + (size_t)s * slot_bytes + (size_t)n * row_bytes, p.src[n] + off,
+                      row_bytes, &full[s]);
+    };
+    if (tid == 0)
+        for (long long k = 0; k < mine && k < S; ++k) fetch(k);
+    float2 wv[4];
+    {
+        const float4* w4 = reinterpret_cast<const float4*>(p.w + (size_t)tid * 8);
+        const float4 a = __ldg(w4), b = __ldg(w4 + 1);
+        wv[0] = make_float2(a.x, a.y);
+        wv[1] = make_float2(a.z, a.w);
+        wv[2] = make_float2(b.x, b.y);
+        wv[3] = make_float2(b.z, b.w);
+    }
+    const float inv_c = 1.f / (float)p.C;
+    long long k = 0;
+    for (; k < mine; ++k) {
+        const int s = (int)(k % S), buf = (int)(k & 1);
+        const bool ok = mbar_wait(&full[s], (uint32_t)(k / S) & 1u, &abort_flag, p.status);
+        if (__syncthreads_or(!ok)) break;
+        float2 x[M][4];
+        float part[P];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    dot[n] = fmaf(x[i], wv[i], dot[n]);
-                    ss[n] = fmaf(x[i], x[i], ss[n]);
-                }
+        for (int n = 0; n < M; ++n) {
+            const uint4 u = lds128(smem_u32(smem + (size_t)s * slot_bytes + (size_t)n * row_bytes) +
+                                   tid * 16);
+            x[n][0] = bf2_to_f2(u.x);
+            x[n][1] = bf2_to_f2(u.y);
+            x[n][2] = bf2_to_f2(u.z);
+            x[n][3] = bf2_to_f2(u.w);
+            float2 d = mul2(x[n][0], wv[0]), q = mul2(x[n][0], x[n][0]);
+#pragma unroll
+            for (int i = 1; i < 4; ++i) {
+                d = fma2(x[n][i], wv[i], d);
+                q = fma2(x[n][i], x[n][i], q);
+            }
+            part[2 * n] = d.x + d.y;
+            part[2 * n + 1] = q.x + q.y;
+        }
+#pragma unroll
+        for (int i = 2 * M; i < P; ++i) part[i] = 0.f;
+        warp_sum_transposed<P>(part, lane);
+        if ((lane & ((1 << kShift) - 1)) == 0) red[buf][wid][lane >> kShift] = part[0];
+        __syncthreads();
+        // the slot is read: refill it with token k + S
+        if (tid == 0 && k + S < mine) fetch(k + S);
+        if (wid == 0) {
+            // lane i < P sums value i over the warps; lanes 2n, 2n + 1 hold
+            // w . s_n and s_n . s_n; then a_n = softmax_n(dot_n / rms_n)
+            float v = 0.f;
+            if (lane < P)
+                for (int w = 0; w < nwarps; ++w) v += red[buf][w][lane];
+            const float q = __shfl_down_sync(0xffffffffu, v, 1);
+            const float logit = v * rsqrtf(q * inv_c + p.eps);
+            float lg[M], mx = -INFINITY;
+#pragma unroll
+            for (int n = 0; n < M; ++n) {
+                lg[n] = __shfl_sync(0xffffffffu, logit, 2 * n);
+                mx = fmaxf(mx, lg[n]);
+            }
+            float den = 0.f;
+#pragma unroll
+            for (int n = 0; n < M; ++n) {
+                lg[n] = __expf(lg[n] - mx);
+                den += lg[n];
+            }
+            if (lane < M) {
+                float mine_a = lg[0];
+#pragma unroll
+                for (int n = 1; n < M; ++n)
+                    if (lane == n) mine_a = lg[n];
+                alpha[buf][lane] = mine_a / den;
             }
         }
-    }
+        __syncthreads();
+        float2 acc[4];
+        {
+            const float a0 = alpha[buf][0];
 #pragma unroll
-    for (int n = 0; n < kAttnResMaxSources; ++n) {
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            dot[n] += __shfl_xor_sync(0xffffffffu, dot[n], off);
-            ss[n] += __shfl_xor_sync(0xffffffffu, ss[n], off);
+            for (int i = 0; i < 4; ++i) acc[i] = mul2(make_float2(a0, a0), x[0][i]);
         }
-    }
-    // a_n = softmax_n(dot_n / rms_n)
-    float a[kAttnResMaxSources], mx = -INFINITY;
 #pragma unroll
-    for (int n = 0; n < kAttnResMaxSources; ++n) {
-        a[n] = n < p.M ? dot[n] * rsqrtf(ss[n] / (float)p.C + p.eps) : -INFINITY;
-        mx = fmaxf(mx, a[n]);
-    }
-    float den = 0.f;
+        for (int n = 1; n < M; ++n) {
+            const float an = alpha[buf][n];
 #pragma unroll
-    for (int n = 0; n < kAttnResMaxSources; ++n) {
-        a[n] = n < p.M ? __expf(a[n] - mx) : 0.f;
-        den += a[n];
-    }
-    const float inv = 1.f / den;
-#pragma unroll
-    for (int n = 0; n < kAttnResMaxSources; ++n) a[n] *= inv;
-
-    const uint64_t last = evict_first_policy();
-    uint4* o = reinterpret_cast<uint4*>(p.out + row);
-#pragma unroll 2
-    for (int ch = 0; ch < chunks; ++ch) {
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int n = 0; n < kAttnResMaxSources; ++n) {
-            if (n < p.M) {
-                float x[8];
-                unpack8(ld_last(p.src[n] + row + ch * 256, last), x);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] = fmaf(a[n], x[i], acc[i]);
-            }
+            for (int i = 0; i < 4; ++i) acc[i] = fma2(make_float2(an, an), x[n][i], acc[i]);
         }
-        o[ch * 32] = make_uint4(f2_to_bf2(acc[0], acc[1]), f2_to_bf2(acc[2], acc[3]),
-                                f2_to_bf2(acc[4], acc[5]), f2_to_bf2(acc[6], acc[7]));
+        const size_t t = (size_t)(blockIdx.x + k * gridDim.x);
+        *reinterpret_cast<uint4*>(p.out + t * p.C + (size_t)tid * 8) =
+            make_uint4(f2_to_bf2(acc[0].x, acc[0].y), f2_to_bf2(acc[1].x, acc[1].y),
+                       f2_to_bf2(acc[2].x, acc[2].y), f2_to_bf2(acc[3].x, acc[3].y));
+        // red[buf] and alpha[buf] are next written two tokens later, after
+        // the next token's first barrier
+    }
+    if (tid == 0 && k < mine) {
+        // gave up: the copies still in flight land before the CTA exits
+        for (long long j = k; j < mine && j < k + S; ++j)
+            mbar_wait_drain(&full[j % S], (uint32_t)(j / S) & 1u);
     }
 }
 
 }  // namespace
 
 cudaError_t launch_attnres(const void* const* sources, int M, long long T, int C, const float* w,
-                           float eps, void* out, cudaStream_t stream) {
+                           float eps, void* out, unsigned* status, cudaStream_t stream) {
     AttnResParams p{};
     for (int n = 0; n < M; ++n) p.src[n] = static_cast<const __nv_bfloat16*>(sources[n]);
     p.M = M;
@@ -157,15 +221,39 @@ cudaError_t launch_attnres(const void* const* sources, int M, long long T, int C
     p.eps = eps;
     p.w = w;
     p.out = static_cast<__nv_bfloat16*>(out);
-    const size_t smem = (size_t)C * sizeof(float);
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(attnres_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
+    p.status = status;
+    p.stages = attnres_stages(M, C);
+    const int threads = C / 8;                      // one 16-byte piece of a row each
+    if (threads % 32 != 0 || threads > kArMaxThreads || p.stages < 1) return cudaErrorInvalidValue;
+    int dev = 0, sms = 148;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+    const size_t smem = (size_t)p.stages * M * C * 2;
+    auto launch = [&](auto kernel) -> cudaError_t {
+        cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (r != cudaSuccess) return r;
+        int per_sm = 1;
+        r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
+        if (r != cudaSuccess) return r;
+        long long blocks = (long long)sms * (per_sm > 0 ? per_sm : 1);
+        if (blocks > T) blocks = T;
+        kernel<<<(unsigned)blocks, threads, smem, stream>>>(p);
+        return cudaGetLastError();
+    };
+    switch (M) {
+        case 1: return launch(attnres_kernel<1>);
+        case 2: return launch(attnres_kernel<2>);
+        case 3: return launch(attnres_kernel<3>);
+        case 4: return launch(attnres_kernel<4>);
+        case 5: return launch(attnres_kernel<5>);
+        case 6: return launch(attnres_kernel<6>);
+        case 7: return launch(attnres_kernel<7>);
+        case 8: return launch(attnres_kernel<8>);
+        default: return cudaErrorInvalidValue;
     }
-    const long long blocks = (T + kArWarps - 1) / kArWarps;
-    attnres_kernel<<<(unsigned)blocks, kArWarps * 32, smem, stream>>>(p);
-    return cudaGetLastError();
 }
 
 }  // namespace sla

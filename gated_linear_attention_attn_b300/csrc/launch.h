@@ -58,10 +58,10 @@ cudaError_t launch_anchor(const void* q, const void* k, const void* v, const voi
 
 // AttnRes aggregation (attnres.cu): x = sum_n softmax_n(w . rmsnorm(s_n)) s_n
 // per token over M <= kAttnResMaxSources bf16 [T][C] summaries, C a multiple
-// of 256; one launch.
+// of 256 up to 4096; one launch.
 constexpr int kAttnResMaxSources = 8;
 cudaError_t launch_attnres(const void* const* sources, int M, long long T, int C, const float* w,
-                           float eps, void* out, cudaStream_t stream);
+                           float eps, void* out, unsigned* status, cudaStream_t stream);
 
 // bf16 path on tcgen05 (tc_forward.cu).  The whole forward needs
 // tc_workspace_bytes of workspace (counters, partial states, the heads'

@@ -293,7 +293,7 @@ sla_status_t sla_anchor_forward(const void* q, const void* k, const void* v, con
  *
  * sources: a HOST array of M device pointers, each a bf16 [T][C] row-major
  * summary (16-byte aligned); 1 <= M <= 8.  C must be a multiple of 256, at
- * most 16384 (SLA_ERR_UNSUPPORTED otherwise).  w: device, C fp32 values (the shared
+ * most 4096 (SLA_ERR_UNSUPPORTED otherwise; 2560 and 4096 in the models).  w: device, C fp32 values (the shared
  * query, any RMS-norm gain folded in), 16-byte aligned.  out: device bf16
  * [T][C], overlapping no source.  eps finite, >= 0.  fp32 arithmetic.
  * Asynchronous on `stream`; the host array may be freed on return.

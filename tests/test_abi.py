@@ -266,7 +266,7 @@ def test_attnres_rejects_bad_arguments_before_cuda():
         (dict(srcs=(A, 0)), sla.INVALID_ARG),
         (dict(srcs=tuple(A + i * STEP for i in range(9)), out=A + 12 * STEP), sla.UNSUPPORTED),
         (dict(C=300), sla.UNSUPPORTED),
-        (dict(C=32768), sla.UNSUPPORTED),
+        (dict(C=4352), sla.UNSUPPORTED),
         (dict(srcs=(A, A + STEP + 8)), sla.ALIGNMENT),
         (dict(w=A + 4 * STEP + 4), sla.ALIGNMENT),
         (dict(out=A + STEP + 1024), sla.INVALID_ARG),          # out overlaps a source
