@@ -87,7 +87,6 @@ attnres_kernel(AttnResParams p) {
     constexpr int kShift = P == 2 ? 4 : P == 4 ? 3 : P == 8 ? 2 : 1;   // 5 - log2 P
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ float red[2][kArMaxThreads / 32][P];
-    __shared__ float alpha[2][M];
     __shared__ uint64_t full[kArStages];
     __shared__ int abort_flag;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -127,7 +126,6 @@ attnres_kernel(AttnResParams p) {
     for (; k < mine; ++k) {
         const int s = (int)(k % S), buf = (int)(k & 1);
         const bool ok = mbar_wait(&full[s], (uint32_t)(k / S) & 1u, &abort_flag, p.status);
-        if (__syncthreads_or(!ok)) break;
         float2 x[M][4];
         float part[P];
 #pragma unroll
@@ -151,47 +149,41 @@ attnres_kernel(AttnResParams p) {
         for (int i = 2 * M; i < P; ++i) part[i] = 0.f;
         warp_sum_transposed<P>(part, lane);
         if ((lane & ((1 << kShift) - 1)) == 0) red[buf][wid][lane >> kShift] = part[0];
-        __syncthreads();
-        // the slot is read: refill it with token k + S
+        // one barrier per token: the warps' partials are in, the slot is read,
+        // and every thread learns whether any wait gave up (then nothing of
+        // this token is stored)
+        if (__syncthreads_or(!ok)) break;
         if (tid == 0 && k + S < mine) fetch(k + S);
-        if (wid == 0) {
-            // lane i < P sums value i over the warps; lanes 2n, 2n + 1 hold
-            // w . s_n and s_n . s_n; then a_n = softmax_n(dot_n / rms_n)
-            float v = 0.f;
-            if (lane < P)
-                for (int w = 0; w < nwarps; ++w) v += red[buf][w][lane];
-            const float q = __shfl_down_sync(0xffffffffu, v, 1);
-            const float logit = v * rsqrtf(q * inv_c + p.eps);
-            float lg[M], mx = -INFINITY;
+        // every warp: lane i < P sums value i over the warps; lanes 2n, 2n + 1
+        // hold w . s_n and s_n . s_n; a_n = softmax_n(dot_n / rms_n).
+        // red[buf] is next written two tokens later, after the next barrier.
+        float v = 0.f;
+        if (lane < P)
+            for (int w = 0; w < nwarps; ++w) v += red[buf][w][lane];
+        const float q = __shfl_down_sync(0xffffffffu, v, 1);
+        const float logit = v * rsqrtf(q * inv_c + p.eps);
+        float a[M], mx = -INFINITY;
 #pragma unroll
-            for (int n = 0; n < M; ++n) {
-                lg[n] = __shfl_sync(0xffffffffu, logit, 2 * n);
-                mx = fmaxf(mx, lg[n]);
-            }
-            float den = 0.f;
-#pragma unroll
-            for (int n = 0; n < M; ++n) {
-                lg[n] = __expf(lg[n] - mx);
-                den += lg[n];
-            }
-            if (lane < M) {
-                float mine_a = lg[0];
-#pragma unroll
-                for (int n = 1; n < M; ++n)
-                    if (lane == n) mine_a = lg[n];
-                alpha[buf][lane] = mine_a / den;
-            }
+        for (int n = 0; n < M; ++n) {
+            a[n] = __shfl_sync(0xffffffffu, logit, 2 * n);
+            mx = fmaxf(mx, a[n]);
         }
-        __syncthreads();
+        float den = 0.f;
+#pragma unroll
+        for (int n = 0; n < M; ++n) {
+            a[n] = __expf(a[n] - mx);
+            den += a[n];
+        }
+        const float inv = 1.f / den;
         float2 acc[4];
         {
-            const float a0 = alpha[buf][0];
+            const float a0 = a[0] * inv;
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[i] = mul2(make_float2(a0, a0), x[0][i]);
         }
 #pragma unroll
         for (int n = 1; n < M; ++n) {
-            const float an = alpha[buf][n];
+            const float an = a[n] * inv;
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[i] = fma2(make_float2(an, an), x[n][i], acc[i]);
         }
@@ -199,8 +191,6 @@ attnres_kernel(AttnResParams p) {
         *reinterpret_cast<uint4*>(p.out + t * p.C + (size_t)tid * 8) =
             make_uint4(f2_to_bf2(acc[0].x, acc[0].y), f2_to_bf2(acc[1].x, acc[1].y),
                        f2_to_bf2(acc[2].x, acc[2].y), f2_to_bf2(acc[3].x, acc[3].y));
-        // red[buf] and alpha[buf] are next written two tokens later, after
-        // the next token's first barrier
     }
     if (tid == 0 && k < mine) {
         // gave up: the copies still in flight land before the CTA exits
