@@ -145,8 +145,9 @@ class ClockSampler:
                 "reasons": sorted(self.reasons)}
 
 
-# The sources the tensor-core kernels are built from.
-KERNEL_SOURCES = ("tc_forward.cu", "tc_ptx.cuh", "common.cuh", "launch.h")
+# The sources the profiled kernels are built from.
+KERNEL_SOURCES = ("tc_forward.cu", "anchor.cu", "attnres.cu", "tc_ptx.cuh", "common.cuh",
+                  "launch.h")
 
 
 def source_hash():
@@ -874,7 +875,8 @@ def run_attnres(args, rank, world, local):
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_src} copy bandwidth",
                      "algorithmic_bytes_per_launch": wl.algorithmic_bytes,
-                     "launch_us": 1e6 * per_step, "traffic": None},
+                     "launch_us": 1e6 * per_step,
+                     "traffic": stored_traffic("attnres_kernel", wl.name)},
         "e2e": e2e,
         "gpu_launches": args.steps,
         "clocks": clocks,
