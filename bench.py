@@ -145,15 +145,21 @@ class ClockSampler:
                 "reasons": sorted(self.reasons)}
 
 
-# The sources the profiled kernels are built from.
-KERNEL_SOURCES = ("tc_forward.cu", "anchor.cu", "attnres.cu", "tc_ptx.cuh", "common.cuh",
-                  "launch.h")
+# The sources each profiled kernel is built from.
+_COMMON_SOURCES = ("tc_ptx.cuh", "common.cuh", "launch.h")
+KERNEL_SOURCES = {
+    "tc_state_kernel": ("tc_forward.cu",) + _COMMON_SOURCES,
+    "tc_apply_kernel": ("tc_forward.cu",) + _COMMON_SOURCES,
+    "tc_fused_kernel": ("tc_forward.cu",) + _COMMON_SOURCES,
+    "anchor_attn_kernel": ("anchor.cu",) + _COMMON_SOURCES,
+    "attnres_kernel": ("attnres.cu",) + _COMMON_SOURCES,
+}
 
 
-def source_hash():
-    """Hash of the kernels' sources, to tell whether a stored ncu traffic figure is current."""
+def source_hash(kernel: str):
+    """Hash of a kernel's sources, to tell whether a stored ncu traffic figure is current."""
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "gated_linear_attention_attn_b300", "csrc", name), "rb") as fh:
             h.update(name.encode())
             h.update(fh.read())
@@ -163,12 +169,12 @@ def source_hash():
 def stored_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from profiles/dram_traffic.txt, if taken on the current sources.
 
-    Lines: `<kernel> <workload> <bytes_per_launch> <source_hash>`.
+    Lines: `<kernel> <workload> <bytes_per_launch> <hash of the kernel's sources>`.
     """
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-    if not os.path.exists(path):
+    if not os.path.exists(path) or kernel not in KERNEL_SOURCES:
         return None
-    current = source_hash()
+    current = source_hash(kernel)
     with open(path) as fh:
         for line in fh:
             parts = line.split()

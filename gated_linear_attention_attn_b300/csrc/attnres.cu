@@ -14,12 +14,13 @@
 //
 // HBM-bound: every summary row is read once and x written once.  Each CTA
 // works through its tokens (token blockIdx.x + k * gridDim.x) with a ring of
-// kArStages token slots in shared memory: one thread keeps bulk copies of the
-// next tokens' M rows in flight (cp.async.bulk, completion counted on the
-// slot's mbarrier), so each SM has several hundred KB of reads outstanding
-// without holding them in registers.  Per token, thread i takes the 16-byte
-// piece i of every row, the CTA reduces w . s_n and s_n . s_n (warp shuffles,
-// then shared memory), and every thread forms the softmax and its piece of x.
+// 2 to 6 token slots in shared memory (at most 110 KB, so two CTAs share an SM):
+// one thread keeps bulk copies of the next tokens' M rows in flight
+// (cp.async.bulk, completion counted on the slot's mbarrier).  Per token,
+// thread i takes the 16-byte piece i of every row, the CTA reduces w . s_n
+// and s_n . s_n (warp shuffles, then shared memory, one barrier), every warp
+// forms the softmax, and thread i writes its piece of x, from registers when
+// the CTA is small enough to keep the rows there, else reading them again.
 // Earlier forms measured slower: re-reading the rows from L2 in a second pass
 // (the rows of the tokens in flight overflow L2 before the second read), and
 // register prefetching one token ahead (too few bytes in flight).
@@ -32,8 +33,8 @@ namespace {
 using namespace ptx;
 
 constexpr int kArMaxThreads = 512;
-constexpr int kArStages = 4;                // at most; fewer when M rows of C fill the space
-constexpr size_t kArSmemBudget = 200 * 1024;
+constexpr int kArStages = 6;                // token slots: 2 .. 6, as many as fit the budget
+constexpr size_t kArSmemBudget = 110 * 1024;  // per CTA, so that two CTAs share an SM
 
 struct AttnResParams {
     const __nv_bfloat16* src[kAttnResMaxSources];
@@ -50,7 +51,7 @@ struct AttnResParams {
 int attnres_stages(int M, int C) {
     const size_t slot = (size_t)M * C * 2;
     const size_t fit = kArSmemBudget / slot;
-    return fit >= (size_t)kArStages ? kArStages : (int)fit;
+    return fit >= (size_t)kArStages ? kArStages : fit < 2 ? 2 : (int)fit;
 }
 
 // Sums P values over the 32 lanes of a warp with P - 1 + 5 - log2(P)
@@ -80,7 +81,9 @@ struct PartCount {                          // 2 M rounded up to a power of two
 };
 
 // blockDim.x * 8 == C: thread i owns columns 8i .. 8i + 7 of every row.
-template <int M>
+// KEEP: the rows stay in registers from the reduction to the output (fewer
+// instructions; more registers, so used when a CTA has at most 384 threads).
+template <int M, bool KEEP>
 __global__ void __launch_bounds__(kArMaxThreads)
 attnres_kernel(AttnResParams p) {
     constexpr int P = PartCount<M>::value;
@@ -126,12 +129,12 @@ attnres_kernel(AttnResParams p) {
     for (; k < mine; ++k) {
         const int s = (int)(k % S), buf = (int)(k & 1);
         const bool ok = mbar_wait(&full[s], (uint32_t)(k / S) & 1u, &abort_flag, p.status);
-        float2 x[M][4];
+        const uint32_t slot = smem_u32(smem + (size_t)s * slot_bytes) + tid * 16;
+        float2 x[M][4];                          // kept to the output when KEEP
         float part[P];
 #pragma unroll
         for (int n = 0; n < M; ++n) {
-            const uint4 u = lds128(smem_u32(smem + (size_t)s * slot_bytes + (size_t)n * row_bytes) +
-                                   tid * 16);
+            const uint4 u = lds128(slot + n * row_bytes);
             x[n][0] = bf2_to_f2(u.x);
             x[n][1] = bf2_to_f2(u.y);
             x[n][2] = bf2_to_f2(u.z);
@@ -149,11 +152,16 @@ attnres_kernel(AttnResParams p) {
         for (int i = 2 * M; i < P; ++i) part[i] = 0.f;
         warp_sum_transposed<P>(part, lane);
         if ((lane & ((1 << kShift) - 1)) == 0) red[buf][wid][lane >> kShift] = part[0];
-        // one barrier per token: the warps' partials are in, the slot is read,
-        // and every thread learns whether any wait gave up (then nothing of
-        // this token is stored)
+        // one barrier per token: the warps' partials are in, and every thread
+        // learns whether any wait gave up (then nothing of this token is
+        // stored).  A slot is free once its rows are read for the last time:
+        // this token's slot now when KEEP, else the previous token's.
         if (__syncthreads_or(!ok)) break;
-        if (tid == 0 && k + S < mine) fetch(k + S);
+        if (KEEP) {
+            if (tid == 0 && k + S < mine) fetch(k + S);
+        } else {
+            if (tid == 0 && k >= 1 && k - 1 + S < mine) fetch(k - 1 + S);
+        }
         // every warp: lane i < P sums value i over the warps; lanes 2n, 2n + 1
         // hold w . s_n and s_n . s_n; a_n = softmax_n(dot_n / rms_n).
         // red[buf] is next written two tokens later, after the next barrier.
@@ -175,14 +183,17 @@ attnres_kernel(AttnResParams p) {
             den += a[n];
         }
         const float inv = 1.f / den;
-        float2 acc[4];
-        {
-            const float a0 = a[0] * inv;
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[i] = mul2(make_float2(a0, a0), x[0][i]);
-        }
-#pragma unroll
-        for (int n = 1; n < M; ++n) {
+        for (int n = 0; n < M; ++n) {
+            if (!KEEP) {                         // the rows again, from shared memory
+                const uint4 u = lds128(slot + n * row_bytes);
+                x[n][0] = bf2_to_f2(u.x);
+                x[n][1] = bf2_to_f2(u.y);
+                x[n][2] = bf2_to_f2(u.z);
+                x[n][3] = bf2_to_f2(u.w);
+            }
             const float an = a[n] * inv;
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[i] = fma2(make_float2(an, an), x[n][i], acc[i]);
@@ -193,8 +204,11 @@ attnres_kernel(AttnResParams p) {
                        f2_to_bf2(acc[2].x, acc[2].y), f2_to_bf2(acc[3].x, acc[3].y));
     }
     if (tid == 0 && k < mine) {
-        // gave up: the copies still in flight land before the CTA exits
-        for (long long j = k; j < mine && j < k + S; ++j)
+        // gave up at token k: tokens k .. k + S - 1 (KEEP) or k .. k + S - 2
+        // (k .. S - 1 when k is 0) were issued and may be in flight; they land
+        // before the CTA exits
+        const long long last = KEEP || k == 0 ? k + S - 1 : k + S - 2;
+        for (long long j = k; j <= last && j < mine; ++j)
             mbar_wait_drain(&full[j % S], (uint32_t)(j / S) & 1u);
     }
 }
@@ -233,15 +247,24 @@ cudaError_t launch_attnres(const void* const* sources, int M, long long T, int C
         kernel<<<(unsigned)blocks, threads, smem, stream>>>(p);
         return cudaGetLastError();
     };
-    switch (M) {
-        case 1: return launch(attnres_kernel<1>);
-        case 2: return launch(attnres_kernel<2>);
-        case 3: return launch(attnres_kernel<3>);
-        case 4: return launch(attnres_kernel<4>);
-        case 5: return launch(attnres_kernel<5>);
-        case 6: return launch(attnres_kernel<6>);
-        case 7: return launch(attnres_kernel<7>);
-        case 8: return launch(attnres_kernel<8>);
+    const bool keep = threads <= 384;
+    switch (M * 2 + (keep ? 1 : 0)) {
+        case 2: return launch(attnres_kernel<1, false>);
+        case 3: return launch(attnres_kernel<1, true>);
+        case 4: return launch(attnres_kernel<2, false>);
+        case 5: return launch(attnres_kernel<2, true>);
+        case 6: return launch(attnres_kernel<3, false>);
+        case 7: return launch(attnres_kernel<3, true>);
+        case 8: return launch(attnres_kernel<4, false>);
+        case 9: return launch(attnres_kernel<4, true>);
+        case 10: return launch(attnres_kernel<5, false>);
+        case 11: return launch(attnres_kernel<5, true>);
+        case 12: return launch(attnres_kernel<6, false>);
+        case 13: return launch(attnres_kernel<6, true>);
+        case 14: return launch(attnres_kernel<7, false>);
+        case 15: return launch(attnres_kernel<7, true>);
+        case 16: return launch(attnres_kernel<8, false>);
+        case 17: return launch(attnres_kernel<8, true>);
         default: return cudaErrorInvalidValue;
     }
 }
