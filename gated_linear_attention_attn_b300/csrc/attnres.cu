@@ -24,6 +24,10 @@
 // Earlier forms measured slower: re-reading the rows from L2 in a second pass
 // (the rows of the tokens in flight overflow L2 before the second read), and
 // register prefetching one token ahead (too few bytes in flight).
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "launch.h"
 #include "tc_ptx.cuh"
 
@@ -229,20 +233,35 @@ cudaError_t launch_attnres(const void* const* sources, int M, long long T, int C
     p.stages = attnres_stages(M, C);
     const int threads = C / 8;                      // one 16-byte piece of a row each
     if (threads % 32 != 0 || threads > kArMaxThreads || p.stages < 1) return cudaErrorInvalidValue;
-    int dev = 0, sms = 148;
+    int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-        return e;
     const size_t smem = (size_t)p.stages * M * C * 2;
+    // the grid (SMs x resident CTAs) per (device, kernel, threads, shared memory), found once:
+    // later calls, also those inside a stream capture, make no attribute or occupancy calls
     auto launch = [&](auto kernel) -> cudaError_t {
-        cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        static std::mutex mu;
+        static std::map<std::tuple<int, const void*, int, size_t>, long long> grids;
+        long long blocks = 0;
+        {
+            std::lock_guard<std::mutex> lock(mu);
+            const auto key = std::make_tuple(dev, reinterpret_cast<const void*>(kernel), threads,
+                                             smem);
+            auto it = grids.find(key);
+            if (it == grids.end()) {
+                int sms = 0, per_sm = 0;
+                cudaError_t r = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+                if (r == cudaSuccess)
+                    r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
-        if (r != cudaSuccess) return r;
-        int per_sm = 1;
-        r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
-        if (r != cudaSuccess) return r;
-        long long blocks = (long long)sms * (per_sm > 0 ? per_sm : 1);
+                if (r == cudaSuccess)
+                    r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads,
+                                                                      smem);
+                if (r != cudaSuccess) return r;
+                it = grids.emplace(key, (long long)sms * (per_sm > 0 ? per_sm : 1)).first;
+            }
+            blocks = it->second;
+        }
         if (blocks > T) blocks = T;
         kernel<<<(unsigned)blocks, threads, smem, stream>>>(p);
         return cudaGetLastError();

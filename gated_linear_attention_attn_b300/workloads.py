@@ -1,8 +1,9 @@
-"""Workload shapes and seeded synthetic inputs for the linear-attention forward.
+"""Workload shapes and seeded synthetic inputs: the linear-attention layer, the
+gated-softmax anchor layer and the AttnRes aggregation.
 
-This module holds no arithmetic of the layer itself: it only names the shapes
-and draws the random inputs, so both the CUDA path and the fp64 oracle can be
-fed the same values.
+This module holds no arithmetic of the layers themselves: it only names the
+shapes and draws the random inputs, so both the CUDA path and the fp64 oracle
+can be fed the same values.
 
 Shapes come from the latent token grids of SANA-Video 2.0 (NVlabs/Sana
 docs/sana_video2.md, "Architecture": 20 heads x 128 for 5B, 32 heads x 128 for

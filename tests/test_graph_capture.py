@@ -98,3 +98,47 @@ def test_noalloc_replays_in_a_graph(cuda_device):
     torch.cuda.synchronize(cuda_device)
     assert int(status.item()) == 0
     assert torch.equal(out, ref)
+
+
+def test_anchor_replays_in_a_graph(cuda_device):
+    """The anchor forward (RoPE pre-pass into the stream's workspace, then the
+    attention kernel) replays bit for bit."""
+    sla = _sla()
+    wl = Workload("graphan", B=1, H=2, grid=(2, 8, 20), d=256, rope=True, split=(88, 84, 84),
+                  layer="anchor")
+    q, k, v, g = (t.to(cuda_device) for t in make_inputs(wl, seed=34))
+    rope = sla.RopeTable(wl.grid, wl.split, wl.base, device=cuda_device)
+    stream = torch.cuda.Stream(cuda_device)
+    stream.wait_stream(torch.cuda.current_stream(cuda_device))
+    with torch.cuda.stream(stream):
+        ref = sla.anchor_forward(q, k, v, g, rope=rope, stream=stream)   # this stream's workspace
+    stream.synchronize()
+    out = torch.full_like(q, float("nan"))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        sla.anchor_forward(q, k, v, g, out=out, rope=rope, stream=stream)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize(cuda_device)
+    assert sla.last_device_status(device=cuda_device) == 0
+    assert torch.equal(out, ref)
+
+
+def test_attnres_replays_in_a_graph(cuda_device):
+    from gated_linear_attention_attn_b300.workloads import make_attnres_inputs
+    sla = _sla()
+    wl = Workload("graphar", B=1, H=4, grid=(1, 1, 300), d=2560, layer="attnres")
+    s, w = (t.to(cuda_device) for t in make_attnres_inputs(wl, seed=35))
+    stream = torch.cuda.Stream(cuda_device)
+    stream.wait_stream(torch.cuda.current_stream(cuda_device))
+    with torch.cuda.stream(stream):
+        ref = sla.attnres_aggregate(s, w, stream=stream)
+    stream.synchronize()
+    out = torch.full_like(ref, float("nan"))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        sla.attnres_aggregate(s, w, out=out, stream=stream)
+    graph.replay()
+    torch.cuda.synchronize(cuda_device)
+    assert sla.last_device_status(device=cuda_device) == 0
+    assert torch.equal(out, ref)
