@@ -20,17 +20,11 @@ size_t simt_workspace_bytes(int BH, int C);
 cudaError_t launch_simt_f32(const float* q, const float* k, const float* v, const float* g,
                             float* out, int B, int H, int N, const RopeView* rope, float eps,
                             float* workspace, int C, cudaStream_t stream);
-cudaError_t launch_simt_bf16(const void* q, const void* k, const void* v, const void* g,
-                             void* out, int B, int H, int N, const RopeView* rope, float eps,
-                             float* workspace, int C, cudaStream_t stream);
 
 // The fp32 SIMT state partials (S_c in [m][n] order, then z_c) of C chunks
 // per head, as simt_state_kernel writes them (simt.cu).
 cudaError_t launch_simt_state_partials(const float* k, const float* v, int B, int H, int N,
                                        const RopeView* rope, float* partial, int C,
-                                       cudaStream_t stream);
-cudaError_t launch_simt_state_partials(const __nv_bfloat16* k, const __nv_bfloat16* v, int B,
-                                       int H, int N, const RopeView* rope, float* partial, int C,
                                        cudaStream_t stream);
 
 // Backward (backward.cu): dq, dk, dv, dg of L = sum(dout * o).  bf16: nine

@@ -18,11 +18,7 @@ constexpr int kSimtTile = 32;                       // tokens per smem tile
 constexpr int kPartialFloats = kHeadDim * kHeadDim + kHeadDim;
 
 __device__ __forceinline__ float load_elem(const float* p) { return __ldg(p); }
-__device__ __forceinline__ float load_elem(const __nv_bfloat16* p) {
-    return __bfloat162float(__ldg(p));
-}
 __device__ __forceinline__ void store_elem(float* p, float x) { *p = x; }
-__device__ __forceinline__ void store_elem(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 
 template <typename T, bool ROPE>
 __global__ void __launch_bounds__(256)
@@ -248,24 +244,10 @@ cudaError_t launch_simt_state_partials(const float* k, const float* v, int B, in
     return launch_state_partials<float>(k, v, B, H, N, rope, partial, C, stream);
 }
 
-cudaError_t launch_simt_state_partials(const __nv_bfloat16* k, const __nv_bfloat16* v, int B,
-                                       int H, int N, const RopeView* rope, float* partial, int C,
-                                       cudaStream_t stream) {
-    return launch_state_partials<__nv_bfloat16>(k, v, B, H, N, rope, partial, C, stream);
-}
-
 cudaError_t launch_simt_f32(const float* q, const float* k, const float* v, const float* g,
                             float* out, int B, int H, int N, const RopeView* rope, float eps,
                             float* workspace, int C, cudaStream_t stream) {
     return launch_simt<float>(q, k, v, g, out, B, H, N, rope, eps, workspace, C, stream);
-}
-
-cudaError_t launch_simt_bf16(const void* q, const void* k, const void* v, const void* g,
-                             void* out, int B, int H, int N, const RopeView* rope, float eps,
-                             float* workspace, int C, cudaStream_t stream) {
-    using bf = __nv_bfloat16;
-    return launch_simt<bf>((const bf*)q, (const bf*)k, (const bf*)v, (const bf*)g, (bf*)out, B,
-                           H, N, rope, eps, workspace, C, stream);
 }
 
 }  // namespace sla
