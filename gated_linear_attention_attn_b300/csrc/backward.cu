@@ -27,6 +27,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "tc_ptx.cuh"
 
 namespace sla {
 namespace {
@@ -311,6 +312,7 @@ bwd_key_kernel(const T* __restrict__ k, const T* __restrict__ v, T* __restrict__
 
 constexpr int kStateBytesB = kHeadDim * kHeadDim * 2 + kHeadDim * 4;   // bf16 S^T, then z
 constexpr int kRowsPerBlock = 16;                 // 16 threads (8 dims each) per row
+constexpr float kLog2eB = 1.4426950408889634f;
 
 __device__ __forceinline__ void bf8_to_f8(uint4 u, float (&f)[8]) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -354,7 +356,8 @@ bwd_terms_kernel(const uint4* __restrict__ q, const uint4* __restrict__ g,
     bf8_to_f8(dout[at], df);
     bf8_to_f8(num[at], nf);
     const float* z = reinterpret_cast<const float*>(
-        states + (size_t)((live ? row : 0) / N) * kStateBytesB + kHeadDim * kHeadDim * 2);
+        states + (size_t)((live ? (unsigned)row : 0u) / (unsigned)N) * kStateBytesB +
+        kHeadDim * kHeadDim * 2);
     const float4 z0 = *reinterpret_cast<const float4*>(z + 8 * c);
     const float4 z1 = *reinterpret_cast<const float4*>(z + 8 * c + 4);
     zf[0] = z0.x; zf[1] = z0.y; zf[2] = z0.z; zf[3] = z0.w;
@@ -366,7 +369,7 @@ bwd_terms_kernel(const uint4* __restrict__ q, const uint4* __restrict__ g,
     float af[8], gg[8], part = 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        const float s = 1.f / (1.f + expf(-gf[j]));
+        const float s = ptx::rcp_approx(1.f + ptx::ex2_approx(-gf[j] * kLog2eB));
         af[j] = df[j] * s * inv;
         gg[j] = df[j] * nf[j] * inv * s * (1.f - s);
         part = fmaf(af[j], nf[j], part);
@@ -393,7 +396,9 @@ bwd_grad_kernel(const uint4* __restrict__ x, const uint4* __restrict__ y,
     float xf[8], yf[8];
     bf8_to_f8(x[at], xf);
     bf8_to_f8(y[at], yf);
-    const int n = (int)(row % N);
+    // rows < 2^31 (the entry point bounds B * H * N): 32-bit division
+    const unsigned bh = (unsigned)row / (unsigned)N;
+    const int n = (int)((unsigned)row - bh * (unsigned)N);
     if (ROPE) {
         // pairs 4c .. 4c + 3 of the token's fp16 (cos, sin) row, turned back
         const uint4 t = __ldg(reinterpret_cast<const uint4*>(rope.tok + (size_t)n * kPairs) + c);
@@ -405,7 +410,7 @@ bwd_grad_kernel(const uint4* __restrict__ x, const uint4* __restrict__ y,
         }
     }
     const float wr = weight ? weight[row] : 1.f;
-    const float* z = reinterpret_cast<const float*>(states + (size_t)(row / N) * kStateBytesB +
+    const float* z = reinterpret_cast<const float*>(states + (size_t)bh * kStateBytesB +
                                                     kHeadDim * kHeadDim * 2) + 8 * c;
     float of[8];
 #pragma unroll
