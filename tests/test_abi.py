@@ -273,3 +273,20 @@ def test_attnres_rejects_bad_arguments_before_cuda():
     ]
     for kw, want in bad:
         assert agg(**kw) == want, kw
+
+
+def test_binding_rejects_bad_anchor_and_attnres_tensors():
+    import torch
+    q = torch.zeros(1, 2, 8, 256, dtype=torch.bfloat16)
+    with pytest.raises(sla.SlaError):
+        sla.anchor_forward(q, q, q, q)                       # CPU tensors
+    with pytest.raises(sla.SlaError):
+        sla.anchor_forward(q.float(), q, q, q)               # not bf16
+    s = torch.zeros(3, 16, 512, dtype=torch.bfloat16)
+    w = torch.zeros(512)
+    with pytest.raises(sla.SlaError):
+        sla.attnres_aggregate(s, w)                          # CPU tensors
+    with pytest.raises(sla.SlaError):
+        sla.attnres_aggregate(s[0], w)                       # not [M, T, C]
+    with pytest.raises(sla.SlaError):
+        sla.attnres_aggregate([], w)
