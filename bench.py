@@ -268,6 +268,9 @@ def _config(wl, world, note="", plan=None):
     if wl.block_frames:
         cfg["block_frames"] = wl.block_frames
         cfg["block_tokens"] = wl.block_tokens
+    if wl.layer == "anchor":              # softmax attention: no eps, keys unscaled
+        cfg["layer"] = "gated-softmax anchor"
+        del cfg["eps"], cfg["k_scale"]
     if plan:
         cfg["launch_plan"] = plan
     if note:
