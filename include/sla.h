@@ -1,6 +1,8 @@
 /*
  * sla.h -- C ABI of the gated bidirectional linear-attention forward
- * (SANA-Video 2.0), a single-GPU CUDA library for B300 (sm_103a).
+ * (SANA-Video 2.0), a single-GPU CUDA library for B300 (sm_103a), with the
+ * layer's backward and block-causal form, the gated-softmax anchor layer and
+ * the AttnRes aggregation (declared further down).
  *
  * The operation.  "SANA-Video 2.0" (NVlabs/Sana docs/sana_video2.md,
  * section "Architecture") builds 75% of its attention layers as gated
@@ -26,10 +28,12 @@
  * Ownership.  The caller owns every buffer passed in.  The library owns a
  * workspace per (device, stream) for the split-N partial states and the
  * heads' states of the two-launch plan (about 66 KB per SM of the device plus
- * 99 KB per head; the fused plan needs none),
+ * 99 KB per head; the fused plan needs none), and for the scratch of the
+ * backward and of the anchor layer with RoPE (sizes at those entry points),
  * allocated with cudaMalloc on the first call that needs it (or more of it)
- * and kept until the process exits.  A call that has to grow the workspace synchronises the
- * device; make the first call of the largest shape outside stream capture.
+ * and kept until the process exits.  A call that has to grow the workspace
+ * synchronises the device; make the first call of the largest shape outside
+ * stream capture.
  *
  * Errors.  Every argument is checked before anything is launched; a call
  * that returns an error has launched nothing.  Calls are asynchronous on
@@ -53,7 +57,7 @@ typedef struct CUstream_st* sla_stream_t;
 typedef enum sla_status {
     SLA_OK = 0,
     SLA_ERR_INVALID_ARG = 1,    /* null pointer, size < 1, bad eps, aliasing, bad RoPE grid */
-    SLA_ERR_UNSUPPORTED = 2,    /* a shape the kernels do not implement (d != 128) */
+    SLA_ERR_UNSUPPORTED = 2,    /* a shape the kernels do not implement (e.g. d != 128) */
     SLA_ERR_ALIGNMENT = 3,      /* a tensor not 16-byte aligned (a RoPE table not 256-byte aligned) */
     SLA_ERR_CUDA = 4,           /* a CUDA runtime call failed (launch, allocation, no device) */
     SLA_ERR_DEVICE_TIMEOUT = 5  /* a kernel gave up a wait and returned early */
