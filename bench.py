@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip timing the oracle on the host")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="on the headline workload, skip timing the other configurations")
     ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "backward"],
                     help="time the layer's forward (the headline) or its backward")
     ap.add_argument("--forward-kernel", default="auto", choices=["auto", "fused", "split"],
@@ -84,11 +86,13 @@ class ClockSampler:
                0x80: "hw_power_brake_slowdown", 0x100: "display_clock"}
     NVML_CLOCK_SM = 1
 
-    def __init__(self, device: torch.device, period_s: float = 0.005):
+    def __init__(self, device: torch.device, period_s: float = 0.002):
         import ctypes
         self.samples, self.reasons = [], set()
         self.max_mhz = None
+        self.regions = 0
         self._stop = threading.Event()
+        self._active = threading.Event()
         self._period = period_s
         self._thread = None
         self.error = None
@@ -124,15 +128,36 @@ class ClockSampler:
 
     def _run(self):
         while not self._stop.is_set():
-            self.sample()
+            if self._active.is_set():
+                self.sample()
             time.sleep(self._period)
 
     def start(self):
+        """Start the sampling thread; it samples only inside `timed()` regions."""
         if self._nv is not None:
             self.samples.clear()
             self.reasons.clear()
             self._thread = threading.Thread(target=self._run, daemon=True)
             self._thread.start()
+
+    class _Region:
+        def __init__(self, owner):
+            self.owner = owner
+
+        def __enter__(self):
+            if self.owner._nv is not None:
+                self.owner.sample()
+            self.owner._active.set()
+
+        def __exit__(self, *exc):
+            self.owner._active.clear()
+            if self.owner._nv is not None:
+                self.owner.sample()
+            self.owner.regions += 1
+            return False
+
+    def timed(self):
+        return ClockSampler._Region(self)
 
     def stop(self):
         if self._thread is not None:
@@ -142,15 +167,17 @@ class ClockSampler:
             return {"error": self.error or "NVML unavailable"}
         return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
                 "sm_max_mhz": self.max_mhz, "samples": len(self.samples),
-                "reasons": sorted(self.reasons)}
+                "timed_regions": self.regions, "reasons": sorted(self.reasons),
+                "note": "sampled every %.0f ms inside every timed region of this run"
+                        % (1e3 * self._period)}
 
 
 # The sources each profiled kernel is built from.
 _COMMON_SOURCES = ("tc_ptx.cuh", "common.cuh", "launch.h")
 KERNEL_SOURCES = {
-    "tc_state_kernel": ("tc_forward.cu",) + _COMMON_SOURCES,
-    "tc_apply_kernel": ("tc_forward.cu",) + _COMMON_SOURCES,
-    "tc_fused_kernel": ("tc_forward.cu",) + _COMMON_SOURCES,
+    "tc_state_kernel": ("tc_forward.cu", "tc_common.cuh") + _COMMON_SOURCES,
+    "tc_apply_kernel": ("tc_forward.cu", "tc_common.cuh") + _COMMON_SOURCES,
+    "tc_fused_kernel": ("tc_forward.cu", "tc_common.cuh") + _COMMON_SOURCES,
     "anchor_attn_kernel": ("anchor.cu",) + _COMMON_SOURCES,
     "attnres_kernel": ("attnres.cu",) + _COMMON_SOURCES,
 }
@@ -246,7 +273,8 @@ def run_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": _config(wl, world, note="one head (full N) per step on the host cores"),
+        "config": _config(wl, world),
+        "note": "one head (full N) per step on the host cores",
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{args.steps} heads of {wl.name}, one per step, full N"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -255,7 +283,7 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def _config(wl, world, note="", plan=None):
+def _config(wl, world):
     cfg = {"workload": wl.name, "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d,
            "grid": list(wl.grid), "rope": wl.rope,
            "rope_split": list(wl.split) if wl.rope else None, "eps": wl.eps,
@@ -271,10 +299,6 @@ def _config(wl, world, note="", plan=None):
     if wl.layer == "anchor":              # softmax attention: no eps, keys unscaled
         cfg["layer"] = "gated-softmax anchor"
         del cfg["eps"], cfg["k_scale"]
-    if plan:
-        cfg["launch_plan"] = plan
-    if note:
-        cfg["note"] = note
     return cfg
 
 
@@ -293,10 +317,36 @@ def _barrier(world):
         torch.distributed.barrier()
 
 
+SAMPLER = None      # the run's ClockSampler; every timed region is sampled
+
+
+def _start_sampler(dev):
+    global SAMPLER
+    SAMPLER = ClockSampler(dev)
+    SAMPLER.start()
+
+
+def _stop_sampler():
+    """The clock record over every timed region so far (then sampling stops)."""
+    global SAMPLER
+    if SAMPLER is None:
+        return {"error": "no timed region"}
+    rec = SAMPLER.stop()
+    SAMPLER = None
+    return rec
+
+
 def _time_steps(fn, steps, stream, flush=None):
     """Device seconds of `steps` calls of fn on `stream`: one event pair around
     all of them, or, with an L2 flush between steps, one pair per step with the
     flush outside the pairs."""
+    if SAMPLER is not None:
+        with SAMPLER.timed():
+            return _time_steps_raw(fn, steps, stream, flush)
+    return _time_steps_raw(fn, steps, stream, flush)
+
+
+def _time_steps_raw(fn, steps, stream, flush=None):
     if flush is None:
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record(stream)
@@ -364,10 +414,8 @@ def run_sla(args, rank, world, local):
     # -------- device-resident timing of the forward: K steps
     _barrier(world)
     torch.cuda.synchronize(dev)
-    sampler = ClockSampler(dev)
-    sampler.start()
+    _start_sampler(dev)
     secs = _time_steps(step, args.steps, stream, scrub)
-    clocks = sampler.stop()
     torch.cuda.synchronize(dev)
     _barrier(world)
     secs = _max_over_ranks(secs, world, dev)
@@ -449,6 +497,10 @@ def run_sla(args, rank, world, local):
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": ke,
                "ms_per_step": 1e3 * esecs / ke}
 
+    workloads = None
+    if world == 1 and wl.name == HEADLINE and not args.no_workloads:
+        workloads = time_workloads(args, dev, stream)
+
     if rank != 0:
         return
     peak, peak_src = measured_peaks()
@@ -478,15 +530,13 @@ def run_sla(args, rank, world, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if bf16 else "f32",
         "data": "synthetic (seeded N(0,1) q,k,v,g on the latent token grid)",
-        "config": _config(wl, world, plan=(
-            "block-causal: state, block scan and apply launches, %d blocks of %d tokens, carried "
-            "state updated in place" % (wl.N // wl.block_tokens, wl.block_tokens) if blocks else
-            "fused, clusters of %d CTAs per head" % cluster if cluster > 0 else
-            "state + apply launches")),
+        "config": _config(wl, world),
+        "launch_plan": _forward_plan(wl, cluster),
         "roofline": roofline,
         "e2e": e2e,
         "gpu_launches": (3 if blocks else 1 if cluster > 0 else 2) * args.steps,
-        "clocks": clocks,
+        "workloads": workloads,
+        "clocks": _stop_sampler(),
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, host)
@@ -494,6 +544,9 @@ def run_sla(args, rank, world, local):
 
 
 BWD_METRIC = "linear-attn bwd token-heads/s; HBM GB/s as % of B300 peak"
+BWD_LAUNCHES = 9
+BWD_PLAN = ("backward: state(k, v), apply raw(q), terms, state(q, a; dden), apply(a; S), "
+            "dq, apply(v; dS), dk, apply(k; dS) (tcgen05 state/apply kernels + elementwise)")
 
 
 def oracle_backward_heads(wl, tensors, heads):
@@ -543,10 +596,8 @@ def run_backward(args, rank, world, local):
         raise RuntimeError("device status after warm-up")
     _barrier(world)
     torch.cuda.synchronize(dev)
-    sampler = ClockSampler(dev)
-    sampler.start()
+    _start_sampler(dev)
     secs = _time_steps(step, args.steps, stream, scrub)
-    clocks = sampler.stop()
     torch.cuda.synchronize(dev)
     _barrier(world)
     secs = _max_over_ranks(secs, world, dev)
@@ -575,9 +626,8 @@ def run_backward(args, rank, world, local):
     peak, peak_src = measured_peaks()
     achieved = alg / per_step / 1e9
     if wl.dtype == torch.bfloat16:
-        launches = 9
-        plan = ("backward: state(k, v), apply raw(q), terms, state(q, a; dden), apply(a; S), "
-                "dq, apply(v; dS), dk, apply(k; dS) (tcgen05 state/apply kernels + elementwise)")
+        launches = BWD_LAUNCHES
+        plan = BWD_PLAN
     else:
         launches = 3
         plan = "backward: state partials, query pass, key pass (fp32 FMA kernels)"
@@ -587,7 +637,8 @@ def run_backward(args, rank, world, local):
         "ms_per_step": 1e3 * per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if wl.dtype == torch.bfloat16 else "f32",
         "data": "synthetic (seeded N(0,1) q,k,v,g and upstream gradient on the latent token grid)",
-        "config": _config(wl, world, plan=plan),
+        "config": _config(wl, world),
+        "launch_plan": plan,
         "roofline": {"bound": "hbm", "kernel": f"backward ({launches} launches)",
                      "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -595,7 +646,7 @@ def run_backward(args, rank, world, local):
                      "algorithmic_bytes_per_launch": alg, "traffic": None},
         "e2e": e2e,
         "gpu_launches": launches * args.steps,
-        "clocks": clocks,
+        "clocks": _stop_sampler(),
     }
     if not args.no_cpu_baseline:
         heads = [(b, h) for b in range(wl.B) for h in range(wl.H)]
@@ -690,10 +741,8 @@ def run_anchor(args, rank, world, local):
         raise RuntimeError("device status after warm-up")
     _barrier(world)
     torch.cuda.synchronize(dev)
-    sampler = ClockSampler(dev)
-    sampler.start()
+    _start_sampler(dev)
     secs = _time_steps(step, args.steps, stream, scrub)
-    clocks = sampler.stop()
     torch.cuda.synchronize(dev)
     _barrier(world)
     secs = _max_over_ranks(secs, world, dev)
@@ -731,10 +780,9 @@ def run_anchor(args, rank, world, local):
         "ms_per_step": 1e3 * per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) q,k,v,g on the latent token grid)",
-        "config": _config(wl, world, plan=(
-            "RoPE pre-pass (rotated q, k) + anchor_attn_kernel (tcgen05, 128 queries x 64-key "
-            "tiles per CTA)" if wl.rope else "anchor_attn_kernel"),
-            note="compute-bound: K and V of a head are re-read from L2 by every CTA"),
+        "config": _config(wl, world),
+        "launch_plan": _anchor_plan(wl),
+        "note": "compute-bound: K and V of a head are re-read from L2 by every CTA",
         "roofline": {"bound": "tensor", "kernel": "anchor_attn_kernel", "achieved": achieved,
                      "peak": burst, "unit": "TFLOP/s", "frac": achieved / burst,
                      "peak_source": f"{src} cuBLAS bf16, burst (bf16_tflops); the SM clock "
@@ -744,7 +792,7 @@ def run_anchor(args, rank, world, local):
                      "step_tflops": flops / per_step / 1e12, "traffic": None},
         "e2e": e2e,
         "gpu_launches": (2 if wl.rope else 1) * args.steps,
-        "clocks": clocks,
+        "clocks": _stop_sampler(),
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = anchor_cpu_baseline(wl, host)
@@ -770,8 +818,9 @@ def run_anchor_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": _config(wl, world, note=f"{min(ANCHOR_ROWS, wl.N)} query rows of one head "
-                                          "(all N keys) per step on the host cores"),
+        "config": _config(wl, world),
+        "note": f"{min(ANCHOR_ROWS, wl.N)} query rows of one head (all N keys) per step on "
+                "the host cores",
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": _blas_threads(),
                          "kind": "oracle",
                          "sample": f"{args.steps} samples of {min(ANCHOR_ROWS, wl.N)} query "
@@ -785,19 +834,18 @@ def run_anchor_reference(args, rank, world):
 ATTNRES_METRIC = "AttnRes aggregation tokens/s; HBM GB/s as % of B300 peak"
 ATTNRES_UNIT = "tokens/s"
 ATTNRES_ROWS = 4096        # tokens per oracle call
+ATTNRES_PLAN = ("attnres_kernel (bulk-copy ring of token slots, a CTA's threads over the "
+                "hidden size, one barrier per token)")
 
 
-def _attnres_config(wl, world, note=""):
+def _attnres_config(wl, world):
     cfg = {"workload": wl.name, "sources": wl.H, "tokens": wl.tokens, "hidden": wl.d,
            "grid": list(wl.grid), "batch": wl.B, "input_dtype": "bfloat16", "query_dtype": "f32",
            "eps": 1e-6, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
            "l2": ("inputs larger than L2 (%.0f MB vs 126 MB), steps back to back"
                   % (wl.algorithmic_bytes / 1e6) if wl.algorithmic_bytes >= 4 * L2_BYTES
                   else "L2 flushed between steps (a 252 MB buffer written outside the "
-                       "timed events)"),
-           "launch_plan": "attnres_kernel (one warp per token, two passes over the rows)"}
-    if note:
-        cfg["note"] = note
+                       "timed events)")}
     return cfg
 
 
@@ -844,10 +892,8 @@ def run_attnres(args, rank, world, local):
         step()
     _barrier(world)
     torch.cuda.synchronize(dev)
-    sampler = ClockSampler(dev)
-    sampler.start()
+    _start_sampler(dev)
     secs = _time_steps(step, args.steps, stream, scrub)
-    clocks = sampler.stop()
     torch.cuda.synchronize(dev)
     _barrier(world)
     secs = _max_over_ranks(secs, world, dev)
@@ -881,6 +927,7 @@ def run_attnres(args, rank, world, local):
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) summaries scaled 1+n, N(0,1)*3/sqrt(C) query)",
         "config": _attnres_config(wl, world),
+        "launch_plan": ATTNRES_PLAN,
         "roofline": {"bound": "hbm", "kernel": "attnres_kernel", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_src} copy bandwidth",
@@ -889,7 +936,7 @@ def run_attnres(args, rank, world, local):
                      "traffic": stored_traffic("attnres_kernel", wl.name)},
         "e2e": e2e,
         "gpu_launches": args.steps,
-        "clocks": clocks,
+        "clocks": _stop_sampler(),
     }
     if not args.no_cpu_baseline:
         done, elapsed, rows = 0, 0.0, 0
@@ -925,8 +972,8 @@ def run_attnres_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": _attnres_config(wl, world, note=f"{min(ATTNRES_ROWS, wl.tokens)} tokens per "
-                                                  "step on the host cores"),
+        "config": _attnres_config(wl, world),
+        "note": f"{min(ATTNRES_ROWS, wl.tokens)} tokens per step on the host cores",
         "cpu_baseline": {"value": value, "unit": ATTNRES_UNIT, "cores": _blas_threads(),
                          "kind": "oracle",
                          "sample": f"{args.steps} samples of {min(ATTNRES_ROWS, wl.tokens)} "
@@ -936,6 +983,145 @@ def run_attnres_reference(args, rank, world):
         "gpu_launches": 0,
     }
     print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------ the other configurations ----
+
+# Timed on the headline line, each with the run's --steps and --warmup: the other
+# forward configurations, the pages' 736-row 720p bucket, the block-causal form, the
+# backward, and the anchor and AttnRes layers.
+EXTRA_WORKLOADS = ("5b_480p", "14b_480p", "5b_720p_60s", "5b_720p_736", "5b_720p_block5",
+                   "5b_720p:backward", "anchor_5b_720p", "anchor_5b_480p", "attnres_5b_720p",
+                   "attnres_14b_480p")
+
+
+def _forward_plan(wl, cluster):
+    if wl.block_frames:
+        return ("block-causal: state, block scan and apply launches, %d blocks of %d tokens, "
+                "carried state updated in place" % (wl.N // wl.block_tokens, wl.block_tokens))
+    if wl.dtype != torch.bfloat16:
+        return "fp32: state partials + apply (FMA units)"
+    if cluster > 0:
+        return "fused, clusters of %d CTAs per head" % cluster
+    return "state + apply launches"
+
+
+def _anchor_plan(wl):
+    return ("RoPE pre-pass (rotated k) + anchor_attn_kernel (tcgen05, 128 queries x 128-key "
+            "tiles per CTA)" if wl.rope else "anchor_attn_kernel")
+
+
+def _device_inputs(wl, dev, count=4):
+    """Seeded N(0, 1) inputs drawn on the device (k scaled by k_scale): the recipe's
+    distribution, drawn where the timing runs; these runs are not compared with the oracle."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    out = []
+    for i in range(count):
+        x = torch.randn((wl.B, wl.H, wl.N, wl.d), generator=gen, device=dev, dtype=torch.float32)
+        if i == 1 and wl.k_scale != 1.0:
+            x.mul_(wl.k_scale)
+        out.append(x.to(wl.dtype))
+        del x
+    return out
+
+
+def time_workloads(args, dev, stream):
+    """ms, throughput and roofline fraction of each EXTRA_WORKLOADS entry."""
+    from gated_linear_attention_attn_b300 import sla
+    peak, _ = measured_peaks()
+    burst, sustained, _ = measured_tensor_peaks()
+    scrub_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+
+    def scrub():
+        scrub_buf.fill_(1)
+
+    def timed(step, alg_bytes):
+        for _ in range(max(args.warmup, 3)):
+            step()
+        flush = scrub if alg_bytes < 4 * L2_BYTES else None
+        secs = _time_steps(step, args.steps, stream, flush) / args.steps
+        if sla.last_device_status(stream, dev) != sla.OK:
+            raise RuntimeError("device status after a workload")
+        return secs, ("L2 flushed between steps" if flush else "inputs larger than L2")
+
+    results = {}
+    for entry in EXTRA_WORKLOADS:
+        name, _, pass_ = entry.partition(":")
+        wl = WORKLOADS[name]
+        rec = {"config": _config(wl, 1)}
+        if wl.layer == "attnres":
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(0)
+            src = torch.randn((wl.H, wl.tokens, wl.d), generator=gen, device=dev)
+            src.mul_(torch.arange(1, wl.H + 1, device=dev, dtype=torch.float32).view(-1, 1, 1))
+            src = src.to(torch.bfloat16)
+            w = torch.randn((wl.d,), generator=gen, device=dev) * (3.0 / wl.d ** 0.5)
+            out = torch.empty(src.shape[1:], dtype=torch.bfloat16, device=dev)
+            srcs = list(src.unbind(0))
+            secs, l2 = timed(lambda: sla.attnres_aggregate(srcs, w, out=out, stream=stream),
+                             wl.algorithmic_bytes)
+            rec.update(ms=1e3 * secs, value=wl.tokens / secs, unit=ATTNRES_UNIT,
+                       hbm_gbs=wl.algorithmic_bytes / secs / 1e9,
+                       hbm_frac=wl.algorithmic_bytes / secs / 1e9 / peak,
+                       launch_plan=ATTNRES_PLAN, l2=l2, gpu_launches_per_step=1)
+            del src, w, out, srcs
+        elif wl.layer == "anchor":
+            q, k, v, g = _device_inputs(wl, dev)
+            rope = sla.RopeTable(wl.grid, wl.split, wl.base, device=dev) if wl.rope else None
+            out = torch.empty_like(q)
+            secs, l2 = timed(lambda: sla.anchor_forward(q, k, v, g, out=out, rope=rope,
+                                                        stream=stream), wl.algorithmic_bytes)
+            tf = wl.algorithmic_flops / secs / 1e12
+            rec.update(ms=1e3 * secs, value=wl.token_heads / secs, unit=UNIT, tflops=tf,
+                       tensor_frac=tf / burst, tensor_frac_of_sustained=tf / sustained,
+                       launch_plan=_anchor_plan(wl), l2=l2,
+                       gpu_launches_per_step=2 if wl.rope else 1)
+            del q, k, v, g, out, rope
+        elif pass_ == "backward":
+            q, k, v, g, dout = _device_inputs(wl, dev, 5)
+            rope = sla.RopeTable(wl.grid, wl.split, wl.base, device=dev) if wl.rope else None
+            grads = tuple(torch.empty_like(q) for _ in range(4))
+            alg = 9 * wl.B * wl.H * wl.N * wl.d * wl.elem_size
+            secs, l2 = timed(lambda: sla.linattn_backward(q, k, v, g, dout, rope=rope,
+                                                          eps=wl.eps, grads=grads,
+                                                          stream=stream), alg)
+            rec.update(ms=1e3 * secs, value=wl.token_heads / secs, unit=UNIT,
+                       hbm_gbs=alg / secs / 1e9, hbm_frac=alg / secs / 1e9 / peak,
+                       algorithmic_bytes=alg, launch_plan=BWD_PLAN, l2=l2,
+                       gpu_launches_per_step=BWD_LAUNCHES)
+            del q, k, v, g, dout, rope, grads
+        else:
+            q, k, v, g = _device_inputs(wl, dev)
+            rope = sla.RopeTable(wl.grid, wl.split, wl.base, device=dev) if wl.rope else None
+            out = torch.empty_like(q)
+            if wl.block_frames:
+                carried = torch.zeros(wl.B, wl.H, sla.CARRIED_FLOATS, dtype=torch.float32,
+                                      device=dev)
+
+                def step():
+                    sla.linattn_forward_block_causal(q, k, v, g, wl.block_tokens, out=out,
+                                                     rope=rope, eps=wl.eps, state_in=carried,
+                                                     state_out=carried, stream=stream)
+                cluster, launches = 0, 3
+            else:
+                def step():
+                    sla.linattn_forward(q, k, v, g, out=out, rope=rope, eps=wl.eps,
+                                        stream=stream)
+                cluster = sla.forward_cluster(wl.B, wl.H, wl.N, wl.rope, device=dev)
+                launches = 1 if cluster > 0 else 2
+            secs, l2 = timed(step, wl.algorithmic_bytes)
+            rec.update(ms=1e3 * secs, value=wl.token_heads / secs, unit=UNIT,
+                       hbm_gbs=wl.algorithmic_bytes / secs / 1e9,
+                       hbm_frac=wl.algorithmic_bytes / secs / 1e9 / peak,
+                       launch_plan=_forward_plan(wl, cluster), l2=l2,
+                       gpu_launches_per_step=launches)
+            del q, k, v, g, out, rope
+        results[entry] = rec
+        torch.cuda.empty_cache()
+    del scrub_buf
+    torch.cuda.empty_cache()
+    return results
 
 
 def main():

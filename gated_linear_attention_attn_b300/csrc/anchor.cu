@@ -131,6 +131,10 @@ anchor_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         mbar_init(mma_done, 1);
         *abort_flag = (smem0 & 1023u) ? 1 : 0;    // the swizzled tiles need 1 KB alignment
         if (smem0 & 1023u) raise_status(p.status, kStatusLayout);
+        if (p.rope && !rope_table_ok(p.rv)) {      // nothing of the table is read
+            *abort_flag = 1;
+            raise_status(p.status, kStatusBadTable);
+        }
         fence_mbar_init();
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
@@ -266,19 +270,20 @@ anchor_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             // column block cb at cb * 16 KB, 16-byte chunk c of row r at
             // position c xor (r mod 8) of the row's 128 bytes
             const uint4* q4 = reinterpret_cast<const uint4*>(p.q + base);
-            TokenPos pos{};
-            if (p.rope) pos = token_pos(p.rv, live ? row : 0);
+            // this token's (cos, sin) pairs; the table is read only when it checked out
+            const float2* cs = p.rope && ok ? rope_pairs(p.rv) + (size_t)(live ? row : 0) * (kAnD / 2)
+                                            : nullptr;
 #pragma unroll 1
             for (int cb = 0; cb < 4; ++cb) {
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     uint4 u = live ? ldg_nc_na128(q4 + cb * 8 + c) : make_uint4(0, 0, 0, 0);
-                    if (p.rope) {
+                    if (cs) {
                         uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             float2 f = bf2_to_f2(w[i]);
-                            rotate_pair(f.x, f.y, rope_cs(p.rv, pos, cb * 32 + c * 4 + i));
+                            rotate_pair(f.x, f.y, __ldg(cs + cb * 32 + c * 4 + i));
                             w[i] = f2_to_bf2(f.x, f.y);
                         }
                         u = make_uint4(w[0], w[1], w[2], w[3]);
@@ -411,14 +416,18 @@ anchor_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 }
 
 // kr = R k per token row (bf16 in and out), 32 threads a row, eight
-// dimensions (four pairs) each; the angles from the table's fp32 axis parts.
+// dimensions (four pairs) each; the angles from the table's fp32 pairs.
 __global__ void __launch_bounds__(256)
 anchor_rope_kernel(const uint4* __restrict__ k, uint4* __restrict__ kr, int N, long long rows,
-                   RopeView rope) {
+                   RopeView rope, unsigned* status) {
     const long long row = (long long)blockIdx.x * 8 + threadIdx.x / 32;
     const int c = threadIdx.x % 32;
+    if (!rope_table_ok(rope)) {               // nothing of the table is read
+        if (blockIdx.x == 0 && threadIdx.x == 0) raise_status(status, kStatusBadTable);
+        return;
+    }
     if (row >= rows) return;
-    const TokenPos pos = token_pos(rope, (int)(row % N));
+    const float2* cs = rope_pairs(rope) + (size_t)(row % N) * (kAnD / 2);
     const size_t at = (size_t)row * (kAnD / 8) + c;
     const uint4 u = __ldg(k + at);
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -426,7 +435,7 @@ anchor_rope_kernel(const uint4* __restrict__ k, uint4* __restrict__ kr, int N, l
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         float2 f = bf2_to_f2(w[i]);
-        rotate_pair(f.x, f.y, rope_cs(rope, pos, 4 * c + i));
+        rotate_pair(f.x, f.y, __ldg(cs + 4 * c + i));
         o[i] = f2_to_bf2(f.x, f.y);
     }
     kr[at] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -476,7 +485,7 @@ cudaError_t launch_anchor(const void* q, const void* k, const void* v, const voi
         uint4* kr = static_cast<uint4*>(workspace);
         const long long rows = (long long)BH * N;
         anchor_rope_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>((const uint4*)k, kr, N,
-                                                                           rows, *rope);
+                                                                           rows, *rope, status);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         ka = kr;

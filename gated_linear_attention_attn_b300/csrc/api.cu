@@ -87,37 +87,28 @@ static sla_status_t check_dims(int B, int H, int N, int d) {
 
 static bool bad_eps(float eps) { return !std::isfinite(eps) || eps < 0.f; }
 
-// The RoPE grid must cover tokens [offset, offset + N) (exactly N tokens when
-// exact) and have bands that sum to d; fills *rv.
-static sla_status_t check_rope_range(const sla_rope_table_t* rope, int N, int d, long long offset,
+// A RoPE table pointer: NULL (no RoPE), else 256-byte aligned; the launch
+// reads tokens [offset, offset + N) (exactly N tokens when exact).  What the
+// table holds is checked on the device against its header (rope_table_ok);
+// fills *rv.
+static sla_status_t check_rope_range(const float* table, int N, int d, long long offset,
                                      bool exact, RopeView* rv) {
-    if (!rope) return SLA_OK;
-    if (!rope->table) return SLA_ERR_INVALID_ARG;
-    if (rope->T < 1 || rope->Hs < 1 || rope->Ws < 1) return SLA_ERR_INVALID_ARG;
-    if (rope->dt < 0 || rope->dh < 0 || rope->dw < 0) return SLA_ERR_INVALID_ARG;
-    if ((rope->dt | rope->dh | rope->dw) & 1) return SLA_ERR_INVALID_ARG;
-    if (rope->dt + rope->dh + rope->dw != d) return SLA_ERR_INVALID_ARG;
-    const long long grid = (long long)rope->T * rope->Hs * rope->Ws;
-    if (exact ? grid != N : (offset < 0 || offset + N > grid)) return SLA_ERR_INVALID_ARG;
-    if (grid > 0x7fffffffLL) return SLA_ERR_UNSUPPORTED;
-    if (misaligned(rope->table, 256)) return SLA_ERR_ALIGNMENT;
-    const float2* base = reinterpret_cast<const float2*>(rope->table);
-    rv->pt = rope->dt / 2;
-    rv->ph = rope->dh / 2;
-    rv->pw = rope->dw / 2;
-    rv->T = rope->T;
-    rv->Hs = rope->Hs;
-    rv->Ws = rope->Ws;
-    rv->tab_t = base;
-    rv->tab_h = base + (size_t)rope->T * rv->pt;
-    rv->tab_w = rv->tab_h + (size_t)rope->Hs * rv->ph;
-    rv->tok = reinterpret_cast<const uint32_t*>(rope->table) +
-              rope_tok_offset_words(rope->T, rope->Hs, rope->Ws, rope->dt, rope->dh, rope->dw);
+    if (!table) return SLA_OK;
+    if (offset < 0) return SLA_ERR_INVALID_ARG;
+    const long long need = offset + N;
+    if (need > 0x7fffffffLL || (long long)rope_total_words(need, d) > 0x7fffffffLL)
+        return SLA_ERR_UNSUPPORTED;
+    if (misaligned(table, 256)) return SLA_ERR_ALIGNMENT;
+    rv->hdr = reinterpret_cast<const uint32_t*>(table);
+    rv->tok = rv->hdr + kRopeHeaderWords;
+    rv->need = (int)need;
+    rv->exact = exact ? 1 : 0;
+    rv->d = d;
     return SLA_OK;
 }
 
-static sla_status_t check_rope(const sla_rope_table_t* rope, int N, int d, RopeView* rv) {
-    return check_rope_range(rope, N, d, 0, true, rv);
+static sla_status_t check_rope(const float* table, int N, int d, RopeView* rv) {
+    return check_rope_range(table, N, d, 0, true, rv);
 }
 
 // Buffers: none null, all 16-byte aligned, the output overlapping no input.
@@ -140,8 +131,7 @@ static sla_status_t check_buffers(const void* const* ins, const size_t* in_bytes
 // bytes.
 sla_status_t check_forward(const void* q, const void* k, const void* v, const void* g,
                            const void* out, int B, int H, int N, int d,
-                           const sla_rope_table_t* rope, float eps, size_t elem,
-                           RopeView* rv) {
+                           const float* rope, float eps, size_t elem, RopeView* rv) {
     if (!q || !k || !v || !g || !out) return SLA_ERR_INVALID_ARG;
     sla_status_t st = check_dims(B, H, N, d);
     if (st == SLA_ERR_INVALID_ARG) return st;
@@ -160,30 +150,48 @@ using namespace sla;
 
 extern "C" {
 
-size_t sla_rope_table_floats(int T, int Hs, int Ws, int dt, int dh, int dw) {
-    if (T < 1 || Hs < 1 || Ws < 1 || dt < 0 || dh < 0 || dw < 0) return 0;
-    if ((dt | dh | dw) & 1) return 0;
-    return rope_total_words(T, Hs, Ws, dt, dh, dw);
+size_t sla_rope_table_floats(int N, int d) {
+    if (N < 1 || d < 2 || (d & 1)) return 0;
+    const size_t words = rope_total_words(N, d);
+    return words > 0x7fffffffULL ? 0 : words;
 }
 
-sla_status_t sla_rope_table_fill(float* table, int T, int Hs, int Ws, int dt, int dh, int dw,
-                                 float base, sla_stream_t stream) {
+sla_status_t sla_rope_table_fill(float* table, int T, int Hs, int Ws, int d, int dt, int dh,
+                                 int dw, float base, sla_stream_t stream) {
     if (!table) return SLA_ERR_INVALID_ARG;
     if (T < 1 || Hs < 1 || Ws < 1 || dt < 0 || dh < 0 || dw < 0) return SLA_ERR_INVALID_ARG;
-    if ((dt | dh | dw) & 1) return SLA_ERR_INVALID_ARG;
+    if ((dt | dh | dw) & 1 || dt + dh + dw != d || d < 2) return SLA_ERR_INVALID_ARG;
     if (!std::isfinite(base) || base <= 0.f) return SLA_ERR_INVALID_ARG;
+    const long long N = (long long)T * Hs * Ws;
+    if (N > 0x7fffffffLL || rope_total_words(N, d) > 0x7fffffffULL) return SLA_ERR_UNSUPPORTED;
     if (misaligned(table, 256)) return SLA_ERR_ALIGNMENT;
-    if (rope_total_words(T, Hs, Ws, dt, dh, dw) > 0x7fffffffULL) return SLA_ERR_UNSUPPORTED;
     if (launch_rope_fill(table, T, Hs, Ws, dt, dh, dw, base, (cudaStream_t)stream) !=
-        cudaSuccess)
+        cudaSuccess) {
+        cudaGetLastError();
         return SLA_ERR_CUDA;
+    }
+    return SLA_OK;
+}
+
+sla_status_t sla_rope_table_from_pairs(float* table, const float* pairs, int N, int d,
+                                       sla_stream_t stream) {
+    if (!table || !pairs || N < 1 || d < 2 || (d & 1)) return SLA_ERR_INVALID_ARG;
+    if (rope_total_words(N, d) > 0x7fffffffULL) return SLA_ERR_UNSUPPORTED;
+    if (misaligned(table, 256) || misaligned(pairs, 8)) return SLA_ERR_ALIGNMENT;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(table), y = reinterpret_cast<uintptr_t>(pairs);
+    const size_t tbytes = rope_total_words(N, d) * 4, pbytes = (size_t)N * d * 4;
+    if (x < y + pbytes && y < x + tbytes) return SLA_ERR_INVALID_ARG;
+    if (launch_rope_from_pairs(table, pairs, N, d, (cudaStream_t)stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SLA_ERR_CUDA;
+    }
     return SLA_OK;
 }
 
 // Shared body of both forward entry points.
 static sla_status_t forward(const void* q, const void* k, const void* v, const void* g,
                             void* out, int B, int H, int N, int d,
-                            const sla_rope_table_t* rope, float eps, sla_stream_t stream,
+                            const float* rope, float eps, sla_stream_t stream,
                             bool is_f32) {
     RopeView rv{};
     sla_status_t st = check_forward(q, k, v, g, out, B, H, N, d, rope, eps,
@@ -206,7 +214,8 @@ static sla_status_t forward(const void* q, const void* k, const void* v, const v
         const int C = simt_chunks(BH, N, ds->num_sms);
         if ((st = workspace(dev, s, simt_workspace_bytes(BH, C), &ws)) != SLA_OK) return st;
         err = launch_simt_f32((const float*)q, (const float*)k, (const float*)v,
-                              (const float*)g, (float*)out, B, H, N, rp, eps, (float*)ws, C, s);
+                              (const float*)g, (float*)out, B, H, N, rp, eps, (float*)ws, C,
+                              ds->status, s);
     } else if (const int C = tc_forward_cluster(dev, BH, N, rp != nullptr, ds->num_sms)) {
         err = launch_tc_fused(q, k, v, g, out, B, H, N, C, rp, eps, ds->status, s);
     } else {
@@ -224,14 +233,14 @@ static sla_status_t forward(const void* q, const void* k, const void* v, const v
 
 sla_status_t sla_linattn_forward(const void* q, const void* k, const void* v, const void* g,
                                  void* out, int B, int H, int N, int d,
-                                 const sla_rope_table_t* rope_table, float eps,
+                                 const float* rope_table, float eps,
                                  sla_stream_t stream) {
     return forward(q, k, v, g, out, B, H, N, d, rope_table, eps, stream, false);
 }
 
 sla_status_t sla_linattn_forward_f32(const float* q, const float* k, const float* v,
                                      const float* g, float* out, int B, int H, int N, int d,
-                                     const sla_rope_table_t* rope_table, float eps,
+                                     const float* rope_table, float eps,
                                      sla_stream_t stream) {
     return forward(q, k, v, g, out, B, H, N, d, rope_table, eps, stream, true);
 }
@@ -239,7 +248,7 @@ sla_status_t sla_linattn_forward_f32(const float* q, const float* k, const float
 // Shared body of both backward entry points.
 static sla_status_t backward(const void* q, const void* k, const void* v, const void* g,
                              const void* dout, void* dq, void* dk, void* dv, void* dg, int B,
-                             int H, int N, int d, const sla_rope_table_t* rope, float eps,
+                             int H, int N, int d, const float* rope, float eps,
                              sla_stream_t stream, bool is_f32) {
     if (!q || !k || !v || !g || !dout || !dq || !dk || !dv || !dg) return SLA_ERR_INVALID_ARG;
     sla_status_t st = check_dims(B, H, N, d);
@@ -283,7 +292,8 @@ static sla_status_t backward(const void* q, const void* k, const void* v, const 
     const cudaError_t err =
         is_f32 ? launch_backward_f32((const float*)q, (const float*)k, (const float*)v,
                                      (const float*)g, (const float*)dout, (float*)dq, (float*)dk,
-                                     (float*)dv, (float*)dg, B, H, N, rp, eps, (float*)ws, C, s)
+                                     (float*)dv, (float*)dg, B, H, N, rp, eps, (float*)ws, C,
+                                     ds->status, s)
                : launch_backward_bf16(q, k, v, g, dout, dq, dk, dv, dg, B, H, N, rp, eps,
                                       (float*)ws, ds->num_sms, ds->status, s);
     if (err != cudaSuccess) {
@@ -296,7 +306,7 @@ static sla_status_t backward(const void* q, const void* k, const void* v, const 
 sla_status_t sla_linattn_backward(const void* q, const void* k, const void* v, const void* g,
                                   const void* dout, void* dq, void* dk, void* dv, void* dg,
                                   int B, int H, int N, int d,
-                                  const sla_rope_table_t* rope_table, float eps,
+                                  const float* rope_table, float eps,
                                   sla_stream_t stream) {
     return backward(q, k, v, g, dout, dq, dk, dv, dg, B, H, N, d, rope_table, eps, stream, false);
 }
@@ -304,14 +314,14 @@ sla_status_t sla_linattn_backward(const void* q, const void* k, const void* v, c
 sla_status_t sla_linattn_backward_f32(const float* q, const float* k, const float* v,
                                       const float* g, const float* dout, float* dq, float* dk,
                                       float* dv, float* dg, int B, int H, int N, int d,
-                                      const sla_rope_table_t* rope_table, float eps,
+                                      const float* rope_table, float eps,
                                       sla_stream_t stream) {
     return backward(q, k, v, g, dout, dq, dk, dv, dg, B, H, N, d, rope_table, eps, stream, true);
 }
 
 sla_status_t sla_anchor_forward(const void* q, const void* k, const void* v, const void* g,
                                 void* out, int B, int H, int N, int d,
-                                const sla_rope_table_t* rope_table, sla_stream_t stream) {
+                                const float* rope_table, sla_stream_t stream) {
     if (!q || !k || !v || !g || !out) return SLA_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || N < 1 || d < 1) return SLA_ERR_INVALID_ARG;
     if (d != 256) return SLA_ERR_UNSUPPORTED;
@@ -386,7 +396,7 @@ size_t sla_linattn_carried_state_bytes(int B, int H, int d) {
 sla_status_t sla_linattn_forward_block_causal(const void* q, const void* k, const void* v,
                                               const void* g, void* out, int B, int H, int N,
                                               int d, int block_tokens,
-                                              const sla_rope_table_t* rope_table,
+                                              const float* rope_table,
                                               int rope_offset, float eps, const float* state_in,
                                               float* state_out, sla_stream_t stream) {
     if (!q || !k || !v || !g || !out) return SLA_ERR_INVALID_ARG;
@@ -465,7 +475,7 @@ size_t sla_linattn_state_bytes(int B, int H, int d) {
 }
 
 sla_status_t sla_linattn_state(const void* k, const void* v, void* state, int B, int H, int N,
-                               int d, const sla_rope_table_t* rope_table, sla_stream_t stream) {
+                               int d, const float* rope_table, sla_stream_t stream) {
     sla_status_t st = check_dims(B, H, N, d);
     if (st != SLA_OK) return st;
     const size_t bytes = (size_t)B * H * N * d * 2;
@@ -495,7 +505,7 @@ sla_status_t sla_linattn_state(const void* k, const void* v, void* state, int B,
 }
 
 sla_status_t sla_linattn_apply(const void* q, const void* g, const void* state, void* out, int B,
-                               int H, int N, int d, const sla_rope_table_t* rope_table, float eps,
+                               int H, int N, int d, const float* rope_table, float eps,
                                sla_stream_t stream) {
     sla_status_t st = check_dims(B, H, N, d);
     if (st == SLA_ERR_INVALID_ARG) return st;
@@ -517,6 +527,27 @@ sla_status_t sla_linattn_apply(const void* q, const void* g, const void* state, 
     if ((st = device_state(dev, &ds)) != SLA_OK) return st;
     if (launch_tc_apply(q, g, state, out, B, H, N, rope_table ? &rv : nullptr, eps, ds->status,
                         ds->num_sms, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return SLA_ERR_CUDA;
+    }
+    return SLA_OK;
+}
+
+sla_status_t sla_selftest_wait_timeout(unsigned int limit_us, sla_stream_t stream) {
+    if (limit_us < 1 || limit_us > 1000000u) return SLA_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SLA_ERR_CUDA;
+    }
+    DeviceState* ds = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        sla_status_t st = device_state(dev, &ds);
+        if (st != SLA_OK) return st;
+    }
+    if (launch_wait_selftest(1000ull * limit_us, ds->status,
+                             reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return SLA_ERR_CUDA;
     }
@@ -552,6 +583,7 @@ sla_status_t sla_last_device_status(sla_stream_t stream) {
     if (word != 0 && cudaMemset(ds->status, 0, sizeof(word)) != cudaSuccess)
         return SLA_ERR_CUDA;
     if (word & kStatusTimeout) return SLA_ERR_DEVICE_TIMEOUT;
+    if (word & kStatusBadTable) return SLA_ERR_INVALID_ARG;
     return word ? SLA_ERR_CUDA : SLA_OK;
 }
 

@@ -83,10 +83,11 @@ __device__ void load_features(const T* x, int base, int cnt, RopeView rope, floa
     }
     if (ROPE) {
         __syncthreads();
+        const float2* cs = rope_pairs(rope);
         for (int e = threadIdx.x; e < cnt * kPairs; e += blockDim.x) {
             const int r = e / kPairs, p = e % kPairs;
             rotate_pair(fr[r * kHeadDim + 2 * p], fr[r * kHeadDim + 2 * p + 1],
-                        rope_cs(rope, token_pos(rope, base + r), p));
+                        __ldg(cs + (size_t)(base + r) * kPairs + p));
         }
     }
 }
@@ -131,10 +132,10 @@ __device__ __forceinline__ void rows_times(const float* X, const float* M, int t
 template <bool ROPE>
 __device__ __forceinline__ void unrotate8(float (&y)[8], const RopeView& rope, int n, int tx) {
     if (!ROPE) return;
-    const TokenPos pos = token_pos(rope, n);
+    const float2* row = rope_pairs(rope) + (size_t)n * kPairs;
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
-        const float2 cs = rope_cs(rope, pos, col_of(tx, 2 * p) / 2);
+        const float2 cs = __ldg(row + col_of(tx, 2 * p) / 2);
         rotate_pair(y[2 * p], y[2 * p + 1], make_float2(cs.x, -cs.y));
     }
 }
@@ -155,6 +156,7 @@ bwd_query_kernel(const T* __restrict__ q, const T* __restrict__ g, const T* __re
     float* den = a + kBTile * kHeadDim;              // [32]
     float* dden = den + kBTile;                      // [32]
     const int bh = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
+    if (ROPE && !rope_table_ok(rope)) return;        // reported by the state partials
     const int ty = tid / 16, tx = tid % 16;
     const size_t head = (size_t)bh * N * kHeadDim;
     // the head's S, z, summed from the fp32 partials
@@ -273,6 +275,7 @@ bwd_key_kernel(const T* __restrict__ k, const T* __restrict__ v, T* __restrict__
     float* kr = kp + kBTile * kHeadDim;              // [32][128] R phi(k)
     float* vs = kr + kBTile * kHeadDim;              // [32][128] v
     const int bh = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
+    if (ROPE && !rope_table_ok(rope)) return;        // reported by the state partials
     const int ty = tid / 16, tx = tid % 16;
     const size_t head = (size_t)bh * N * kHeadDim;
     sum_partials(grad_partial + (size_t)bh * C * kBPartial, C, dS, dSt, dz);
@@ -392,6 +395,7 @@ bwd_grad_kernel(const uint4* __restrict__ x, const uint4* __restrict__ y,
     const long long row = (long long)blockIdx.x * kRowsPerBlock + threadIdx.x / 16;
     const int c = threadIdx.x % 16;
     if (row >= rows) return;
+    if (ROPE && !rope_table_ok(rope)) return;        // reported by the state kernel
     const size_t at = (size_t)row * 16 + c;
     float xf[8], yf[8];
     bf8_to_f8(x[at], xf);
@@ -421,7 +425,8 @@ bwd_grad_kernel(const uint4* __restrict__ x, const uint4* __restrict__ y,
 template <typename T>
 cudaError_t launch_backward(const T* q, const T* k, const T* v, const T* g, const T* dout, T* dq,
                             T* dk, T* dv, T* dg, int B, int H, int N, const RopeView* rope,
-                            float eps, float* workspace, int C, cudaStream_t stream) {
+                            float eps, float* workspace, int C, unsigned* status,
+                            cudaStream_t stream) {
     const int BH = B * H;
     const int tiles = (N + kBTile - 1) / kBTile;
     const int chunk = ((tiles + C - 1) / C) * kBTile;
@@ -429,8 +434,8 @@ cudaError_t launch_backward(const T* q, const T* k, const T* v, const T* g, cons
     float* state_partial = workspace;
     float* grad_partial = workspace + (size_t)BH * C * kBPartial;
     cudaError_t e = cudaSuccess;
-    if ((e = launch_simt_state_partials(k, v, B, H, N, rope, state_partial, C, stream)) !=
-        cudaSuccess)
+    if ((e = launch_simt_state_partials(k, v, B, H, N, rope, state_partial, C, status,
+                                        stream)) != cudaSuccess)
         return e;
     const dim3 grid(C, BH);
     if (rope) {
@@ -523,9 +528,9 @@ cudaError_t launch_backward_bf16(const void* q, const void* k, const void* v, co
 cudaError_t launch_backward_f32(const float* q, const float* k, const float* v, const float* g,
                                 const float* dout, float* dq, float* dk, float* dv, float* dg,
                                 int B, int H, int N, const RopeView* rope, float eps,
-                                float* workspace, int C, cudaStream_t stream) {
+                                float* workspace, int C, unsigned* status, cudaStream_t stream) {
     return launch_backward<float>(q, k, v, g, dout, dq, dk, dv, dg, B, H, N, rope, eps, workspace,
-                                  C, stream);
+                                  C, status, stream);
 }
 
 }  // namespace sla

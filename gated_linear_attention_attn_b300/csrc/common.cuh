@@ -1,5 +1,5 @@
-// Shared device helpers of the linear-attention library: the RoPE table view,
-// the device status word, bf16 packing.
+// Shared device helpers of the linear-attention library: the RoPE table
+// layout and view, the device status word, bf16 packing.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -14,54 +14,56 @@ constexpr int kPairs = kHeadDim / 2;
 // Bits of the device status word (one 32-bit word per device).
 constexpr unsigned kStatusTimeout = 1u;   // a bounded wait gave up
 constexpr unsigned kStatusLayout = 2u;    // shared memory not 1 KB aligned: nothing ran
+constexpr unsigned kStatusBadTable = 4u;  // a RoPE table's header does not fit the call
 
-// Layout of a RoPE table buffer, in 4-byte words: the separable fp32
-// (cos, sin) pairs of each axis ([T][dt/2], [Hs][dh/2], [Ws][dw/2]), then,
-// from the next 256-byte boundary, one row per token of d/2 (cos, sin) pairs
-// as two fp16 values in a word (cos in the low half).
-inline size_t rope_sep_words(int T, int Hs, int Ws, int dt, int dh, int dw) {
-    return (size_t)T * dt + (size_t)Hs * dh + (size_t)Ws * dw;
-}
-inline size_t rope_tok_offset_words(int T, int Hs, int Ws, int dt, int dh, int dw) {
-    return (rope_sep_words(T, Hs, Ws, dt, dh, dw) + 63) & ~size_t(63);
-}
-inline size_t rope_total_words(int T, int Hs, int Ws, int dt, int dh, int dw) {
-    return rope_tok_offset_words(T, Hs, Ws, dt, dh, dw) +
-           (size_t)T * Hs * Ws * (size_t)((dt + dh + dw) / 2);
+// Layout of a RoPE table buffer, in 4-byte words, for a grid of N tokens and
+// head dimension d (P = d/2 pairs):
+//   [0, 64)                 header (kRopeHdr* below)
+//   [64, 64 + N*P)          per-token rows: pair p of token n is one word,
+//                           fp16 cos in the low half, fp16 sin in the high half
+//   [64 + N*P, 64 + 3*N*P)  per-token pairs [N][P][2] as fp32 (cos, sin)
+constexpr int kRopeHeaderWords = 64;
+constexpr uint32_t kRopeMagic = 0x33414c53u;     // "SLA3" in little-endian bytes
+constexpr uint32_t kRopeVersion = 1u;
+// header words
+constexpr int kRopeHdrMagic = 0, kRopeHdrVersion = 1, kRopeHdrN = 2, kRopeHdrD = 3;
+constexpr int kRopeHdrT = 4, kRopeHdrHs = 5, kRopeHdrWs = 6;
+constexpr int kRopeHdrDt = 7, kRopeHdrDh = 8, kRopeHdrDw = 9, kRopeHdrBase = 10;
+constexpr int kRopeHdrRows = 11, kRopeHdrPairs = 12;   // word offsets of the two parts
+
+inline size_t rope_total_words(long long N, int d) {
+    return (size_t)kRopeHeaderWords + (size_t)N * (size_t)(d / 2) * 3;
 }
 
-// Device view of a filled RoPE table: (cos, sin) pairs per axis, each axis
-// [extent][band pairs], axes in the order t, h, w; and the per-token rows.
+// Device view of a RoPE table: which tokens a launch reads and which head
+// dimension it expects.  The kernels check the header against it before they
+// read anything else of the table (rope_table_ok).
 struct RopeView {
-    const float2* tab_t;   // [T][pt]
-    const float2* tab_h;   // [Hs][ph]
-    const float2* tab_w;   // [Ws][pw]
-    const uint32_t* tok;   // [N][64] fp16 (cos, sin) per pair, 256 bytes per token
-    int T, Hs, Ws;
-    int pt, ph, pw;        // pairs per band: dt/2, dh/2, dw/2
+    const uint32_t* hdr;   // the table: header, fp16 rows, fp32 pairs
+    const uint32_t* tok;   // the fp16 rows (hdr + kRopeHeaderWords): [tokens][d/2]
+    int need;              // the launch reads tokens [0, need) of the table
+    int exact;             // nonzero: the table must have exactly `need` tokens
+    int d;                 // head dimension the table must be built for
 };
 
-// Grid coordinates of token n: n = (t*Hs + h)*Ws + w.
-struct TokenPos {
-    int t, h, w;
-};
-
-__device__ __forceinline__ TokenPos token_pos(const RopeView& r, int n) {
-    TokenPos p;
-    int hw = n / r.Ws;
-    p.w = n - hw * r.Ws;
-    p.t = hw / r.Hs;
-    p.h = hw - p.t * r.Hs;
-    return p;
+// The header written by sla_rope_table_fill / sla_rope_table_from_pairs, and
+// enough tokens for the launch.
+__device__ __forceinline__ bool rope_table_ok(const RopeView& r) {
+    if (!r.hdr) return false;
+    const uint32_t magic = __ldg(r.hdr + kRopeHdrMagic);
+    const uint32_t ver = __ldg(r.hdr + kRopeHdrVersion);
+    const uint32_t n = __ldg(r.hdr + kRopeHdrN);
+    const uint32_t d = __ldg(r.hdr + kRopeHdrD);
+    const uint32_t rows = __ldg(r.hdr + kRopeHdrRows);
+    const uint32_t pairs = __ldg(r.hdr + kRopeHdrPairs);
+    if (magic != kRopeMagic || ver != kRopeVersion || d != (uint32_t)r.d) return false;
+    if (rows != (uint32_t)kRopeHeaderWords || pairs != rows + n * (d / 2)) return false;
+    return r.exact ? n == (uint32_t)r.need : n >= (uint32_t)r.need;
 }
 
-// (cos, sin) of pair p (0 <= p < 64) for a token at `pos`.
-__device__ __forceinline__ float2 rope_cs(const RopeView& r, const TokenPos& pos, int p) {
-    if (p < r.pt) return __ldg(r.tab_t + (size_t)pos.t * r.pt + p);
-    p -= r.pt;
-    if (p < r.ph) return __ldg(r.tab_h + (size_t)pos.h * r.ph + p);
-    p -= r.ph;
-    return __ldg(r.tab_w + (size_t)pos.w * r.pw + p);
+// The fp32 (cos, sin) pairs of the table, [tokens][d/2].
+__device__ __forceinline__ const float2* rope_pairs(const RopeView& r) {
+    return reinterpret_cast<const float2*>(r.hdr + __ldg(r.hdr + kRopeHdrPairs));
 }
 
 // Complex rotation of the pair (x0, x1) by (c, s).

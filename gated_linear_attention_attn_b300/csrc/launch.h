@@ -12,20 +12,20 @@ namespace sla {
 // Argument checks of the forward entry points (api.cu); fills *rv when RoPE is on.
 sla_status_t check_forward(const void* q, const void* k, const void* v, const void* g,
                            const void* out, int B, int H, int N, int d,
-                           const sla_rope_table_t* rope, float eps, size_t elem, RopeView* rv);
+                           const float* rope, float eps, size_t elem, RopeView* rv);
 
 // fp32 SIMT path (simt.cu).
 int simt_chunks(int BH, int N, int num_sms);
 size_t simt_workspace_bytes(int BH, int C);
 cudaError_t launch_simt_f32(const float* q, const float* k, const float* v, const float* g,
                             float* out, int B, int H, int N, const RopeView* rope, float eps,
-                            float* workspace, int C, cudaStream_t stream);
+                            float* workspace, int C, unsigned* status, cudaStream_t stream);
 
 // The fp32 SIMT state partials (S_c in [m][n] order, then z_c) of C chunks
 // per head, as simt_state_kernel writes them (simt.cu).
 cudaError_t launch_simt_state_partials(const float* k, const float* v, int B, int H, int N,
                                        const RopeView* rope, float* partial, int C,
-                                       cudaStream_t stream);
+                                       unsigned* status, cudaStream_t stream);
 
 // Backward (backward.cu): dq, dk, dv, dg of L = sum(dout * o).  bf16: nine
 // launches on the tensor-core state and apply kernels plus three elementwise
@@ -40,7 +40,7 @@ cudaError_t launch_backward_bf16(const void* q, const void* k, const void* v, co
 cudaError_t launch_backward_f32(const float* q, const float* k, const float* v, const float* g,
                                 const float* dout, float* dq, float* dk, float* dv, float* dg,
                                 int B, int H, int N, const RopeView* rope, float eps,
-                                float* workspace, int C, cudaStream_t stream);
+                                float* workspace, int C, unsigned* status, cudaStream_t stream);
 
 // Gated-softmax anchor forward (anchor.cu), bf16, head dim 256: the RoPE
 // pre-pass (rotated k into workspace, anchor_workspace_bytes of it) when rope
@@ -95,8 +95,16 @@ cudaError_t launch_tc_apply(const void* q, const void* g, const void* state, voi
                             int H, int N, const RopeView* rope, float eps, unsigned* status,
                             int num_sms, cudaStream_t stream, int mode = kApplyGate);
 
-// RoPE table (rope_table.cu).
+// RoPE table (rope_table.cu): the header, then every token's pairs as fp16
+// and as fp32, from the grid and band split or from caller-given fp32 pairs.
 cudaError_t launch_rope_fill(float* table, int T, int Hs, int Ws, int dt, int dh, int dw,
                              float base, cudaStream_t stream);
+cudaError_t launch_rope_from_pairs(float* table, const float* pairs, int N, int d,
+                                   cudaStream_t stream);
+
+// A one-thread kernel that waits on an mbarrier nobody arrives at and gives up
+// after limit_ns, as every wait of the library's kernels does (selftest.cu).
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, unsigned* status,
+                                 cudaStream_t stream);
 
 }  // namespace sla

@@ -60,7 +60,7 @@ using namespace sla;
 extern "C" sla_status_t sla_linattn_forward_noalloc(const void* q, const void* k, const void* v,
                                                     const void* g, void* out, int B, int H,
                                                     int N, int d,
-                                                    const sla_rope_table_t* rope_table,
+                                                    const float* rope_table,
                                                     float eps, unsigned int* device_status,
                                                     sla_stream_t stream) {
     RopeView rv{};

@@ -23,10 +23,15 @@ __device__ __forceinline__ void store_elem(float* p, float x) { *p = x; }
 template <typename T, bool ROPE>
 __global__ void __launch_bounds__(256)
 simt_state_kernel(const T* __restrict__ k, const T* __restrict__ v, int N, int C,
-                  int chunk, RopeView rope, float* __restrict__ partial) {
+                  int chunk, RopeView rope, float* __restrict__ partial, unsigned* rope_status) {
     __shared__ float ks[kSimtTile][kHeadDim];
     __shared__ float vs[kSimtTile][kHeadDim];
     const int bh = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
+    if (ROPE && !rope_table_ok(rope)) {        // the whole block leaves; nothing is read
+        if (tid == 0 && c == 0 && bh == 0) raise_status(rope_status, kStatusBadTable);
+        return;
+    }
+    const float2* cs = ROPE ? rope_pairs(rope) : nullptr;
     const int ty = tid / 16, tx = tid % 16;
     const size_t head = (size_t)bh * N * kHeadDim;
     const int n0 = c * chunk;
@@ -59,8 +64,8 @@ simt_state_kernel(const T* __restrict__ k, const T* __restrict__ v, int N, int C
             __syncthreads();
             for (int e = tid; e < cnt * kPairs; e += blockDim.x) {
                 const int r = e / kPairs, p = e % kPairs;
-                const TokenPos pos = token_pos(rope, base + r);
-                rotate_pair(ks[r][2 * p], ks[r][2 * p + 1], rope_cs(rope, pos, p));
+                rotate_pair(ks[r][2 * p], ks[r][2 * p + 1],
+                            __ldg(cs + (size_t)(base + r) * kPairs + p));
             }
         }
         __syncthreads();
@@ -93,6 +98,7 @@ __global__ void __launch_bounds__(256)
 simt_apply_kernel(const T* __restrict__ q, const T* __restrict__ g,
                   T* __restrict__ out, int N, int C, const float* __restrict__ partial,
                   float eps, RopeView rope) {
+    if (ROPE && !rope_table_ok(rope)) return;   // reported by the state kernel
     extern __shared__ float smem[];
     float* S = smem;                                 // [128][128]
     float* z = S + kHeadDim * kHeadDim;              // [128]
@@ -143,9 +149,8 @@ simt_apply_kernel(const T* __restrict__ q, const T* __restrict__ g,
         __syncthreads();
         for (int e = tid; e < cnt * kPairs; e += blockDim.x) {
             const int r = e / kPairs, p = e % kPairs;
-            const TokenPos pos = token_pos(rope, base + r);
             rotate_pair(qs[r * kHeadDim + 2 * p], qs[r * kHeadDim + 2 * p + 1],
-                        rope_cs(rope, pos, p));
+                        __ldg(rope_pairs(rope) + (size_t)(base + r) * kPairs + p));
         }
     }
     __syncthreads();
@@ -199,7 +204,7 @@ int simt_chunks(int BH, int N, int num_sms) {
 template <typename T>
 static cudaError_t launch_simt(const T* q, const T* k, const T* v, const T* g, T* out, int B,
                                int H, int N, const RopeView* rope, float eps, float* workspace,
-                               int C, cudaStream_t stream) {
+                               int C, unsigned* status, cudaStream_t stream) {
     const int BH = B * H;
     const int tiles = (N + kSimtTile - 1) / kSimtTile;
     const int chunk = ((tiles + C - 1) / C) * kSimtTile;
@@ -210,13 +215,15 @@ static cudaError_t launch_simt(const T* q, const T* k, const T* v, const T* g, T
     if (rope) {
         cudaFuncSetAttribute(simt_apply_kernel<T, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)apply_smem);
-        simt_state_kernel<T, true><<<gs, 256, 0, stream>>>(k, v, N, C, chunk, rv, workspace);
+        simt_state_kernel<T, true><<<gs, 256, 0, stream>>>(k, v, N, C, chunk, rv, workspace,
+                                                            status);
         simt_apply_kernel<T, true><<<ga, 256, apply_smem, stream>>>(q, g, out, N, C, workspace,
                                                                      eps, rv);
     } else {
         cudaFuncSetAttribute(simt_apply_kernel<T, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)apply_smem);
-        simt_state_kernel<T, false><<<gs, 256, 0, stream>>>(k, v, N, C, chunk, rv, workspace);
+        simt_state_kernel<T, false><<<gs, 256, 0, stream>>>(k, v, N, C, chunk, rv, workspace,
+                                                             status);
         simt_apply_kernel<T, false><<<ga, 256, apply_smem, stream>>>(q, g, out, N, C,
                                                                       workspace, eps, rv);
     }
@@ -226,28 +233,30 @@ static cudaError_t launch_simt(const T* q, const T* k, const T* v, const T* g, T
 template <typename T>
 static cudaError_t launch_state_partials(const T* k, const T* v, int B, int H, int N,
                                          const RopeView* rope, float* partial, int C,
-                                         cudaStream_t stream) {
+                                         unsigned* status, cudaStream_t stream) {
     const int tiles = (N + kSimtTile - 1) / kSimtTile;
     const int chunk = ((tiles + C - 1) / C) * kSimtTile;
     const RopeView rv = rope ? *rope : RopeView{};
     const dim3 gs(C, B * H);
     if (rope)
-        simt_state_kernel<T, true><<<gs, 256, 0, stream>>>(k, v, N, C, chunk, rv, partial);
+        simt_state_kernel<T, true><<<gs, 256, 0, stream>>>(k, v, N, C, chunk, rv, partial,
+                                                            status);
     else
-        simt_state_kernel<T, false><<<gs, 256, 0, stream>>>(k, v, N, C, chunk, rv, partial);
+        simt_state_kernel<T, false><<<gs, 256, 0, stream>>>(k, v, N, C, chunk, rv, partial,
+                                                             status);
     return cudaGetLastError();
 }
 
 cudaError_t launch_simt_state_partials(const float* k, const float* v, int B, int H, int N,
                                        const RopeView* rope, float* partial, int C,
-                                       cudaStream_t stream) {
-    return launch_state_partials<float>(k, v, B, H, N, rope, partial, C, stream);
+                                       unsigned* status, cudaStream_t stream) {
+    return launch_state_partials<float>(k, v, B, H, N, rope, partial, C, status, stream);
 }
 
 cudaError_t launch_simt_f32(const float* q, const float* k, const float* v, const float* g,
                             float* out, int B, int H, int N, const RopeView* rope, float eps,
-                            float* workspace, int C, cudaStream_t stream) {
-    return launch_simt<float>(q, k, v, g, out, B, H, N, rope, eps, workspace, C, stream);
+                            float* workspace, int C, unsigned* status, cudaStream_t stream) {
+    return launch_simt<float>(q, k, v, g, out, B, H, N, rope, eps, workspace, C, status, stream);
 }
 
 }  // namespace sla

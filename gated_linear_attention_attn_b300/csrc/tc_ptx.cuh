@@ -84,17 +84,18 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 constexpr uint32_t kWaitSleepNs = 20000;
 
 // Waits for the phase of `bar` with the given parity to complete.  Gives up
-// when *abort is set by another role, or after kWaitLimitNs; on a timeout it
-// raises the status word and sets *abort.  Returns true when the phase
-// completed.
+// when *abort is set by another role, or after limit_ns (kWaitLimitNs unless a
+// caller asks for less); on a timeout it raises the status word and sets
+// *abort.  Returns true when the phase completed.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort, unsigned* status) {
+                                          volatile int* abort, unsigned* status,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (;;) {
         if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
         if (*abort) return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
+        if (global_ns() - t0 > limit_ns) {
             raise_status(status, kStatusTimeout);
             *abort = 1;
             return false;

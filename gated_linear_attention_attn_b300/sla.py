@@ -28,41 +28,35 @@ OK, INVALID_ARG, UNSUPPORTED, ALIGNMENT, CUDA_ERROR, DEVICE_TIMEOUT = range(6)
 HEAD_DIM = 128
 
 
-class RopeTableC(ctypes.Structure):
-    """Mirror of sla_rope_table_t."""
-    _fields_ = [("table", ctypes.c_void_p),
-                ("T", ctypes.c_int), ("Hs", ctypes.c_int), ("Ws", ctypes.c_int),
-                ("dt", ctypes.c_int), ("dh", ctypes.c_int), ("dw", ctypes.c_int)]
-
-
 _vp, _int, _flt = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
-_lib.sla_rope_table_floats.argtypes = [_int] * 6
+_lib.sla_rope_table_floats.argtypes = [_int] * 2
 _lib.sla_rope_table_floats.restype = ctypes.c_size_t
-_lib.sla_rope_table_fill.argtypes = [_vp] + [_int] * 6 + [_flt, _vp]
+_lib.sla_rope_table_fill.argtypes = [_vp] + [_int] * 7 + [_flt, _vp]
 _lib.sla_rope_table_fill.restype = _int
-_FWD_ARGS = [_vp] * 5 + [_int] * 4 + [ctypes.POINTER(RopeTableC), _flt, _vp]
+_lib.sla_rope_table_from_pairs.argtypes = [_vp, _vp, _int, _int, _vp]
+_lib.sla_rope_table_from_pairs.restype = _int
+_FWD_ARGS = [_vp] * 5 + [_int] * 4 + [_vp, _flt, _vp]
 for _name in ("sla_linattn_forward", "sla_linattn_forward_f32"):
     getattr(_lib, _name).argtypes = _FWD_ARGS
     getattr(_lib, _name).restype = _int
 _lib.sla_linattn_state_bytes.argtypes = [_int] * 3
 _lib.sla_linattn_state_bytes.restype = ctypes.c_size_t
-_lib.sla_linattn_state.argtypes = [_vp] * 3 + [_int] * 4 + [ctypes.POINTER(RopeTableC), _vp]
+_lib.sla_linattn_state.argtypes = [_vp] * 3 + [_int] * 4 + [_vp, _vp]
 _lib.sla_linattn_state.restype = _int
-_lib.sla_linattn_apply.argtypes = [_vp] * 4 + [_int] * 4 + [ctypes.POINTER(RopeTableC), _flt, _vp]
+_lib.sla_linattn_apply.argtypes = [_vp] * 4 + [_int] * 4 + [_vp, _flt, _vp]
 _lib.sla_linattn_apply.restype = _int
 _lib.sla_linattn_forward_noalloc.argtypes = _FWD_ARGS[:-1] + [_vp, _vp]
 _lib.sla_linattn_forward_noalloc.restype = _int
 _lib.sla_linattn_carried_state_bytes.argtypes = [_int] * 3
 _lib.sla_linattn_carried_state_bytes.restype = ctypes.c_size_t
 _lib.sla_linattn_forward_block_causal.argtypes = ([_vp] * 5 + [_int] * 5 +
-                                                  [ctypes.POINTER(RopeTableC), _int, _flt,
-                                                   _vp, _vp, _vp])
+                                                  [_vp, _int, _flt, _vp, _vp, _vp])
 _lib.sla_linattn_forward_block_causal.restype = _int
-_BWD_ARGS = [_vp] * 9 + [_int] * 4 + [ctypes.POINTER(RopeTableC), _flt, _vp]
+_BWD_ARGS = [_vp] * 9 + [_int] * 4 + [_vp, _flt, _vp]
 for _name in ("sla_linattn_backward", "sla_linattn_backward_f32"):
     getattr(_lib, _name).argtypes = _BWD_ARGS
     getattr(_lib, _name).restype = _int
-_lib.sla_anchor_forward.argtypes = [_vp] * 5 + [_int] * 4 + [ctypes.POINTER(RopeTableC), _vp]
+_lib.sla_anchor_forward.argtypes = [_vp] * 5 + [_int] * 4 + [_vp, _vp]
 _lib.sla_anchor_forward.restype = _int
 _lib.sla_attnres_aggregate.argtypes = [ctypes.POINTER(_vp), _int, _int, _int, _vp, _flt, _vp,
                                        _vp]
@@ -73,13 +67,17 @@ _lib.sla_status_string.argtypes = [_int]
 _lib.sla_status_string.restype = ctypes.c_char_p
 _lib.sla_last_device_status.argtypes = [_vp]
 _lib.sla_last_device_status.restype = _int
+_lib.sla_selftest_wait_timeout.argtypes = [ctypes.c_uint, _vp]
+_lib.sla_selftest_wait_timeout.restype = _int
 
-EXPORTED = ("sla_rope_table_floats", "sla_rope_table_fill", "sla_linattn_forward",
+EXPORTED = ("sla_rope_table_floats", "sla_rope_table_fill", "sla_rope_table_from_pairs",
+            "sla_linattn_forward",
             "sla_linattn_forward_f32", "sla_linattn_state_bytes", "sla_linattn_state",
             "sla_linattn_apply", "sla_linattn_forward_noalloc", "sla_linattn_forward_cluster",
             "sla_linattn_carried_state_bytes", "sla_linattn_forward_block_causal",
             "sla_linattn_backward", "sla_linattn_backward_f32", "sla_anchor_forward",
-            "sla_attnres_aggregate", "sla_status_string", "sla_last_device_status")
+            "sla_attnres_aggregate", "sla_status_string", "sla_last_device_status",
+            "sla_selftest_wait_timeout")
 
 
 class SlaError(RuntimeError):
@@ -104,55 +102,79 @@ def _stream_handle(stream: Optional[torch.cuda.Stream], device: torch.device) ->
 
 
 class RopeTable:
-    """A filled 3D RoPE table on one device, plus its grid and band split.
+    """A RoPE table on one device (``sla_rope_table_fill``): a header, then every
+    token's d/2 (cos, sin) pairs as fp16 and as fp32 (layout in ``include/sla.h``).
 
-    The table holds, for each axis, the (cos, sin) of every coordinate value
-    times every frequency of that axis's band in fp32, and for every token its
-    d/2 (cos, sin) pairs in fp16 (see ``sla_rope_table_t``).
+    ``RopeTable(grid, split, base)`` builds the 3D table of a latent grid;
+    ``RopeTable.from_pairs(pairs)`` wraps caller-given fp32 pairs [N, d/2, 2].
     """
 
     def __init__(self, grid: Sequence[int], split: Sequence[int] = (44, 42, 42),
                  base: float = 10000.0, device="cuda", stream=None):
         T, Hs, Ws = (int(x) for x in grid)
         dt, dh, dw = (int(x) for x in split)
-        n = _lib.sla_rope_table_floats(T, Hs, Ws, dt, dh, dw)
-        if n == 0 and (dt or dh or dw):
-            raise SlaError(INVALID_ARG, "sla_rope_table_floats")
+        d = dt + dh + dw
         self.device = torch.device(device)
-        self.grid, self.split, self.base = (T, Hs, Ws), (dt, dh, dw), float(base)
-        self.table = torch.empty(max(int(n), 2), dtype=torch.float32, device=self.device)
+        self.grid, self.split, self.base, self.d = (T, Hs, Ws), (dt, dh, dw), float(base), d
+        self.n_tokens = T * Hs * Ws
+        self.table = self._alloc(self.n_tokens, d)
         with torch.cuda.device(self.device):
-            _check(_lib.sla_rope_table_fill(self.table.data_ptr(), T, Hs, Ws, dt, dh, dw,
+            _check(_lib.sla_rope_table_fill(self.table.data_ptr(), T, Hs, Ws, d, dt, dh, dw,
                                             self.base, _stream_handle(stream, self.device)),
                    "sla_rope_table_fill")
 
-    @property
-    def n_tokens(self) -> int:
-        T, Hs, Ws = self.grid
-        return T * Hs * Ws
+    def _alloc(self, n: int, d: int) -> torch.Tensor:
+        words = int(_lib.sla_rope_table_floats(n, d))
+        if words == 0:
+            raise SlaError(INVALID_ARG, "sla_rope_table_floats")
+        return torch.empty(words, dtype=torch.float32, device=self.device)
 
-    def c_struct(self) -> RopeTableC:
-        return RopeTableC(self.table.data_ptr(), *self.grid, *self.split)
+    @classmethod
+    def from_pairs(cls, pairs: torch.Tensor, stream=None) -> "RopeTable":
+        """A table from an fp32 CUDA tensor [N, d/2, 2] of (cos, sin) per token and pair
+        (``sla_rope_table_from_pairs``)."""
+        if pairs.dtype != torch.float32 or pairs.dim() != 3 or pairs.shape[2] != 2 \
+                or pairs.device.type != "cuda" or not pairs.is_contiguous():
+            raise SlaError(INVALID_ARG, "from_pairs: pairs must be a contiguous fp32 "
+                                        "[N, d/2, 2] CUDA tensor")
+        self = cls.__new__(cls)
+        self.device = pairs.device
+        self.grid, self.split, self.base = None, None, None
+        self.n_tokens, self.d = int(pairs.shape[0]), 2 * int(pairs.shape[1])
+        self.table = self._alloc(self.n_tokens, self.d)
+        with torch.cuda.device(self.device):
+            _check(_lib.sla_rope_table_from_pairs(self.table.data_ptr(), pairs.data_ptr(),
+                                                  self.n_tokens, self.d,
+                                                  _stream_handle(stream, self.device)),
+                   "sla_rope_table_from_pairs")
+        return self
+
+    @property
+    def ptr(self) -> int:
+        """The table's device address: the ``rope_table`` argument of the C ABI."""
+        return self.table.data_ptr()
+
+    def header(self):
+        """The header words as a list of ints (tag, version, N, d, T, Hs, Ws, dt, dh, dw,
+        base bits, offset of the fp16 rows, offset of the fp32 pairs)."""
+        return self.table[:13].view(torch.int32).cpu().tolist()
 
     def token_rows(self):
-        """The per-token rows as an [N, d/2, 2] float16 tensor of (cos, sin)."""
-        T, Hs, Ws = self.grid
-        dt, dh, dw = self.split
-        sep = T * dt + Hs * dh + Ws * dw
-        off = (sep + 63) // 64 * 64
-        n = T * Hs * Ws
-        p = (dt + dh + dw) // 2
-        return self.table[off:off + n * p].view(torch.float16).view(n, p, 2)
+        """The fp16 part as an [N, d/2, 2] float16 tensor of (cos, sin)."""
+        p = self.d // 2
+        off = 64
+        return self.table[off:off + self.n_tokens * p].view(torch.float16).view(
+            self.n_tokens, p, 2)
 
-    def axis_tables(self):
-        """The (cos, sin) rows of each axis as [extent, pairs, 2] float tensors."""
-        T, Hs, Ws = self.grid
-        dt, dh, dw = self.split
-        flat = self.table.view(-1, 2)
-        a = T * (dt // 2)
-        b = a + Hs * (dh // 2)
-        return (flat[:a].view(T, dt // 2, 2), flat[a:b].view(Hs, dh // 2, 2),
-                flat[b:b + Ws * (dw // 2)].view(Ws, dw // 2, 2))
+    def pairs(self):
+        """The fp32 part as an [N, d/2, 2] float32 tensor of (cos, sin)."""
+        p = self.d // 2
+        off = 64 + self.n_tokens * p
+        return self.table[off:off + 2 * self.n_tokens * p].view(self.n_tokens, p, 2)
+
+
+def _rope_ptr(rope: Optional[RopeTable]):
+    return rope.ptr if rope is not None else None
 
 
 def linattn_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
@@ -186,9 +208,7 @@ def linattn_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.
             or out.device != q.device:
         raise SlaError(INVALID_ARG, "linattn_forward: out must match q")
     B, H, N, d = q.shape
-    rope_c = None
-    if rope is not None:
-        rope_c = ctypes.byref(rope.c_struct())
+    rope_c = _rope_ptr(rope)
     with torch.cuda.device(q.device):
         _check(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(), out.data_ptr(),
                   B, H, N, d, rope_c, float(eps), _stream_handle(stream, q.device)),
@@ -213,7 +233,7 @@ def anchor_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.T
     else:
         _check_bf16("out", out, like=q)
     B, H, N, d = q.shape
-    rope_c = ctypes.byref(rope.c_struct()) if rope is not None else None
+    rope_c = _rope_ptr(rope)
     with torch.cuda.device(q.device):
         _check(_lib.sla_anchor_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(),
                                        out.data_ptr(), B, H, N, d, rope_c,
@@ -285,7 +305,7 @@ def linattn_state(k: torch.Tensor, v: torch.Tensor, rope: Optional[RopeTable] = 
         state = torch.empty(nbytes, dtype=torch.uint8, device=k.device)
     elif state.numel() * state.element_size() < nbytes or not state.is_contiguous():
         raise SlaError(INVALID_ARG, "linattn_state: state buffer too small")
-    rope_c = ctypes.byref(rope.c_struct()) if rope is not None else None
+    rope_c = _rope_ptr(rope)
     with torch.cuda.device(k.device):
         _check(_lib.sla_linattn_state(k.data_ptr(), v.data_ptr(), state.data_ptr(), B, H, N, d,
                                       rope_c, _stream_handle(stream, k.device)),
@@ -307,7 +327,7 @@ def linattn_apply(q: torch.Tensor, g: torch.Tensor, state: torch.Tensor,
         out = torch.empty_like(q)
     else:
         _check_bf16("out", out, like=q)
-    rope_c = ctypes.byref(rope.c_struct()) if rope is not None else None
+    rope_c = _rope_ptr(rope)
     with torch.cuda.device(q.device):
         _check(_lib.sla_linattn_apply(q.data_ptr(), g.data_ptr(), state.data_ptr(),
                                       out.data_ptr(), B, H, N, d, rope_c, float(eps),
@@ -321,6 +341,16 @@ def last_device_status(stream: Optional[torch.cuda.Stream] = None, device="cuda"
     dev = torch.device(device)
     with torch.cuda.device(dev):
         return _lib.sla_last_device_status(_stream_handle(stream, dev))
+
+
+def selftest_wait_timeout(limit_us: int = 1000, stream: Optional[torch.cuda.Stream] = None,
+                          device="cuda") -> None:
+    """Launch the bounded-wait self-test (``sla_selftest_wait_timeout``): one thread waits
+    on an mbarrier nobody arrives at and gives up after ``limit_us`` microseconds."""
+    dev = torch.device(device)
+    with torch.cuda.device(dev):
+        _check(_lib.sla_selftest_wait_timeout(int(limit_us), _stream_handle(stream, dev)),
+               "sla_selftest_wait_timeout")
 
 
 def linattn_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
@@ -350,7 +380,7 @@ def linattn_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch
                 or not t.is_contiguous():
             raise SlaError(INVALID_ARG, "linattn_backward: gradient tensors must match q")
     B, H, N, d = q.shape
-    rope_c = ctypes.byref(rope.c_struct()) if rope is not None else None
+    rope_c = _rope_ptr(rope)
     with torch.cuda.device(q.device):
         _check(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(), dout.data_ptr(),
                   *(t.data_ptr() for t in grads), B, H, N, d, rope_c, float(eps),
@@ -398,7 +428,7 @@ def linattn_forward_block_causal(q: torch.Tensor, k: torch.Tensor, v: torch.Tens
                               or not t.is_contiguous() or t.numel() != B * H * CARRIED_FLOATS):
             raise SlaError(INVALID_ARG, f"{name} must be a contiguous float32 [B, H, "
                                         f"{CARRIED_FLOATS}] tensor on q's device")
-    rope_c = ctypes.byref(rope.c_struct()) if rope is not None else None
+    rope_c = _rope_ptr(rope)
     with torch.cuda.device(q.device):
         _check(_lib.sla_linattn_forward_block_causal(
             q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(), out.data_ptr(),

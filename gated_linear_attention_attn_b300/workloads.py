@@ -104,6 +104,10 @@ WORKLOADS = {
     "5b_720p_60s": Workload(
         "5b_720p_60s", B=1, H=20, grid=(181, 22, 40), rope=True, k_scale=0.5,
         description="long clip, 720p/60 s: B=1 H=20 N=159280 (181x22x40) bf16, 3D RoPE, k x 0.5"),
+    "5b_720p_736": Workload(
+        "5b_720p_736", B=2, H=20, grid=(25, 23, 40), rope=True,
+        description="5B shape, 720p/193 frames in the 736x1280 bucket: B=2 H=20 "
+                    "N=23000 (25x23x40) bf16, 3D RoPE 44/42/42"),
     "5b_720p_block5": Workload(
         "5b_720p_block5", B=2, H=20, grid=(25, 22, 40), rope=True, block_frames=5,
         description="block-causal form of the 720p shape: 5 blocks of 5 latent frames "

@@ -19,7 +19,7 @@
  *
  * The sums run over all N tokens (bidirectional: no causal mask).  The gate
  * g has the shape of q and acts elementwise.  R_n is the 3D rotary embedding
- * of token n, applied to the numerator only (see sla_rope_table_t).
+ * of token n, applied to the numerator only (see the RoPE table below).
  *
  * Layout.  q, k, v, g and out are [B][H][N][d] row-major and contiguous
  * (d fastest), all in device memory of the current device.  out has the
@@ -51,12 +51,12 @@
 extern "C" {
 #endif
 
-/* A CUDA stream handle (the same object as cudaStream_t). */
+/* A CUDA stream handle: the same type as cudaStream_t. */
 typedef struct CUstream_st* sla_stream_t;
 
 typedef enum sla_status {
     SLA_OK = 0,
-    SLA_ERR_INVALID_ARG = 1,    /* null pointer, size < 1, bad eps, aliasing, bad RoPE grid */
+    SLA_ERR_INVALID_ARG = 1,    /* null pointer, size < 1, bad eps, aliasing, bad RoPE table */
     SLA_ERR_UNSUPPORTED = 2,    /* a shape the kernels do not implement (e.g. d != 128) */
     SLA_ERR_ALIGNMENT = 3,      /* a tensor not 16-byte aligned (a RoPE table not 256-byte aligned) */
     SLA_ERR_CUDA = 4,           /* a CUDA runtime call failed (launch, allocation, no device) */
@@ -72,47 +72,70 @@ typedef enum sla_status {
  * a band of width W, pair j = (x_{2p}, x_{2p+1}) turns by pos * base^(-2j/W)
  * radians (complex multiplication of x_{2p} + i x_{2p+1}).
  *
- * `table` is a device buffer of sla_rope_table_floats(...) 4-byte words
- * written by sla_rope_table_fill, in two parts.  First the angles separated
- * by axis, as fp32 (cos, sin) pairs: for t in [0,T) x j in [0,dt/2), then for
- * h in [0,Hs) x j in [0,dh/2), then for w in [0,Ws) x j in [0,dw/2)
- * (T*dt + Hs*dh + Ws*dw words; the fp32 kernels read these).  Then, from the
- * next multiple of 64 words, one row per token n of its d/2 pairs, each pair
- * one word holding fp16 cos (low half) and fp16 sin (high half): 256 bytes
- * per token for d = 128, streamed by the bf16 kernels next to the token's
- * row of q or k.
+ * The RoPE table argument of every entry point (`rope_table`) is NULL for no
+ * rotation, or a device buffer of sla_rope_table_floats(N, d) 4-byte words,
+ * 256-byte aligned, written by sla_rope_table_fill or
+ * sla_rope_table_from_pairs.  With P = d/2 pairs per token it holds:
+ *
+ *   words [0, 64)               a header: word 0 the tag 0x33414c53, word 1
+ *                               the layout version (1), word 2 the number of
+ *                               tokens N, word 3 d, words 4-6 the grid
+ *                               (T, Hs, Ws), words 7-9 the bands (dt, dh, dw),
+ *                               word 10 the base as an fp32 bit pattern (grid,
+ *                               bands and base are 0 for a table made from
+ *                               pairs), word 11 the offset of the fp16 rows
+ *                               (64), word 12 the offset of the fp32 pairs
+ *                               (64 + N*P); the rest 0;
+ *   words [64, 64 + N*P)        per token n, its P pairs as fp16 (cos, sin)
+ *                               (cos in the low half of the word), read by the
+ *                               tensor-core kernels next to the token's row;
+ *   words [64 + N*P, 64 + 3N*P) per token n, its P pairs as fp32 (cos, sin):
+ *                               the plain [N][d/2][2] table, read by the fp32
+ *                               and anchor kernels.
+ *
+ * The host checks only the pointer (NULL or 256-byte aligned).  Every kernel
+ * that rotates first checks the header: the tag, the version, d, and the
+ * number of tokens (exactly the call's N, or at least rope_offset + N for the
+ * block-causal form).  On a mismatch it reads nothing more of the table and
+ * sets a bit of the device status word, which sla_last_device_status reports
+ * as SLA_ERR_INVALID_ARG; the call's outputs are then undefined.  The buffer
+ * must hold at least the 64 header words.
  */
-typedef struct sla_rope_table {
-    const float* table;   /* device pointer, 256-byte aligned */
-    int T, Hs, Ws;        /* latent grid; N must equal T*Hs*Ws */
-    int dt, dh, dw;       /* even band widths, dt + dh + dw == d */
-} sla_rope_table_t;
 
-/* Number of 4-byte words of the RoPE table for this grid and split (0 if invalid). */
-size_t sla_rope_table_floats(int T, int Hs, int Ws, int dt, int dh, int dw);
+/* 4-byte words of a RoPE table for N tokens of head dimension d (0 if invalid). */
+size_t sla_rope_table_floats(int N, int d);
 
 /*
- * Writes the RoPE table (layout above) for base `base` (10000 for the Wan
- * embedding) into `table` (device, sla_rope_table_floats(...) words, 256-byte
- * aligned).  The angles are formed and the cosine and sine taken in double
- * precision and rounded to fp32 (first part); the second part holds the same
- * values rounded from fp32 to fp16.
+ * Writes the RoPE table (layout above) of a T x Hs x Ws grid, N = T*Hs*Ws,
+ * bands (dt, dh, dw) with dt + dh + dw == d, all even (44/42/42 for d = 128,
+ * 88/84/84 for d = 256), base `base` (10000 for the Wan embedding), into
+ * `table`.  The angles are formed and the cosine and sine taken in double
+ * precision, rounded to fp32, and the fp32 values rounded to fp16.
  * Asynchronous on `stream`.
  */
-sla_status_t sla_rope_table_fill(float* table, int T, int Hs, int Ws, int dt, int dh,
+sla_status_t sla_rope_table_fill(float* table, int T, int Hs, int Ws, int d, int dt, int dh,
                                  int dw, float base, sla_stream_t stream);
+
+/*
+ * Writes a RoPE table (layout above) from caller-given angles: `pairs` is a
+ * device array [N][d/2][2] of fp32 (cos, sin), 8-byte aligned, not
+ * overlapping `table`; it is copied into the fp32 part and rounded to fp16 for
+ * the other.  For callers that already hold a plain per-token table.
+ * Asynchronous on `stream`; `pairs` may be freed once the copy has run.
+ */
+sla_status_t sla_rope_table_from_pairs(float* table, const float* pairs, int N, int d,
+                                       sla_stream_t stream);
 
 /*
  * The forward with bf16 q, k, v, g and out (IEEE bfloat16, 2 bytes each),
  * fp32 accumulation.  B, H, N >= 1; d must be 128.  rope_table: NULL for no
- * RoPE, else a host pointer to a filled sla_rope_table_t whose grid has N
- * tokens and whose bands sum to d.  eps: finite, >= 0 (1e-6 in the
- * workloads).  All five tensors 16-byte aligned; out must not overlap any
- * input.  Asynchronous on `stream`.
+ * RoPE, else a RoPE table (layout above) of exactly N tokens built for d.
+ * eps: finite, >= 0 (1e-6 in the workloads).  All five tensors 16-byte
+ * aligned; out must not overlap any input.  Asynchronous on `stream`.
  */
 sla_status_t sla_linattn_forward(const void* q, const void* k, const void* v, const void* g,
                                  void* out, int B, int H, int N, int d,
-                                 const sla_rope_table_t* rope_table, float eps,
+                                 const float* rope_table, float eps,
                                  sla_stream_t stream);
 
 /*
@@ -121,7 +144,7 @@ sla_status_t sla_linattn_forward(const void* q, const void* k, const void* v, co
  */
 sla_status_t sla_linattn_forward_f32(const float* q, const float* k, const float* v,
                                      const float* g, float* out, int B, int H, int N, int d,
-                                     const sla_rope_table_t* rope_table, float eps,
+                                     const float* rope_table, float eps,
                                      sla_stream_t stream);
 
 /*
@@ -171,7 +194,7 @@ size_t sla_linattn_state_bytes(int B, int H, int d);   /* 0 if the shape is inva
  * Uses the library's per-stream workspace for the split-N partial states.
  */
 sla_status_t sla_linattn_state(const void* k, const void* v, void* state, int B, int H, int N,
-                               int d, const sla_rope_table_t* rope_table, sla_stream_t stream);
+                               int d, const float* rope_table, sla_stream_t stream);
 
 /*
  * Phase 2: out = sigmoid(g) * (R phi(q)) S~ / (phi(q) . z + eps) for bf16 q
@@ -181,7 +204,7 @@ sla_status_t sla_linattn_state(const void* k, const void* v, void* state, int B,
  * out must overlap neither q, g nor the state.
  */
 sla_status_t sla_linattn_apply(const void* q, const void* g, const void* state, void* out, int B,
-                               int H, int N, int d, const sla_rope_table_t* rope_table, float eps,
+                               int H, int N, int d, const float* rope_table, float eps,
                                sla_stream_t stream);
 
 /*
@@ -203,10 +226,10 @@ sla_status_t sla_linattn_apply(const void* q, const void* g, const void* state, 
  * state_in, give the same result as one call on the whole sequence.
  *
  * Arguments as for sla_linattn_forward (bf16 q, k, v, g, out), plus:
- * block_tokens: >= 1, dividing N.  rope_table: NULL or a table whose grid
- * covers tokens [rope_offset, rope_offset + N): this call's token n is token
- * rope_offset + n of the grid (absolute positions, so a later stretch of a
- * video passes its first token's index); rope_offset must be 0 without RoPE.
+ * block_tokens: >= 1, dividing N.  rope_table: NULL or a table of at least
+ * rope_offset + N tokens: this call's token n is token rope_offset + n of the
+ * table (absolute positions, so a later stretch of a video passes its first
+ * token's index); rope_offset must be 0 without RoPE.
  * state_in, state_out: NULL (a zero incoming state; no outgoing state) or
  * device buffers of sla_linattn_carried_state_bytes(B, H, d) bytes, 16-byte
  * aligned: per head (b-major) S as 128 x 128 fp32 row-major (row m = key
@@ -220,7 +243,7 @@ size_t sla_linattn_carried_state_bytes(int B, int H, int d);   /* 0 if the shape
 sla_status_t sla_linattn_forward_block_causal(const void* q, const void* k, const void* v,
                                               const void* g, void* out, int B, int H, int N,
                                               int d, int block_tokens,
-                                              const sla_rope_table_t* rope_table,
+                                              const float* rope_table,
                                               int rope_offset, float eps, const float* state_in,
                                               float* state_out, sla_stream_t stream);
 
@@ -252,12 +275,12 @@ sla_status_t sla_linattn_forward_block_causal(const void* q, const void* k, cons
 sla_status_t sla_linattn_backward(const void* q, const void* k, const void* v, const void* g,
                                   const void* dout, void* dq, void* dk, void* dv, void* dg,
                                   int B, int H, int N, int d,
-                                  const sla_rope_table_t* rope_table, float eps,
+                                  const float* rope_table, float eps,
                                   sla_stream_t stream);
 sla_status_t sla_linattn_backward_f32(const float* q, const float* k, const float* v,
                                       const float* g, const float* dout, float* dq, float* dk,
                                       float* dv, float* dg, int B, int H, int N, int d,
-                                      const sla_rope_table_t* rope_table, float eps,
+                                      const float* rope_table, float eps,
                                       sla_stream_t stream);
 
 /*
@@ -273,8 +296,8 @@ sla_status_t sla_linattn_backward_f32(const float* q, const float* k, const floa
  * over all N keys (no mask), the gate elementwise.  q, k, v, g, out: bf16
  * [B][H][N][d] row-major and contiguous in device memory, 16-byte aligned,
  * out overlapping no input; d must be 256 (SLA_ERR_UNSUPPORTED otherwise),
- * B * H <= 65535.  rope_table: NULL, or a filled table whose grid has N
- * tokens and whose bands sum to 256 (the Wan split is 88/84/84).  Scores and
+ * B * H <= 65535.  rope_table: NULL, or a RoPE table of exactly N tokens
+ * built for d = 256 (the Wan split is 88/84/84).  Scores and
  * the output are accumulated in fp32 on the tensor cores; the rotated q and k
  * and the softmax weights enter the products rounded to bf16.  With RoPE the
  * rotated k goes to the library's per-stream workspace (B*H*N*d*2 bytes).
@@ -282,7 +305,7 @@ sla_status_t sla_linattn_backward_f32(const float* q, const float* k, const floa
  */
 sla_status_t sla_anchor_forward(const void* q, const void* k, const void* v, const void* g,
                                 void* out, int B, int H, int N, int d,
-                                const sla_rope_table_t* rope_table, sla_stream_t stream);
+                                const float* rope_table, sla_stream_t stream);
 
 /*
  * Block Attention Residual (AttnRes) aggregation ("SANA-Video 2.0",
@@ -320,8 +343,9 @@ sla_status_t sla_attnres_aggregate(const void* const* sources, int M, int T, int
  *
  * Arguments, layout and checks are those of sla_linattn_forward, plus:
  * device_status: NULL, or a caller-owned device pointer to a 4-byte aligned
- * unsigned int into which the kernels OR a nonzero value if one of their
- * waits gives up (the word is never cleared by the library).  With NULL,
+ * unsigned int into which the kernels OR a nonzero value when they return
+ * early: 1 if one of their waits gave up, 4 if the RoPE table's header does
+ * not fit the call (the word is never cleared by the library).  With NULL,
  * such an early return is not reported.
  *
  * Size limit: the fused launch (see sla_linattn_forward_cluster) needs no
@@ -335,15 +359,27 @@ sla_status_t sla_attnres_aggregate(const void* const* sources, int M, int T, int
  * capture.  Every call on a device shares the one array, which keeps the
  * last call's contents.  Nothing in it has to be cleared between calls: the
  * only values a call reads before writing them are per-head counters, which
- * carry the tag of the call that wrote them, so a count left by an earlier
- * call reads as zero (the array starts zeroed when the library loads).  Calls
- * that overlap on the GPU (other streams, other host threads) race on the
- * array; order them on one stream or with events.
+ * the state kernel returns to zero before it exits (the array starts zeroed
+ * when the library loads), and which also carry a tag of the call that set
+ * them, so that a count left by a call that gave up a wait reads as zero to
+ * the next call.  Calls that overlap on the GPU (other streams, other host
+ * threads) race on the array; order them on one stream or with events.
  */
 sla_status_t sla_linattn_forward_noalloc(const void* q, const void* k, const void* v,
                                          const void* g, void* out, int B, int H, int N, int d,
-                                         const sla_rope_table_t* rope_table, float eps,
+                                         const float* rope_table, float eps,
                                          unsigned int* device_status, sla_stream_t stream);
+
+/*
+ * Self-test of the kernels' bounded waits: launches one thread that waits on
+ * an mbarrier nobody arrives at, with the same wait the library's kernels use,
+ * and gives up after limit_us microseconds (1 .. 1000000), setting the device
+ * status word as a kernel does when a wait runs out.  The next
+ * sla_last_device_status(stream) then returns SLA_ERR_DEVICE_TIMEOUT (and
+ * clears the word).  Nothing else runs and no memory but the status word is
+ * touched, so the device stays usable.  Asynchronous on `stream`.
+ */
+sla_status_t sla_selftest_wait_timeout(unsigned int limit_us, sla_stream_t stream);
 
 /* A static, human-readable name for a status code. */
 const char* sla_status_string(sla_status_t status);
@@ -351,7 +387,9 @@ const char* sla_status_string(sla_status_t status);
 /*
  * Synchronises `stream`, then reads and clears the device status word of the
  * current device: SLA_ERR_DEVICE_TIMEOUT if a kernel gave up a wait since the
- * last read, SLA_ERR_CUDA if the synchronisation failed, else SLA_OK.
+ * last read, SLA_ERR_INVALID_ARG if a kernel found a RoPE table whose header
+ * does not fit its call, SLA_ERR_CUDA if the synchronisation failed, else
+ * SLA_OK.
  */
 sla_status_t sla_last_device_status(sla_stream_t stream);
 

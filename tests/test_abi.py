@@ -74,40 +74,53 @@ def test_forward_rejects_bad_arguments(f32):
         assert _fwd(f32=f32, **kw) == want, kw
 
 
-def _rope(**kw):
-    args = dict(table=A + 5 * STEP, T=4, Hs=8, Ws=8, dt=44, dh=42, dw=42)
-    args.update(kw)
-    return sla.RopeTableC(args["table"], args["T"], args["Hs"], args["Ws"], args["dt"],
-                          args["dh"], args["dw"])
+TABLE = A + 5 * STEP          # a fake, 256-byte aligned RoPE table address
 
 
-def test_forward_rejects_bad_rope():
-    bad = [
-        (dict(table=0), sla.INVALID_ARG),
-        (dict(T=5), sla.INVALID_ARG),                 # grid has 320 tokens, N = 256
-        (dict(dt=45, dh=41), sla.INVALID_ARG),        # odd band
-        (dict(dt=40), sla.INVALID_ARG),               # bands sum to 124
-        (dict(dw=-2, dt=46, dh=84), sla.INVALID_ARG),
-        (dict(Hs=0), sla.INVALID_ARG),
-        (dict(table=A + 5 * STEP + 4), sla.ALIGNMENT),
-    ]
-    for kw, want in bad:
-        assert _fwd(rope=_rope(**kw)) == want, kw
+def test_forward_rejects_bad_rope_pointers():
+    """The host checks only the table pointer; its contents are checked on the device."""
+    assert _fwd(rope=ctypes.c_void_p(TABLE + 4)) == sla.ALIGNMENT
+    assert _fwd(rope=ctypes.c_void_p(TABLE + 128)) == sla.ALIGNMENT
+    assert _fwd(rope=ctypes.c_void_p(TABLE + 4), f32=True) == sla.ALIGNMENT
+    # a bad table pointer never hides an earlier argument error
+    assert _fwd(q=0, rope=ctypes.c_void_p(TABLE + 4)) == sla.INVALID_ARG
 
 
 def test_rope_table_sizes():
     f = sla.raw_lib().sla_rope_table_floats
-    # fp32 axis rows (rounded up to 64 words), then 64 fp16 pairs per token
-    assert f(25, 22, 40, 44, 42, 42) == 3712 + 22000 * 64
-    assert f(181, 22, 40, 44, 42, 42) == 10624 + 159280 * 64
-    assert f(1, 1, 1, 2, 2, 2) == 64 + 3
-    assert f(0, 1, 1, 2, 2, 2) == 0
-    assert f(1, 1, 1, 3, 2, 2) == 0
+    # 64 header words, then N * d/2 fp16 pair words and N * d fp32 words
+    assert f(22000, 128) == 64 + 22000 * 192
+    assert f(159280, 128) == 64 + 159280 * 192
+    assert f(4290, 256) == 64 + 4290 * 384
+    assert f(1, 2) == 64 + 3
+    assert f(0, 128) == 0
+    assert f(10, 127) == 0
+    assert f(10, 0) == 0
+    assert f(1 << 30, 128) == 0                        # more words than a 32-bit offset holds
     fill = sla.raw_lib().sla_rope_table_fill
-    assert fill(None, 1, 1, 1, 2, 2, 2, 10000.0, None) == sla.INVALID_ARG
-    assert fill(A, 1, 1, 1, 3, 2, 2, 10000.0, None) == sla.INVALID_ARG
-    assert fill(A, 1, 1, 1, 2, 2, 2, 0.0, None) == sla.INVALID_ARG
-    assert fill(A + 4, 1, 1, 1, 2, 2, 2, 10000.0, None) == sla.ALIGNMENT
+    assert fill(None, 1, 1, 1, 6, 2, 2, 2, 10000.0, None) == sla.INVALID_ARG
+    assert fill(A, 1, 1, 1, 7, 3, 2, 2, 10000.0, None) == sla.INVALID_ARG     # odd band
+    assert fill(A, 1, 1, 1, 8, 2, 2, 2, 10000.0, None) == sla.INVALID_ARG     # bands sum to 6
+    assert fill(A, 0, 1, 1, 6, 2, 2, 2, 10000.0, None) == sla.INVALID_ARG
+    assert fill(A, 1, 1, 1, 6, 2, 2, 2, 0.0, None) == sla.INVALID_ARG
+    assert fill(A, 1, 1, 1, 6, 2, 2, 2, float("nan"), None) == sla.INVALID_ARG
+    assert fill(A + 4, 1, 1, 1, 6, 2, 2, 2, 10000.0, None) == sla.ALIGNMENT
+    assert fill(A, 1 << 12, 1 << 10, 1 << 10, 128, 44, 42, 42, 10000.0, None) == \
+        sla.UNSUPPORTED
+    pairs = sla.raw_lib().sla_rope_table_from_pairs
+    assert pairs(None, A + STEP, 10, 128, None) == sla.INVALID_ARG
+    assert pairs(A, None, 10, 128, None) == sla.INVALID_ARG
+    assert pairs(A, A + STEP, 0, 128, None) == sla.INVALID_ARG
+    assert pairs(A, A + STEP, 10, 127, None) == sla.INVALID_ARG
+    assert pairs(A + 64, A + STEP, 10, 128, None) == sla.ALIGNMENT
+    assert pairs(A, A + STEP + 4, 10, 128, None) == sla.ALIGNMENT
+    assert pairs(A, A + 1024, 10, 128, None) == sla.INVALID_ARG       # pairs inside the table
+
+
+def test_selftest_rejects_bad_limits_before_cuda():
+    lib = sla.raw_lib()
+    assert lib.sla_selftest_wait_timeout(0, None) == sla.INVALID_ARG
+    assert lib.sla_selftest_wait_timeout(1000001, None) == sla.INVALID_ARG
 
 
 def test_binding_rejects_mismatched_tensors():
@@ -155,8 +168,8 @@ def test_phase_entry_points_reject_bad_arguments():
     assert ap(Q, G, S, S, 1, 2, 256, 128, None, 1e-6, None) == sla.INVALID_ARG  # out is state
     assert ap(Q, G, S, O + 4, 1, 2, 256, 128, None, 1e-6, None) == sla.ALIGNMENT
     assert ap(Q, 0, S, O, 1, 2, 256, 128, None, 1e-6, None) == sla.INVALID_ARG
-    r = ctypes.byref(_rope(T=5))
-    assert ap(Q, G, S, O, 1, 2, 256, 128, r, 1e-6, None) == sla.INVALID_ARG
+    assert ap(Q, G, S, O, 1, 2, 256, 128, TABLE + 16, 1e-6, None) == sla.ALIGNMENT
+    assert st(K, V, S, 1, 2, 256, 128, TABLE + 16, None) == sla.ALIGNMENT
 
 
 def test_forward_cluster_rejects_bad_shapes_before_cuda():
@@ -168,9 +181,8 @@ def test_forward_cluster_rejects_bad_shapes_before_cuda():
 
 def _bc(q=A, k=A + STEP, v=A + 2 * STEP, g=A + 3 * STEP, out=A + 4 * STEP, B=1, H=2, N=256,
         d=128, bt=64, rope=None, off=0, eps=1e-6, sin=None, sout=None):
-    r = ctypes.byref(rope) if rope is not None else None
-    return sla.raw_lib().sla_linattn_forward_block_causal(q, k, v, g, out, B, H, N, d, bt, r, off,
-                                                          eps, sin, sout, None)
+    return sla.raw_lib().sla_linattn_forward_block_causal(q, k, v, g, out, B, H, N, d, bt, rope,
+                                                          off, eps, sin, sout, None)
 
 
 def test_block_causal_rejects_bad_arguments_before_cuda():
@@ -184,9 +196,9 @@ def test_block_causal_rejects_bad_arguments_before_cuda():
         (dict(eps=-1.0), sla.INVALID_ARG),
         (dict(d=64), sla.UNSUPPORTED),
         (dict(off=64), sla.INVALID_ARG),              # an offset without a RoPE table
-        (dict(rope=_rope(T=4), off=1), sla.INVALID_ARG),    # tokens 1..256 of a 256-token grid
-        (dict(rope=_rope(T=3)), sla.INVALID_ARG),     # a 192-token grid
-        (dict(rope=_rope(T=5), off=-1), sla.INVALID_ARG),
+        (dict(rope=TABLE, off=-1), sla.INVALID_ARG),
+        (dict(rope=TABLE + 32), sla.ALIGNMENT),
+        (dict(rope=TABLE, off=0x7fffffff - 100), sla.UNSUPPORTED),   # tokens past 2^31
         (dict(sin=S + 4), sla.ALIGNMENT),
         (dict(sout=S + 8), sla.ALIGNMENT),
         (dict(sout=A + 4 * STEP + 1024), sla.INVALID_ARG),  # state out inside out
@@ -240,10 +252,7 @@ def test_anchor_rejects_bad_arguments_before_cuda():
         (dict(B=256, H=256), sla.UNSUPPORTED),             # more than 65535 heads
         (dict(v=A + 4 * STEP + 4), sla.ALIGNMENT),
         (dict(out=A + 6 * STEP + 4096), sla.INVALID_ARG),  # out overlaps g
-        (dict(rope=ctypes.byref(sla.RopeTableC(A + 12 * STEP, 4, 8, 8, 44, 42, 42))),
-         sla.INVALID_ARG),                                 # bands sum to 128, not 256
-        (dict(rope=ctypes.byref(sla.RopeTableC(A + 12 * STEP, 4, 8, 4, 88, 84, 84))),
-         sla.INVALID_ARG),                                 # the grid has 128 tokens, not 256
+        (dict(rope=A + 12 * STEP + 8), sla.ALIGNMENT),     # the table is not 256-byte aligned
     ]
     for kw, want in bad:
         assert anchor(**kw) == want, kw

@@ -32,6 +32,9 @@ def test_reference_arm_line(workload, unit):
     assert line["steps"] == 1 and line["warmup"] == 0 and line["n_gpus"] == 1
     assert line["higher_is_better"] is True and line["gpu_launches"] == 0
     assert line["config"]["workload"] == workload
+    # the config names the workload only: no run notes or launch plans in it, so both
+    # arms of a workload carry the same config
+    assert "note" not in line["config"] and "launch_plan" not in line["config"]
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1
     e2e = line["e2e"]

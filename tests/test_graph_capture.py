@@ -47,6 +47,76 @@ def test_forward_replays_in_a_graph(path, cuda_device, monkeypatch):
     assert torch.equal(out, ref)
 
 
+def test_split_forward_replays_with_new_inputs(cuda_device, monkeypatch):
+    """Every head spans many CTAs of the state kernel, whose shared merge counts the
+    contributors in a per-head counter.  A replay reuses the captured launch's
+    parameters, so the counters must be back at zero when a launch ends: with inputs
+    changed between replays, each replay must give the eager call's result for its own
+    inputs, bit for bit."""
+    sla = _sla()
+    monkeypatch.setenv("SLA_FORWARD_KERNEL", "split")
+    wl = Workload("graph_multi", B=2, H=4, grid=(4, 10, 110), rope=True)
+    rope = sla.RopeTable(wl.grid, wl.split, wl.base, device=cuda_device)
+    q, k, v, g = (t.to(cuda_device) for t in make_inputs(wl, seed=36))
+    out = torch.empty_like(q)
+    stream = torch.cuda.Stream(cuda_device)
+    stream.wait_stream(torch.cuda.current_stream(cuda_device))
+    with torch.cuda.stream(stream):
+        sla.linattn_forward(q, k, v, g, out=out, rope=rope, stream=stream)  # workspace
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        sla.linattn_forward(q, k, v, g, out=out, rope=rope, stream=stream)
+    for seed in (37, 38, 39):
+        fresh = [t.to(cuda_device) for t in make_inputs(wl, seed=seed)]
+        with torch.cuda.stream(stream):
+            for dst, src in zip((q, k, v, g), fresh):
+                dst.copy_(src)
+            graph.replay()
+            ref = sla.linattn_forward(*fresh, rope=rope, stream=stream)
+        stream.synchronize()
+        assert sla.last_device_status(stream, device=cuda_device) == 0
+        assert torch.equal(out, ref), seed
+
+
+def test_noalloc_split_replays_with_new_inputs(cuda_device, monkeypatch):
+    """The same for the allocation-free entry point, whose counters live in its fixed
+    array."""
+    sla = _sla()
+    lib = sla.raw_lib()
+    monkeypatch.setenv("SLA_FORWARD_KERNEL", "split")
+    wl = Workload("graph_multi_na", B=2, H=4, grid=(4, 10, 110), rope=True)
+    rope = sla.RopeTable(wl.grid, wl.split, wl.base, device=cuda_device)
+    q, k, v, g = (t.to(cuda_device) for t in make_inputs(wl, seed=40))
+    out = torch.empty_like(q)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    B, H, N, d = q.shape
+    stream = torch.cuda.Stream(cuda_device)
+
+    def call():
+        return lib.sla_linattn_forward_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                               g.data_ptr(), out.data_ptr(), B, H, N, d,
+                                               rope.ptr, 1e-6, status.data_ptr(),
+                                               stream.cuda_stream)
+
+    with torch.cuda.device(cuda_device):
+        assert call() == sla.OK               # looks up the array's address, outside capture
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        assert call() == sla.OK
+    for seed in (41, 42, 43):
+        fresh = [t.to(cuda_device) for t in make_inputs(wl, seed=seed)]
+        with torch.cuda.stream(stream):
+            for dst, src in zip((q, k, v, g), fresh):
+                dst.copy_(src)
+            graph.replay()
+            ref = sla.linattn_forward(*fresh, rope=rope, stream=stream)
+        stream.synchronize()
+        assert int(status.item()) == 0
+        assert torch.equal(out, ref), seed
+
+
 def test_block_causal_replays_in_a_graph(cuda_device):
     sla = _sla()
     wl = Workload("graphbc", B=1, H=3, grid=(4, 8, 10), rope=True, block_frames=2)

@@ -156,7 +156,8 @@ def _full_size_case(name):
 
 
 @pytest.mark.parametrize("path", ["auto", "split"])
-@pytest.mark.parametrize("name", ["5b_480p", "5b_720p", "14b_480p", "5b_720p_60s"])
+@pytest.mark.parametrize("name", ["5b_480p", "5b_720p", "14b_480p", "5b_720p_60s",
+                                  "5b_720p_736"])
 def test_full_size_sampled_rows(name, path, cuda_device):
     """"auto" is the plan the benchmark times."""
     wl = WORKLOADS[name]

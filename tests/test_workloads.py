@@ -44,6 +44,8 @@ def test_derived_sizes():
     assert an.algorithmic_flops == 4 * 2 * 10 * 22000 * 22000 * 256
     ar = WORKLOADS["attnres_5b_720p"]
     assert ar.tokens == 44000 and ar.algorithmic_bytes == 5 * 44000 * 2560 * 2
+    b736 = WORKLOADS["5b_720p_736"]
+    assert b736.N == 25 * 23 * 40 == 23000 and b736.rope
     bc = WORKLOADS["5b_720p_block5"]
     assert bc.block_tokens == 5 * 22 * 40 and bc.N % bc.block_tokens == 0
 
