@@ -1001,7 +1001,7 @@ def _forward_plan(wl, cluster):
                 "carried state updated in place" % (wl.N // wl.block_tokens, wl.block_tokens))
     if wl.dtype != torch.bfloat16:
         return "fp32: state partials + apply (FMA units)"
-    if cluster > 0:
+    if cluster > 1:
         return "fused, clusters of %d CTAs per head" % cluster
     return "state + apply launches"
 

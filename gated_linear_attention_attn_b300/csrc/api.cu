@@ -22,6 +22,7 @@ struct DeviceState {
 struct Workspace {
     void* ptr = nullptr;
     size_t bytes = 0;
+    size_t clean = 0;   // bytes at the start known to be zero when the stream's next launch runs
 };
 
 std::mutex g_mutex;
@@ -46,8 +47,14 @@ sla_status_t device_state(int dev, DeviceState** out) {
 // The workspace of (dev, stream), grown to at least `bytes`.  Calls on one
 // stream are ordered, so they can share it; calls on different streams get
 // different workspaces.  Growing frees the old buffer (cudaFree waits for the
-// device).  Called with g_mutex held.
-sla_status_t workspace(int dev, cudaStream_t stream, size_t bytes, void** out) {
+// device).  The first `counters` bytes hold per-head counters that must read
+// zero when the launch starts: a completed launch leaves its counters at zero
+// and writes its data after them, so the start of the buffer is cleared (on
+// the stream, before the launch) only when a call's counters reach past what
+// the previous call left zero, that is when the shape or the plan changes.
+// Called with g_mutex held.
+sla_status_t workspace(int dev, cudaStream_t stream, size_t bytes, void** out,
+                       size_t counters = 0) {
     Workspace& ws = g_workspaces[{dev, reinterpret_cast<uintptr_t>(stream)}];
     if (ws.bytes < bytes) {
         if (ws.ptr) {
@@ -68,7 +75,13 @@ sla_status_t workspace(int dev, cudaStream_t stream, size_t bytes, void** out) {
             return SLA_ERR_CUDA;
         }
         ws.bytes = rounded;
+        ws.clean = rounded;
     }
+    if (counters > ws.clean && cudaMemsetAsync(ws.ptr, 0, counters, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SLA_ERR_CUDA;
+    }
+    ws.clean = counters;
     *out = ws.ptr;
     return SLA_OK;
 }
@@ -219,7 +232,8 @@ static sla_status_t forward(const void* q, const void* k, const void* v, const v
     } else if (const int C = tc_forward_cluster(dev, BH, N, rp != nullptr, ds->num_sms)) {
         err = launch_tc_fused(q, k, v, g, out, B, H, N, C, rp, eps, ds->status, s);
     } else {
-        if ((st = workspace(dev, s, tc_workspace_bytes(BH, N, ds->num_sms), &ws)) != SLA_OK)
+        if ((st = workspace(dev, s, tc_workspace_bytes(BH, N, ds->num_sms), &ws,
+                            tc_counter_bytes(BH))) != SLA_OK)
             return st;
         err = launch_tc_two_phase(q, k, v, g, out, B, H, N, rp, eps, (float*)ws, ds->status,
                                   ds->num_sms, s);
@@ -287,7 +301,8 @@ static sla_status_t backward(const void* q, const void* k, const void* v, const 
     void* ws = nullptr;
     const size_t ws_bytes = is_f32 ? backward_workspace_bytes(B * H, C)
                                    : backward_bf16_workspace_bytes(B * H, N, ds->num_sms);
-    if ((st = workspace(dev, s, ws_bytes, &ws)) != SLA_OK) return st;
+    if ((st = workspace(dev, s, ws_bytes, &ws, is_f32 ? 0 : tc_counter_bytes(B * H))) != SLA_OK)
+        return st;
     const RopeView* rp = rope ? &rv : nullptr;
     const cudaError_t err =
         is_f32 ? launch_backward_f32((const float*)q, (const float*)k, (const float*)v,
@@ -444,8 +459,8 @@ sla_status_t sla_linattn_forward_block_causal(const void* q, const void* k, cons
     DeviceState* ds = nullptr;
     if ((st = device_state(dev, &ds)) != SLA_OK) return st;
     void* ws = nullptr;
-    if ((st = workspace(dev, s, tc_workspace_bytes(B * H * nb, block_tokens, ds->num_sms), &ws)) !=
-        SLA_OK)
+    if ((st = workspace(dev, s, tc_workspace_bytes(B * H * nb, block_tokens, ds->num_sms), &ws,
+                        tc_counter_bytes(B * H * nb))) != SLA_OK)
         return st;
     if (launch_tc_block_causal(q, k, v, g, out, B, H, N, block_tokens,
                                rope_table ? &rv : nullptr, rope_offset, eps, state_in, state_out,
@@ -494,7 +509,8 @@ sla_status_t sla_linattn_state(const void* k, const void* v, void* state, int B,
     DeviceState* ds = nullptr;
     if ((st = device_state(dev, &ds)) != SLA_OK) return st;
     void* ws = nullptr;
-    if ((st = workspace(dev, s, tc_state_workspace_bytes(B * H, N, ds->num_sms), &ws)) != SLA_OK)
+    if ((st = workspace(dev, s, tc_state_workspace_bytes(B * H, N, ds->num_sms), &ws,
+                        tc_counter_bytes(B * H))) != SLA_OK)
         return st;
     if (launch_tc_state(k, v, state, B, H, N, rope_table ? &rv : nullptr, ws, ds->status,
                         ds->num_sms, s) != cudaSuccess) {

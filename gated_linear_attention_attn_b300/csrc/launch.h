@@ -62,6 +62,10 @@ cudaError_t launch_attnres(const void* const* sources, int M, long long T, int C
 // states); the state phase alone needs tc_state_workspace_bytes and writes
 // tc_state_bytes of state.
 size_t tc_workspace_bytes(int BH, int N, int num_sms);
+// Bytes at the start of a workspace that hold the state kernel's per-head
+// counters, which must read as zero when a launch starts (two-launch plan,
+// state phase, backward, block-causal form).
+size_t tc_counter_bytes(int BH);
 size_t tc_state_workspace_bytes(int BH, int N, int num_sms);
 size_t tc_state_bytes(int BH);
 // The forward runs either as one fused launch (one cluster of C CTAs per

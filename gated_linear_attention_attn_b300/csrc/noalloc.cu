@@ -24,6 +24,7 @@ struct NoAllocDevice {
     bool ready = false;
     int num_sms = 0;
     unsigned char* scratch = nullptr;   // device address of g_noalloc_scratch
+    size_t clean = kScratchBytes;       // bytes at its start known to be zero (all, at load)
 };
 
 std::mutex g_noalloc_mutex;
@@ -80,12 +81,26 @@ extern "C" sla_status_t sla_linattn_forward_noalloc(const void* q, const void* k
     const RopeView* rp = rope_table ? &rv : nullptr;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t err;
-    if (const int C = tc_forward_cluster(dev, BH, N, rp != nullptr, nd->num_sms)) {
+    const int C = tc_forward_cluster(dev, BH, N, rp != nullptr, nd->num_sms);
+    // The per-head counters at the start of the array must read zero: a
+    // completed call leaves its own at zero and its data after them, so the
+    // start is cleared (a memset on the stream, no allocation) only when this
+    // call's counters reach past what the previous call left zero.
+    auto counters_clean = [&](size_t counters) -> bool {
+        if (counters > nd->clean && cudaMemsetAsync(nd->scratch, 0, counters, s) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        nd->clean = counters;
+        return true;
+    };
+    if (C != 0) {
         // the fused kernel needs no scratch
         err = launch_tc_fused(q, k, v, g, out, B, H, N, C, rp, eps, device_status, s);
     } else {
         // the whole scratch this shape needs must fit in the fixed array
         if (tc_workspace_bytes(BH, N, nd->num_sms) > kScratchBytes) return SLA_ERR_UNSUPPORTED;
+        if (!counters_clean(tc_counter_bytes(BH))) return SLA_ERR_CUDA;
         err = launch_tc_two_phase(q, k, v, g, out, B, H, N, rp, eps,
                                   reinterpret_cast<float*>(nd->scratch), device_status,
                                   nd->num_sms, s);

@@ -1,4 +1,4 @@
-// Shared pieces of the bf16 tensor-core kernels (tc_forward.cu, tc_persist.cu):
+// Shared pieces of the bf16 tensor-core kernels (tc_forward.cu, backward.cu):
 // tile geometry, the stream-K split, the feature map, RoPE and gate helpers
 // on 16-byte chunks, the per-head contributor counters, and the TMA tensor
 // maps of [heads][N][128] bf16 tensors and of the per-token RoPE rows.
@@ -165,7 +165,7 @@ __host__ __device__ __forceinline__ uint32_t sw128_off(int r, int c, int half) {
 // if the atomic kept failing (status raised).  A launch that completes leaves
 // every counter it used at zero (see the flush warps), so the tag matters only
 // after a launch that gave up a wait.
-__device__ uint32_t count_contributor(unsigned long long* ctr, uint32_t epoch, unsigned* status) {
+__device__ inline uint32_t count_contributor(unsigned long long* ctr, uint32_t epoch, unsigned* status) {
     unsigned long long seen = *reinterpret_cast<volatile unsigned long long*>(ctr);
     for (int it = 0; it < (1 << 20); ++it) {
         const unsigned long long want = (uint32_t)(seen >> 32) == epoch
@@ -183,7 +183,7 @@ __device__ uint32_t count_contributor(unsigned long long* ctr, uint32_t epoch, u
 // Every contributor is resident (the state kernel is a cooperative launch) and
 // counts itself without waiting for anyone, so the wait ends; it still gives
 // up after kWaitLimitNs.
-__device__ bool wait_count(const unsigned long long* ctr, uint32_t epoch, uint32_t k,
+__device__ inline bool wait_count(const unsigned long long* ctr, uint32_t epoch, uint32_t k,
                            volatile int* abort, unsigned* status) {
     const uint64_t t0 = global_ns();
     for (;;) {
@@ -200,7 +200,7 @@ __device__ bool wait_count(const unsigned long long* ctr, uint32_t epoch, uint32
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
         void* ptr = nullptr;
@@ -216,7 +216,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // A [BH][N][128] bf16 tensor seen as 3D (d fastest), boxes of 64 columns x
 // `rows` tokens x 1 head, 128-byte swizzle; rows past N read as zero and are
 // not written by stores.
-bool make_map(CUtensorMap* m, const void* base, int N, int BH, int rows) {
+inline bool make_map(CUtensorMap* m, const void* base, int N, int BH, int rows) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)N, (cuuint64_t)BH};
@@ -231,7 +231,7 @@ bool make_map(CUtensorMap* m, const void* base, int N, int BH, int rows) {
 
 // The per-token RoPE rows, [N][64] 4-byte (cos, sin) fp16 pairs, 256 bytes per
 // token, boxes of `rows` tokens; rows past N read as zero.
-bool make_rope_map(CUtensorMap* m, const uint32_t* base, int N, int rows) {
+inline bool make_rope_map(CUtensorMap* m, const uint32_t* base, int N, int rows) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)kPairs, (cuuint64_t)N};

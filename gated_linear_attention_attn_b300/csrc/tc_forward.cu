@@ -2010,6 +2010,8 @@ int current_device() {
 
 }  // namespace
 
+size_t tc_counter_bytes(int BH) { return counters_bytes(BH); }
+
 size_t tc_state_workspace_bytes(int BH, int N, int num_sms) {
     return counters_bytes(BH) + partial_bytes(BH, N, num_sms);
 }

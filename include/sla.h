@@ -33,7 +33,11 @@
  * allocated with cudaMalloc on the first call that needs it (or more of it)
  * and kept until the process exits.  A call that has to grow the workspace
  * synchronises the device; make the first call of the largest shape outside
- * stream capture.
+ * stream capture.  The start of a workspace holds per-head counters that
+ * must read zero when a kernel starts; a call of another shape or plan on the
+ * same stream may clear it first (cudaMemsetAsync on the stream), so a
+ * captured graph expects no call of another shape on its stream between its
+ * capture and its replays.
  *
  * Errors.  Every argument is checked before anything is launched; a call
  * that returns an error has launched nothing.  Calls are asynchronous on
@@ -357,12 +361,14 @@ sla_status_t sla_attnres_aggregate(const void* const* sources, int M, int T, int
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
  * capture.  Every call on a device shares the one array, which keeps the
- * last call's contents.  Nothing in it has to be cleared between calls: the
- * only values a call reads before writing them are per-head counters, which
- * the state kernel returns to zero before it exits (the array starts zeroed
- * when the library loads), and which also carry a tag of the call that set
- * them, so that a count left by a call that gave up a wait reads as zero to
- * the next call.  Calls that overlap on the GPU (other streams, other host
+ * last call's contents.  The only values a call reads before writing them are
+ * per-head counters at the start of the array, which must read zero: the state
+ * kernel returns the counters it used to zero before it exits, and a call
+ * whose counters reach past those the previous call left zero (a call with
+ * more heads) first clears the start of the array with cudaMemsetAsync on
+ * `stream` (no allocation).  The counters also carry a tag of the call that
+ * set them, so a count left by a call that gave up a wait reads as zero to the
+ * next call.  Calls that overlap on the GPU (other streams, other host
  * threads) race on the array; order them on one stream or with events.
  */
 sla_status_t sla_linattn_forward_noalloc(const void* q, const void* k, const void* v,

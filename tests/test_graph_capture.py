@@ -47,14 +47,15 @@ def test_forward_replays_in_a_graph(path, cuda_device, monkeypatch):
     assert torch.equal(out, ref)
 
 
-def test_split_forward_replays_with_new_inputs(cuda_device, monkeypatch):
+@pytest.mark.parametrize("path", ["split"])
+def test_forward_replays_with_new_inputs(path, cuda_device, monkeypatch):
     """Every head spans many CTAs of the state kernel, whose shared merge counts the
     contributors in a per-head counter.  A replay reuses the captured launch's
     parameters, so the counters must be back at zero when a launch ends: with inputs
     changed between replays, each replay must give the eager call's result for its own
     inputs, bit for bit."""
     sla = _sla()
-    monkeypatch.setenv("SLA_FORWARD_KERNEL", "split")
+    monkeypatch.setenv("SLA_FORWARD_KERNEL", path)
     wl = Workload("graph_multi", B=2, H=4, grid=(4, 10, 110), rope=True)
     rope = sla.RopeTable(wl.grid, wl.split, wl.base, device=cuda_device)
     q, k, v, g = (t.to(cuda_device) for t in make_inputs(wl, seed=36))
@@ -79,12 +80,13 @@ def test_split_forward_replays_with_new_inputs(cuda_device, monkeypatch):
         assert torch.equal(out, ref), seed
 
 
-def test_noalloc_split_replays_with_new_inputs(cuda_device, monkeypatch):
+@pytest.mark.parametrize("path", ["split"])
+def test_noalloc_replays_with_new_inputs(path, cuda_device, monkeypatch):
     """The same for the allocation-free entry point, whose counters live in its fixed
     array."""
     sla = _sla()
     lib = sla.raw_lib()
-    monkeypatch.setenv("SLA_FORWARD_KERNEL", "split")
+    monkeypatch.setenv("SLA_FORWARD_KERNEL", path)
     wl = Workload("graph_multi_na", B=2, H=4, grid=(4, 10, 110), rope=True)
     rope = sla.RopeTable(wl.grid, wl.split, wl.base, device=cuda_device)
     q, k, v, g = (t.to(cuda_device) for t in make_inputs(wl, seed=40))

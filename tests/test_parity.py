@@ -168,6 +168,31 @@ def test_full_size_sampled_rows(name, path, cuda_device):
     assert np.all(np.isfinite(_np64(out[0, 0])))
 
 
+def test_shapes_and_plans_alternate_on_one_stream(cuda_device):
+    """One stream's workspace serves calls of every shape and plan: each call's per-head
+    counters must start at zero although a call of another shape may have left partial
+    states where they lie.  Each (shape, plan) must give its first result bit for bit
+    every time, and match the oracle."""
+    sla = _sla()
+    shapes = [Workload("alt_a", B=2, H=50, grid=(1, 10, 60), rope=True),     # 100 heads
+              Workload("alt_b", B=1, H=64, grid=(1, 4, 100), rope=False),    # 64 heads
+              Workload("alt_c", B=1, H=3, grid=(3, 10, 20), rope=True)]
+    first = {}
+    order = [(0, "split"), (1, "split"), (2, "fused"), (0, "split"), (2, "split"),
+             (1, "fused"), (0, "split"), (1, "split"), (2, "split"), (0, "fused")]
+    inputs = {i: make_inputs(wl, seed=50 + i) for i, wl in enumerate(shapes)}
+    for i, path in order:
+        wl = shapes[i]
+        out = _run(wl, inputs[i], cuda_device, path)
+        key = (i, path)
+        if key not in first:
+            first[key] = out
+            ref = ol.linattn_forward(*inputs[i], eps=wl.eps, rope=_spec(wl))
+            assert _rel(_np64(out), ref) <= TOL[torch.bfloat16], key
+        else:
+            assert torch.equal(out, first[key]), key
+
+
 def test_dead_query_rows_are_zero(cuda_device):
     wl = Workload("dead", B=1, H=2, grid=(3, 10, 10), rope=True)
     q, k, v, g = make_inputs(wl, seed=3)
