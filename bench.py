@@ -544,9 +544,10 @@ def run_sla(args, rank, world, local):
 
 
 BWD_METRIC = "linear-attn bwd token-heads/s; HBM GB/s as % of B300 peak"
-BWD_LAUNCHES = 9
-BWD_PLAN = ("backward: state(k, v), apply raw(q), terms, state(q, a; dden), apply(a; S), "
-            "dq, apply(v; dS), dk, apply(k; dS) (tcgen05 state/apply kernels + elementwise)")
+BWD_LAUNCHES = 8
+BWD_PLAN = ("backward: state(k, v), apply gate terms(q, g, dout; S), state(q, a; dden), "
+            "apply(a; S), dq, apply(v; dS), dk, apply(k; dS) (tcgen05 state/apply kernels "
+            "+ elementwise)")
 
 
 def oracle_backward_heads(wl, tensors, heads):

@@ -14,7 +14,7 @@
 //
 // HBM-bound: every summary row is read once and x written once.  Each CTA
 // works through its tokens (token blockIdx.x + k * gridDim.x) with a ring of
-// 2 to 6 token slots in shared memory (at most 110 KB, so two CTAs share an SM):
+// 2 to 6 token slots in shared memory (about 70 KB, so several CTAs share an SM):
 // one thread keeps bulk copies of the next tokens' M rows in flight
 // (cp.async.bulk, completion counted on the slot's mbarrier).  Per token,
 // thread i takes the 16-byte piece i of every row, the CTA reduces w . s_n
@@ -38,7 +38,10 @@ using namespace ptx;
 
 constexpr int kArMaxThreads = 512;
 constexpr int kArStages = 6;                // token slots: 2 .. 6, as many as fit the budget
-constexpr size_t kArSmemBudget = 110 * 1024;  // per CTA, so that two CTAs share an SM
+// Per CTA: small rings and more CTAs per SM measured faster than deep rings
+// (5B shape, 20 KB token slots: three slots and three CTAs per SM 209 us,
+// five slots and two CTAs 225 us); a 40 KB slot (14B shape) still gets two.
+constexpr size_t kArSmemBudget = 70 * 1024;
 
 struct AttnResParams {
     const __nv_bfloat16* src[kAttnResMaxSources];
@@ -238,7 +241,9 @@ cudaError_t launch_attnres(const void* const* sources, int M, long long T, int C
     if (e != cudaSuccess) return e;
     const size_t smem = (size_t)p.stages * M * C * 2;
     // the grid (SMs x resident CTAs) per (device, kernel, threads, shared memory), found once:
-    // later calls, also those inside a stream capture, make no attribute or occupancy calls
+    // later calls, also those inside a stream capture, make no attribute or occupancy calls.
+    // The kernel's dynamic shared memory limit is raised to the device's whole opt-in
+    // amount the first time, so that every later size (any C) launches without a call.
     auto launch = [&](auto kernel) -> cudaError_t {
         static std::mutex mu;
         static std::map<std::tuple<int, const void*, int, size_t>, long long> grids;
@@ -251,9 +256,15 @@ cudaError_t launch_attnres(const void* const* sources, int M, long long T, int C
             if (it == grids.end()) {
                 int sms = 0, per_sm = 0;
                 cudaError_t r = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+                cudaFuncAttributes fa{};
+                int optin = 0;
+                if (r == cudaSuccess) r = cudaFuncGetAttributes(&fa, kernel);
+                if (r == cudaSuccess)
+                    r = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                               dev);
                 if (r == cudaSuccess)
                     r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
+                                             optin - (int)fa.sharedSizeBytes);
                 if (r == cudaSuccess)
                     r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads,
                                                                       smem);

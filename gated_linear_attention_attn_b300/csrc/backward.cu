@@ -10,16 +10,16 @@
 //     dk_j   = [k_j > 0] (R_j^T (dS v_j) + dz)    dv_j = dS^T kr_j
 //
 // bf16 inputs: the contractions run on the tensor cores through the state and
-// apply kernels, glued by three elementwise kernels:
+// apply kernels, with an elementwise kernel for the masked gradients:
 //   1. state(k, v)                  S (bf16, as the forward uses it), z
-//   2. apply, raw(q; S)             num
-//   3. bwd_terms_kernel             a, dg, dden
-//   4. state(q, a; weights dden)    dS, dz
-//   5. apply, raw MN(a; S)          S a
-//   6. bwd_grad_kernel              dq
-//   7. apply, raw MN(v; dS)         dS v
-//   8. bwd_grad_kernel              dk
-//   9. apply, raw(k; dS)            dv = dS^T kr
+//   2. apply, gate terms(q, g, dO; S)   num on the tensor cores; a, dg, dden in
+//                                   the epilogue
+//   3. state(q, a; weights dden)    dS, dz
+//   4. apply, raw MN(a; S)          S a
+//   5. bwd_grad_kernel              dq
+//   6. apply, raw MN(v; dS)         dS v
+//   7. bwd_grad_kernel              dk
+//   8. apply, raw(k; dS)            dv = dS^T kr
 // fp32 inputs: fp32 FMA kernels in three launches, each over (chunk of tokens,
 // head): the state partials (simt_state_kernel); bwd_query_kernel (num, a, dg,
 // dden, dq and the chunk's dS, dz); bwd_key_kernel (dk, dv).
@@ -341,50 +341,6 @@ __device__ __forceinline__ float row_sum16(float x) {
     return x;
 }
 
-// a = dO s / den, dg = dO num / den s (1 - s), dden = -(a . num) / den, with
-// den = phi(q) . z + eps and z from the head's state; thread (row, c) holds
-// dims 8c .. 8c + 7 of one row.
-__global__ void __launch_bounds__(256)
-bwd_terms_kernel(const uint4* __restrict__ q, const uint4* __restrict__ g,
-                 const uint4* __restrict__ dout, const uint4* __restrict__ num,
-                 const uint8_t* __restrict__ states, int N, long long rows, float eps,
-                 uint4* __restrict__ a, uint4* __restrict__ dg, float* __restrict__ dden) {
-    const long long row = (long long)blockIdx.x * kRowsPerBlock + threadIdx.x / 16;
-    const int c = threadIdx.x % 16;
-    const bool live = row < rows;
-    const size_t at = (size_t)(live ? row : 0) * 16 + c;
-    float qf[8], gf[8], df[8], nf[8], zf[8];
-    bf8_to_f8(q[at], qf);
-    bf8_to_f8(g[at], gf);
-    bf8_to_f8(dout[at], df);
-    bf8_to_f8(num[at], nf);
-    const float* z = reinterpret_cast<const float*>(
-        states + (size_t)((live ? (unsigned)row : 0u) / (unsigned)N) * kStateBytesB +
-        kHeadDim * kHeadDim * 2);
-    const float4 z0 = *reinterpret_cast<const float4*>(z + 8 * c);
-    const float4 z1 = *reinterpret_cast<const float4*>(z + 8 * c + 4);
-    zf[0] = z0.x; zf[1] = z0.y; zf[2] = z0.z; zf[3] = z0.w;
-    zf[4] = z1.x; zf[5] = z1.y; zf[6] = z1.z; zf[7] = z1.w;
-    float d = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) d = fmaf(fmaxf(qf[j], 0.f), zf[j], d);
-    const float den = row_sum16(d) + eps, inv = 1.f / den;
-    float af[8], gg[8], part = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const float s = ptx::rcp_approx(1.f + ptx::ex2_approx(-gf[j] * kLog2eB));
-        af[j] = df[j] * s * inv;
-        gg[j] = df[j] * nf[j] * inv * s * (1.f - s);
-        part = fmaf(af[j], nf[j], part);
-    }
-    const float dd = -row_sum16(part) * inv;
-    if (live) {
-        a[at] = f8_to_bf8(af);
-        dg[at] = f8_to_bf8(gg);
-        if (c == 0) dden[row] = dd;
-    }
-}
-
 // out = [x > 0] (R^T y + w z) per row, with w = weight[row] (1 without
 // weights) and z from the head's state: dq from S a, dk from dS v.
 template <bool ROPE>
@@ -480,7 +436,7 @@ cudaError_t launch_backward_bf16(const void* q, const void* k, const void* v, co
     const long long rows = (long long)BH * N;
     const size_t tensor = (size_t)rows * kHeadDim * 2;
     // workspace: the state kernel's, the two states, two [rows][128] bf16
-    // tensors (X: num, then S a, then dS v; A: a), then dden
+    // tensors (X: S a, then dS v; A: a), then dden
     uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
     uint8_t* S = ws + tc_state_workspace_bytes(BH, N, num_sms);
     uint8_t* dS = S + (size_t)BH * kStateBytesB;
@@ -492,13 +448,10 @@ cudaError_t launch_backward_bf16(const void* q, const void* k, const void* v, co
     cudaError_t e;
     if ((e = launch_tc_state(k, v, S, B, H, N, rope, ws, status, num_sms, stream)) != cudaSuccess)
         return e;
-    if ((e = launch_tc_apply(q, q, S, X, B, H, N, rope, eps, status, num_sms, stream,
-                             kApplyRaw)) != cudaSuccess)
+    // num on the tensor cores, the gate terms in the apply kernel's epilogue: a, dg, dden
+    if ((e = launch_tc_apply(q, g, S, A, B, H, N, rope, eps, status, num_sms, stream,
+                             kApplyTerms, dout, dg, dden)) != cudaSuccess)
         return e;
-    bwd_terms_kernel<<<blocks, 256, 0, stream>>>(
-        (const uint4*)q, (const uint4*)g, (const uint4*)dout, (const uint4*)X, S, N, rows, eps,
-        (uint4*)A, (uint4*)dg, dden);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = launch_tc_state(q, A, dS, B, H, N, rope, ws, status, num_sms, stream, dden)) !=
         cudaSuccess)
         return e;

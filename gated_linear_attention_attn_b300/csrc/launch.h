@@ -93,11 +93,16 @@ cudaError_t launch_tc_block_causal(const void* q, const void* k, const void* v, 
 cudaError_t launch_tc_state(const void* k, const void* v, void* state, int B, int H, int N,
                             const RopeView* rope, void* workspace, unsigned* status, int num_sms,
                             cudaStream_t stream, const float* zweight = nullptr);
-// mode: 0 the gated apply; 1 out = (R phi(q))^T S; 2 out = S q (q as it is, g unread).
-constexpr int kApplyGate = 0, kApplyRaw = 1, kApplyRawMN = 2;
+// mode: 0 the gated apply; 1 out = (R phi(q))^T S; 2 out = S q (q as it is, g unread);
+// 3 the backward's gate terms: with num = (R phi(q))^T S, den = phi(q) . z + eps and
+// s = sigmoid(g), out = a = dout s / den, dg = dout num s (1 - s) / den and
+// dden = -(a . num) / den per row ([B*H][N] fp32).
+constexpr int kApplyGate = 0, kApplyRaw = 1, kApplyRawMN = 2, kApplyTerms = 3;
 cudaError_t launch_tc_apply(const void* q, const void* g, const void* state, void* out, int B,
                             int H, int N, const RopeView* rope, float eps, unsigned* status,
-                            int num_sms, cudaStream_t stream, int mode = kApplyGate);
+                            int num_sms, cudaStream_t stream, int mode = kApplyGate,
+                            const void* dout = nullptr, void* dg = nullptr,
+                            float* dden = nullptr);
 
 // RoPE table (rope_table.cu): the header, then every token's pairs as fp16
 // and as fp32, from the grid and band split or from caller-given fp32 pairs.

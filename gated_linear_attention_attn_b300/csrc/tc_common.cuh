@@ -61,10 +61,23 @@ constexpr int kApXThreads = 32 * kApXWarps;
 constexpr int kApThreads = 32 * (3 + kApXWarps + kApEWarps);   // + the G producer warp
 constexpr int kApORows = 32;                      // rows of o one epilogue warp stores
 constexpr int kApTmemCols = 256;
-// tc_apply_kernel modes: the gated apply, and two raw products for the backward
-constexpr int kApGate = 0, kApRaw = 1, kApRawMN = 2;
-static_assert(kApGate == kApplyGate && kApRaw == kApplyRaw && kApRawMN == kApplyRawMN,
+// tc_apply_kernel modes: the gated apply, and for the backward two raw
+// products and the gate terms
+constexpr int kApGate = 0, kApRaw = 1, kApRawMN = 2, kApTerms = 3;
+static_assert(kApGate == kApplyGate && kApRaw == kApplyRaw && kApRawMN == kApplyRawMN &&
+                  kApTerms == kApplyTerms,
               "apply modes of the launcher");
+
+// Ring geometry of the apply kernel per mode: Q stages, G stages, the bytes
+// of a G stage and the den slots.  The gate terms stage g and dout tiles
+// together, in two stages of each ring.
+template <int MODE>
+struct ApGeo {
+    static constexpr int kQS = MODE == kApTerms ? 2 : kApQStages;
+    static constexpr int kGS = MODE == kApTerms ? 2 : kApGStages;
+    static constexpr int kGT = MODE == kApTerms ? 2 * kApTile : kApTile;
+    static constexpr int kDS = MODE == kApTerms ? 2 : kApDSlots;   // den slots
+};
 constexpr int kApRowsPerThread = kApTok * 16 / kApXThreads;   // 8
 
 static_assert(kStRowsPerThread == 4 && kApRowsPerThread == 8, "thread/tile split");
@@ -145,6 +158,37 @@ __device__ __forceinline__ uint4 gate_chunk(uint4 g8, const uint32_t* num, float
         ow[e] = f2_to_bf2(o.x, o.y);
     }
     return make_uint4(ow[0], ow[1], ow[2], ow[3]);
+}
+
+// The gate terms of eight elements of one row: g8 and d8 hold g and dout,
+// num the eight fp32 numerators, inv_den 1 / den of the row.  With s =
+// sigmoid(g) (as in gate_chunk): a = dout s / den (to a8), dg = dout num
+// s (1 - s) / den (to g8o), and part += a . num.
+__device__ __forceinline__ void terms_chunk(uint4 g8, uint4 d8, const uint32_t* num,
+                                            float inv_den, uint4& a8, uint4& g8o, float& part) {
+    constexpr float kLog2e = 1.4426950408889634f;
+    const uint32_t gw[4] = {g8.x, g8.y, g8.z, g8.w};
+    const uint32_t dw[4] = {d8.x, d8.y, d8.z, d8.w};
+    uint32_t aw[4], ow[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 gp = make_float2(__uint_as_float(gw[e] << 16),
+                                      __uint_as_float(gw[e] & 0xffff0000u));
+        const float2 dp = make_float2(__uint_as_float(dw[e] << 16),
+                                      __uint_as_float(dw[e] & 0xffff0000u));
+        const float2 np = make_float2(__uint_as_float(num[2 * e]), __uint_as_float(num[2 * e + 1]));
+        const float2 t = mul2(gp, make_float2(-kLog2e, -kLog2e));
+        const float2 e2 = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+        const float2 sg = make_float2(rcp_approx(1.f + e2.x), rcp_approx(1.f + e2.y));
+        const float2 av = mul2(mul2(dp, make_float2(inv_den, inv_den)), sg);   // a
+        const float2 one_m = make_float2(1.f - sg.x, 1.f - sg.y);
+        const float2 gv = mul2(mul2(av, np), one_m);                           // dg
+        part = fmaf(av.x, np.x, fmaf(av.y, np.y, part));
+        aw[e] = f2_to_bf2(av.x, av.y);
+        ow[e] = f2_to_bf2(gv.x, gv.y);
+    }
+    a8 = make_uint4(aw[0], aw[1], aw[2], aw[3]);
+    g8o = make_uint4(ow[0], ow[1], ow[2], ow[3]);
 }
 
 // warp_wait for phases completed by arrivals from other CTAs of the cluster.

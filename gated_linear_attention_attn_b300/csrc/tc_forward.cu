@@ -93,6 +93,7 @@ struct ApplyParams {
     float eps;
     unsigned* status;
     int nb, tok0;                   // as in StateParams
+    float* dden;                    // kApTerms: -(a . num) / den per row, [heads][N]
 };
 
 // =================================================================== state ==
@@ -649,30 +650,44 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 //   kApRaw    out_i = (R_i phi(x_i))^T S, the forward's numerator;
 //   kApRawMN  out_i[m] = sum_n x_i[n] S[m][n] = S x_i, x taken as it is (no
 //             feature map, no rotation) and the buffer read as an MN-major
-//             B operand.
+//             B operand;
+// and for the gate terms of the backward:
+//   kApTerms  with num_i = (R_i phi(q_i))^T S, den_i and s_i = sigmoid(g_i):
+//             out (a) = dout s / den, dg = dout num s (1 - s) / den (both bf16,
+//             written over dout and g in the G slot and stored with TMA
+//             through tm_o32 and tm_dg) and dden_i = -(a_i . num_i) / den_i
+//             (fp32, p.dden); g and dout stream in together through the G
+//             ring (tm_g, tm_d).
 template <bool ROPE, int MODE>
 __global__ void __launch_bounds__(kApThreads, 1)
 tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_g,
-                const __grid_constant__ CUtensorMap tm_o32, ApplyParams p) {
+                const __grid_constant__ CUtensorMap tm_o32, const __grid_constant__ CUtensorMap tm_d,
+                const __grid_constant__ CUtensorMap tm_dg, ApplyParams p) {
+    constexpr int QS = ApGeo<MODE>::kQS, GS = ApGeo<MODE>::kGS, GT = ApGeo<MODE>::kGT;
+    constexpr int DS = ApGeo<MODE>::kDS;
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint8_t* qring = smem;                                      // [kApQStages][32 KB]
-    uint8_t* gring = smem + kApQStages * kApTile;               // [kApGStages][32 KB]
-    uint8_t* sbuf = gring + kApGStages * kApTile;               // S^T bf16 (B operand), then z
+    uint8_t* qring = smem;                                      // [QS][32 KB]
+    uint8_t* gring = smem + QS * kApTile;                       // [GS][GT]
+    uint8_t* sbuf = gring + GS * GT;                            // S^T bf16 (B operand), then z
     float* zs = reinterpret_cast<float*>(sbuf + kStateSBytes);  // [128]
-    float* dens = zs + kHeadDim;                // [kApDSlots][128] phi(q) . z + eps
-    uint64_t* qfull = reinterpret_cast<uint64_t*>(dens + kApDSlots * kApTok);
-    uint64_t* qready = qfull + kApQStages;       // Q tile transformed (MMA may read it)
-    uint64_t* qempty = qready + kApQStages;      // Q tile read by the MMA
-    uint64_t* gfull = qempty + kApQStages;
-    uint64_t* gempty = gfull + kApGStages;       // o stored from the G slot
-    uint64_t* dready = gempty + kApGStages;      // [kApDSlots] den of a tile written
-    uint64_t* dfree = dready + kApDSlots;        // [kApDSlots] den of a tile read
-    uint64_t* accfull = dfree + kApDSlots;       // [2]
+    float* dens = zs + kHeadDim;                // [DS][128] phi(q) . z + eps
+    // kApTerms: a . num over the second column half of each row, two tiles deep
+    float* dpart = dens + DS * kApTok;          // [2][128]
+    constexpr int kDPart = MODE == kApTerms ? 2 * kApTok : 0;
+    uint64_t* qfull = reinterpret_cast<uint64_t*>(dpart + kDPart);
+    uint64_t* qready = qfull + QS;       // Q tile transformed (MMA may read it)
+    uint64_t* qempty = qready + QS;      // Q tile read by the MMA
+    uint64_t* gfull = qempty + QS;
+    uint64_t* gempty = gfull + GS;       // o stored from the G slot
+    uint64_t* dready = gempty + GS;      // [DS] den of a tile written
+    uint64_t* dfree = dready + DS;        // [DS] den of a tile read
+    uint64_t* accfull = dfree + DS;       // [2]
     uint64_t* accempty = accfull + 2;            // [2]
     uint64_t* sready = accempty + 2;
     uint64_t* sfree = sready + 1;
     uint64_t* mma_done = sfree + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    uint64_t* pairdone = mma_done + 1;           // kApTerms: [2] the tile's dpart written
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pairdone + (MODE == kApTerms ? 2 : 0));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -681,16 +696,20 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t smem0 = smem_u32(smem);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kApQStages; ++s) {
+        if (MODE == kApTerms) {
+            mbar_init(&pairdone[0], kApEWarps);
+            mbar_init(&pairdone[1], kApEWarps);
+        }
+        for (int s = 0; s < QS; ++s) {
             mbar_init(&qfull[s], 1);
             mbar_init(&qready[s], kApXWarps);
             mbar_init(&qempty[s], 1);
         }
-        for (int s = 0; s < kApGStages; ++s) {
+        for (int s = 0; s < GS; ++s) {
             mbar_init(&gfull[s], 1);
             mbar_init(&gempty[s], kApEWarps);
         }
-        for (int s = 0; s < kApDSlots; ++s) {
+        for (int s = 0; s < DS; ++s) {
             mbar_init(&dready[s], kApXWarps);
             mbar_init(&dfree[s], kApEWarps);
         }
@@ -711,6 +730,10 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_g);
         prefetch_tmap(&tm_o32);
+        if (MODE == kApTerms) {
+            prefetch_tmap(&tm_d);
+            prefetch_tmap(&tm_dg);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, kApTmemCols);
@@ -786,9 +809,9 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     ++heads;
                     cur_h = h;
                 }
-                if (first_pending && it == kApQStages) load_first();
-                const int s = (int)(it % kApQStages);
-                const uint32_t round = (uint32_t)(it / kApQStages);
+                if (first_pending && it == QS) load_first();
+                const int s = (int)(it % QS);
+                const uint32_t round = (uint32_t)(it / QS);
                 if (!(ok = wait_stage(s, (round & 1) ^ 1))) break;
                 uint8_t* st = qring + s * kApTile;
                 mbar_arrive_expect_tx(&qfull[s], kApTile);
@@ -798,9 +821,9 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (ok && first_pending && first_h >= 0) load_first();
             if (ok) resolve_pending();
             // every copy issued has landed before the CTA may exit
-            const long long first = it > kApQStages ? it - kApQStages : 0;
+            const long long first = it > QS ? it - QS : 0;
             for (long long j = first; j < it; ++j)
-                mbar_wait_drain(&qfull[j % kApQStages], (uint32_t)((j / kApQStages) & 1));
+                mbar_wait_drain(&qfull[j % QS], (uint32_t)((j / QS) & 1));
             if (loads > 0) mbar_wait_drain(sready, (loads - 1) & 1);
         }
     } else if (warp == 1) {
@@ -820,8 +843,8 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     ++heads;
                     cur_h = h;
                 }
-                const int s = (int)(it % kApQStages);
-                const uint32_t round = (uint32_t)(it / kApQStages);
+                const int s = (int)(it % QS);
+                const uint32_t round = (uint32_t)(it / QS);
                 const int a = (int)(it & 1);
                 const uint32_t around = (uint32_t)(it >> 1);
                 ok = mbar_wait(&accempty[a], (around & 1) ^ 1, abort_flag, p.status) &&
@@ -887,10 +910,10 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 ++heads;
                 cur_h = h;
             }
-            const int s = (int)(it % kApQStages);
-            const uint32_t round = (uint32_t)(it / kApQStages);
-            const int ds = (int)(it % kApDSlots);
-            const uint32_t dround = (uint32_t)(it / kApDSlots);
+            const int s = (int)(it % QS);
+            const uint32_t round = (uint32_t)(it / QS);
+            const int ds = (int)(it % DS);
+            const uint32_t dround = (uint32_t)(it / DS);
             if (!(ok = warp_wait(&qfull[s], round & 1, abort_flag, p.status))) break;
             // the epilogue has read the den slot's previous tile
             if (dround > 0 && !(ok = warp_wait(&dfree[ds], (dround - 1) & 1, abort_flag, p.status)))
@@ -973,20 +996,22 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         bool ok = !*abort_flag;
         for (long long u = u0; ok && u < u1; ++u, ++it) {
             const int h = (int)(u / p.Tq), tile = (int)(u % p.Tq);
-            const int gs = (int)(it % kApGStages);
-            const uint32_t ground = (uint32_t)(it / kApGStages);
-            const int ds = (int)(it % kApDSlots);
+            const int gs = (int)(it % GS);
+            const uint32_t ground = (uint32_t)(it / GS);
+            const int ds = (int)(it % DS);
             const int a = (int)(it & 1);
             const uint32_t around = (uint32_t)(it >> 1);
             ok = warp_wait(&accfull[a], around & 1, abort_flag, p.status) &&
-                 warp_wait(&dready[ds], (uint32_t)(it / kApDSlots) & 1, abort_flag, p.status) &&
+                 warp_wait(&dready[ds], (uint32_t)(it / DS) & 1, abort_flag, p.status) &&
                  warp_wait(&gfull[gs], ground & 1, abort_flag, p.status);
             if (!ok) break;
             tc_fence_after();
             const float den = dens[ds * kApTok + r];
+            const float inv_den = 1.f / den;
+            float part = 0.f;
             __syncwarp();
             if (lane == 0) mbar_arrive(&dfree[ds]);
-            const uint32_t gb = smem0 + kApQStages * kApTile + gs * kApTile;
+            const uint32_t gb = smem0 + QS * kApTile + gs * GT;
 #pragma unroll 1
             for (int ch = 0; ch < 2; ++ch) {
                 uint32_t addr[4];
@@ -994,14 +1019,27 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                 for (int sub = 0; sub < 4; ++sub) {
                     addr[sub] = gb + sw128_off(r, hf * 8 + ch * 4 + sub, kApHalf);
-                    if (MODE == kApGate) gv[sub] = lds128(addr[sub]);
+                    if (MODE == kApGate || MODE == kApTerms) gv[sub] = lds128(addr[sub]);
+                }
+                uint4 dv[4];                          // kApTerms: dout, in the stage's second tile
+                if constexpr (MODE == kApTerms) {
+#pragma unroll
+                    for (int sub = 0; sub < 4; ++sub) dv[sub] = lds128(addr[sub] + kApTile);
                 }
                 uint32_t v[32];
                 tmem_ld32(tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)a * 128 + hf * 64 +
                               ch * 32,
                           v);
                 tmem_ld_wait();
-                if constexpr (MODE == kApGate) {
+                if constexpr (MODE == kApTerms) {
+                    // a over dout, dg over g; part collects a . num of the row
+#pragma unroll
+                    for (int sub = 0; sub < 4; ++sub) {
+                        uint4 av;
+                        terms_chunk(gv[sub], dv[sub], v + 8 * sub, inv_den, av, gv[sub], part);
+                        sts128(addr[sub] + kApTile, av);
+                    }
+                } else if constexpr (MODE == kApGate) {
 #pragma unroll
                     for (int sub = 0; sub < 4; ++sub) gv[sub] = gate_chunk(gv[sub], v + 8 * sub, den);
                 } else {
@@ -1020,17 +1058,34 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             tc_fence_before();
             fence_proxy_async_smem();
+            if constexpr (MODE == kApTerms) {
+                // dden of the row from the two column halves (the warp of the
+                // other half has the same rows)
+                const int pb = (int)(it & 1);
+                if (hf == 1) dpart[pb * kApTok + r] = part;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&pairdone[pb]);
+                if (!(ok = warp_wait(&pairdone[pb], (uint32_t)(it >> 1) & 1, abort_flag,
+                                     p.status)))
+                    break;
+                const int row = tile * kApTok + r;
+                if (hf == 0 && row < p.N)
+                    p.dden[(size_t)h * p.N + row] = -(part + dpart[pb * kApTok + r]) * inv_den;
+            }
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&accempty[a]);
                 // this warp's rows 32*quad.. of column half hf, 4 KB of the tile
-                tma_store_3d(&tm_o32, gring + gs * kApTile + hf * kApHalf +
-                                          quad * kApORows * 128,
+                tma_store_3d(&tm_o32, gring + gs * GT + hf * kApHalf + quad * kApORows * 128 +
+                                          (MODE == kApTerms ? kApTile : 0),
                              64 * hf, tile * kApTok + quad * kApORows, h);
+                if (MODE == kApTerms)               // dg, from the g half of the slot
+                    tma_store_3d(&tm_dg, gring + gs * GT + hf * kApHalf + quad * kApORows * 128,
+                                 64 * hf, tile * kApTok + quad * kApORows, h);
                 bulk_commit();
                 // the previous tile's store has read its G slot, which may be refilled
                 bulk_wait_read_one();
-                if (it > 0) mbar_arrive(&gempty[(it - 1) % kApGStages]);
+                if (it > 0) mbar_arrive(&gempty[(it - 1) % GS]);
             }
         }
         if (lane == 0) bulk_wait_all();
@@ -1041,21 +1096,26 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             long long it = 0;
             for (long long u = u0; u < u1; ++u, ++it) {
                 const int h = (int)(u / p.Tq), tile = (int)(u % p.Tq);
-                const int s = (int)(it % kApGStages);
-                const uint32_t round = (uint32_t)(it / kApGStages);
+                const int s = (int)(it % GS);
+                const uint32_t round = (uint32_t)(it / GS);
                 if (!mbar_wait(&gempty[s], (round & 1) ^ 1, abort_flag, p.status)) break;
-                if constexpr (MODE != kApGate) {
+                if constexpr (MODE == kApRaw || MODE == kApRawMN) {
                     mbar_arrive(&gfull[s]);         // the slot only stages the output
                     continue;
                 }
-                uint8_t* st = gring + s * kApTile;
-                mbar_arrive_expect_tx(&gfull[s], kApTile);
+                uint8_t* st = gring + s * GT;
+                mbar_arrive_expect_tx(&gfull[s], GT);
                 tma_load_3d(st, &tm_g, &gfull[s], 0, tile * kApTok, h, policy);
                 tma_load_3d(st + kApHalf, &tm_g, &gfull[s], 64, tile * kApTok, h, policy);
+                if (MODE == kApTerms) {             // dout next to g
+                    tma_load_3d(st + kApTile, &tm_d, &gfull[s], 0, tile * kApTok, h, policy);
+                    tma_load_3d(st + kApTile + kApHalf, &tm_d, &gfull[s], 64, tile * kApTok, h,
+                                policy);
+                }
             }
-            const long long first = it > kApGStages ? it - kApGStages : 0;
+            const long long first = it > GS ? it - GS : 0;
             for (long long j = first; j < it; ++j)
-                mbar_wait_drain(&gfull[j % kApGStages], (uint32_t)((j / kApGStages) & 1));
+                mbar_wait_drain(&gfull[j % GS], (uint32_t)((j / GS) & 1));
         }
     }
 
@@ -1744,11 +1804,12 @@ constexpr size_t st_smem() {
     return (size_t)kStRing + 2 * kStXWarps * kHeadDim * sizeof(float) +
            (3 * StGeo<ROPE>::kStages + 13) * 8 + 16;
 }
-template <bool ROPE>
+template <bool ROPE, int MODE = kApGate>
 constexpr size_t ap_smem() {
-    return (size_t)(kApQStages + kApGStages) * kApTile + kStateBytes +
-           kApDSlots * kApTok * sizeof(float) +
-           (3 * kApQStages + 2 * kApGStages + 2 * kApDSlots + 7) * 8 + 16;
+    using G = ApGeo<MODE>;
+    return (size_t)G::kQS * kApTile + (size_t)G::kGS * G::kGT + kStateBytes +
+           (G::kDS + (MODE == kApTerms ? 2 : 0)) * kApTok * sizeof(float) +
+           (3 * G::kQS + 2 * G::kGS + 2 * G::kDS + 7 + (MODE == kApTerms ? 2 : 0)) * 8 + 16;
 }
 // fused: the ring, the state, the denominators, then 3*stages + 7 phase-1 and
 // cluster mbarriers, the apply kernel's 3*Q + 2*G + 2*den + 5 and two words.
@@ -1762,6 +1823,7 @@ constexpr size_t fu_smem() {
 static_assert(fu_smem<true>() <= 232448 && fu_smem<false>() <= 232448, "fused kernel smem");
 static_assert(st_smem<true>() <= 232448 && st_smem<false>() <= 232448, "state kernel smem");
 static_assert(ap_smem<true>() <= 232448 && ap_smem<false>() <= 232448, "apply kernel smem");
+static_assert(ap_smem<true, kApTerms>() <= 232448, "apply kernel smem, gate terms");
 
 struct Plan {
     int Tk, Tq;
@@ -1804,6 +1866,11 @@ cudaError_t configure(int dev) {
     if ((e = set_smem(tc_apply_kernel<false, kApRaw>, ap_smem<false>())) != cudaSuccess) return e;
     if ((e = set_smem(tc_apply_kernel<true, kApRaw>, ap_smem<true>())) != cudaSuccess) return e;
     if ((e = set_smem(tc_apply_kernel<false, kApRawMN>, ap_smem<false>())) != cudaSuccess)
+        return e;
+    if ((e = set_smem(tc_apply_kernel<false, kApTerms>, ap_smem<false, kApTerms>())) !=
+        cudaSuccess)
+        return e;
+    if ((e = set_smem(tc_apply_kernel<true, kApTerms>, ap_smem<true, kApTerms>())) != cudaSuccess)
         return e;
     if ((e = set_smem(tc_fused_kernel<false>, fu_smem<false>())) != cudaSuccess) return e;
     if ((e = set_smem(tc_fused_kernel<true>, fu_smem<true>())) != cudaSuccess) return e;
@@ -1856,11 +1923,16 @@ cudaError_t launch_state(const void* k, const void* v, int BH, int N, const Rope
 cudaError_t launch_apply(const void* q, const void* g, const uint8_t* state, void* out, int BH,
                          int N, const RopeView* rope, float eps, unsigned* status, int num_sms,
                          bool after_state, cudaStream_t stream, int nb = 1, int tok0 = 0,
-                         int mode = kApGate) {
+                         int mode = kApGate, const void* dout = nullptr, void* dg = nullptr,
+                         float* dden = nullptr) {
     const Plan pl = make_plan(BH, N, num_sms);
     CUtensorMap mq, mg, mo;
     if (!make_map(&mq, q, N, BH, kApTok) || !make_map(&mg, g, N, BH, kApTok) ||
         !make_map(&mo, out, N, BH, kApORows))
+        return cudaErrorInvalidValue;
+    CUtensorMap md = mg, mdg = mo;     // read and written only by the gate terms
+    if (mode == kApTerms &&
+        (!make_map(&md, dout, N, BH, kApTok) || !make_map(&mdg, dg, N, BH, kApORows)))
         return cudaErrorInvalidValue;
     ApplyParams ap{};
     ap.N = N;
@@ -1871,11 +1943,14 @@ cudaError_t launch_apply(const void* q, const void* g, const uint8_t* state, voi
     ap.status = status;
     ap.nb = nb;
     ap.tok0 = tok0;
+    ap.dden = dden;
     if (rope) ap.rope = *rope;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(pl.ap.G);
     cfg.blockDim = dim3(kApThreads);
-    cfg.dynamicSmemBytes = rope ? ap_smem<true>() : ap_smem<false>();
+    cfg.dynamicSmemBytes = mode == kApTerms ? (rope ? ap_smem<true, kApTerms>()
+                                                    : ap_smem<false, kApTerms>())
+                                            : (rope ? ap_smem<true>() : ap_smem<false>());
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1885,13 +1960,20 @@ cudaError_t launch_apply(const void* q, const void* g, const uint8_t* state, voi
     cfg.attrs = attr;
     cfg.numAttrs = after_state ? 1 : 0;
     if (mode == kApRawMN)
-        return cudaLaunchKernelEx(&cfg, tc_apply_kernel<false, kApRawMN>, mq, mg, mo, ap);
+        return cudaLaunchKernelEx(&cfg, tc_apply_kernel<false, kApRawMN>, mq, mg, mo, md, mdg, ap);
     if (mode == kApRaw) {
-        if (rope) return cudaLaunchKernelEx(&cfg, tc_apply_kernel<true, kApRaw>, mq, mg, mo, ap);
-        return cudaLaunchKernelEx(&cfg, tc_apply_kernel<false, kApRaw>, mq, mg, mo, ap);
+        if (rope)
+            return cudaLaunchKernelEx(&cfg, tc_apply_kernel<true, kApRaw>, mq, mg, mo, md, mdg, ap);
+        return cudaLaunchKernelEx(&cfg, tc_apply_kernel<false, kApRaw>, mq, mg, mo, md, mdg, ap);
     }
-    if (rope) return cudaLaunchKernelEx(&cfg, tc_apply_kernel<true, kApGate>, mq, mg, mo, ap);
-    return cudaLaunchKernelEx(&cfg, tc_apply_kernel<false, kApGate>, mq, mg, mo, ap);
+    if (mode == kApTerms) {
+        if (rope)
+            return cudaLaunchKernelEx(&cfg, tc_apply_kernel<true, kApTerms>, mq, mg, mo, md, mdg, ap);
+        return cudaLaunchKernelEx(&cfg, tc_apply_kernel<false, kApTerms>, mq, mg, mo, md, mdg, ap);
+    }
+    if (rope)
+        return cudaLaunchKernelEx(&cfg, tc_apply_kernel<true, kApGate>, mq, mg, mo, md, mdg, ap);
+    return cudaLaunchKernelEx(&cfg, tc_apply_kernel<false, kApGate>, mq, mg, mo, md, mdg, ap);
 }
 
 template <bool ROPE>
@@ -2033,11 +2115,12 @@ cudaError_t launch_tc_state(const void* k, const void* v, void* state, int B, in
 
 cudaError_t launch_tc_apply(const void* q, const void* g, const void* state, void* out, int B,
                             int H, int N, const RopeView* rope, float eps, unsigned* status,
-                            int num_sms, cudaStream_t stream, int mode) {
+                            int num_sms, cudaStream_t stream, int mode, const void* dout,
+                            void* dg, float* dden) {
     cudaError_t e = configure(current_device());
     if (e != cudaSuccess) return e;
     return launch_apply(q, g, static_cast<const uint8_t*>(state), out, B * H, N, rope, eps,
-                        status, num_sms, false, stream, 1, 0, mode);
+                        status, num_sms, false, stream, 1, 0, mode, dout, dg, dden);
 }
 
 int tc_forward_cluster(int dev, int BH, int N, bool rope, int num_sms) {

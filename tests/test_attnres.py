@@ -61,3 +61,16 @@ def test_attnres_full_size_sampled_tokens(name, cuda_device):
     want = oa.attnres_aggregate(s[:, rows].double().numpy(), w.double().numpy(), EPS)
     assert _rel(got[rows].double().cpu().numpy(), want) <= TOL
     assert torch.isfinite(got.float()).all()
+
+
+def test_attnres_hidden_sizes_alternate(cuda_device):
+    """One kernel (same source count, same rows-in-registers choice) launched with
+    different shared-memory sizes in turn: a larger size after a smaller one must still
+    launch (the kernel's shared-memory limit is not lowered by a smaller call)."""
+    sla = _sla()
+    for C in (2560, 512, 1024, 2560, 256, 2560):
+        s, w = make_attnres_inputs(_wl(4, 33, C), seed=13)
+        got = sla.attnres_aggregate(s.to(cuda_device), w.to(cuda_device), eps=EPS)
+        assert sla.last_device_status(device=cuda_device) == sla.OK
+        want = oa.attnres_aggregate(s.double().numpy(), w.double().numpy(), EPS)
+        assert _rel(got.double().cpu().numpy(), want) <= TOL, C
