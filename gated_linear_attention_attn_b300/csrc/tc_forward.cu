@@ -1722,6 +1722,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 
 constexpr int kScanRows = 16;
 constexpr int kScanThreads = kScanRows * 16;      // one thread per (row, 8 key dims)
+constexpr int kScanBatch = 4;                     // slots whose loads are in flight at once
 
 struct ScanParams {
     const float* partial;       // the state kernel's slots (cta + segment)
@@ -1754,12 +1755,12 @@ block_scan_kernel(ScanParams p) {
         const int sh = head * p.nb + b;
         const int lo = p.split.owner((long long)sh * p.Tk);
         const int hi = p.split.owner((long long)(sh + 1) * p.Tk - 1);
-        // the block's slots, four loaded before any is added, added in order
-        for (int c0 = lo; c0 <= hi; c0 += 4) {
-            float4 x0[4], x1[4];
-            float zx[4];
+        // the block's slots, kScanBatch loaded before any is added, added in order
+        for (int c0 = lo; c0 <= hi; c0 += kScanBatch) {
+            float4 x0[kScanBatch], x1[kScanBatch];
+            float zx[kScanBatch];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < kScanBatch; ++j) {
                 if (c0 + j <= hi) {
                     const float* slot = p.partial + (size_t)(c0 + j + sh) * kPartialFloats;
                     const float4* src = reinterpret_cast<const float4*>(slot + n * kHeadDim + cc * 8);
@@ -1769,7 +1770,7 @@ block_scan_kernel(ScanParams p) {
                 }
             }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < kScanBatch; ++j) {
                 if (c0 + j <= hi) {
                     acc[0] += x0[j].x; acc[1] += x0[j].y; acc[2] += x0[j].z; acc[3] += x0[j].w;
                     acc[4] += x1[j].x; acc[5] += x1[j].y; acc[6] += x1[j].z; acc[7] += x1[j].w;
