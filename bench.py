@@ -544,10 +544,10 @@ def run_sla(args, rank, world, local):
 
 
 BWD_METRIC = "linear-attn bwd token-heads/s; HBM GB/s as % of B300 peak"
-BWD_LAUNCHES = 8
+BWD_LAUNCHES = 6
 BWD_PLAN = ("backward: state(k, v), apply gate terms(q, g, dout; S), state(q, a; dden), "
-            "apply(a; S), dq, apply(v; dS), dk, apply(k; dS) (tcgen05 state/apply kernels "
-            "+ elementwise)")
+            "apply masked gradient(a; S, q) -> dq, apply masked gradient(v; dS, k) -> dk, "
+            "apply raw(k; dS) -> dv (tcgen05 state/apply kernels)")
 
 
 def oracle_backward_heads(wl, tensors, heads):

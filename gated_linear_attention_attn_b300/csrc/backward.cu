@@ -10,16 +10,15 @@
 //     dk_j   = [k_j > 0] (R_j^T (dS v_j) + dz)    dv_j = dS^T kr_j
 //
 // bf16 inputs: the contractions run on the tensor cores through the state and
-// apply kernels, with an elementwise kernel for the masked gradients:
-//   1. state(k, v)                  S (bf16, as the forward uses it), z
+// apply kernels, the elementwise terms in the apply kernel's epilogue:
+//   1. state(k, v)                      S (bf16, as the forward uses it), z
 //   2. apply, gate terms(q, g, dO; S)   num on the tensor cores; a, dg, dden in
-//                                   the epilogue
-//   3. state(q, a; weights dden)    dS, dz
-//   4. apply, raw MN(a; S)          S a
-//   5. bwd_grad_kernel              dq
-//   6. apply, raw MN(v; dS)         dS v
-//   7. bwd_grad_kernel              dk
-//   8. apply, raw(k; dS)            dv = dS^T kr
+//                                       the epilogue
+//   3. state(q, a; weights dden)        dS, dz
+//   4. apply, masked gradient(a; S, q)  S a on the tensor cores; dq in the
+//                                       epilogue (mask of q, R^T, + dden z)
+//   5. apply, masked gradient(v; dS, k) dS v; dk (mask of k, R^T, + dz)
+//   6. apply, raw(k; dS)                dv = dS^T kr
 // fp32 inputs: fp32 FMA kernels in three launches, each over (chunk of tokens,
 // head): the state partials (simt_state_kernel); bwd_query_kernel (num, a, dg,
 // dden, dq and the chunk's dS, dz); bwd_key_kernel (dk, dv).
@@ -314,69 +313,6 @@ bwd_key_kernel(const T* __restrict__ k, const T* __restrict__ v, T* __restrict__
 // ------------------------------------------------ bf16, on the tensor cores
 
 constexpr int kStateBytesB = kHeadDim * kHeadDim * 2 + kHeadDim * 4;   // bf16 S^T, then z
-constexpr int kRowsPerBlock = 16;                 // 16 threads (8 dims each) per row
-constexpr float kLog2eB = 1.4426950408889634f;
-
-__device__ __forceinline__ void bf8_to_f8(uint4 u, float (&f)[8]) {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 t = bf2_to_f2(w[i]);
-        f[2 * i] = t.x;
-        f[2 * i + 1] = t.y;
-    }
-}
-
-__device__ __forceinline__ uint4 f8_to_bf8(const float (&f)[8]) {
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) w[i] = f2_to_bf2(f[2 * i], f[2 * i + 1]);
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// Sum over the 16 lanes of a row (lanes 16 (lane / 16) .. + 15 of the warp).
-__device__ __forceinline__ float row_sum16(float x) {
-#pragma unroll
-    for (int off = 8; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-    return x;
-}
-
-// out = [x > 0] (R^T y + w z) per row, with w = weight[row] (1 without
-// weights) and z from the head's state: dq from S a, dk from dS v.
-template <bool ROPE>
-__global__ void __launch_bounds__(256)
-bwd_grad_kernel(const uint4* __restrict__ x, const uint4* __restrict__ y,
-                const float* __restrict__ weight, const uint8_t* __restrict__ states, int N,
-                long long rows, RopeView rope, uint4* __restrict__ out) {
-    const long long row = (long long)blockIdx.x * kRowsPerBlock + threadIdx.x / 16;
-    const int c = threadIdx.x % 16;
-    if (row >= rows) return;
-    if (ROPE && !rope_table_ok(rope)) return;        // reported by the state kernel
-    const size_t at = (size_t)row * 16 + c;
-    float xf[8], yf[8];
-    bf8_to_f8(x[at], xf);
-    bf8_to_f8(y[at], yf);
-    // rows < 2^31 (the entry point bounds B * H * N): 32-bit division
-    const unsigned bh = (unsigned)row / (unsigned)N;
-    const int n = (int)((unsigned)row - bh * (unsigned)N);
-    if (ROPE) {
-        // pairs 4c .. 4c + 3 of the token's fp16 (cos, sin) row, turned back
-        const uint4 t = __ldg(reinterpret_cast<const uint4*>(rope.tok + (size_t)n * kPairs) + c);
-        const uint32_t w[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const float2 cs = __half22float2(*reinterpret_cast<const __half2*>(&w[p]));
-            rotate_pair(yf[2 * p], yf[2 * p + 1], make_float2(cs.x, -cs.y));
-        }
-    }
-    const float wr = weight ? weight[row] : 1.f;
-    const float* z = reinterpret_cast<const float*>(states + (size_t)bh * kStateBytesB +
-                                                    kHeadDim * kHeadDim * 2) + 8 * c;
-    float of[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) of[j] = xf[j] > 0.f ? fmaf(wr, z[j], yf[j]) : 0.f;
-    out[at] = f8_to_bf8(of);
-}
 
 template <typename T>
 cudaError_t launch_backward(const T* q, const T* k, const T* v, const T* g, const T* dout, T* dq,
@@ -424,8 +360,8 @@ size_t backward_workspace_bytes(int BH, int C) {
 
 size_t backward_bf16_workspace_bytes(int BH, int N, int num_sms) {
     const size_t tensor = (size_t)BH * N * kHeadDim * 2;
-    return tc_state_workspace_bytes(BH, N, num_sms) + 2 * (size_t)BH * kStateBytesB +
-           2 * tensor + (size_t)BH * N * sizeof(float) + 1024;
+    return tc_state_workspace_bytes(BH, N, num_sms) + 2 * (size_t)BH * kStateBytesB + tensor +
+           (size_t)BH * N * sizeof(float) + 1024;
 }
 
 cudaError_t launch_backward_bf16(const void* q, const void* k, const void* v, const void* g,
@@ -433,18 +369,13 @@ cudaError_t launch_backward_bf16(const void* q, const void* k, const void* v, co
                                  int H, int N, const RopeView* rope, float eps, float* workspace,
                                  int num_sms, unsigned* status, cudaStream_t stream) {
     const int BH = B * H;
-    const long long rows = (long long)BH * N;
-    const size_t tensor = (size_t)rows * kHeadDim * 2;
-    // workspace: the state kernel's, the two states, two [rows][128] bf16
-    // tensors (X: S a, then dS v; A: a), then dden
+    const size_t tensor = (size_t)BH * N * kHeadDim * 2;
+    // workspace: the state kernel's, the two states, a ([rows][128] bf16), then dden
     uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
     uint8_t* S = ws + tc_state_workspace_bytes(BH, N, num_sms);
     uint8_t* dS = S + (size_t)BH * kStateBytesB;
-    uint8_t* X = dS + (size_t)BH * kStateBytesB;
-    uint8_t* A = X + tensor;
+    uint8_t* A = dS + (size_t)BH * kStateBytesB;
     float* dden = reinterpret_cast<float*>(A + tensor);
-    const unsigned blocks = (unsigned)((rows + kRowsPerBlock - 1) / kRowsPerBlock);
-    const RopeView rv = rope ? *rope : RopeView{};
     cudaError_t e;
     if ((e = launch_tc_state(k, v, S, B, H, N, rope, ws, status, num_sms, stream)) != cudaSuccess)
         return e;
@@ -455,26 +386,13 @@ cudaError_t launch_backward_bf16(const void* q, const void* k, const void* v, co
     if ((e = launch_tc_state(q, A, dS, B, H, N, rope, ws, status, num_sms, stream, dden)) !=
         cudaSuccess)
         return e;
-    if ((e = launch_tc_apply(A, A, S, X, B, H, N, nullptr, eps, status, num_sms, stream,
-                             kApplyRawMN)) != cudaSuccess)
+    // dq = [q > 0] (R^T (S a) + dden z), dk = [k > 0] (R^T (dS v) + dz)
+    if ((e = launch_tc_apply(A, q, S, dq, B, H, N, rope, eps, status, num_sms, stream,
+                             kApplyGrad, nullptr, nullptr, dden)) != cudaSuccess)
         return e;
-    if (rope)
-        bwd_grad_kernel<true><<<blocks, 256, 0, stream>>>((const uint4*)q, (const uint4*)X, dden,
-                                                          S, N, rows, rv, (uint4*)dq);
-    else
-        bwd_grad_kernel<false><<<blocks, 256, 0, stream>>>((const uint4*)q, (const uint4*)X, dden,
-                                                           S, N, rows, rv, (uint4*)dq);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = launch_tc_apply(v, v, dS, X, B, H, N, nullptr, eps, status, num_sms, stream,
-                             kApplyRawMN)) != cudaSuccess)
+    if ((e = launch_tc_apply(v, k, dS, dk, B, H, N, rope, eps, status, num_sms, stream,
+                             kApplyGrad)) != cudaSuccess)
         return e;
-    if (rope)
-        bwd_grad_kernel<true><<<blocks, 256, 0, stream>>>((const uint4*)k, (const uint4*)X,
-                                                          nullptr, dS, N, rows, rv, (uint4*)dk);
-    else
-        bwd_grad_kernel<false><<<blocks, 256, 0, stream>>>((const uint4*)k, (const uint4*)X,
-                                                           nullptr, dS, N, rows, rv, (uint4*)dk);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     return launch_tc_apply(k, k, dS, dv, B, H, N, rope, eps, status, num_sms, stream, kApplyRaw);
 }
 

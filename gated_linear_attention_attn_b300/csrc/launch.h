@@ -27,9 +27,9 @@ cudaError_t launch_simt_state_partials(const float* k, const float* v, int B, in
                                        const RopeView* rope, float* partial, int C,
                                        unsigned* status, cudaStream_t stream);
 
-// Backward (backward.cu): dq, dk, dv, dg of L = sum(dout * o).  bf16: nine
-// launches on the tensor-core state and apply kernels plus three elementwise
-// kernels, workspace backward_bf16_workspace_bytes(BH, N, num_sms).  fp32:
+// Backward (backward.cu): dq, dk, dv, dg of L = sum(dout * o).  bf16: six
+// launches of the tensor-core state and apply kernels, workspace
+// backward_bf16_workspace_bytes(BH, N, num_sms).  fp32:
 // three launches over C chunks per head, workspace backward_workspace_bytes(BH, C).
 size_t backward_workspace_bytes(int BH, int C);
 size_t backward_bf16_workspace_bytes(int BH, int N, int num_sms);
@@ -93,11 +93,14 @@ cudaError_t launch_tc_block_causal(const void* q, const void* k, const void* v, 
 cudaError_t launch_tc_state(const void* k, const void* v, void* state, int B, int H, int N,
                             const RopeView* rope, void* workspace, unsigned* status, int num_sms,
                             cudaStream_t stream, const float* zweight = nullptr);
-// mode: 0 the gated apply; 1 out = (R phi(q))^T S; 2 out = S q (q as it is, g unread);
-// 3 the backward's gate terms: with num = (R phi(q))^T S, den = phi(q) . z + eps and
-// s = sigmoid(g), out = a = dout s / den, dg = dout num s (1 - s) / den and
-// dden = -(a . num) / den per row ([B*H][N] fp32).
-constexpr int kApplyGate = 0, kApplyRaw = 1, kApplyRawMN = 2, kApplyTerms = 3;
+// mode: 0 the gated apply; 1 out = (R phi(q))^T S; 2 the backward's gate terms:
+// with num = (R phi(q))^T S, den = phi(q) . z + eps and s = sigmoid(g), out = a =
+// dout s / den, dg = dout num s (1 - s) / den and dden = -(a . num) / den per row
+// ([B*H][N] fp32); 3 the masked gradient: out = [g > 0] (R^T (S q) + w z) with q
+// as it is, g the tensor whose feature map is differentiated, z the state's, w =
+// dden per row (1 when dden is null) and R the token's rotation (none without a
+// table).
+constexpr int kApplyGate = 0, kApplyRaw = 1, kApplyTerms = 2, kApplyGrad = 3;
 cudaError_t launch_tc_apply(const void* q, const void* g, const void* state, void* out, int B,
                             int H, int N, const RopeView* rope, float eps, unsigned* status,
                             int num_sms, cudaStream_t stream, int mode = kApplyGate,

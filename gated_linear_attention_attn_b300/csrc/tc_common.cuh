@@ -61,19 +61,21 @@ constexpr int kApXThreads = 32 * kApXWarps;
 constexpr int kApThreads = 32 * (3 + kApXWarps + kApEWarps);   // + the G producer warp
 constexpr int kApORows = 32;                      // rows of o one epilogue warp stores
 constexpr int kApTmemCols = 256;
-// tc_apply_kernel modes: the gated apply, and for the backward two raw
-// products and the gate terms
-constexpr int kApGate = 0, kApRaw = 1, kApRawMN = 2, kApTerms = 3;
-static_assert(kApGate == kApplyGate && kApRaw == kApplyRaw && kApRawMN == kApplyRawMN &&
-                  kApTerms == kApplyTerms,
+// tc_apply_kernel modes: the gated apply, and for the backward the raw
+// product, the gate terms and the masked gradient
+constexpr int kApGate = 0, kApRaw = 1, kApTerms = 2, kApGrad = 3;
+static_assert(kApGate == kApplyGate && kApRaw == kApplyRaw && kApTerms == kApplyTerms &&
+                  kApGrad == kApplyGrad,
               "apply modes of the launcher");
 
 // Ring geometry of the apply kernel per mode: Q stages, G stages, the bytes
 // of a G stage and the den slots.  The gate terms stage g and dout tiles
-// together, in two stages of each ring.
+// together, in two stages of each ring.  The masked gradient holds a Q tile
+// only from its load to its MMA (two stages), and gives the third stage's
+// room to the RoPE rows on their way to TMEM.
 template <int MODE>
 struct ApGeo {
-    static constexpr int kQS = MODE == kApTerms ? 2 : kApQStages;
+    static constexpr int kQS = MODE == kApTerms || MODE == kApGrad ? 2 : kApQStages;
     static constexpr int kGS = MODE == kApTerms ? 2 : kApGStages;
     static constexpr int kGT = MODE == kApTerms ? 2 * kApTile : kApTile;
     static constexpr int kDS = MODE == kApTerms ? 2 : kApDSlots;   // den slots
@@ -191,6 +193,42 @@ __device__ __forceinline__ void terms_chunk(uint4 g8, uint4 d8, const uint32_t* 
     g8o = make_uint4(ow[0], ow[1], ow[2], ow[3]);
 }
 
+// Eight elements of a masked gradient row: out = [x > 0] (R^T y + w z), with
+// x8 the bf16 input whose feature map is differentiated, y the eight fp32
+// products of the tensor cores, cs4 the four (cos, sin) fp16 pairs of the
+// chunk (R^T turns each pair back: (y0 c + y1 s, -y0 s + y1 c)) when ROPE,
+// w the row's weight and z8 the eight matching entries of z.
+template <bool ROPE>
+__device__ __forceinline__ uint4 grad_chunk(uint4 x8, const uint32_t* y, uint4 cs4, float w,
+                                            const float* z8) {
+    float f[8];
+    unpack8(x8, f);
+    float yv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) yv[j] = __uint_as_float(y[j]);
+    if (ROPE) {
+        float2 cs[4];
+        unpack_cs(cs4, cs);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float a = yv[2 * i], b = yv[2 * i + 1];
+            yv[2 * i] = a * cs[i].x + b * cs[i].y;
+            yv[2 * i + 1] = b * cs[i].x - a * cs[i].y;
+        }
+    }
+    const float4 za = *reinterpret_cast<const float4*>(z8);
+    const float4 zb = *reinterpret_cast<const float4*>(z8 + 4);
+    const float zv[8] = {za.x, za.y, za.z, za.w, zb.x, zb.y, zb.z, zb.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float a = f[2 * i] > 0.f ? fmaf(w, zv[2 * i], yv[2 * i]) : 0.f;
+        const float b = f[2 * i + 1] > 0.f ? fmaf(w, zv[2 * i + 1], yv[2 * i + 1]) : 0.f;
+        o[i] = f2_to_bf2(a, b);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // warp_wait for phases completed by arrivals from other CTAs of the cluster.
 __device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity,
                                                   volatile int* abort, unsigned* status) {
@@ -284,6 +322,22 @@ inline bool make_rope_map(CUtensorMap* m, const uint32_t* base, int N, int rows)
     cuuint32_t es[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(base), dims, strides,
               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The per-token RoPE rows again, in boxes of 32 words (128 bytes: half a
+// token's pairs) x 32 tokens with 128-byte swizzle: chunk c of box row r lands
+// at r * 128 + ((c ^ (r & 7)) << 4).  Rows past N read as zero.
+inline bool make_rope_box_map(CUtensorMap* m, const uint32_t* base, int N) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)kPairs, (cuuint64_t)N};
+    cuuint64_t strides[1] = {(cuuint64_t)kPairs * 4};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(base), dims, strides,
+              box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -93,7 +93,8 @@ struct ApplyParams {
     float eps;
     unsigned* status;
     int nb, tok0;                   // as in StateParams
-    float* dden;                    // kApTerms: -(a . num) / den per row, [heads][N]
+    float* dden;                    // [heads][N]: kApTerms writes -(a . num) / den,
+                                    // kApGrad reads the row weight (null: 1)
 };
 
 // =================================================================== state ==
@@ -644,20 +645,32 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 
 // =================================================================== apply ==
 
-// MODE kApGate is the layer's apply.  The backward reuses the kernel for plain
-// products of a [N][128] bf16 tensor x with a head's state buffer, which
-// holds some 128 x 128 matrix S as S^T rows (g is not read, nothing is gated):
-//   kApRaw    out_i = (R_i phi(x_i))^T S, the forward's numerator;
-//   kApRawMN  out_i[m] = sum_n x_i[n] S[m][n] = S x_i, x taken as it is (no
-//             feature map, no rotation) and the buffer read as an MN-major
-//             B operand;
-// and for the gate terms of the backward:
+// MODE kApGate is the layer's apply.  The backward reuses the kernel with a
+// head's state buffer that holds some 128 x 128 matrix S as S^T rows:
+//   kApRaw    out_i = (R_i phi(x_i))^T S, the forward's numerator (g is not
+//             read, nothing is gated);
+// for the gate terms of the backward:
 //   kApTerms  with num_i = (R_i phi(q_i))^T S, den_i and s_i = sigmoid(g_i):
 //             out (a) = dout s / den, dg = dout num s (1 - s) / den (both bf16,
 //             written over dout and g in the G slot and stored with TMA
 //             through tm_o32 and tm_dg) and dden_i = -(a_i . num_i) / den_i
 //             (fp32, p.dden); g and dout stream in together through the G
-//             ring (tm_g, tm_d).
+//             ring (tm_g, tm_d);
+// and for the masked gradients dq and dk:
+//   kApGrad   out_i = [g_i > 0] (R_i^T (S x_i) + w_i z), with (S x_i)[m] =
+//             sum_n x_i[n] S[m][n]: x is taken as it is (no feature map, no
+//             rotation) and the buffer is read as an MN-major B operand; g is
+//             the tensor whose feature map is differentiated (q or k, streamed
+//             through the G ring in place of the gate), z the state's, w_i =
+//             p.dden[row] (1 when null) and R_i the token's rotation (ROPE).
+//             The epilogue reads z from the state buffer, which it releases
+//             after the head's last tile.  The transform warps have no tile to
+//             transform: with ROPE they move the RoPE rows of the tiles into
+//             TMEM (columns 256 + 64 ds, one lane per token), up to DS tiles
+//             ahead of the epilogue, which reads them beside the product.
+//             Each warp takes 32 tokens x 32 words per tile by one TMA load
+//             (tm_d is then the table's box map) into its 4 KB of shared
+//             memory, and reads them back one token row per lane.
 template <bool ROPE, int MODE>
 __global__ void __launch_bounds__(kApThreads, 1)
 tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_g,
@@ -665,14 +678,26 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const __grid_constant__ CUtensorMap tm_dg, ApplyParams p) {
     constexpr int QS = ApGeo<MODE>::kQS, GS = ApGeo<MODE>::kGS, GT = ApGeo<MODE>::kGT;
     constexpr int DS = ApGeo<MODE>::kDS;
+    // kApGrad: the Q tile is an operand as it is (no feature map, no
+    // rotation), the state an MN-major B operand; the den slots carry the
+    // RoPE rows in TMEM, or nothing without RoPE
+    constexpr bool kGrad = MODE == kApGrad;
+    constexpr bool kTmemRope = kGrad && ROPE;
+    constexpr bool kSlots = !kGrad || ROPE;
+    constexpr uint32_t kCols = kTmemRope ? 512 : kApTmemCols;
+    constexpr uint32_t kRopeCol = 256;           // kTmemRope: [DS][64] columns of RoPE words
+    static_assert(!kTmemRope || kRopeCol + DS * 64 <= kCols, "TMEM columns");
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t* qring = smem;                                      // [QS][32 KB]
     uint8_t* gring = smem + QS * kApTile;                       // [GS][GT]
-    uint8_t* sbuf = gring + GS * GT;                            // S^T bf16 (B operand), then z
+    uint8_t* rscr = gring + GS * GT;                            // kTmemRope: [8 warps][4 KB]
+    constexpr int kRScr = kTmemRope ? kApXWarps * 4096 : 0;
+    uint8_t* sbuf = rscr + kRScr;                               // S^T bf16 (B operand), then z
     float* zs = reinterpret_cast<float*>(sbuf + kStateSBytes);  // [128]
-    float* dens = zs + kHeadDim;                // [DS][128] phi(q) . z + eps
+    float* dens = zs + kHeadDim;                // [DS][128] phi(q) . z + eps (not kApGrad)
+    constexpr int kDens = MODE == kApGrad ? 0 : DS * kApTok;
     // kApTerms: a . num over the second column half of each row, two tiles deep
-    float* dpart = dens + DS * kApTok;          // [2][128]
+    float* dpart = dens + kDens;                // [2][128]
     constexpr int kDPart = MODE == kApTerms ? 2 * kApTok : 0;
     uint64_t* qfull = reinterpret_cast<uint64_t*>(dpart + kDPart);
     uint64_t* qready = qfull + QS;       // Q tile transformed (MMA may read it)
@@ -687,7 +712,8 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint64_t* sfree = sready + 1;
     uint64_t* mma_done = sfree + 1;
     uint64_t* pairdone = mma_done + 1;           // kApTerms: [2] the tile's dpart written
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pairdone + (MODE == kApTerms ? 2 : 0));
+    uint64_t* rfull = pairdone + (MODE == kApTerms ? 2 : 0);   // kTmemRope: [8] a warp's rows landed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rfull + (kTmemRope ? kApXWarps : 0));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -700,6 +726,8 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_init(&pairdone[0], kApEWarps);
             mbar_init(&pairdone[1], kApEWarps);
         }
+        if (kTmemRope)
+            for (int w = 0; w < kApXWarps; ++w) mbar_init(&rfull[w], 1);
         for (int s = 0; s < QS; ++s) {
             mbar_init(&qfull[s], 1);
             mbar_init(&qready[s], kApXWarps);
@@ -718,7 +746,10 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_init(&accempty[a], kApEWarps);
         }
         mbar_init(sready, 1);
-        mbar_init(sfree, 1 + kApXWarps);
+        // the state is free once its MMAs are done and every warp that reads
+        // z is done with it: the transform warps (a copy in registers), or
+        // with kApGrad the epilogue's (after the head's last tile)
+        mbar_init(sfree, 1 + (kGrad ? kApEWarps : kApXWarps));
         mbar_init(mma_done, 1);
         *abort_flag = (smem0 & 1023u) ? 1 : 0;
         if (smem0 & 1023u) raise_status(p.status, kStatusLayout);
@@ -734,9 +765,10 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             prefetch_tmap(&tm_d);
             prefetch_tmap(&tm_dg);
         }
+        if (kTmemRope) prefetch_tmap(&tm_d);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, kApTmemCols);
+        tmem_alloc(tmem_slot, kCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -829,7 +861,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16(128, 128, false, MODE == kApRawMN);
+            constexpr uint32_t idesc = idesc_bf16(128, 128, false, kGrad);
             const uint32_t sb = smem_u32(sbuf);
             long long it = 0;
             int heads = 0, cur_h = -1;
@@ -847,8 +879,9 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const uint32_t round = (uint32_t)(it / QS);
                 const int a = (int)(it & 1);
                 const uint32_t around = (uint32_t)(it >> 1);
+                // (kApGrad: the tile is multiplied as it landed)
                 ok = mbar_wait(&accempty[a], (around & 1) ^ 1, abort_flag, p.status) &&
-                     mbar_wait(&qready[s], round & 1, abort_flag, p.status) &&
+                     (kGrad || mbar_wait(&qready[s], round & 1, abort_flag, p.status)) &&
                      mbar_wait(&qfull[s], round & 1, abort_flag, p.status);
                 if (!ok) break;
                 tc_fence_after();
@@ -860,7 +893,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     const uint64_t ad = smem_desc_sw128(qb + off, 16, 1024);
                     // K-major: the buffer's rows are N; MN-major: its rows are K
                     // (16 rows = 2048 bytes a step, the two N halves kStateHalf apart)
-                    const uint64_t bd = MODE == kApRawMN
+                    const uint64_t bd = kGrad
                                             ? smem_desc_sw128(sb + ks * 2048, kStateHalf, 1024)
                                             : smem_desc_sw128(sb + off, 16, 1024);
                     mma_bf16(tmem + (uint32_t)a * 128, ad, bd, idesc, ks > 0 ? 1u : 0u);
@@ -870,6 +903,66 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             mma_commit(mma_done);
             mbar_wait_drain(mma_done, 0);
+        }
+    } else if (kGrad && warp < 2 + kApXWarps) {
+        // ------------------------------------------------ kApGrad: RoPE rows to TMEM
+        if constexpr (kTmemRope) {
+            // this warp's 32 tokens (its TMEM lanes) x 32 words of their RoPE
+            // rows: TMA to its 4 KB, then one token row per lane to TMEM
+            const int xw = warp - 2, tquad = warp & 3, part = xw >> 2;
+            uint8_t* scr = rscr + xw * 4096;
+            const uint32_t scr_a = smem_u32(scr);
+            uint64_t* bar = &rfull[xw];
+            const uint64_t keep = policy_evict_last();
+            auto issue = [&](long long u) {
+                if (lane == 0) {
+                    const int h = (int)(u / p.Tq), tile = (int)(u % p.Tq);
+                    const int row0 = (p.nb == 1 ? 0 : (h % p.nb) * p.N) + p.tok0 + tile * kApTok +
+                                     32 * tquad;
+                    mbar_arrive_expect_tx(bar, 4096);
+                    tma_load_2d(scr, &tm_d, bar, 32 * part, row0, keep);
+                }
+            };
+            bool ok = !*abort_flag;
+            long long issued = 0;
+            if (ok && u0 < u1) {
+                issue(u0);
+                issued = 1;
+            }
+            long long it = 0;
+            for (long long u = u0; ok && u < u1; ++u, ++it) {
+                if (!(ok = warp_wait(bar, (uint32_t)(it & 1), abort_flag, p.status))) break;
+                uint32_t wv[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 x = lds128(scr_a + lane * 128 + ((c ^ (lane & 7)) << 4));
+                    wv[4 * c] = x.x;
+                    wv[4 * c + 1] = x.y;
+                    wv[4 * c + 2] = x.z;
+                    wv[4 * c + 3] = x.w;
+                }
+                // every lane's reads are done before the next tile's copy lands there
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (u + 1 < u1) {
+                    issue(u + 1);
+                    ++issued;
+                }
+                const int ds = (int)(it % DS);
+                const uint32_t dround = (uint32_t)(it / DS);
+                // the epilogue has read the slot's previous tile
+                if (dround > 0 && !(ok = warp_wait(&dfree[ds], (dround - 1) & 1, abort_flag, p.status)))
+                    break;
+                tmem_st32(tmem + ((uint32_t)(32 * tquad) << 16) + kRopeCol + (uint32_t)ds * 64 +
+                              32 * part,
+                          wv);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&dready[ds]);
+            }
+            // no copy of ours may still be landing when the CTA exits
+            if (lane == 0 && issued > it) mbar_wait_drain(bar, (uint32_t)((issued - 1) & 1));
         }
     } else if (warp < 2 + kApXWarps) {
         // ------------------------------------------------ transform: phi, RoPE, den
@@ -919,8 +1012,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (dround > 0 && !(ok = warp_wait(&dfree[ds], (dround - 1) & 1, abort_flag, p.status)))
                 break;
             const uint32_t qb = smem0 + s * kApTile;
-            // (kApRawMN multiplies the tile as it is: nothing to transform)
-            if constexpr (MODE != kApRawMN) {
+            {
             // two batches of four rows; in each, all loads first
 #pragma unroll
             for (int b4 = 0; b4 < kApRowsPerThread; b4 += 4) {
@@ -993,6 +1085,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int quad = warp & 3, hf = ew >> 2;     // TMEM lanes 32*quad.., columns 64*hf..
         const int r = 32 * quad + lane;              // TMEM lane = token row of the tile
         long long it = 0;
+        int eheads = 0, ecur_h = -1;                 // kApGrad: heads begun
         bool ok = !*abort_flag;
         for (long long u = u0; ok && u < u1; ++u, ++it) {
             const int h = (int)(u / p.Tq), tile = (int)(u % p.Tq);
@@ -1001,16 +1094,35 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const int ds = (int)(it % DS);
             const int a = (int)(it & 1);
             const uint32_t around = (uint32_t)(it >> 1);
+            // kApGrad: the row's weight, loaded before the waits (rows past N
+            // are not stored: any row serves)
+            float w = 1.f;
+            if constexpr (MODE == kApGrad) {
+                if (p.dden) w = p.dden[(size_t)h * p.N + min(tile * kApTok + r, p.N - 1)];
+            }
             ok = warp_wait(&accfull[a], around & 1, abort_flag, p.status) &&
-                 warp_wait(&dready[ds], (uint32_t)(it / DS) & 1, abort_flag, p.status) &&
+                 (!kSlots || warp_wait(&dready[ds], (uint32_t)(it / DS) & 1, abort_flag, p.status)) &&
                  warp_wait(&gfull[gs], ground & 1, abort_flag, p.status);
             if (!ok) break;
             tc_fence_after();
-            const float den = dens[ds * kApTok + r];
+            const float den = kGrad ? 1.f : dens[ds * kApTok + r];   // (kApGrad: none)
             const float inv_den = 1.f / den;
             float part = 0.f;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&dfree[ds]);
+            // (with the RoPE rows in the slot's TMEM columns, the slot is
+            // freed after the chunks)
+            if constexpr (!kGrad) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&dfree[ds]);
+            }
+            if constexpr (MODE == kApGrad) {
+                if (h != ecur_h) {
+                    // the head's state has landed (sready) and stays until this
+                    // warp, among others, is done with its z (sfree)
+                    if (!(ok = warp_wait(sready, eheads & 1, abort_flag, p.status))) break;
+                    ++eheads;
+                    ecur_h = h;
+                }
+            }
             const uint32_t gb = smem0 + QS * kApTile + gs * GT;
 #pragma unroll 1
             for (int ch = 0; ch < 2; ++ch) {
@@ -1019,7 +1131,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                 for (int sub = 0; sub < 4; ++sub) {
                     addr[sub] = gb + sw128_off(r, hf * 8 + ch * 4 + sub, kApHalf);
-                    if (MODE == kApGate || MODE == kApTerms) gv[sub] = lds128(addr[sub]);
+                    if (MODE != kApRaw) gv[sub] = lds128(addr[sub]);
                 }
                 uint4 dv[4];                          // kApTerms: dout, in the stage's second tile
                 if constexpr (MODE == kApTerms) {
@@ -1030,6 +1142,11 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tmem_ld32(tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)a * 128 + hf * 64 +
                               ch * 32,
                           v);
+                uint32_t csw[16];                     // kTmemRope: the chunk's 16 pairs
+                if constexpr (kTmemRope)
+                    tmem_ld16(tmem + ((uint32_t)(32 * quad) << 16) + kRopeCol + (uint32_t)ds * 64 +
+                                  32 * hf + 16 * ch,
+                              csw);
                 tmem_ld_wait();
                 if constexpr (MODE == kApTerms) {
                     // a over dout, dg over g; part collects a . num of the row
@@ -1042,6 +1159,16 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 } else if constexpr (MODE == kApGate) {
 #pragma unroll
                     for (int sub = 0; sub < 4; ++sub) gv[sub] = gate_chunk(gv[sub], v + 8 * sub, den);
+                } else if constexpr (MODE == kApGrad) {
+                    const float* zw = zs + 64 * hf + ch * 32;
+#pragma unroll
+                    for (int sub = 0; sub < 4; ++sub) {
+                        uint4 cs = {};
+                        if constexpr (kTmemRope)
+                            cs = make_uint4(csw[4 * sub], csw[4 * sub + 1], csw[4 * sub + 2],
+                                            csw[4 * sub + 3]);
+                        gv[sub] = grad_chunk<ROPE>(gv[sub], v + 8 * sub, cs, w, zw + 8 * sub);
+                    }
                 } else {
 #pragma unroll
                     for (int sub = 0; sub < 4; ++sub) {
@@ -1058,6 +1185,17 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             tc_fence_before();
             fence_proxy_async_smem();
+            if constexpr (kTmemRope) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&dfree[ds]);
+            }
+            if constexpr (MODE == kApGrad) {
+                // the head's last tile here: its state may be replaced
+                if (u + 1 == u1 || (int)((u + 1) / p.Tq) != h) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sfree);
+                }
+            }
             if constexpr (MODE == kApTerms) {
                 // dden of the row from the two column halves (the warp of the
                 // other half has the same rows)
@@ -1099,7 +1237,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const int s = (int)(it % GS);
                 const uint32_t round = (uint32_t)(it / GS);
                 if (!mbar_wait(&gempty[s], (round & 1) ^ 1, abort_flag, p.status)) break;
-                if constexpr (MODE == kApRaw || MODE == kApRawMN) {
+                if constexpr (MODE == kApRaw) {
                     mbar_arrive(&gfull[s]);         // the slot only stages the output
                     continue;
                 }
@@ -1124,7 +1262,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     tc_fence_after();
     if (warp == 1) {
         __syncwarp();
-        tmem_dealloc(tmem, kApTmemCols);
+        tmem_dealloc(tmem, kCols);
     }
 }
 
@@ -1808,9 +1946,14 @@ constexpr size_t st_smem() {
 template <bool ROPE, int MODE = kApGate>
 constexpr size_t ap_smem() {
     using G = ApGeo<MODE>;
-    return (size_t)G::kQS * kApTile + (size_t)G::kGS * G::kGT + kStateBytes +
-           (G::kDS + (MODE == kApTerms ? 2 : 0)) * kApTok * sizeof(float) +
-           (3 * G::kQS + 2 * G::kGS + 2 * G::kDS + 7 + (MODE == kApTerms ? 2 : 0)) * 8 + 16;
+    constexpr bool kTmemRope = MODE == kApGrad && ROPE;
+    return (size_t)G::kQS * kApTile + (size_t)G::kGS * G::kGT + (kTmemRope ? kApXWarps * 4096 : 0) +
+           kStateBytes +
+           ((MODE == kApGrad ? 0 : G::kDS) + (MODE == kApTerms ? 2 : 0)) * kApTok * sizeof(float) +
+           (3 * G::kQS + 2 * G::kGS + 2 * G::kDS + 7 + (MODE == kApTerms ? 2 : 0) +
+            (kTmemRope ? kApXWarps : 0)) *
+               8 +
+           16;
 }
 // fused: the ring, the state, the denominators, then 3*stages + 7 phase-1 and
 // cluster mbarriers, the apply kernel's 3*Q + 2*G + 2*den + 5 and two words.
@@ -1825,6 +1968,7 @@ static_assert(fu_smem<true>() <= 232448 && fu_smem<false>() <= 232448, "fused ke
 static_assert(st_smem<true>() <= 232448 && st_smem<false>() <= 232448, "state kernel smem");
 static_assert(ap_smem<true>() <= 232448 && ap_smem<false>() <= 232448, "apply kernel smem");
 static_assert(ap_smem<true, kApTerms>() <= 232448, "apply kernel smem, gate terms");
+static_assert(ap_smem<true, kApGrad>() <= 232448, "apply kernel smem, masked gradient");
 
 struct Plan {
     int Tk, Tq;
@@ -1866,12 +2010,14 @@ cudaError_t configure(int dev) {
     if ((e = set_smem(tc_apply_kernel<true, kApGate>, ap_smem<true>())) != cudaSuccess) return e;
     if ((e = set_smem(tc_apply_kernel<false, kApRaw>, ap_smem<false>())) != cudaSuccess) return e;
     if ((e = set_smem(tc_apply_kernel<true, kApRaw>, ap_smem<true>())) != cudaSuccess) return e;
-    if ((e = set_smem(tc_apply_kernel<false, kApRawMN>, ap_smem<false>())) != cudaSuccess)
-        return e;
     if ((e = set_smem(tc_apply_kernel<false, kApTerms>, ap_smem<false, kApTerms>())) !=
         cudaSuccess)
         return e;
     if ((e = set_smem(tc_apply_kernel<true, kApTerms>, ap_smem<true, kApTerms>())) != cudaSuccess)
+        return e;
+    if ((e = set_smem(tc_apply_kernel<false, kApGrad>, ap_smem<false, kApGrad>())) != cudaSuccess)
+        return e;
+    if ((e = set_smem(tc_apply_kernel<true, kApGrad>, ap_smem<true, kApGrad>())) != cudaSuccess)
         return e;
     if ((e = set_smem(tc_fused_kernel<false>, fu_smem<false>())) != cudaSuccess) return e;
     if ((e = set_smem(tc_fused_kernel<true>, fu_smem<true>())) != cudaSuccess) return e;
@@ -1935,6 +2081,9 @@ cudaError_t launch_apply(const void* q, const void* g, const uint8_t* state, voi
     if (mode == kApTerms &&
         (!make_map(&md, dout, N, BH, kApTok) || !make_map(&mdg, dg, N, BH, kApORows)))
         return cudaErrorInvalidValue;
+    // the masked gradient with RoPE: md is the table's box map
+    if (mode == kApGrad && rope && !make_rope_box_map(&md, rope->tok, rope->need))
+        return cudaErrorInvalidValue;
     ApplyParams ap{};
     ap.N = N;
     ap.Tq = pl.Tq;
@@ -1949,9 +2098,10 @@ cudaError_t launch_apply(const void* q, const void* g, const uint8_t* state, voi
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(pl.ap.G);
     cfg.blockDim = dim3(kApThreads);
-    cfg.dynamicSmemBytes = mode == kApTerms ? (rope ? ap_smem<true, kApTerms>()
-                                                    : ap_smem<false, kApTerms>())
-                                            : (rope ? ap_smem<true>() : ap_smem<false>());
+    cfg.dynamicSmemBytes =
+        mode == kApTerms  ? (rope ? ap_smem<true, kApTerms>() : ap_smem<false, kApTerms>())
+        : mode == kApGrad ? (rope ? ap_smem<true, kApGrad>() : ap_smem<false, kApGrad>())
+                          : (rope ? ap_smem<true>() : ap_smem<false>());
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1960,8 +2110,6 @@ cudaError_t launch_apply(const void* q, const void* g, const uint8_t* state, voi
     // complete before this grid starts, whatever wrote them.
     cfg.attrs = attr;
     cfg.numAttrs = after_state ? 1 : 0;
-    if (mode == kApRawMN)
-        return cudaLaunchKernelEx(&cfg, tc_apply_kernel<false, kApRawMN>, mq, mg, mo, md, mdg, ap);
     if (mode == kApRaw) {
         if (rope)
             return cudaLaunchKernelEx(&cfg, tc_apply_kernel<true, kApRaw>, mq, mg, mo, md, mdg, ap);
@@ -1971,6 +2119,11 @@ cudaError_t launch_apply(const void* q, const void* g, const uint8_t* state, voi
         if (rope)
             return cudaLaunchKernelEx(&cfg, tc_apply_kernel<true, kApTerms>, mq, mg, mo, md, mdg, ap);
         return cudaLaunchKernelEx(&cfg, tc_apply_kernel<false, kApTerms>, mq, mg, mo, md, mdg, ap);
+    }
+    if (mode == kApGrad) {
+        if (rope)
+            return cudaLaunchKernelEx(&cfg, tc_apply_kernel<true, kApGrad>, mq, mg, mo, md, mdg, ap);
+        return cudaLaunchKernelEx(&cfg, tc_apply_kernel<false, kApGrad>, mq, mg, mo, md, mdg, ap);
     }
     if (rope)
         return cudaLaunchKernelEx(&cfg, tc_apply_kernel<true, kApGate>, mq, mg, mo, md, mdg, ap);

@@ -55,6 +55,8 @@ CASES = [
     (1, 2, (3, 10, 10), torch.bfloat16, True),
     (2, 4, (2, 9, 17), torch.bfloat16, True),
     (3, 1, (1, 1, 1000), torch.bfloat16, False),
+    # 240 query tiles: more than one per CTA, with heads changing inside a CTA
+    (2, 40, (1, 4, 75), torch.bfloat16, True),
     (1, 2, (4, 8, 8), torch.float32, True),
     (2, 1, (1, 1, 300), torch.float32, False),
 ]
