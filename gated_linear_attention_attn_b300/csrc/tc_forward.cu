@@ -684,6 +684,11 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     constexpr bool kGrad = MODE == kApGrad;
     constexpr bool kTmemRope = kGrad && ROPE;
     constexpr bool kSlots = !kGrad || ROPE;
+    // The G producer stores the outputs the epilogue staged in a G slot and
+    // refills the slot as soon as the stores have read it (otherwise each
+    // epilogue warp stores its own part and frees the previous tile's slot).
+    constexpr bool kPStore = MODE == kApTerms;
+    static_assert(kPStore || MODE != kApTerms, "the gate terms' two outputs go out from the producer");
     constexpr uint32_t kCols = kTmemRope ? 512 : kApTmemCols;
     constexpr uint32_t kRopeCol = 256;           // kTmemRope: [DS][64] columns of RoPE words
     static_assert(!kTmemRope || kRopeCol + DS * 64 <= kCols, "TMEM columns");
@@ -703,7 +708,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint64_t* qready = qfull + QS;       // Q tile transformed (MMA may read it)
     uint64_t* qempty = qready + QS;      // Q tile read by the MMA
     uint64_t* gfull = qempty + QS;
-    uint64_t* gempty = gfull + GS;       // o stored from the G slot
+    uint64_t* gempty = gfull + GS;       // o stored from the G slot (kPStore: staged in it)
     uint64_t* dready = gempty + GS;      // [DS] den of a tile written
     uint64_t* dfree = dready + DS;        // [DS] den of a tile read
     uint64_t* accfull = dfree + DS;       // [2]
@@ -1213,30 +1218,61 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&accempty[a]);
-                // this warp's rows 32*quad.. of column half hf, 4 KB of the tile
-                tma_store_3d(&tm_o32, gring + gs * GT + hf * kApHalf + quad * kApORows * 128 +
-                                          (MODE == kApTerms ? kApTile : 0),
-                             64 * hf, tile * kApTok + quad * kApORows, h);
-                if (MODE == kApTerms)               // dg, from the g half of the slot
-                    tma_store_3d(&tm_dg, gring + gs * GT + hf * kApHalf + quad * kApORows * 128,
+                if constexpr (kPStore) {
+                    mbar_arrive(&gempty[gs]);       // this warp's part is staged
+                } else {
+                    // this warp's rows 32*quad.. of column half hf, 4 KB of the tile
+                    tma_store_3d(&tm_o32, gring + gs * GT + hf * kApHalf + quad * kApORows * 128,
                                  64 * hf, tile * kApTok + quad * kApORows, h);
-                bulk_commit();
-                // the previous tile's store has read its G slot, which may be refilled
-                bulk_wait_read_one();
-                if (it > 0) mbar_arrive(&gempty[(it - 1) % GS]);
+                    bulk_commit();
+                    // the previous tile's store has read its G slot, which may be refilled
+                    bulk_wait_read_one();
+                    if (it > 0) mbar_arrive(&gempty[(it - 1) % GS]);
+                }
             }
         }
-        if (lane == 0) bulk_wait_all();
+        if (!kPStore && lane == 0) bulk_wait_all();
     } else {
         // ------------------------------------------------ G producer
         if (lane == 0 && !*abort_flag) {
             const uint64_t policy = policy_evict_first();
-            long long it = 0;
+            // kPStore: the outputs of tile j, staged in its slot, go out from here
+            // (kApTerms: a over the dout half, dg over the g half)
+            auto store_tile = [&](long long j) -> bool {
+                const long long uj = u0 + j;
+                const int h = (int)(uj / p.Tq), tile = (int)(uj % p.Tq);
+                const int s = (int)(j % GS);
+                if (!mbar_wait(&gempty[s], (uint32_t)((j / GS) & 1), abort_flag, p.status))
+                    return false;
+                const uint8_t* st = gring + s * GT;
+#pragma unroll 1
+                for (int b = 0; b < 8; ++b) {
+                    const int hf = b >> 2, quad = b & 3;
+                    const uint8_t* box = st + hf * kApHalf + quad * kApORows * 128;
+                    tma_store_3d(&tm_o32, box + (MODE == kApTerms ? kApTile : 0), 64 * hf,
+                                 tile * kApTok + quad * kApORows, h);
+                    if (MODE == kApTerms)
+                        tma_store_3d(&tm_dg, box, 64 * hf, tile * kApTok + quad * kApORows, h);
+                }
+                bulk_commit();
+                return true;
+            };
+            long long it = 0, stored = 0;
+            bool ok = true;
             for (long long u = u0; u < u1; ++u, ++it) {
                 const int h = (int)(u / p.Tq), tile = (int)(u % p.Tq);
                 const int s = (int)(it % GS);
                 const uint32_t round = (uint32_t)(it / GS);
-                if (!mbar_wait(&gempty[s], (round & 1) ^ 1, abort_flag, p.status)) break;
+                if constexpr (kPStore) {
+                    // the slot's previous tile is stored and read out of it
+                    if (it >= GS) {
+                        if (!(ok = store_tile(it - GS))) break;
+                        ++stored;
+                        bulk_wait_read_all();
+                    }
+                } else if (!mbar_wait(&gempty[s], (round & 1) ^ 1, abort_flag, p.status)) {
+                    break;
+                }
                 if constexpr (MODE == kApRaw) {
                     mbar_arrive(&gfull[s]);         // the slot only stages the output
                     continue;
@@ -1250,6 +1286,11 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     tma_load_3d(st + kApTile + kApHalf, &tm_d, &gfull[s], 64, tile * kApTok, h,
                                 policy);
                 }
+            }
+            // the last tiles' outputs; every store is complete before the CTA exits
+            if constexpr (kPStore) {
+                for (; ok && stored < it; ++stored) ok = store_tile(stored);
+                bulk_wait_all();
             }
             const long long first = it > GS ? it - GS : 0;
             for (long long j = first; j < it; ++j)

@@ -223,6 +223,11 @@ __device__ __forceinline__ void bulk_wait_read_one() {
     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
+// Waits until no committed bulk group still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
