@@ -545,9 +545,10 @@ def run_sla(args, rank, world, local):
 
 BWD_METRIC = "linear-attn bwd token-heads/s; HBM GB/s as % of B300 peak"
 BWD_LAUNCHES = 6
-BWD_PLAN = ("backward: state(k, v), apply gate terms(q, g, dout; S), state(q, a; dden), "
-            "apply masked gradient(a; S, q) -> dq, apply masked gradient(v; dS, k) -> dk, "
-            "apply raw(k; dS) -> dv (tcgen05 state/apply kernels)")
+BWD_PLAN = ("backward: state(k, v), apply gate terms(q, g, dout; S) + dS partials, "
+            "apply masked gradient(a; S, q) -> dq + dz partials, dS merge, "
+            "apply masked gradient(v; dS, k) -> dk, apply raw(k; dS) -> dv "
+            "(tcgen05 state/apply kernels)")
 
 
 def oracle_backward_heads(wl, tensors, heads):

@@ -13,10 +13,11 @@
 // apply kernels, the elementwise terms in the apply kernel's epilogue:
 //   1. state(k, v)                      S (bf16, as the forward uses it), z
 //   2. apply, gate terms(q, g, dO; S)   num on the tensor cores; a, dg, dden in
-//                                       the epilogue
-//   3. state(q, a; weights dden)        dS, dz
-//   4. apply, masked gradient(a; S, q)  S a on the tensor cores; dq in the
-//                                       epilogue (mask of q, R^T, + dden z)
+//                                       the epilogue; dS partials from qr and a
+//   3. apply, masked gradient(a; S, q)  S a on the tensor cores; dq in the
+//                                       epilogue (mask of q, R^T, + dden z);
+//                                       dz partials from the q tiles
+//   4. dS merge                         dS (bf16, as S), dz
 //   5. apply, masked gradient(v; dS, k) dS v; dk (mask of k, R^T, + dz)
 //   6. apply, raw(k; dS)                dv = dS^T kr
 // fp32 inputs: fp32 FMA kernels in three launches, each over (chunk of tokens,
@@ -358,10 +359,13 @@ size_t backward_workspace_bytes(int BH, int C) {
     return 2 * (size_t)BH * C * kBPartial * sizeof(float);
 }
 
+static size_t round_up(size_t x) { return (x + 255) & ~size_t(255); }
+
 size_t backward_bf16_workspace_bytes(int BH, int N, int num_sms) {
     const size_t tensor = (size_t)BH * N * kHeadDim * 2;
     return tc_state_workspace_bytes(BH, N, num_sms) + 2 * (size_t)BH * kStateBytesB + tensor +
-           (size_t)BH * N * sizeof(float) + 1024;
+           round_up((size_t)BH * N * sizeof(float)) + tc_apply_partial_bytes(BH, N, num_sms) +
+           tc_apply_zpart_bytes(BH, N, num_sms) + 1024;
 }
 
 cudaError_t launch_backward_bf16(const void* q, const void* k, const void* v, const void* g,
@@ -370,26 +374,32 @@ cudaError_t launch_backward_bf16(const void* q, const void* k, const void* v, co
                                  int num_sms, unsigned* status, cudaStream_t stream) {
     const int BH = B * H;
     const size_t tensor = (size_t)BH * N * kHeadDim * 2;
-    // workspace: the state kernel's, the two states, a ([rows][128] bf16), then dden
+    // workspace: the state kernel's, the two states, a ([rows][128] bf16), dden,
+    // then the partials of dS and of dz
     uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
     uint8_t* S = ws + tc_state_workspace_bytes(BH, N, num_sms);
     uint8_t* dS = S + (size_t)BH * kStateBytesB;
     uint8_t* A = dS + (size_t)BH * kStateBytesB;
     float* dden = reinterpret_cast<float*>(A + tensor);
+    float* dspart = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dden) +
+                                             round_up((size_t)BH * N * sizeof(float)));
+    float* dzpart = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dspart) +
+                                             tc_apply_partial_bytes(BH, N, num_sms));
     cudaError_t e;
     if ((e = launch_tc_state(k, v, S, B, H, N, rope, ws, status, num_sms, stream)) != cudaSuccess)
         return e;
-    // num on the tensor cores, the gate terms in the apply kernel's epilogue: a, dg, dden
+    // num on the tensor cores, the gate terms in the apply kernel's epilogue (a, dg,
+    // dden), and dS = sum qr a^T from the same tiles
     if ((e = launch_tc_apply(q, g, S, A, B, H, N, rope, eps, status, num_sms, stream,
-                             kApplyTerms, dout, dg, dden)) != cudaSuccess)
+                             kApplyTerms, dout, dg, dden, dspart)) != cudaSuccess)
         return e;
-    if ((e = launch_tc_state(q, A, dS, B, H, N, rope, ws, status, num_sms, stream, dden)) !=
-        cudaSuccess)
-        return e;
-    // dq = [q > 0] (R^T (S a) + dden z), dk = [k > 0] (R^T (dS v) + dz)
+    // dq = [q > 0] (R^T (S a) + dden z), and dz = sum dden phi(q) from its q tiles
     if ((e = launch_tc_apply(A, q, S, dq, B, H, N, rope, eps, status, num_sms, stream,
-                             kApplyGrad, nullptr, nullptr, dden)) != cudaSuccess)
+                             kApplyGrad, nullptr, nullptr, dden, nullptr, dzpart)) != cudaSuccess)
         return e;
+    if ((e = launch_tc_ds_merge(dspart, dzpart, dS, B, H, N, num_sms, stream)) != cudaSuccess)
+        return e;
+    // dk = [k > 0] (R^T (dS v) + dz), dv = dS^T kr
     if ((e = launch_tc_apply(v, k, dS, dk, B, H, N, rope, eps, status, num_sms, stream,
                              kApplyGrad)) != cudaSuccess)
         return e;

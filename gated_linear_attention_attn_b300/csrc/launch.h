@@ -96,16 +96,25 @@ cudaError_t launch_tc_state(const void* k, const void* v, void* state, int B, in
 // mode: 0 the gated apply; 1 out = (R phi(q))^T S; 2 the backward's gate terms:
 // with num = (R phi(q))^T S, den = phi(q) . z + eps and s = sigmoid(g), out = a =
 // dout s / den, dg = dout num s (1 - s) / den and dden = -(a . num) / den per row
-// ([B*H][N] fp32); 3 the masked gradient: out = [g > 0] (R^T (S q) + w z) with q
+// ([B*H][N] fp32), and the partials of dS = sum (R phi(q)) a^T; 3 the masked gradient: out = [g > 0] (R^T (S q) + w z) with q
 // as it is, g the tensor whose feature map is differentiated, z the state's, w =
 // dden per row (1 when dden is null) and R the token's rotation (none without a
 // table).
 constexpr int kApplyGate = 0, kApplyRaw = 1, kApplyTerms = 2, kApplyGrad = 3;
+// dspart (mode 2): the dS partial slots, tc_apply_partial_bytes; dzpart (mode 3,
+// nullable): the dz partials sum_i dden_i phi(g_i), tc_apply_zpart_bytes.
 cudaError_t launch_tc_apply(const void* q, const void* g, const void* state, void* out, int B,
                             int H, int N, const RopeView* rope, float eps, unsigned* status,
                             int num_sms, cudaStream_t stream, int mode = kApplyGate,
                             const void* dout = nullptr, void* dg = nullptr,
-                            float* dden = nullptr);
+                            float* dden = nullptr, float* dspart = nullptr,
+                            float* dzpart = nullptr);
+size_t tc_apply_partial_bytes(int BH, int N, int num_sms);
+size_t tc_apply_zpart_bytes(int BH, int N, int num_sms);
+// The dS state (bf16 S^T rows and fp32 z, as the state kernel writes a state)
+// from the gate terms' dS partials and the masked gradient's dz partials.
+cudaError_t launch_tc_ds_merge(const float* dspart, const float* dzpart, void* state, int B, int H,
+                               int N, int num_sms, cudaStream_t stream);
 
 // RoPE table (rope_table.cu): the header, then every token's pairs as fp16
 // and as fp32, from the grid and band split or from caller-given fp32 pairs.

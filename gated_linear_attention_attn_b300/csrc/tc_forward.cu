@@ -95,6 +95,9 @@ struct ApplyParams {
     int nb, tok0;                   // as in StateParams
     float* dden;                    // [heads][N]: kApTerms writes -(a . num) / den,
                                     // kApGrad reads the row weight (null: 1)
+    float* dspart;                  // kApTerms: dS partial slots (cta + head), S^T layout
+    float* dzpart;                  // kApGrad (null: none): sum_i w_i phi(g_i) per
+                                    // slot (cta + head) and transform warp, [.][8][128]
 };
 
 // =================================================================== state ==
@@ -280,6 +283,16 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         bool ok = !*abort_flag;
         // (head uh, tile ut) of unit u, advanced without divisions
         int uh = (int)(u0 / p.Tk), ut = (int)(u0 % p.Tk);
+        // the rows' weights of z, one tile ahead
+        float zw_next[kStRowsPerThread];
+        auto load_weights = [&](int h, int t) {
+#pragma unroll
+            for (int i = 0; i < kStRowsPerThread; ++i) {
+                const int tok = t * kStTok + rl + 16 * i;
+                zw_next[i] = tok < p.N ? __ldg(p.zweight + (size_t)h * p.N + tok) : 0.f;
+            }
+        };
+        if (p.zweight && ok && u0 < u1) load_weights(uh, ut);
         for (long long u = u0; ok && u < u1; ++u, ++it, ut = ut + 1 == p.Tk ? 0 : ut + 1, uh += ut == 0) {
             const int h = uh;
             if (h != cur_h) {
@@ -289,14 +302,12 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             }
             const int s = (int)(it % kStStages);
             const uint32_t round = (uint32_t)(it / kStStages);
-            // the rows' weights of z, loaded while the tile lands
             float zw[kStRowsPerThread];
             if (p.zweight) {
 #pragma unroll
-                for (int i = 0; i < kStRowsPerThread; ++i) {
-                    const int tok = ut * kStTok + rl + 16 * i;
-                    zw[i] = tok < p.N ? __ldg(p.zweight + (size_t)h * p.N + tok) : 0.f;
-                }
+                for (int i = 0; i < kStRowsPerThread; ++i) zw[i] = zw_next[i];
+                // the next unit is the next tile of this head, or tile 0 of the next
+                if (u + 1 < u1) load_weights(ut + 1 == p.Tk ? h + 1 : h, ut + 1 == p.Tk ? 0 : ut + 1);
             }
             if (!(ok = warp_wait(&full[s], round & 1, abort_flag, p.status))) break;
             const uint32_t kb = smem0 + s * kStStage;
@@ -655,7 +666,11 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 //             written over dout and g in the G slot and stored with TMA
 //             through tm_o32 and tm_dg) and dden_i = -(a_i . num_i) / den_i
 //             (fp32, p.dden); g and dout stream in together through the G
-//             ring (tm_g, tm_d);
+//             ring (tm_g, tm_d).  The tensor cores also accumulate dS = sum_i
+//             (R_i phi(q_i)) a_i^T over each head segment of the CTA from the
+//             tile's rotated q (Q slot) and a (G slot), both MN-major; the
+//             epilogue writes each segment's dS into partial slot (cta + head)
+//             of p.dspart;
 // and for the masked gradients dq and dk:
 //   kApGrad   out_i = [g_i > 0] (R_i^T (S x_i) + w_i z), with (S x_i)[m] =
 //             sum_n x_i[n] S[m][n]: x is taken as it is (no feature map, no
@@ -670,7 +685,10 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 //             ahead of the epilogue, which reads them beside the product.
 //             Each warp takes 32 tokens x 32 words per tile by one TMA load
 //             (tm_d is then the table's box map) into its 4 KB of shared
-//             memory, and reads them back one token row per lane.
+//             memory, and reads them back one token row per lane.  With
+//             p.dzpart they also sum w_i phi(g_i) from the G slot before the
+//             epilogue writes over it: a partial of dz per head segment and
+//             warp.
 template <bool ROPE, int MODE>
 __global__ void __launch_bounds__(kApThreads, 1)
 tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_g,
@@ -680,17 +698,18 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     constexpr int DS = ApGeo<MODE>::kDS;
     // kApGrad: the Q tile is an operand as it is (no feature map, no
     // rotation), the state an MN-major B operand; the den slots carry the
-    // RoPE rows in TMEM, or nothing without RoPE
+    // RoPE rows in TMEM (or nothing without RoPE)
     constexpr bool kGrad = MODE == kApGrad;
     constexpr bool kTmemRope = kGrad && ROPE;
-    constexpr bool kSlots = !kGrad || ROPE;
+    constexpr bool kDS = MODE == kApTerms;       // dS accumulated beside the numerators
     // The G producer stores the outputs the epilogue staged in a G slot and
     // refills the slot as soon as the stores have read it (otherwise each
     // epilogue warp stores its own part and frees the previous tile's slot).
     constexpr bool kPStore = MODE == kApTerms;
     static_assert(kPStore || MODE != kApTerms, "the gate terms' two outputs go out from the producer");
-    constexpr uint32_t kCols = kTmemRope ? 512 : kApTmemCols;
+    constexpr uint32_t kCols = kTmemRope || kDS ? 512 : kApTmemCols;
     constexpr uint32_t kRopeCol = 256;           // kTmemRope: [DS][64] columns of RoPE words
+    constexpr uint32_t kDsCol = 256;             // kDS: [2][128] columns, one per head segment
     static_assert(!kTmemRope || kRopeCol + DS * 64 <= kCols, "TMEM columns");
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t* qring = smem;                                      // [QS][32 KB]
@@ -718,7 +737,10 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint64_t* mma_done = sfree + 1;
     uint64_t* pairdone = mma_done + 1;           // kApTerms: [2] the tile's dpart written
     uint64_t* rfull = pairdone + (MODE == kApTerms ? 2 : 0);   // kTmemRope: [8] a warp's rows landed
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rfull + (kTmemRope ? kApXWarps : 0));
+    uint64_t* dsfull = rfull + (kTmemRope ? kApXWarps : 0);   // kDS: [2] a segment's dS final
+    uint64_t* dsfree = dsfull + (kDS ? 2 : 0);                // kDS: [2] written out
+    uint64_t* gread = dsfree + (kDS ? 2 : 0);                 // kDS: [GS] a read by the MMA
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gread + (kDS ? GS : 0));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -733,6 +755,13 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         if (kTmemRope)
             for (int w = 0; w < kApXWarps; ++w) mbar_init(&rfull[w], 1);
+        if (kDS) {
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(&dsfull[b], 1);
+                mbar_init(&dsfree[b], kApEWarps);
+            }
+            for (int b = 0; b < GS; ++b) mbar_init(&gread[b], 1);
+        }
         for (int s = 0; s < QS; ++s) {
             mbar_init(&qfull[s], 1);
             mbar_init(&qready[s], kApXWarps);
@@ -871,6 +900,42 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             long long it = 0;
             int heads = 0, cur_h = -1;
             bool ok = !*abort_flag;
+            // kDS: dS of tile j once the epilogue has staged its a; frees the
+            // tile's Q slot and, for the producer, its G slot
+            int dseg = -1;
+            auto issue_ds = [&](long long j) -> bool {
+                const long long uj = u0 + j;
+                const int hj = (int)(uj / p.Tq);
+                const bool start = j == 0 || (int)((uj - 1) / p.Tq) != hj;
+                const bool end = uj + 1 == u1 || (int)((uj + 1) / p.Tq) != hj;
+                if (start) {
+                    ++dseg;
+                    // the buffer's segment before last is written out
+                    if (dseg >= 2 &&
+                        !mbar_wait(&dsfree[dseg & 1], ((dseg >> 1) - 1) & 1, abort_flag, p.status))
+                        return false;
+                }
+                const int gsj = (int)(j % GS);
+                if (!mbar_wait(&gempty[gsj], (uint32_t)((j / GS) & 1), abort_flag, p.status))
+                    return false;
+                tc_fence_after();
+                constexpr uint32_t idesc_ds = idesc_bf16(128, 128, true, true);
+                const uint32_t qb = smem0 + (uint32_t)(j % QS) * kApTile;
+                const uint32_t ab = smem0 + QS * kApTile + (uint32_t)gsj * GT + kApTile;
+#pragma unroll
+                for (int ks = 0; ks < kApTok / 16; ++ks) {
+                    // 16 tokens = two 8-row swizzle atoms; the two 64-wide
+                    // halves of M (and N) sit kApHalf apart
+                    const uint64_t ad = smem_desc_sw128(qb + ks * 2048, kApHalf, 1024);
+                    const uint64_t bd = smem_desc_sw128(ab + ks * 2048, kApHalf, 1024);
+                    mma_bf16(tmem + kDsCol + (uint32_t)(dseg & 1) * 128, ad, bd, idesc_ds,
+                             (start && ks == 0) ? 0u : 1u);
+                }
+                mma_commit(&qempty[j % QS]);
+                mma_commit(&gread[gsj]);
+                if (end) mma_commit(&dsfull[dseg & 1]);
+                return true;
+            };
             for (long long u = u0; ok && u < u1; ++u, ++it) {
                 const int h = (int)(u / p.Tq);
                 if (h != cur_h) {
@@ -904,47 +969,71 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     mma_bf16(tmem + (uint32_t)a * 128, ad, bd, idesc, ks > 0 ? 1u : 0u);
                 }
                 mma_commit(&accfull[a]);
-                mma_commit(&qempty[s]);                   // the Q slot may be refilled
+                if constexpr (kDS) {
+                    if (it >= 1 && !(ok = issue_ds(it - 1))) break;
+                } else {
+                    mma_commit(&qempty[s]);               // the Q slot may be refilled
+                }
             }
+            if (kDS && ok && it >= 1) issue_ds(it - 1);
             mma_commit(mma_done);
             mbar_wait_drain(mma_done, 0);
         }
     } else if (kGrad && warp < 2 + kApXWarps) {
-        // ------------------------------------------------ kApGrad: RoPE rows to TMEM
-        if constexpr (kTmemRope) {
-            // this warp's 32 tokens (its TMEM lanes) x 32 words of their RoPE
-            // rows: TMA to its 4 KB, then one token row per lane to TMEM
-            const int xw = warp - 2, tquad = warp & 3, part = xw >> 2;
-            uint8_t* scr = rscr + xw * 4096;
-            const uint32_t scr_a = smem_u32(scr);
-            uint64_t* bar = &rfull[xw];
-            const uint64_t keep = policy_evict_last();
-            auto issue = [&](long long u) {
-                if (lane == 0) {
-                    const int h = (int)(u / p.Tq), tile = (int)(u % p.Tq);
-                    const int row0 = (p.nb == 1 ? 0 : (h % p.nb) * p.N) + p.tok0 + tile * kApTok +
-                                     32 * tquad;
-                    mbar_arrive_expect_tx(bar, 4096);
-                    tma_load_2d(scr, &tm_d, bar, 32 * part, row0, keep);
-                }
-            };
-            bool ok = !*abort_flag;
-            long long issued = 0;
-            if (ok && u0 < u1) {
+        // ------------------------------------------------ kApGrad: RoPE rows to TMEM, dz
+        // ROPE: this warp's 32 tokens (its TMEM lanes) x 32 words of their
+        // RoPE rows, by TMA to its 4 KB, then one token row per lane to TMEM.
+        // p.dzpart: w_i phi(g_i) summed over rows rl + 16 i, dims 8c.., from
+        // the G slot.
+        const int xw = warp - 2, tquad = warp & 3, part = xw >> 2;
+        const int tt = threadIdx.x - 64, c = tt & 15, rl = tt >> 4;
+        uint8_t* scr = rscr + xw * 4096;
+        const uint32_t scr_a = smem_u32(scr);
+        uint64_t* bar = &rfull[xw];
+        const uint64_t keep = policy_evict_last();
+        auto issue = [&](long long u) {
+            if (lane == 0) {
+                const int h = (int)(u / p.Tq), tile = (int)(u % p.Tq);
+                const int row0 = (p.nb == 1 ? 0 : (h % p.nb) * p.N) + p.tok0 + tile * kApTok +
+                                 32 * tquad;
+                mbar_arrive_expect_tx(bar, 4096);
+                tma_load_2d(scr, &tm_d, bar, 32 * part, row0, keep);
+            }
+        };
+        const bool dz = p.dzpart != nullptr;
+        float wnext[kApRowsPerThread], zacc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) zacc[j] = 0.f;
+        // the rows' weights, one tile ahead (rows past N weigh nothing)
+        auto load_w = [&](long long u) {
+            const int h = (int)(u / p.Tq), tile = (int)(u % p.Tq);
+#pragma unroll
+            for (int i = 0; i < kApRowsPerThread; ++i) {
+                const int row = tile * kApTok + rl + 16 * i;
+                wnext[i] = row < p.N ? (p.dden ? __ldg(p.dden + (size_t)h * p.N + row) : 1.f) : 0.f;
+            }
+        };
+        bool ok = !*abort_flag;
+        long long issued = 0;
+        if (ok && u0 < u1) {
+            if (ROPE) {
                 issue(u0);
                 issued = 1;
             }
-            long long it = 0;
-            for (long long u = u0; ok && u < u1; ++u, ++it) {
+            if (dz) load_w(u0);
+        }
+        long long it = 0;
+        for (long long u = u0; ok && u < u1; ++u, ++it) {
+            uint32_t wv[32];
+            if constexpr (ROPE) {
                 if (!(ok = warp_wait(bar, (uint32_t)(it & 1), abort_flag, p.status))) break;
-                uint32_t wv[32];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint4 x = lds128(scr_a + lane * 128 + ((c ^ (lane & 7)) << 4));
-                    wv[4 * c] = x.x;
-                    wv[4 * c + 1] = x.y;
-                    wv[4 * c + 2] = x.z;
-                    wv[4 * c + 3] = x.w;
+                for (int cc = 0; cc < 8; ++cc) {
+                    const uint4 x = lds128(scr_a + lane * 128 + ((cc ^ (lane & 7)) << 4));
+                    wv[4 * cc] = x.x;
+                    wv[4 * cc + 1] = x.y;
+                    wv[4 * cc + 2] = x.z;
+                    wv[4 * cc + 3] = x.w;
                 }
                 // every lane's reads are done before the next tile's copy lands there
                 fence_proxy_async_smem();
@@ -953,22 +1042,63 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     issue(u + 1);
                     ++issued;
                 }
-                const int ds = (int)(it % DS);
-                const uint32_t dround = (uint32_t)(it / DS);
-                // the epilogue has read the slot's previous tile
-                if (dround > 0 && !(ok = warp_wait(&dfree[ds], (dround - 1) & 1, abort_flag, p.status)))
-                    break;
+            }
+            const int ds = (int)(it % DS);
+            const uint32_t dround = (uint32_t)(it / DS);
+            // the epilogue has read the slot's previous tile
+            if (dround > 0 && !(ok = warp_wait(&dfree[ds], (dround - 1) & 1, abort_flag, p.status)))
+                break;
+            if constexpr (ROPE) {
                 tmem_st32(tmem + ((uint32_t)(32 * tquad) << 16) + kRopeCol + (uint32_t)ds * 64 +
                               32 * part,
                           wv);
                 tmem_st_wait();
                 tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&dready[ds]);
             }
-            // no copy of ours may still be landing when the CTA exits
-            if (lane == 0 && issued > it) mbar_wait_drain(bar, (uint32_t)((issued - 1) & 1));
+            if (dz) {
+                // the G slot's tile, read before the epilogue writes over it
+                const int h = (int)(u / p.Tq);
+                const int gs = (int)(it % GS);
+                float w[kApRowsPerThread];
+#pragma unroll
+                for (int i = 0; i < kApRowsPerThread; ++i) w[i] = wnext[i];
+                if (u + 1 < u1) load_w(u + 1);
+                if (!(ok = warp_wait(&gfull[gs], (uint32_t)(it / GS) & 1, abort_flag, p.status)))
+                    break;
+                const uint32_t gb = smem0 + QS * kApTile + (uint32_t)gs * GT;
+#pragma unroll
+                for (int b4 = 0; b4 < kApRowsPerThread; b4 += 4) {
+                    uint4 x[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) x[i] = lds128(gb + sw128_off(rl + 16 * (b4 + i), c, kApHalf));
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        float f[8];
+                        unpack8(x[i], f);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) zacc[j] = fmaf(w[b4 + i], fmaxf(f[j], 0.f), zacc[j]);
+                    }
+                }
+                // the head segment's last tile: this warp's partial of dz
+                if (u + 1 == u1 || (int)((u + 1) / p.Tq) != h) {
+                    // lanes l and l ^ 16 hold the same dims for neighbouring rows
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) zacc[j] += __shfl_xor_sync(0xffffffffu, zacc[j], 16);
+                    if (lane < 16) {
+                        float4* zp = reinterpret_cast<float4*>(
+                            p.dzpart + ((size_t)(cta + h) * kApXWarps + xw) * kHeadDim + c * 8);
+                        zp[0] = make_float4(zacc[0], zacc[1], zacc[2], zacc[3]);
+                        zp[1] = make_float4(zacc[4], zacc[5], zacc[6], zacc[7]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) zacc[j] = 0.f;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&dready[ds]);
         }
+        // no copy of ours may still be landing when the CTA exits
+        if (ROPE && lane == 0 && issued > it) mbar_wait_drain(bar, (uint32_t)((issued - 1) & 1));
     } else if (warp < 2 + kApXWarps) {
         // ------------------------------------------------ transform: phi, RoPE, den
         const int tt = threadIdx.x - 64;            // 0..255
@@ -1091,6 +1221,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int r = 32 * quad + lane;              // TMEM lane = token row of the tile
         long long it = 0;
         int eheads = 0, ecur_h = -1;                 // kApGrad: heads begun
+        int eseg = 0;                                // kDS: head segments written out
         bool ok = !*abort_flag;
         for (long long u = u0; ok && u < u1; ++u, ++it) {
             const int h = (int)(u / p.Tq), tile = (int)(u % p.Tq);
@@ -1106,7 +1237,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (p.dden) w = p.dden[(size_t)h * p.N + min(tile * kApTok + r, p.N - 1)];
             }
             ok = warp_wait(&accfull[a], around & 1, abort_flag, p.status) &&
-                 (!kSlots || warp_wait(&dready[ds], (uint32_t)(it / DS) & 1, abort_flag, p.status)) &&
+                 warp_wait(&dready[ds], (uint32_t)(it / DS) & 1, abort_flag, p.status) &&
                  warp_wait(&gfull[gs], ground & 1, abort_flag, p.status);
             if (!ok) break;
             tc_fence_after();
@@ -1190,7 +1321,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             tc_fence_before();
             fence_proxy_async_smem();
-            if constexpr (kTmemRope) {
+            if constexpr (kGrad) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&dfree[ds]);
             }
@@ -1219,7 +1350,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (lane == 0) {
                 mbar_arrive(&accempty[a]);
                 if constexpr (kPStore) {
-                    mbar_arrive(&gempty[gs]);       // this warp's part is staged
+                    mbar_arrive(&gempty[gs]);       // this warp's part is staged (a, dg)
                 } else {
                     // this warp's rows 32*quad.. of column half hf, 4 KB of the tile
                     tma_store_3d(&tm_o32, gring + gs * GT + hf * kApHalf + quad * kApORows * 128,
@@ -1228,6 +1359,33 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     // the previous tile's store has read its G slot, which may be refilled
                     bulk_wait_read_one();
                     if (it > 0) mbar_arrive(&gempty[(it - 1) % GS]);
+                }
+            }
+            if constexpr (kDS) {
+                // the head segment's last tile here: its dS (rows r of S^T's
+                // columns, as the state kernel's slots hold them) to slot cta + h
+                if (u + 1 == u1 || (int)((u + 1) / p.Tq) != h) {
+                    const int sb = eseg & 1;
+                    if (!(ok = warp_wait(&dsfull[sb], (uint32_t)(eseg >> 1) & 1, abort_flag,
+                                         p.status)))
+                        break;
+                    tc_fence_after();
+                    float* slot = p.dspart + (size_t)(cta + h) * kPartialFloats;
+#pragma unroll 1
+                    for (int ch = 0; ch < 2; ++ch) {
+                        uint32_t v[32];
+                        tmem_ld32(tmem + ((uint32_t)(32 * quad) << 16) + kDsCol + (uint32_t)sb * 128 +
+                                      hf * 64 + ch * 32,
+                                  v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            slot[(size_t)(hf * 64 + ch * 32 + j) * kHeadDim + r] = __uint_as_float(v[j]);
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&dsfree[sb]);
+                    ++eseg;
                 }
             }
         }
@@ -1269,6 +1427,10 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         if (!(ok = store_tile(it - GS))) break;
                         ++stored;
                         bulk_wait_read_all();
+                        // kDS: and the MMA has read the tile's a for dS
+                        if (kDS && !(ok = mbar_wait(&gread[s], (uint32_t)(((it - GS) / GS) & 1),
+                                                    abort_flag, p.status)))
+                            break;
                     }
                 } else if (!mbar_wait(&gempty[s], (round & 1) ^ 1, abort_flag, p.status)) {
                     break;
@@ -1974,6 +2136,66 @@ block_scan_kernel(ScanParams p) {
     }
 }
 
+// The backward's dS state from the apply kernel's partials: for every head,
+// the dS^T slots (cta + head) of the CTAs whose range holds the head's query
+// tiles, summed in CTA order as bf16 rows in the MMA layout, and z from the
+// slots' per-warp partials (warp order within a CTA).
+struct DsMergeParams {
+    const float* dspart;        // [slots][kPartialFloats] (the z part unused)
+    const float* dzpart;        // [slots][8 warps][128]
+    uint8_t* states;            // [heads][kStateBytes]
+    Split split;                // the apply kernel's units (head, 128-token tile)
+    int Tq;
+};
+
+__global__ void __launch_bounds__(kScanThreads)
+ds_merge_kernel(DsMergeParams p) {
+    const int head = blockIdx.x, rg = blockIdx.y, t = threadIdx.x;
+    const int n = kScanRows * rg + (t >> 4), cc = t & 15;
+    const bool with_z = rg == 0 && t < kHeadDim;
+    const int lo = p.split.owner((long long)head * p.Tq);
+    const int hi = p.split.owner((long long)(head + 1) * p.Tq - 1);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int c0 = lo; c0 <= hi; c0 += kScanBatch) {
+        float4 x0[kScanBatch], x1[kScanBatch];
+#pragma unroll
+        for (int j = 0; j < kScanBatch; ++j) {
+            if (c0 + j <= hi) {
+                const float4* src = reinterpret_cast<const float4*>(
+                    p.dspart + (size_t)(c0 + j + head) * kPartialFloats + n * kHeadDim + cc * 8);
+                x0[j] = __ldcg(src);
+                x1[j] = __ldcg(src + 1);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kScanBatch; ++j) {
+            if (c0 + j <= hi) {
+                acc[0] += x0[j].x; acc[1] += x0[j].y; acc[2] += x0[j].z; acc[3] += x0[j].w;
+                acc[4] += x1[j].x; acc[5] += x1[j].y; acc[6] += x1[j].z; acc[7] += x1[j].w;
+            }
+        }
+    }
+    uint8_t* dst = p.states + (size_t)head * kStateBytes;
+    uint4 w;
+    w.x = f2_to_bf2(acc[0], acc[1]);
+    w.y = f2_to_bf2(acc[2], acc[3]);
+    w.z = f2_to_bf2(acc[4], acc[5]);
+    w.w = f2_to_bf2(acc[6], acc[7]);
+    *reinterpret_cast<uint4*>(dst + sw128_off(n, cc, kStateHalf)) = w;
+    if (with_z) {
+        float z = 0.f;
+        for (int c = lo; c <= hi; ++c) {
+            const float* zp = p.dzpart + (size_t)(c + head) * kApXWarps * kHeadDim + t;
+            float x[kApXWarps];
+#pragma unroll
+            for (int w8 = 0; w8 < kApXWarps; ++w8) x[w8] = __ldcg(zp + w8 * kHeadDim);
+#pragma unroll
+            for (int w8 = 0; w8 < kApXWarps; ++w8) z += x[w8];
+        }
+        reinterpret_cast<float*>(dst + kStateSBytes)[t] = z;
+    }
+}
+
 // ==================================================================== host ==
 
 // Barriers and flags follow the buffers: state 3*stages + 13 mbarriers plus
@@ -1991,7 +2213,7 @@ constexpr size_t ap_smem() {
     return (size_t)G::kQS * kApTile + (size_t)G::kGS * G::kGT + (kTmemRope ? kApXWarps * 4096 : 0) +
            kStateBytes +
            ((MODE == kApGrad ? 0 : G::kDS) + (MODE == kApTerms ? 2 : 0)) * kApTok * sizeof(float) +
-           (3 * G::kQS + 2 * G::kGS + 2 * G::kDS + 7 + (MODE == kApTerms ? 2 : 0) +
+           (3 * G::kQS + 2 * G::kGS + 2 * G::kDS + 7 + (MODE == kApTerms ? 2 + 4 + G::kGS : 0) +
             (kTmemRope ? kApXWarps : 0)) *
                8 +
            16;
@@ -2112,7 +2334,7 @@ cudaError_t launch_apply(const void* q, const void* g, const uint8_t* state, voi
                          int N, const RopeView* rope, float eps, unsigned* status, int num_sms,
                          bool after_state, cudaStream_t stream, int nb = 1, int tok0 = 0,
                          int mode = kApGate, const void* dout = nullptr, void* dg = nullptr,
-                         float* dden = nullptr) {
+                         float* dden = nullptr, float* dspart = nullptr, float* dzpart = nullptr) {
     const Plan pl = make_plan(BH, N, num_sms);
     CUtensorMap mq, mg, mo;
     if (!make_map(&mq, q, N, BH, kApTok) || !make_map(&mg, g, N, BH, kApTok) ||
@@ -2135,6 +2357,8 @@ cudaError_t launch_apply(const void* q, const void* g, const uint8_t* state, voi
     ap.nb = nb;
     ap.tok0 = tok0;
     ap.dden = dden;
+    ap.dspart = dspart;
+    ap.dzpart = dzpart;
     if (rope) ap.rope = *rope;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(pl.ap.G);
@@ -2311,11 +2535,30 @@ cudaError_t launch_tc_state(const void* k, const void* v, void* state, int B, in
 cudaError_t launch_tc_apply(const void* q, const void* g, const void* state, void* out, int B,
                             int H, int N, const RopeView* rope, float eps, unsigned* status,
                             int num_sms, cudaStream_t stream, int mode, const void* dout,
-                            void* dg, float* dden) {
+                            void* dg, float* dden, float* dspart, float* dzpart) {
     cudaError_t e = configure(current_device());
     if (e != cudaSuccess) return e;
     return launch_apply(q, g, static_cast<const uint8_t*>(state), out, B * H, N, rope, eps,
-                        status, num_sms, false, stream, 1, 0, mode, dout, dg, dden);
+                        status, num_sms, false, stream, 1, 0, mode, dout, dg, dden, dspart,
+                        dzpart);
+}
+
+size_t tc_apply_partial_bytes(int BH, int N, int num_sms) {
+    const Plan pl = make_plan(BH, N, num_sms);
+    return ((size_t)pl.ap.G + BH) * kPartialFloats * sizeof(float);
+}
+
+size_t tc_apply_zpart_bytes(int BH, int N, int num_sms) {
+    const Plan pl = make_plan(BH, N, num_sms);
+    return ((size_t)pl.ap.G + BH) * kApXWarps * kHeadDim * sizeof(float);
+}
+
+cudaError_t launch_tc_ds_merge(const float* dspart, const float* dzpart, void* state, int B, int H,
+                               int N, int num_sms, cudaStream_t stream) {
+    const Plan pl = make_plan(B * H, N, num_sms);
+    DsMergeParams mp{dspart, dzpart, static_cast<uint8_t*>(state), pl.ap, pl.Tq};
+    ds_merge_kernel<<<dim3(B * H, kHeadDim / kScanRows), kScanThreads, 0, stream>>>(mp);
+    return cudaGetLastError();
 }
 
 int tc_forward_cluster(int dev, int BH, int N, bool rope, int num_sms) {
