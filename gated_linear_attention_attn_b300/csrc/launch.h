@@ -89,10 +89,9 @@ cudaError_t launch_tc_block_causal(const void* q, const void* k, const void* v, 
                                    const RopeView* rope, int rope_offset, float eps,
                                    const float* state_in, float* state_out, float* workspace,
                                    unsigned* status, int num_sms, cudaStream_t stream);
-// zweight: null, or a weight per token ([B*H][N] fp32) for z = sum_j w_j phi(k_j).
 cudaError_t launch_tc_state(const void* k, const void* v, void* state, int B, int H, int N,
                             const RopeView* rope, void* workspace, unsigned* status, int num_sms,
-                            cudaStream_t stream, const float* zweight = nullptr);
+                            cudaStream_t stream);
 // mode: 0 the gated apply; 1 out = (R phi(q))^T S; 2 the backward's gate terms:
 // with num = (R phi(q))^T S, den = phi(q) . z + eps and s = sigmoid(g), out = a =
 // dout s / den, dg = dout num s (1 - s) / den and dden = -(a . num) / den per row

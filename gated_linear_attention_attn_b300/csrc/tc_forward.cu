@@ -81,8 +81,6 @@ struct StateParams {
     // covers tokens [(hh % nb) * N + tok0, ...) of the RoPE grid.  merge = 0
     // leaves the partial slots unmerged (the block scan sums them).
     int nb, tok0, merge;
-    // null, or a weight per token ([heads][N] fp32): z = sum_j w_j phi(k_j)
-    const float* zweight;
 };
 
 struct ApplyParams {
@@ -283,16 +281,6 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         bool ok = !*abort_flag;
         // (head uh, tile ut) of unit u, advanced without divisions
         int uh = (int)(u0 / p.Tk), ut = (int)(u0 % p.Tk);
-        // the rows' weights of z, one tile ahead
-        float zw_next[kStRowsPerThread];
-        auto load_weights = [&](int h, int t) {
-#pragma unroll
-            for (int i = 0; i < kStRowsPerThread; ++i) {
-                const int tok = t * kStTok + rl + 16 * i;
-                zw_next[i] = tok < p.N ? __ldg(p.zweight + (size_t)h * p.N + tok) : 0.f;
-            }
-        };
-        if (p.zweight && ok && u0 < u1) load_weights(uh, ut);
         for (long long u = u0; ok && u < u1; ++u, ++it, ut = ut + 1 == p.Tk ? 0 : ut + 1, uh += ut == 0) {
             const int h = uh;
             if (h != cur_h) {
@@ -302,13 +290,6 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             }
             const int s = (int)(it % kStStages);
             const uint32_t round = (uint32_t)(it / kStStages);
-            float zw[kStRowsPerThread];
-            if (p.zweight) {
-#pragma unroll
-                for (int i = 0; i < kStRowsPerThread; ++i) zw[i] = zw_next[i];
-                // the next unit is the next tile of this head, or tile 0 of the next
-                if (u + 1 < u1) load_weights(ut + 1 == p.Tk ? h + 1 : h, ut + 1 == p.Tk ? 0 : ut + 1);
-            }
             if (!(ok = warp_wait(&full[s], round & 1, abort_flag, p.status))) break;
             const uint32_t kb = smem0 + s * kStStage;
             // all loads of the tile first, so their latencies overlap
@@ -334,13 +315,8 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 x[i].w = relu_bf2(x[i].w);
                 float f[8];
                 unpack8(x[i], f);
-                if (p.zweight) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) zacc[j] = fmaf(zw[i], f[j], zacc[j]);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) zacc[j] += f[j];
-                }
+                for (int j = 0; j < 8; ++j) zacc[j] += f[j];
                 if (ROPE) x[i] = rotate_chunk(f, cs[i]);
             }
 #pragma unroll
@@ -1167,11 +1143,14 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     x[i].w = relu_bf2(x[i].w);
                     float f[8];
                     unpack8(x[i], f);
-                    float2 d2 = mul2(make_float2(f[0], f[1]), make_float2(zc[0], zc[1]));
+                    if constexpr (MODE != kApRaw) {     // (the raw product has no den)
+                        float2 d2 = mul2(make_float2(f[0], f[1]), make_float2(zc[0], zc[1]));
 #pragma unroll
-                    for (int j = 2; j < 8; j += 2)
-                        d2 = fma2(make_float2(f[j], f[j + 1]), make_float2(zc[j], zc[j + 1]), d2);
-                    den[i] = d2.x + d2.y;
+                        for (int j = 2; j < 8; j += 2)
+                            d2 = fma2(make_float2(f[j], f[j + 1]), make_float2(zc[j], zc[j + 1]),
+                                      d2);
+                        den[i] = d2.x + d2.y;
+                    }
                     if (ROPE) {
                         float2 cs[4];
                         unpack_cs(trow[b4 + i], cs);
@@ -1186,6 +1165,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     fetch_rows(next_tile == 0 ? h + 1 : h, next_tile, 0);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) sts128(addr[i], x[i]);
+                if constexpr (MODE == kApRaw) continue;
                 // Sum den over the 16 chunk lanes of each row: each step halves the
                 // rows a lane holds, so lane c ends with row b4 + ((c >> 2) & 3).
                 const bool b3 = (c >> 3) & 1, b2 = (c >> 2) & 1;
@@ -2292,8 +2272,7 @@ cudaError_t configure(int dev) {
 // per head, starting at token tok0 of the RoPE grid, and merge is 0.
 cudaError_t launch_state(const void* k, const void* v, int BH, int N, const RopeView* rope,
                          void* workspace, uint8_t* state, unsigned* status, int num_sms,
-                         cudaStream_t stream, int nb = 1, int tok0 = 0, bool merge = true,
-                         const float* zweight = nullptr) {
+                         cudaStream_t stream, int nb = 1, int tok0 = 0, bool merge = true) {
     const Plan pl = make_plan(BH, N, num_sms);
     CUtensorMap mk, mv;
     if (!make_map(&mk, k, N, BH, kStTok) || !make_map(&mv, v, N, BH, kStTok))
@@ -2310,7 +2289,6 @@ cudaError_t launch_state(const void* k, const void* v, int BH, int N, const Rope
     sp.nb = nb;
     sp.tok0 = tok0;
     sp.merge = merge ? 1 : 0;
-    sp.zweight = zweight;
     CUtensorMap mt = mk;   // without RoPE the table map is never read
     if (rope && !make_rope_map(&mt, rope->tok, rope->need, kStTok)) return cudaErrorInvalidValue;
     if (rope) sp.rope = *rope;
@@ -2525,11 +2503,11 @@ size_t tc_state_bytes(int BH) { return (size_t)BH * kStateBytes; }
 
 cudaError_t launch_tc_state(const void* k, const void* v, void* state, int B, int H, int N,
                             const RopeView* rope, void* workspace, unsigned* status, int num_sms,
-                            cudaStream_t stream, const float* zweight) {
+                            cudaStream_t stream) {
     cudaError_t e = configure(current_device());
     if (e != cudaSuccess) return e;
     return launch_state(k, v, B * H, N, rope, workspace, static_cast<uint8_t*>(state), status,
-                        num_sms, stream, 1, 0, true, zweight);
+                        num_sms, stream, 1, 0, true);
 }
 
 cudaError_t launch_tc_apply(const void* q, const void* g, const void* state, void* out, int B,
