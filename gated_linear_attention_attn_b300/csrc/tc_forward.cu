@@ -1083,6 +1083,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // This thread's 16 bytes of the RoPE rows of its 8 rows in the next
         // tile, loaded while the current tile is transformed.
         uint4 trow[kApRowsPerThread];
+        const uint64_t keep = policy_evict_last();  // the table serves every head
         // (tile `tile` of head hh; head hh is block hh % nb of its head's
         // tokens, which start at RoPE grid token (hh % nb) * N + tok0)
         auto fetch_rows = [&](int hh, int tile, int i0) {
@@ -1090,7 +1091,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
             for (int i = i0; i < i0 + 4; ++i) {
                 const int n = min(tile * kApTok + rl + 16 * i, p.N - 1);   // rows past N are zero
-                trow[i] = ldg_nc_na128(p.rope.tok + (size_t)(base + n) * kPairs + c * 4);
+                trow[i] = ldg_nc_na128_hint(p.rope.tok + (size_t)(base + n) * kPairs + c * 4, keep);
             }
         };
         if (ROPE && u0 < u1 && !*abort_flag) {
@@ -1763,11 +1764,12 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             zc[4] = zb.x; zc[5] = zb.y; zc[6] = zb.z; zc[7] = zb.w;
         }
         uint4 trow[kApRowsPerThread];
+        const uint64_t keep = policy_evict_last();  // the table serves every head
         auto fetch_rows = [&](int tile, int i0) {
 #pragma unroll
             for (int i = i0; i < i0 + 4; ++i) {
                 const int n = min(tile * kApTok + rl + 16 * i, p.N - 1);
-                trow[i] = ldg_nc_na128(p.rope.tok + (size_t)n * kPairs + c * 4);
+                trow[i] = ldg_nc_na128_hint(p.rope.tok + (size_t)n * kPairs + c * 4, keep);
             }
         };
         if (ROPE && ok && q0 < q1) {

@@ -468,6 +468,16 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     return v;
 }
 
+// The same, with an L2 cache policy (createpolicy): for small tables that
+// every CTA reads again while large streams pass through L2.
+__device__ __forceinline__ uint4 ldg_nc_na128_hint(const void* p, uint64_t policy) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.b32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(policy));
+    return v;
+}
+
 // 16-byte read-only global load that does not allocate in L1 (data read once
 // per SM, kept in L2).
 __device__ __forceinline__ uint4 ldg_nc_na128(const void* p) {
