@@ -19,8 +19,9 @@
 // (cp.async.bulk, completion counted on the slot's mbarrier).  Per token,
 // thread i takes the 16-byte piece i of every row, the CTA reduces w . s_n
 // and s_n . s_n (warp shuffles, then shared memory, one barrier), every warp
-// forms the softmax, and thread i writes its piece of x, from registers when
-// the CTA is small enough to keep the rows there, else reading them again.
+// forms the softmax, and thread i writes its piece of x from the rows it kept
+// in registers (fp32 in CTAs of up to 384 threads, bf16 above that while they
+// fit), else reading them again.
 // Earlier forms measured slower: re-reading the rows from L2 in a second pass
 // (the rows of the tokens in flight overflow L2 before the second read), and
 // register prefetching one token ahead (too few bytes in flight).
@@ -87,12 +88,20 @@ struct PartCount {                          // 2 M rounded up to a power of two
     static constexpr int value = M <= 1 ? 2 : M <= 2 ? 4 : M <= 4 ? 8 : 16;
 };
 
+// How a thread holds its pieces of the token's rows between the reduction
+// and the output.
+constexpr int kArReread = 0;                // read again from shared memory
+constexpr int kArKeepF32 = 1;               // in registers as fp32 (CTAs of <= 384 threads)
+constexpr int kArKeepBf16 = 2;              // in registers as bf16: 4 words a row, so two
+                                            // CTAs of 512 threads fit an SM (64 registers)
+
 // blockDim.x * 8 == C: thread i owns columns 8i .. 8i + 7 of every row.
-// KEEP: the rows stay in registers from the reduction to the output (fewer
-// instructions; more registers, so used when a CTA has at most 384 threads).
-template <int M, bool KEEP>
-__global__ void __launch_bounds__(kArMaxThreads)
+// Kept rows free their slot at the token's barrier, so the next fetch into
+// it is issued one token earlier than when the rows are read again.
+template <int M, int HOLD>
+__global__ void __launch_bounds__(kArMaxThreads, HOLD == kArKeepBf16 ? 2 : 1)
 attnres_kernel(AttnResParams p) {
+    constexpr bool KEEP = HOLD != kArReread;
     constexpr int P = PartCount<M>::value;
     constexpr int kShift = P == 2 ? 4 : P == 4 ? 3 : P == 8 ? 2 : 1;   // 5 - log2 P
     extern __shared__ __align__(128) uint8_t smem[];
@@ -122,26 +131,38 @@ attnres_kernel(AttnResParams p) {
     };
     if (tid == 0)
         for (long long k = 0; k < mine && k < S; ++k) fetch(k);
-    float2 wv[4];
-    {
+    // this thread's eight query weights; kArKeepBf16 reads them (from L1) for
+    // every token instead of holding them, to stay within 64 registers
+    auto load_w = [&](float2 (&wv)[4]) {
         const float4* w4 = reinterpret_cast<const float4*>(p.w + (size_t)tid * 8);
         const float4 a = __ldg(w4), b = __ldg(w4 + 1);
         wv[0] = make_float2(a.x, a.y);
         wv[1] = make_float2(a.z, a.w);
         wv[2] = make_float2(b.x, b.y);
         wv[3] = make_float2(b.z, b.w);
-    }
+    };
+    float2 wheld[4];
+    if (HOLD != kArKeepBf16) load_w(wheld);
     const float inv_c = 1.f / (float)p.C;
     long long k = 0;
     for (; k < mine; ++k) {
         const int s = (int)(k % S), buf = (int)(k & 1);
+        float2 wv[4];
+        if (HOLD == kArKeepBf16) {
+            load_w(wv);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) wv[i] = wheld[i];
+        }
         const bool ok = mbar_wait(&full[s], (uint32_t)(k / S) & 1u, &abort_flag, p.status);
         const uint32_t slot = smem_u32(smem + (size_t)s * slot_bytes) + tid * 16;
-        float2 x[M][4];                          // kept to the output when KEEP
+        float2 x[M][4];                          // kept to the output when kArKeepF32
+        uint4 raw[M];                            // kept to the output when kArKeepBf16
         float part[P];
 #pragma unroll
         for (int n = 0; n < M; ++n) {
             const uint4 u = lds128(slot + n * row_bytes);
+            if (HOLD == kArKeepBf16) raw[n] = u;
             x[n][0] = bf2_to_f2(u.x);
             x[n][1] = bf2_to_f2(u.y);
             x[n][2] = bf2_to_f2(u.z);
@@ -194,8 +215,8 @@ attnres_kernel(AttnResParams p) {
                          make_float2(0.f, 0.f)};
 #pragma unroll
         for (int n = 0; n < M; ++n) {
-            if (!KEEP) {                         // the rows again, from shared memory
-                const uint4 u = lds128(slot + n * row_bytes);
+            if (HOLD != kArKeepF32) {            // the rows again: from shared memory or bf16
+                const uint4 u = HOLD == kArKeepBf16 ? raw[n] : lds128(slot + n * row_bytes);
                 x[n][0] = bf2_to_f2(u.x);
                 x[n][1] = bf2_to_f2(u.y);
                 x[n][2] = bf2_to_f2(u.z);
@@ -277,24 +298,26 @@ cudaError_t launch_attnres(const void* const* sources, int M, long long T, int C
         kernel<<<(unsigned)blocks, threads, smem, stream>>>(p);
         return cudaGetLastError();
     };
-    const bool keep = threads <= 384;
-    switch (M * 2 + (keep ? 1 : 0)) {
-        case 2: return launch(attnres_kernel<1, false>);
-        case 3: return launch(attnres_kernel<1, true>);
-        case 4: return launch(attnres_kernel<2, false>);
-        case 5: return launch(attnres_kernel<2, true>);
-        case 6: return launch(attnres_kernel<3, false>);
-        case 7: return launch(attnres_kernel<3, true>);
-        case 8: return launch(attnres_kernel<4, false>);
-        case 9: return launch(attnres_kernel<4, true>);
-        case 10: return launch(attnres_kernel<5, false>);
-        case 11: return launch(attnres_kernel<5, true>);
-        case 12: return launch(attnres_kernel<6, false>);
-        case 13: return launch(attnres_kernel<6, true>);
-        case 14: return launch(attnres_kernel<7, false>);
-        case 15: return launch(attnres_kernel<7, true>);
-        case 16: return launch(attnres_kernel<8, false>);
-        case 17: return launch(attnres_kernel<8, true>);
+    // rows held as fp32 up to 384 threads; above, as bf16 while that fits 64
+    // registers without spilling much (M <= 5), else read again
+    const int hold = threads <= 384 ? kArKeepF32 : M <= 5 ? kArKeepBf16 : kArReread;
+    switch (M * 4 + hold) {
+        case 5: return launch(attnres_kernel<1, kArKeepF32>);
+        case 6: return launch(attnres_kernel<1, kArKeepBf16>);
+        case 9: return launch(attnres_kernel<2, kArKeepF32>);
+        case 10: return launch(attnres_kernel<2, kArKeepBf16>);
+        case 13: return launch(attnres_kernel<3, kArKeepF32>);
+        case 14: return launch(attnres_kernel<3, kArKeepBf16>);
+        case 17: return launch(attnres_kernel<4, kArKeepF32>);
+        case 18: return launch(attnres_kernel<4, kArKeepBf16>);
+        case 21: return launch(attnres_kernel<5, kArKeepF32>);
+        case 22: return launch(attnres_kernel<5, kArKeepBf16>);
+        case 24: return launch(attnres_kernel<6, kArReread>);
+        case 25: return launch(attnres_kernel<6, kArKeepF32>);
+        case 28: return launch(attnres_kernel<7, kArReread>);
+        case 29: return launch(attnres_kernel<7, kArKeepF32>);
+        case 32: return launch(attnres_kernel<8, kArReread>);
+        case 33: return launch(attnres_kernel<8, kArKeepF32>);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -33,7 +33,10 @@ def _wl(M, T, C):
     return Workload("attnres", B=1, H=M, grid=(1, 1, T), d=C, layer="attnres")
 
 
-CASES = [(1, 1, 256), (2, 7, 256), (4, 13, 2560), (5, 9, 4096), (8, 17, 512), (3, 100, 768)]
+CASES = [(1, 1, 256), (2, 7, 256), (4, 13, 2560), (5, 9, 4096), (8, 17, 512), (3, 100, 768),
+         # more than 384 threads a CTA: rows held in bf16 (M <= 5) or read again (M > 5),
+         # and more tokens than resident CTAs, so that every slot is refilled
+         (1, 5, 4096), (2, 50, 3328), (5, 1500, 4096), (6, 9, 3584), (8, 700, 4096)]
 
 
 @pytest.mark.parametrize("M,T,C", CASES, ids=[f"M{m}T{t}C{c}" for m, t, c in CASES])
