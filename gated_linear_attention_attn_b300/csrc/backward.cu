@@ -386,24 +386,33 @@ cudaError_t launch_backward_bf16(const void* q, const void* k, const void* v, co
     float* dzpart = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dspart) +
                                              tc_apply_partial_bytes(BH, N, num_sms));
     cudaError_t e;
+    // Each launch after the first is a programmatic dependent of the one before:
+    // its CTAs set up (and, where its tiles are inputs of the call, prefetch) as
+    // the previous grid's CTAs leave their SMs.
     if ((e = launch_tc_state(k, v, S, B, H, N, rope, ws, status, num_sms, stream)) != cudaSuccess)
         return e;
     // num on the tensor cores, the gate terms in the apply kernel's epilogue (a, dg,
     // dden), and dS = sum qr a^T from the same tiles
     if ((e = launch_tc_apply(q, g, S, A, B, H, N, rope, eps, status, num_sms, stream,
-                             kApplyTerms, dout, dg, dden, dspart)) != cudaSuccess)
+                             kApplyTerms, dout, dg, dden, dspart, nullptr, kPdlState)) !=
+        cudaSuccess)
         return e;
     // dq = [q > 0] (R^T (S a) + dden z), and dz = sum dden phi(q) from its q tiles
+    // (a and dden come from the launch before: nothing is read before it ends)
     if ((e = launch_tc_apply(A, q, S, dq, B, H, N, rope, eps, status, num_sms, stream,
-                             kApplyGrad, nullptr, nullptr, dden, nullptr, dzpart)) != cudaSuccess)
+                             kApplyGrad, nullptr, nullptr, dden, nullptr, dzpart,
+                             kPdlWaitAll)) != cudaSuccess)
         return e;
-    if ((e = launch_tc_ds_merge(dspart, dzpart, dS, B, H, N, num_sms, stream)) != cudaSuccess)
+    if ((e = launch_tc_ds_merge(dspart, dzpart, dS, B, H, N, num_sms, stream, true)) !=
+        cudaSuccess)
         return e;
-    // dk = [k > 0] (R^T (dS v) + dz), dv = dS^T kr
+    // dk = [k > 0] (R^T (dS v) + dz), dv = dS^T kr; v and k prefetched, dS waited for
     if ((e = launch_tc_apply(v, k, dS, dk, B, H, N, rope, eps, status, num_sms, stream,
-                             kApplyGrad)) != cudaSuccess)
+                             kApplyGrad, nullptr, nullptr, nullptr, nullptr, nullptr,
+                             kPdlState)) != cudaSuccess)
         return e;
-    return launch_tc_apply(k, k, dS, dv, B, H, N, rope, eps, status, num_sms, stream, kApplyRaw);
+    return launch_tc_apply(k, k, dS, dv, B, H, N, rope, eps, status, num_sms, stream, kApplyRaw,
+                           nullptr, nullptr, nullptr, nullptr, nullptr, kPdlState);
 }
 
 cudaError_t launch_backward_f32(const float* q, const float* k, const float* v, const float* g,

@@ -102,18 +102,23 @@ cudaError_t launch_tc_state(const void* k, const void* v, void* state, int B, in
 constexpr int kApplyGate = 0, kApplyRaw = 1, kApplyTerms = 2, kApplyGrad = 3;
 // dspart (mode 2): the dS partial slots, tc_apply_partial_bytes; dzpart (mode 3,
 // nullable): the dz partials sum_i dden_i phi(g_i), tc_apply_zpart_bytes.
+// pdl: kPdlNone a plain launch; kPdlState a programmatic dependent of a kernel
+// of ours that writes only the state (tiles are prefetched, the state waited
+// for); kPdlWaitAll a programmatic dependent that waits before any read.
+constexpr int kPdlNone = 0, kPdlState = 1, kPdlWaitAll = 2;
 cudaError_t launch_tc_apply(const void* q, const void* g, const void* state, void* out, int B,
                             int H, int N, const RopeView* rope, float eps, unsigned* status,
                             int num_sms, cudaStream_t stream, int mode = kApplyGate,
                             const void* dout = nullptr, void* dg = nullptr,
                             float* dden = nullptr, float* dspart = nullptr,
-                            float* dzpart = nullptr);
+                            float* dzpart = nullptr, int pdl = kPdlNone);
 size_t tc_apply_partial_bytes(int BH, int N, int num_sms);
 size_t tc_apply_zpart_bytes(int BH, int N, int num_sms);
 // The dS state (bf16 S^T rows and fp32 z, as the state kernel writes a state)
 // from the gate terms' dS partials and the masked gradient's dz partials.
+// (pdl: launched as a programmatic dependent of the kernel before it)
 cudaError_t launch_tc_ds_merge(const float* dspart, const float* dzpart, void* state, int B, int H,
-                               int N, int num_sms, cudaStream_t stream);
+                               int N, int num_sms, cudaStream_t stream, bool pdl = false);
 
 // RoPE table (rope_table.cu): the header, then every token's pairs as fp16
 // and as fp32, from the grid and band split or from caller-given fp32 pairs.

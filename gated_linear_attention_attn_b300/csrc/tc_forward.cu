@@ -96,6 +96,9 @@ struct ApplyParams {
     float* dspart;                  // kApTerms: dS partial slots (cta + head), S^T layout
     float* dzpart;                  // kApGrad (null: none): sum_i w_i phi(g_i) per
                                     // slot (cta + head) and transform warp, [.][8][128]
+    int wait_all;                   // launched as a dependent whose tiles, weights or
+                                    // partials the preceding grid writes: every thread
+                                    // waits for it before its first read
 };
 
 // =================================================================== state ==
@@ -776,6 +779,9 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             prefetch_tmap(&tm_dg);
         }
         if (kTmemRope) prefetch_tmap(&tm_d);
+        // a dependent launch of ours may start its prologue (its CTAs take an
+        // SM as ours leave it)
+        griddep_launch_dependents();
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, kCols);
@@ -785,6 +791,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if (p.wait_all) griddep_wait();
 
     if (warp == 0) {
         // ------------------------------------------------ Q producer (+ the heads' states)
@@ -2132,6 +2139,9 @@ struct DsMergeParams {
 
 __global__ void __launch_bounds__(kScanThreads)
 ds_merge_kernel(DsMergeParams p) {
+    // (launched as a programmatic dependent: the partials are complete after this)
+    griddep_wait();
+    griddep_launch_dependents();
     const int head = blockIdx.x, rg = blockIdx.y, t = threadIdx.x;
     const int n = kScanRows * rg + (t >> 4), cc = t & 15;
     const bool with_z = rg == 0 && t < kHeadDim;
@@ -2312,7 +2322,7 @@ cudaError_t launch_state(const void* k, const void* v, int BH, int N, const Rope
 
 cudaError_t launch_apply(const void* q, const void* g, const uint8_t* state, void* out, int BH,
                          int N, const RopeView* rope, float eps, unsigned* status, int num_sms,
-                         bool after_state, cudaStream_t stream, int nb = 1, int tok0 = 0,
+                         int pdl, cudaStream_t stream, int nb = 1, int tok0 = 0,
                          int mode = kApGate, const void* dout = nullptr, void* dg = nullptr,
                          float* dden = nullptr, float* dspart = nullptr, float* dzpart = nullptr) {
     const Plan pl = make_plan(BH, N, num_sms);
@@ -2339,6 +2349,7 @@ cudaError_t launch_apply(const void* q, const void* g, const uint8_t* state, voi
     ap.dden = dden;
     ap.dspart = dspart;
     ap.dzpart = dzpart;
+    ap.wait_all = pdl == kPdlWaitAll ? 1 : 0;
     if (rope) ap.rope = *rope;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(pl.ap.G);
@@ -2351,10 +2362,11 @@ cudaError_t launch_apply(const void* q, const void* g, const uint8_t* state, voi
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    // Only right after our own state (or block scan) kernel: Q and G are then
-    // complete before this grid starts, whatever wrote them.
+    // A programmatic dependent only right after a kernel of ours: kPdlState when
+    // that kernel writes nothing but the state (Q and G are then complete before
+    // this grid starts, whatever wrote them), kPdlWaitAll otherwise.
     cfg.attrs = attr;
-    cfg.numAttrs = after_state ? 1 : 0;
+    cfg.numAttrs = pdl != kPdlNone ? 1 : 0;
     if (mode == kApRaw) {
         if (rope)
             return cudaLaunchKernelEx(&cfg, tc_apply_kernel<true, kApRaw>, mq, mg, mo, md, mdg, ap);
@@ -2515,11 +2527,11 @@ cudaError_t launch_tc_state(const void* k, const void* v, void* state, int B, in
 cudaError_t launch_tc_apply(const void* q, const void* g, const void* state, void* out, int B,
                             int H, int N, const RopeView* rope, float eps, unsigned* status,
                             int num_sms, cudaStream_t stream, int mode, const void* dout,
-                            void* dg, float* dden, float* dspart, float* dzpart) {
+                            void* dg, float* dden, float* dspart, float* dzpart, int pdl) {
     cudaError_t e = configure(current_device());
     if (e != cudaSuccess) return e;
     return launch_apply(q, g, static_cast<const uint8_t*>(state), out, B * H, N, rope, eps,
-                        status, num_sms, false, stream, 1, 0, mode, dout, dg, dden, dspart,
+                        status, num_sms, pdl, stream, 1, 0, mode, dout, dg, dden, dspart,
                         dzpart);
 }
 
@@ -2534,11 +2546,19 @@ size_t tc_apply_zpart_bytes(int BH, int N, int num_sms) {
 }
 
 cudaError_t launch_tc_ds_merge(const float* dspart, const float* dzpart, void* state, int B, int H,
-                               int N, int num_sms, cudaStream_t stream) {
+                               int N, int num_sms, cudaStream_t stream, bool pdl) {
     const Plan pl = make_plan(B * H, N, num_sms);
     DsMergeParams mp{dspart, dzpart, static_cast<uint8_t*>(state), pl.ap, pl.Tq};
-    ds_merge_kernel<<<dim3(B * H, kHeadDim / kScanRows), kScanThreads, 0, stream>>>(mp);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(B * H, kHeadDim / kScanRows);
+    cfg.blockDim = dim3(kScanThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, ds_merge_kernel, mp);
 }
 
 int tc_forward_cluster(int dev, int BH, int N, bool rope, int num_sms) {
@@ -2591,8 +2611,8 @@ cudaError_t launch_tc_block_causal(const void* q, const void* k, const void* v, 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if ((e = cudaLaunchKernelEx(&cfg, block_scan_kernel, sp)) != cudaSuccess) return e;
-    return launch_apply(q, g, states, out, BHs, block_tokens, rope, eps, status, num_sms, true,
-                        stream, nb, rope_offset);
+    return launch_apply(q, g, states, out, BHs, block_tokens, rope, eps, status, num_sms,
+                        kPdlState, stream, nb, rope_offset);
 }
 
 cudaError_t launch_tc_two_phase(const void* q, const void* k, const void* v, const void* g,
@@ -2607,7 +2627,7 @@ cudaError_t launch_tc_two_phase(const void* q, const void* k, const void* v, con
     if ((e = launch_state(k, v, BH, N, rope, workspace, state, status, num_sms, stream)) !=
         cudaSuccess)
         return e;
-    return launch_apply(q, g, state, out, BH, N, rope, eps, status, num_sms, true, stream);
+    return launch_apply(q, g, state, out, BH, N, rope, eps, status, num_sms, kPdlState, stream);
 }
 
 }  // namespace sla
