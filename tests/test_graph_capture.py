@@ -214,3 +214,42 @@ def test_attnres_replays_in_a_graph(cuda_device):
     torch.cuda.synchronize(cuda_device)
     assert sla.last_device_status(device=cuda_device) == 0
     assert torch.equal(out, ref)
+
+
+def test_backward_replays_with_new_inputs(cuda_device):
+    """The bf16 backward's six launches, each after the first a programmatic dependent of
+    the one before, captured into one graph: with new inputs copied into the captured
+    buffers before each replay, every replay gives the eager call's gradients for those
+    inputs, bit for bit (heads span several CTAs, so the state kernel's counters and the
+    dS and dz partial slots are all used)."""
+    sla = _sla()
+    wl = Workload("graph_bwd", B=2, H=4, grid=(4, 10, 110), rope=True)
+    rope = sla.RopeTable(wl.grid, wl.split, wl.base, device=cuda_device)
+
+    def inputs(seed):
+        q, k, v, g = make_inputs(wl, seed=seed)
+        gen = torch.Generator().manual_seed(seed + 1000)
+        dout = torch.randn(q.shape, generator=gen).to(wl.dtype)
+        return [t.to(cuda_device) for t in (q, k, v, g, dout)]
+
+    bufs = inputs(36)
+    stream = torch.cuda.Stream(cuda_device)
+    stream.wait_stream(torch.cuda.current_stream(cuda_device))
+    with torch.cuda.stream(stream):
+        sla.linattn_backward(*bufs, rope=rope, stream=stream)      # this stream's workspace
+    stream.synchronize()
+    grads = [torch.full_like(bufs[0], float("nan")) for _ in range(4)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        sla.linattn_backward(*bufs, rope=rope, grads=grads, stream=stream)
+    for seed in (37, 38):
+        new = inputs(seed)
+        with torch.cuda.stream(stream):
+            for dst, src in zip(bufs, new):
+                dst.copy_(src)
+            graph.replay()
+            want = sla.linattn_backward(*new, rope=rope, stream=stream)
+        stream.synchronize()
+        assert sla.last_device_status(device=cuda_device) == 0
+        for name, a, b in zip(("dq", "dk", "dv", "dg"), grads, want):
+            assert torch.equal(a, b), (seed, name)
