@@ -919,24 +919,10 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (end) mma_commit(&dsfull[dseg & 1]);
                 return true;
             };
-            for (long long u = u0; ok && u < u1; ++u, ++it) {
-                const int h = (int)(u / p.Tq);
-                if (h != cur_h) {
-                    if (heads > 0) mma_commit(sfree);      // old state no longer read
-                    ok = mbar_wait(sready, heads & 1, abort_flag, p.status);
-                    if (!ok) break;
-                    ++heads;
-                    cur_h = h;
-                }
-                const int s = (int)(it % QS);
-                const uint32_t round = (uint32_t)(it / QS);
-                const int a = (int)(it & 1);
-                const uint32_t around = (uint32_t)(it >> 1);
-                // (kApGrad: the tile is multiplied as it landed)
-                ok = mbar_wait(&accempty[a], (around & 1) ^ 1, abort_flag, p.status) &&
-                     (kGrad || mbar_wait(&qready[s], round & 1, abort_flag, p.status)) &&
-                     mbar_wait(&qfull[s], round & 1, abort_flag, p.status);
-                if (!ok) break;
+            // num of tile i (its waits passed)
+            auto issue_num = [&](long long i) {
+                const int s = (int)(i % QS);
+                const int a = (int)(i & 1);
                 tc_fence_after();
                 const uint32_t qb = smem0 + s * kApTile;
 #pragma unroll
@@ -952,13 +938,96 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     mma_bf16(tmem + (uint32_t)a * 128, ad, bd, idesc, ks > 0 ? 1u : 0u);
                 }
                 mma_commit(&accfull[a]);
-                if constexpr (kDS) {
-                    if (it >= 1 && !(ok = issue_ds(it - 1))) break;
-                } else {
+            };
+            if constexpr (kDS) {
+                // num of tile nn and dS of tile nd < nn in whichever order their
+                // inputs are ready: a tile's dS goes out as soon as its a is staged,
+                // which frees its Q and G slots for the loads two tiles ahead
+                // (behind the next num it would hold both rings a tile longer)
+                const long long T = u1 - u0;
+                long long nn = 0, nd = 0;
+                int nh = (int)(u0 / p.Tq), ntile = (int)(u0 % p.Tq);   // of unit u0 + nn
+                int dtile = ntile;                                      // of unit u0 + nd
+                bool released = false;
+                uint64_t last = global_ns();
+                while (ok && nd < T) {
+                    bool progress = false;
+                    if (nn < T) {
+                        if (nh != cur_h) {
+                            if (heads > 0 && !released) {
+                                mma_commit(sfree);         // old state no longer read
+                                released = true;
+                            }
+                            if (mbar_test_wait(sready, heads & 1)) {
+                                ++heads;
+                                cur_h = nh;
+                                released = false;
+                                progress = true;
+                            }
+                        }
+                        const int s = (int)(nn % QS), a = (int)(nn & 1);
+                        const uint32_t round = (uint32_t)(nn / QS), around = (uint32_t)(nn >> 1);
+                        if (nh == cur_h && mbar_test_wait(&accempty[a], (around & 1) ^ 1) &&
+                            mbar_test_wait(&qready[s], round & 1) &&
+                            mbar_test_wait(&qfull[s], round & 1)) {
+                            issue_num(nn);
+                            ++nn;
+                            if (++ntile == p.Tq) {
+                                ntile = 0;
+                                ++nh;
+                            }
+                            progress = true;
+                        }
+                    }
+                    if (nd < nn) {
+                        // a head segment's first dS: its buffer's segment before last
+                        // is written out
+                        const bool start = nd == 0 || dtile == 0;
+                        const int sg = dseg + (start ? 1 : 0);
+                        if ((!start || sg < 2 ||
+                             mbar_test_wait(&dsfree[sg & 1], (uint32_t)(((sg >> 1) - 1) & 1))) &&
+                            mbar_test_wait(&gempty[nd % GS], (uint32_t)((nd / GS) & 1))) {
+                            if (!(ok = issue_ds(nd))) break;
+                            ++nd;
+                            if (++dtile == p.Tq) dtile = 0;
+                            progress = true;
+                        }
+                    }
+                    if (progress) {
+                        last = global_ns();
+                    } else if (*abort_flag) {
+                        ok = false;
+                    } else if (global_ns() - last > kWaitLimitNs) {
+                        raise_status(p.status, kStatusTimeout);
+                        *abort_flag = 1;
+                        ok = false;
+                    } else {
+                        __nanosleep(32);
+                    }
+                }
+            } else {
+                for (long long u = u0; ok && u < u1; ++u, ++it) {
+                    const int h = (int)(u / p.Tq);
+                    if (h != cur_h) {
+                        if (heads > 0) mma_commit(sfree);      // old state no longer read
+                        ok = mbar_wait(sready, heads & 1, abort_flag, p.status);
+                        if (!ok) break;
+                        ++heads;
+                        cur_h = h;
+                    }
+                    const int s = (int)(it % QS);
+                    const uint32_t round = (uint32_t)(it / QS);
+                    const int a = (int)(it & 1);
+                    const uint32_t around = (uint32_t)(it >> 1);
+                    // (kApGrad: the tile is multiplied as it landed)
+                    ok = mbar_wait(&accempty[a], (around & 1) ^ 1, abort_flag, p.status) &&
+                         (kGrad || mbar_wait(&qready[s], round & 1, abort_flag, p.status)) &&
+                         mbar_wait(&qfull[s], round & 1, abort_flag, p.status);
+                    if (!ok) break;
+                    issue_num(it);
                     mma_commit(&qempty[s]);               // the Q slot may be refilled
                 }
             }
-            if (kDS && ok && it >= 1) issue_ds(it - 1);
             mma_commit(mma_done);
             mbar_wait_drain(mma_done, 0);
         }
