@@ -384,6 +384,67 @@ class L2Scrub:
         torch.sum(self.read, dim=0, out=self.sink)
 
 
+E2E_NOTE = ("pinned host buffers, two device buffer sets: every step uploads its inputs, runs the "
+            "call and reads its outputs back; the upload of step i+1 overlaps the read-back of "
+            "step i (the host link is full duplex)")
+
+
+def pipelined_e2e(dev, stream, ke, dev_ins, host_ins, dev_outs, run):
+    """Device seconds of ke end-to-end steps, their bytes in and out.
+
+    Each step copies host_ins (pinned) to a set of device inputs on an upload stream, runs
+    run(inputs, outputs) on `stream`, and copies the outputs back to pinned host buffers on a
+    download stream. Two sets of device buffers alternate, so that one step's upload overlaps
+    the previous step's read-back; every step still moves all of its own bytes.
+    """
+    ins = [list(dev_ins), [torch.empty_like(t) for t in dev_ins]]
+    outs = [list(dev_outs), [torch.empty_like(t) for t in dev_outs]]
+    houts = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_outs]
+             for _ in range(2)]
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    uploaded, computed, read = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
+
+    def one(i):
+        sl = i & 1
+        if i >= 2:
+            up.wait_event(computed[sl])          # step i - 2 has consumed these inputs
+        with torch.cuda.stream(up):
+            for d, h in zip(ins[sl], host_ins):
+                d.copy_(h, non_blocking=True)
+        uploaded[sl].record(up)
+        stream.wait_event(uploaded[sl])
+        if i >= 2:
+            stream.wait_event(read[sl])          # and its outputs are read back
+        run(ins[sl], outs[sl])
+        computed[sl].record(stream)
+        down.wait_event(computed[sl])
+        with torch.cuda.stream(down):
+            for h, d in zip(houts[sl], outs[sl]):
+                h.copy_(d, non_blocking=True)
+        read[sl].record(down)
+
+    for i in range(2):
+        one(i)
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed():
+        t0.record(up)
+        for i in range(ke):
+            one(i)
+        t1.record(down)
+        t1.synchronize()
+
+    if SAMPLER is not None:
+        with SAMPLER.timed():
+            timed()
+    else:
+        timed()
+    bi = sum(t.numel() * t.element_size() for t in host_ins)
+    bo = sum(t.numel() * t.element_size() for t in dev_outs)
+    return t0.elapsed_time(t1) / 1e3, bi, bo
+
+
 def run_sla(args, rank, world, local):
     from gated_linear_attention_attn_b300 import sla
 
@@ -489,26 +550,24 @@ def run_sla(args, rank, world, local):
     # -------- end to end through the public call, host buffers in pinned memory
     e2e = None
     if not args.no_e2e:
-        hq, hk, hv, hg = (t.pin_memory() for t in host)
-        hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-        bi = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg))
-        bo = hout.numel() * hout.element_size()
+        def run_e2e(ins, outs):
+            if blocks:
+                sla.linattn_forward_block_causal(*ins, wl.block_tokens, out=outs[0], rope=rope,
+                                                 eps=wl.eps, state_in=carried,
+                                                 state_out=carried, stream=stream)
+            else:
+                sla.linattn_forward(*ins, out=outs[0], rope=rope, eps=wl.eps, stream=stream)
 
-        def e2e_step():
-            for dst, src in ((q, hq), (k, hk), (v, hv), (g, hg)):
-                dst.copy_(src, non_blocking=True)
-            step()
-            hout.copy_(out, non_blocking=True)
-
-        e2e_step()
         ke = max(3, min(args.steps, 10))
         _barrier(world)
         torch.cuda.synchronize(dev)
-        esecs = _max_over_ranks(_time_steps(e2e_step, ke, stream), world, dev)
+        esecs, bi, bo = pipelined_e2e(dev, stream, ke, (q, k, v, g),
+                                      tuple(t.pin_memory() for t in host), (out,), run_e2e)
+        esecs = _max_over_ranks(esecs, world, dev)
         _barrier(world)
         e2e = {"value": world * wl.token_heads * ke / esecs, "unit": UNIT,
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": ke,
-               "ms_per_step": 1e3 * esecs / ke}
+               "ms_per_step": 1e3 * esecs / ke, "note": E2E_NOTE}
 
     workloads = None
     if world == 1 and wl.name == HEADLINE and not args.no_workloads:
@@ -614,23 +673,16 @@ def run_backward(args, rank, world, local):
     per_step = secs / args.steps
     e2e = None
     if not args.no_e2e:
-        hin = tuple(t.pin_memory() for t in host)
-        hout = tuple(torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in range(4))
+        def run_e2e(ins, outs):
+            sla.linattn_backward(*ins, rope=rope, eps=wl.eps, grads=outs, stream=stream)
 
-        def e2e_step():
-            for dst, src in zip((q, k, v, g, dout), hin):
-                dst.copy_(src, non_blocking=True)
-            step()
-            for dst, src in zip(hout, grads):
-                dst.copy_(src, non_blocking=True)
-
-        e2e_step()
         ke = max(3, min(args.steps, 10))
-        esecs = _max_over_ranks(_time_steps(e2e_step, ke, stream), world, dev)
+        esecs, bi, bo = pipelined_e2e(dev, stream, ke, (q, k, v, g, dout),
+                                      tuple(t.pin_memory() for t in host), tuple(grads), run_e2e)
+        esecs = _max_over_ranks(esecs, world, dev)
         e2e = {"value": world * wl.token_heads * ke / esecs, "unit": UNIT,
-               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin),
-               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout),
-               "steps": ke, "ms_per_step": 1e3 * esecs / ke}
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+               "steps": ke, "ms_per_step": 1e3 * esecs / ke, "note": E2E_NOTE}
     if rank != 0:
         return
     peak, peak_src = measured_peaks()
@@ -759,22 +811,16 @@ def run_anchor(args, rank, world, local):
         raise RuntimeError("device status after timing")
     e2e = None
     if not args.no_e2e:
-        hin = tuple(t.pin_memory() for t in host)
-        hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        def run_e2e(ins, outs):
+            sla.anchor_forward(*ins, out=outs[0], rope=rope, stream=stream)
 
-        def e2e_step():
-            for dst, src in zip((q, k, v, g), hin):
-                dst.copy_(src, non_blocking=True)
-            step()
-            hout.copy_(out, non_blocking=True)
-
-        e2e_step()
         ke = max(3, min(args.steps, 10))
-        esecs = _max_over_ranks(_time_steps(e2e_step, ke, stream), world, dev)
+        esecs, bi, bo = pipelined_e2e(dev, stream, ke, (q, k, v, g),
+                                      tuple(t.pin_memory() for t in host), (out,), run_e2e)
+        esecs = _max_over_ranks(esecs, world, dev)
         e2e = {"value": world * wl.token_heads * ke / esecs, "unit": UNIT,
-               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin),
-               "d2h_bytes_per_step": hout.numel() * hout.element_size(),
-               "steps": ke, "ms_per_step": 1e3 * esecs / ke}
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+               "steps": ke, "ms_per_step": 1e3 * esecs / ke, "note": E2E_NOTE}
     if rank != 0:
         return
     burst, sustained, src = measured_tensor_peaks()
@@ -900,22 +946,17 @@ def run_attnres(args, rank, world, local):
     per_step = secs / args.steps
     e2e = None
     if not args.no_e2e:
-        hs, hw = host[0].pin_memory(), host[1].pin_memory()
-        hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        def run_e2e(ins, outs):
+            sla.attnres_aggregate(ins[0], ins[1], eps=1e-6, out=outs[0], stream=stream)
 
-        def e2e_step():
-            s.copy_(hs, non_blocking=True)
-            w.copy_(hw, non_blocking=True)
-            step()
-            hout.copy_(out, non_blocking=True)
-
-        e2e_step()
         ke = max(3, min(args.steps, 10))
-        esecs = _max_over_ranks(_time_steps(e2e_step, ke, stream), world, dev)
+        esecs, bi, bo = pipelined_e2e(dev, stream, ke, (s, w),
+                                      (host[0].pin_memory(), host[1].pin_memory()), (out,),
+                                      run_e2e)
+        esecs = _max_over_ranks(esecs, world, dev)
         e2e = {"value": world * wl.tokens * ke / esecs, "unit": ATTNRES_UNIT,
-               "h2d_bytes_per_step": hs.numel() * hs.element_size() + hw.numel() * 4,
-               "d2h_bytes_per_step": hout.numel() * hout.element_size(),
-               "steps": ke, "ms_per_step": 1e3 * esecs / ke}
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+               "steps": ke, "ms_per_step": 1e3 * esecs / ke, "note": E2E_NOTE}
     if rank != 0:
         return
     peak, peak_src = measured_peaks()
