@@ -1956,8 +1956,9 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             }
         }
         // every warp of this CTA has written its share: tell the cluster
+        // (each arrive releases at cluster scope what this thread has seen
+        // through flushdone: the other warps' partial rows and z)
         if (rt == 0 && ok && mbar_wait(flushdone, 0, abort_flag, p.status)) {
-            fence_acq_rel_cluster();
             for (int q = 0; q < C; ++q) mbar_arrive_cluster(mapa_shared(smem_u32(pready), q));
         }
         if (ok) ok = warp_wait_cluster(pready, 0, abort_flag, p.status);
@@ -2015,8 +2016,9 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             fence_proxy_async_all();
             __syncwarp();
             if (lane == 0) mbar_arrive(reddone);
+            // (each arrive releases at cluster scope the rows every warp wrote
+            // into the cluster's state buffers, as seen through reddone)
             if (rt == 0 && mbar_wait(reddone, 0, abort_flag, p.status)) {
-                fence_acq_rel_cluster();
                 for (int q = 0; q < C; ++q) mbar_arrive_cluster(mapa_shared(smem_u32(sready), q));
             }
         }
