@@ -1589,7 +1589,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     uint64_t* pready = flushdone + 1;        // every CTA's partial written (C arrivals)
     uint64_t* zready = pready + 1;           // z of the head in zs (4 warps)
     uint64_t* reddone = zready + 1;          // this CTA's rows written everywhere (8 warps)
-    uint64_t* sready = reddone + 1;          // the state is complete here (C arrivals)
+    uint64_t* sready = reddone + 1;          // the state is complete here (own rows, others' bytes)
     uint64_t* qfull = sready + 1;
     uint64_t* qready = qfull + kApQStages;
     uint64_t* qempty = qready + kApQStages;
@@ -1624,7 +1624,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         mbar_init(pready, C);
         mbar_init(zready, kStFWarps);
         mbar_init(reddone, kApEWarps);
-        mbar_init(sready, C);
+        mbar_init(sready, 1);
         for (int s = 0; s < kApQStages; ++s) {
             mbar_init(&qfull[s], 1);
             mbar_init(&qready[s], kApXWarps);
@@ -1978,8 +1978,8 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             if (lane == 0) mbar_arrive(zready);
         }
         // rows [rank*128/C, (rank+1)*128/C) of S^T, summed in rank order from
-        // every CTA's partial (four CTAs' loads in flight at a time) and written
-        // as bf16 into every CTA's state buffer
+        // every CTA's partial (four CTAs' loads in flight at a time), written as
+        // bf16 into this CTA's state buffer and pushed from there to the others
         if (ok) {
             const int r0 = (int)rank * kHeadDim / C, r1 = ((int)rank + 1) * kHeadDim / C;
             const int tasks = (r1 - r0) * 16;
@@ -2010,16 +2010,27 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 w.y = f2_to_bf2(a0.z, a0.w);
                 w.z = f2_to_bf2(a1.x, a1.y);
                 w.w = f2_to_bf2(a1.z, a1.w);
-                const uint32_t dst = sbase + sw128_off(n, cc, kStateHalf);
-                for (int q = 0; q < C; ++q) st_cluster_u4(mapa_shared(dst, q), w);
+                sts128(sbase + sw128_off(n, cc, kStateHalf), w);
             }
-            fence_proxy_async_all();
+            fence_proxy_async_smem();                    // the rows are read by bulk copies
             __syncwarp();
             if (lane == 0) mbar_arrive(reddone);
-            // (each arrive releases at cluster scope the rows every warp wrote
-            // into the cluster's state buffers, as seen through reddone)
             if (rt == 0 && mbar_wait(reddone, 0, abort_flag, p.status)) {
-                for (int q = 0; q < C; ++q) mbar_arrive_cluster(mapa_shared(smem_u32(sready), q));
+                // the rows are contiguous in each 64-column half of the buffer; a
+                // CTA's state is complete when its own rows are written (this
+                // arrival) and the other CTAs' rows have landed (their bytes)
+                const uint32_t rows = (uint32_t)(r1 - r0) * 128;
+                for (int q = 0; q < C; ++q) {
+                    if (q == (int)rank) continue;
+                    const uint32_t bar = mapa_shared(smem_u32(sready), q);
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const uint32_t off = (uint32_t)hh * kStateHalf + (uint32_t)r0 * 128;
+                        bulk_push_cluster(mapa_shared(sbase + off, q), sbase + off, rows, bar);
+                    }
+                }
+                bulk_commit();
+                mbar_arrive_expect_tx(sready, (uint32_t)(kHeadDim - (r1 - r0)) * 256);
+                bulk_wait_read_all();                    // (before the CTA may exit)
             }
         }
         // phase 2: the epilogue of the apply kernel

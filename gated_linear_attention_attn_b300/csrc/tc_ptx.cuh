@@ -228,6 +228,18 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
+// Contiguous bulk copy from this CTA's shared memory into another CTA's of the
+// cluster (dst and bar are shared::cluster addresses: mapa_shared), completion
+// counted in bytes on that CTA's mbarrier; addresses and size 16-byte multiples.
+__device__ __forceinline__ void bulk_push_cluster(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                  uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];" ::"r"(dst),
+        "r"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -306,10 +318,6 @@ __device__ __forceinline__ void st_cluster_u4(uint32_t addr, uint4 v) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
                  : "memory");
-}
-
-__device__ __forceinline__ void fence_acq_rel_cluster() {
-    asm volatile("fence.acq_rel.cluster;" ::: "memory");
 }
 
 // Orders this thread's generic-proxy writes (also those to other CTAs' shared
