@@ -580,24 +580,14 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 const bool done = mbar_wait(slotdone, sg & 1, abort_flag, p.status);
                 int action = 0;                      // 0 none, 1 whole merge, 2 a block of rows
                 if (done && p.merge) {
-                    __threadfence();
+                    // (every flush thread fenced its rows of the slot before slotdone)
                     if (k == 1) {
                         action = 1;                  // one contributor: no count needed
                     } else {
-                        unsigned long long* ctr = p.counters + hh;
-                        count_contributor(ctr, p.epoch, p.status);
-                        if (last_seg && wait_count(ctr, p.epoch, (uint32_t)k, abort_flag,
-                                                   p.status)) {
+                        count_contributor(p.counters + hh, p.epoch, p.status);
+                        if (last_seg && wait_count(p.counters + hh, p.epoch, (uint32_t)k,
+                                                   abort_flag, p.status))
                             action = 2;
-                            // Each of the m CTAs sharing the merge counts once more
-                            // after it has seen all k contributors; the one that
-                            // reaches k + m returns the counter to zero, so the
-                            // next launch (a graph replay reuses its epoch) starts
-                            // from an empty count.
-                            const uint32_t m = (uint32_t)(e_hi - lo + 1);
-                            if (count_contributor(ctr, p.epoch, p.status) == (uint32_t)k + m)
-                                atomicExch(ctr, 0ull);
-                        }
                     }
                     __threadfence();
                 }
@@ -618,6 +608,16 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 const int m = e_hi - lo + 1, j = cta - lo;
                 // a shared merge happens only at the CTA's last segment: the ring is idle
                 ok = merge_rows_bulk(hh, lo, hi, j * kHeadDim / m, (j + 1) * kHeadDim / m, j == 0);
+                // Each of the m CTAs sharing the merge counts once more after it has
+                // seen all k contributors (here, after its merge, off the way to the
+                // state); the one that reaches k + m returns the counter to zero, so
+                // the next launch (a graph replay reuses its epoch) starts from an
+                // empty count.
+                if (ft == 0) {
+                    unsigned long long* ctr = p.counters + hh;
+                    if (count_contributor(ctr, p.epoch, p.status) == (uint32_t)(k + m))
+                        atomicExch(ctr, 0ull);
+                }
             }
         }
         // no bulk copy of ours may still be landing when the CTA exits
