@@ -72,11 +72,16 @@ static_assert(kApGate == kApplyGate && kApRaw == kApplyRaw && kApTerms == kApply
 // of a G stage and the den slots.  The gate terms stage g and dout tiles
 // together, in two stages of each ring.  The masked gradient holds a Q tile
 // only from its load to its MMA (two stages), and gives the third stage's
-// room to the RoPE rows on their way to TMEM.
+// room to the RoPE rows on their way to TMEM.  The raw product reads only Q:
+// its G slots just stage the output, two of them suffice (a slot is refilled
+// once the store of the tile before has read it), and the third becomes a
+// fourth Q stage, so more of the one input stream is in flight.
 template <int MODE>
 struct ApGeo {
-    static constexpr int kQS = MODE == kApTerms || MODE == kApGrad ? 2 : kApQStages;
-    static constexpr int kGS = MODE == kApTerms ? 2 : kApGStages;
+    static constexpr int kQS = MODE == kApTerms || MODE == kApGrad ? 2
+                               : MODE == kApRaw                    ? kApQStages + 1
+                                                                   : kApQStages;
+    static constexpr int kGS = MODE == kApTerms || MODE == kApRaw ? 2 : kApGStages;
     static constexpr int kGT = MODE == kApTerms ? 2 * kApTile : kApTile;
     static constexpr int kDS = MODE == kApTerms ? 2 : kApDSlots;   // den slots
 };

@@ -2306,6 +2306,7 @@ static_assert(st_smem<true>() <= 232448 && st_smem<false>() <= 232448, "state ke
 static_assert(ap_smem<true>() <= 232448 && ap_smem<false>() <= 232448, "apply kernel smem");
 static_assert(ap_smem<true, kApTerms>() <= 232448, "apply kernel smem, gate terms");
 static_assert(ap_smem<true, kApGrad>() <= 232448, "apply kernel smem, masked gradient");
+static_assert(ap_smem<true, kApRaw>() <= 232448, "apply kernel smem, raw product");
 
 struct Plan {
     int Tk, Tq;
@@ -2345,8 +2346,10 @@ cudaError_t configure(int dev) {
     if ((e = set_smem(tc_state_kernel<true>, st_smem<true>())) != cudaSuccess) return e;
     if ((e = set_smem(tc_apply_kernel<false, kApGate>, ap_smem<false>())) != cudaSuccess) return e;
     if ((e = set_smem(tc_apply_kernel<true, kApGate>, ap_smem<true>())) != cudaSuccess) return e;
-    if ((e = set_smem(tc_apply_kernel<false, kApRaw>, ap_smem<false>())) != cudaSuccess) return e;
-    if ((e = set_smem(tc_apply_kernel<true, kApRaw>, ap_smem<true>())) != cudaSuccess) return e;
+    if ((e = set_smem(tc_apply_kernel<false, kApRaw>, ap_smem<false, kApRaw>())) != cudaSuccess)
+        return e;
+    if ((e = set_smem(tc_apply_kernel<true, kApRaw>, ap_smem<true, kApRaw>())) != cudaSuccess)
+        return e;
     if ((e = set_smem(tc_apply_kernel<false, kApTerms>, ap_smem<false, kApTerms>())) !=
         cudaSuccess)
         return e;
@@ -2439,6 +2442,7 @@ cudaError_t launch_apply(const void* q, const void* g, const uint8_t* state, voi
     cfg.dynamicSmemBytes =
         mode == kApTerms  ? (rope ? ap_smem<true, kApTerms>() : ap_smem<false, kApTerms>())
         : mode == kApGrad ? (rope ? ap_smem<true, kApGrad>() : ap_smem<false, kApGrad>())
+        : mode == kApRaw  ? (rope ? ap_smem<true, kApRaw>() : ap_smem<false, kApRaw>())
                           : (rope ? ap_smem<true>() : ap_smem<false>());
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
