@@ -617,6 +617,8 @@ def run_sla(args, rank, world, local):
 
 BWD_METRIC = "linear-attn bwd token-heads/s; HBM GB/s as % of B300 peak"
 BWD_LAUNCHES = 6
+BWD_FROM_STATE_PLAN = ("backward from the forward's kept state: the same launches without "
+                       "the state kernel")
 BWD_PLAN = ("backward: state(k, v), apply gate terms(q, g, dout; S) + dS partials, "
             "apply masked gradient(a; S, q) -> dq + dz partials, dS merge, "
             "apply masked gradient(v; dS, k) -> dk, apply raw(k; dS) -> dv "
@@ -671,6 +673,32 @@ def run_backward(args, rank, world, local):
     _barrier(world)
     secs = _max_over_ranks(secs, world, dev)
     per_step = secs / args.steps
+    # bf16: the same backward from the state a forward kept (in training the
+    # forward writes each head's state and the backward reuses it)
+    from_state = None
+    if wl.dtype == torch.bfloat16:
+        _, state = sla.linattn_forward_keep_state(q, k, v, g, rope=rope, eps=wl.eps,
+                                                  stream=stream)
+
+        def step_from_state():
+            sla.linattn_backward(q, k, v, g, dout, rope=rope, eps=wl.eps, grads=grads,
+                                 stream=stream, state=state)
+
+        for _ in range(max(args.warmup, 3)):
+            step_from_state()
+        _barrier(world)
+        torch.cuda.synchronize(dev)
+        fsecs = _time_steps(step_from_state, args.steps, stream, scrub)
+        torch.cuda.synchronize(dev)
+        _barrier(world)
+        fsecs = _max_over_ranks(fsecs, world, dev) / args.steps
+        if sla.last_device_status(stream, dev) != sla.OK:
+            raise RuntimeError("device status after the backward from a kept state")
+        from_state = {"ms_per_step": 1e3 * fsecs, "value": world * wl.token_heads / fsecs,
+                      "unit": UNIT, "hbm_frac": alg / fsecs / 1e9 / measured_peaks()[0],
+                      "launch_plan": BWD_FROM_STATE_PLAN,
+                      "gpu_launches_per_step": BWD_LAUNCHES - 1}
+        del state
     e2e = None
     if not args.no_e2e:
         def run_e2e(ins, outs):
@@ -710,6 +738,8 @@ def run_backward(args, rank, world, local):
         "gpu_launches": launches * args.steps,
         "clocks": _stop_sampler(),
     }
+    if from_state is not None:
+        line["from_state"] = from_state
     if not args.no_cpu_baseline:
         heads = [(b, h) for b in range(wl.B) for h in range(wl.H)]
         done, elapsed = 0, 0.0
@@ -1032,7 +1062,8 @@ def run_attnres_reference(args, rank, world):
 # forward configurations, the pages' 736-row 720p bucket, the block-causal form, the
 # backward, and the anchor and AttnRes layers.
 EXTRA_WORKLOADS = ("5b_480p", "14b_480p", "5b_720p_60s", "5b_720p_736", "5b_720p_block5",
-                   "5b_720p:backward", "anchor_5b_720p", "anchor_5b_480p", "attnres_5b_720p",
+                   "5b_720p:backward", "5b_720p:backward_from_state", "5b_720p:train_step",
+                   "5b_480p:train_step", "anchor_5b_720p", "anchor_5b_480p", "attnres_5b_720p",
                    "attnres_14b_480p")
 
 
@@ -1129,6 +1160,39 @@ def time_workloads(args, dev, stream):
                        algorithmic_bytes=alg, launch_plan=BWD_PLAN, l2=l2,
                        gpu_launches_per_step=BWD_LAUNCHES)
             del q, k, v, g, dout, rope, grads
+        elif pass_ in ("backward_from_state", "train_step"):
+            # training: the forward keeps each head's state and the backward reuses
+            # it; backward_from_state times the backward alone (the state kept by
+            # one forward before the timing), train_step the forward and backward
+            q, k, v, g, dout = _device_inputs(wl, dev, 5)
+            rope = sla.RopeTable(wl.grid, wl.split, wl.base, device=dev) if wl.rope else None
+            grads = tuple(torch.empty_like(q) for _ in range(4))
+            out = torch.empty_like(q)
+            _, state = sla.linattn_forward_keep_state(q, k, v, g, out=out, rope=rope, eps=wl.eps,
+                                                      stream=stream)
+            cluster = sla.forward_cluster(wl.B, wl.H, wl.N, wl.rope, device=dev)
+            tensor = wl.B * wl.H * wl.N * wl.d * wl.elem_size
+
+            def bwd():
+                sla.linattn_backward(q, k, v, g, dout, rope=rope, eps=wl.eps, grads=grads,
+                                     stream=stream, state=state)
+            if pass_ == "train_step":
+                def step():
+                    sla.linattn_forward_keep_state(q, k, v, g, out=out, rope=rope, eps=wl.eps,
+                                                   state=state, stream=stream)
+                    bwd()
+                alg, launches = 14 * tensor, (1 if cluster > 0 else 2) + BWD_LAUNCHES - 1
+                plan = (_forward_plan(wl, cluster) + ", keeping the state; then "
+                        + BWD_FROM_STATE_PLAN)
+            else:
+                step, alg, launches = bwd, 9 * tensor, BWD_LAUNCHES - 1
+                plan = BWD_FROM_STATE_PLAN
+            secs, l2 = timed(step, alg)
+            rec.update(ms=1e3 * secs, value=wl.token_heads / secs, unit=UNIT,
+                       hbm_gbs=alg / secs / 1e9, hbm_frac=alg / secs / 1e9 / peak,
+                       algorithmic_bytes=alg, launch_plan=plan, l2=l2,
+                       gpu_launches_per_step=launches)
+            del q, k, v, g, dout, rope, grads, out, state
         else:
             q, k, v, g = _device_inputs(wl, dev)
             rope = sla.RopeTable(wl.grid, wl.split, wl.base, device=dev) if wl.rope else None

@@ -201,15 +201,23 @@ sla_status_t sla_rope_table_from_pairs(float* table, const float* pairs, int N, 
     return SLA_OK;
 }
 
-// Shared body of both forward entry points.
+// Shared body of the forward entry points; state_out (bf16 only) receives the
+// heads' states when not null.
 static sla_status_t forward(const void* q, const void* k, const void* v, const void* g,
                             void* out, int B, int H, int N, int d,
                             const float* rope, float eps, sla_stream_t stream,
-                            bool is_f32) {
+                            bool is_f32, void* state_out = nullptr) {
     RopeView rv{};
     sla_status_t st = check_forward(q, k, v, g, out, B, H, N, d, rope, eps,
                                     is_f32 ? sizeof(float) : 2, &rv);
     if (st != SLA_OK) return st;
+    if (state_out) {                       // a further output: overlaps no other buffer
+        const size_t bytes = (size_t)B * H * N * d * 2;
+        const void* ins[5] = {q, k, v, g, out};
+        const size_t sizes[5] = {bytes, bytes, bytes, bytes, bytes};
+        if ((st = check_buffers(ins, sizes, 5, state_out, tc_state_bytes(B * H))) != SLA_OK)
+            return st;
+    }
     const RopeView* rp = rope ? &rv : nullptr;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -230,13 +238,13 @@ static sla_status_t forward(const void* q, const void* k, const void* v, const v
                               (const float*)g, (float*)out, B, H, N, rp, eps, (float*)ws, C,
                               ds->status, s);
     } else if (const int C = tc_forward_cluster(dev, BH, N, rp != nullptr, ds->num_sms)) {
-        err = launch_tc_fused(q, k, v, g, out, B, H, N, C, rp, eps, ds->status, s);
+        err = launch_tc_fused(q, k, v, g, out, B, H, N, C, rp, eps, ds->status, s, state_out);
     } else {
         if ((st = workspace(dev, s, tc_workspace_bytes(BH, N, ds->num_sms), &ws,
                             tc_counter_bytes(BH))) != SLA_OK)
             return st;
         err = launch_tc_two_phase(q, k, v, g, out, B, H, N, rp, eps, (float*)ws, ds->status,
-                                  ds->num_sms, s);
+                                  ds->num_sms, s, state_out);
     }
     if (err != cudaSuccess) {
         cudaGetLastError();
@@ -259,22 +267,32 @@ sla_status_t sla_linattn_forward_f32(const float* q, const float* k, const float
     return forward(q, k, v, g, out, B, H, N, d, rope_table, eps, stream, true);
 }
 
-// Shared body of both backward entry points.
+sla_status_t sla_linattn_forward_keep_state(const void* q, const void* k, const void* v,
+                                            const void* g, void* out, int B, int H, int N, int d,
+                                            const float* rope_table, float eps, void* state,
+                                            sla_stream_t stream) {
+    if (!state) return SLA_ERR_INVALID_ARG;
+    return forward(q, k, v, g, out, B, H, N, d, rope_table, eps, stream, false, state);
+}
+
+// Shared body of the backward entry points; `state` (bf16 only) is the heads'
+// states of the forward, or null to recompute them.
 static sla_status_t backward(const void* q, const void* k, const void* v, const void* g,
                              const void* dout, void* dq, void* dk, void* dv, void* dg, int B,
                              int H, int N, int d, const float* rope, float eps,
-                             sla_stream_t stream, bool is_f32) {
+                             sla_stream_t stream, bool is_f32, const void* state = nullptr) {
     if (!q || !k || !v || !g || !dout || !dq || !dk || !dv || !dg) return SLA_ERR_INVALID_ARG;
     sla_status_t st = check_dims(B, H, N, d);
     if (st == SLA_ERR_INVALID_ARG) return st;
     if (bad_eps(eps)) return SLA_ERR_INVALID_ARG;
     if (st != SLA_OK) return st;
     const size_t bytes = (size_t)B * H * N * d * (is_f32 ? 4 : 2);
-    const void* ins[5] = {q, k, v, g, dout};
-    const size_t sizes[5] = {bytes, bytes, bytes, bytes, bytes};
+    const void* ins[6] = {q, k, v, g, dout, state};
+    const size_t sizes[6] = {bytes, bytes, bytes, bytes, bytes, tc_state_bytes(B * H)};
+    const int n_ins = state ? 6 : 5;
     void* outs[4] = {dq, dk, dv, dg};
     for (int i = 0; i < 4; ++i)
-        if ((st = check_buffers(ins, sizes, 5, outs[i], bytes)) != SLA_OK) return st;
+        if ((st = check_buffers(ins, sizes, n_ins, outs[i], bytes)) != SLA_OK) return st;
     for (int i = 0; i < 4; ++i)                      // the gradients overlap one another neither
         for (int j = i + 1; j < 4; ++j) {
             const uintptr_t x = reinterpret_cast<uintptr_t>(outs[i]);
@@ -310,7 +328,7 @@ static sla_status_t backward(const void* q, const void* k, const void* v, const 
                                      (float*)dv, (float*)dg, B, H, N, rp, eps, (float*)ws, C,
                                      ds->status, s)
                : launch_backward_bf16(q, k, v, g, dout, dq, dk, dv, dg, B, H, N, rp, eps,
-                                      (float*)ws, ds->num_sms, ds->status, s);
+                                      (float*)ws, ds->num_sms, ds->status, s, state);
     if (err != cudaSuccess) {
         cudaGetLastError();
         return SLA_ERR_CUDA;
@@ -332,6 +350,16 @@ sla_status_t sla_linattn_backward_f32(const float* q, const float* k, const floa
                                       const float* rope_table, float eps,
                                       sla_stream_t stream) {
     return backward(q, k, v, g, dout, dq, dk, dv, dg, B, H, N, d, rope_table, eps, stream, true);
+}
+
+sla_status_t sla_linattn_backward_from_state(const void* q, const void* k, const void* v,
+                                             const void* g, const void* dout, const void* state,
+                                             void* dq, void* dk, void* dv, void* dg, int B, int H,
+                                             int N, int d, const float* rope_table, float eps,
+                                             sla_stream_t stream) {
+    if (!state) return SLA_ERR_INVALID_ARG;
+    return backward(q, k, v, g, dout, dq, dk, dv, dg, B, H, N, d, rope_table, eps, stream, false,
+                    state);
 }
 
 sla_status_t sla_anchor_forward(const void* q, const void* k, const void* v, const void* g,

@@ -371,14 +371,16 @@ size_t backward_bf16_workspace_bytes(int BH, int N, int num_sms) {
 cudaError_t launch_backward_bf16(const void* q, const void* k, const void* v, const void* g,
                                  const void* dout, void* dq, void* dk, void* dv, void* dg, int B,
                                  int H, int N, const RopeView* rope, float eps, float* workspace,
-                                 int num_sms, unsigned* status, cudaStream_t stream) {
+                                 int num_sms, unsigned* status, cudaStream_t stream,
+                                 const void* state) {
     const int BH = B * H;
     const size_t tensor = (size_t)BH * N * kHeadDim * 2;
     // workspace: the state kernel's, the two states, a ([rows][128] bf16), dden,
     // then the partials of dS and of dz
     uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
-    uint8_t* S = ws + tc_state_workspace_bytes(BH, N, num_sms);
-    uint8_t* dS = S + (size_t)BH * kStateBytesB;
+    uint8_t* own_S = ws + tc_state_workspace_bytes(BH, N, num_sms);
+    const void* S = state ? state : own_S;      // a given state is only read
+    uint8_t* dS = own_S + (size_t)BH * kStateBytesB;
     uint8_t* A = dS + (size_t)BH * kStateBytesB;
     float* dden = reinterpret_cast<float*>(A + tensor);
     float* dspart = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dden) +
@@ -389,13 +391,17 @@ cudaError_t launch_backward_bf16(const void* q, const void* k, const void* v, co
     // Each launch after the first is a programmatic dependent of the one before:
     // its CTAs set up (and, where its tiles are inputs of the call, prefetch) as
     // the previous grid's CTAs leave their SMs.
-    if ((e = launch_tc_state(k, v, S, B, H, N, rope, ws, status, num_sms, stream)) != cudaSuccess)
+    // (with a given state the gate terms are the call's first launch, and wait
+    // for whatever ran before on the stream, as its tiles may come from there)
+    if (!state &&
+        (e = launch_tc_state(k, v, own_S, B, H, N, rope, ws, status, num_sms, stream)) !=
+            cudaSuccess)
         return e;
     // num on the tensor cores, the gate terms in the apply kernel's epilogue (a, dg,
     // dden), and dS = sum qr a^T from the same tiles
     if ((e = launch_tc_apply(q, g, S, A, B, H, N, rope, eps, status, num_sms, stream,
-                             kApplyTerms, dout, dg, dden, dspart, nullptr, kPdlState)) !=
-        cudaSuccess)
+                             kApplyTerms, dout, dg, dden, dspart, nullptr,
+                             state ? kPdlNone : kPdlState)) != cudaSuccess)
         return e;
     // dq = [q > 0] (R^T (S a) + dden z), and dz = sum dden phi(q) from its q tiles
     // (a and dden come from the launch before: nothing is read before it ends)

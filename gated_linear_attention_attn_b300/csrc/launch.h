@@ -28,15 +28,17 @@ cudaError_t launch_simt_state_partials(const float* k, const float* v, int B, in
                                        unsigned* status, cudaStream_t stream);
 
 // Backward (backward.cu): dq, dk, dv, dg of L = sum(dout * o).  bf16: six
-// launches of the tensor-core state and apply kernels, workspace
-// backward_bf16_workspace_bytes(BH, N, num_sms).  fp32:
+// launches of the tensor-core state and apply kernels (five when the heads'
+// states are given: state, tc_state_bytes as launch_tc_state writes them),
+// workspace backward_bf16_workspace_bytes(BH, N, num_sms).  fp32:
 // three launches over C chunks per head, workspace backward_workspace_bytes(BH, C).
 size_t backward_workspace_bytes(int BH, int C);
 size_t backward_bf16_workspace_bytes(int BH, int N, int num_sms);
 cudaError_t launch_backward_bf16(const void* q, const void* k, const void* v, const void* g,
                                  const void* dout, void* dq, void* dk, void* dv, void* dg, int B,
                                  int H, int N, const RopeView* rope, float eps, float* workspace,
-                                 int num_sms, unsigned* status, cudaStream_t stream);
+                                 int num_sms, unsigned* status, cudaStream_t stream,
+                                 const void* state = nullptr);
 cudaError_t launch_backward_f32(const float* q, const float* k, const float* v, const float* g,
                                 const float* dout, float* dq, float* dk, float* dv, float* dg,
                                 int B, int H, int N, const RopeView* rope, float eps,
@@ -71,15 +73,16 @@ size_t tc_state_bytes(int BH);
 // The forward runs either as one fused launch (one cluster of C CTAs per
 // head, no workspace) or as the state and apply launches.
 // tc_forward_cluster gives C for the shape on device `dev`, 0 for the two
-// launches.
+// launches.  Either also writes the heads' states (tc_state_bytes, the layout
+// launch_tc_state writes) to state_out when it is not null.
 int tc_forward_cluster(int dev, int BH, int N, bool rope, int num_sms);
 cudaError_t launch_tc_fused(const void* q, const void* k, const void* v, const void* g, void* out,
                             int B, int H, int N, int C, const RopeView* rope, float eps,
-                            unsigned* status, cudaStream_t stream);
+                            unsigned* status, cudaStream_t stream, void* state_out = nullptr);
 cudaError_t launch_tc_two_phase(const void* q, const void* k, const void* v, const void* g,
                                 void* out, int B, int H, int N, const RopeView* rope, float eps,
                                 float* workspace, unsigned* status, int num_sms,
-                                cudaStream_t stream);
+                                cudaStream_t stream, void* state_out = nullptr);
 // Block-causal form (tc_forward.cu): N = nb * block_tokens tokens per head,
 // the RoPE rows of tokens [rope_offset, rope_offset + N) of the grid, carried
 // states in and out (null for none).  Workspace: tc_workspace_bytes(B*H*nb,

@@ -1538,7 +1538,9 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 // CTA r sums rows [r*128/C, (r+1)*128/C) of the C partial S^T through
 // distributed shared memory and writes them, as bf16 in the MMA layout, into
 // every CTA's state buffer.  Phase 2: CTA r applies the state to its share of
-// the head's Q and G tiles as the apply kernel does.  The cluster meets only
+// the head's Q and G tiles as the apply kernel does.  With p.state_out, CTA r
+// also copies its rows of the state (and CTA 0 the head's z) to global memory,
+// in the layout the state kernel writes, for a backward that reuses it.  The cluster meets only
 // on mbarriers with bounded waits, and on one cluster barrier just before
 // exit, which every thread reaches after bounded work.
 //
@@ -1561,6 +1563,7 @@ struct FusedParams {
     RopeView rope;
     float eps;
     unsigned* status;
+    uint8_t* state_out;         // null, or the heads' states (kStateBytes each) written out
 };
 
 template <bool ROPE>
@@ -1974,6 +1977,7 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             for (int q = 0; q < kFuMaxCluster; ++q)
                 if (q < C) z += zq[q];
             zs[rt] = z;
+            if (p.state_out) fence_proxy_async_smem();   // z is read by a bulk copy
             __syncwarp();
             if (lane == 0) mbar_arrive(zready);
         }
@@ -2027,6 +2031,17 @@ tc_fused_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                         const uint32_t off = (uint32_t)hh * kStateHalf + (uint32_t)r0 * 128;
                         bulk_push_cluster(mapa_shared(sbase + off, q), sbase + off, rows, bar);
                     }
+                }
+                if (p.state_out) {
+                    // the same rows to the head's state in global memory, and z from
+                    // CTA 0 (this thread is one of z's writers; it waits for the rest)
+                    uint8_t* dst = p.state_out + (size_t)h * kStateBytes;
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const uint32_t off = (uint32_t)hh * kStateHalf + (uint32_t)r0 * 128;
+                        bulk_store(dst + off, sbase + off, rows);
+                    }
+                    if (rank == 0 && mbar_wait(zready, 0, abort_flag, p.status))
+                        bulk_store(dst + kStateSBytes, smem_u32(zs), kHeadDim * 4);
                 }
                 bulk_commit();
                 mbar_arrive_expect_tx(sready, (uint32_t)(kHeadDim - (r1 - r0)) * 256);
@@ -2556,7 +2571,7 @@ int fused_cluster(int dev, int BH, int N, bool rope, int num_sms) {
 
 cudaError_t launch_fused(const void* q, const void* k, const void* v, const void* g, void* out,
                          int BH, int N, int C, const RopeView* rope, float eps, unsigned* status,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, uint8_t* state_out) {
     CUtensorMap mk, mv, mq, mg, mo;
     if (!make_map(&mk, k, N, BH, kStTok) || !make_map(&mv, v, N, BH, kStTok) ||
         !make_map(&mq, q, N, BH, kApTok) || !make_map(&mg, g, N, BH, kApTok) ||
@@ -2572,6 +2587,7 @@ cudaError_t launch_fused(const void* q, const void* k, const void* v, const void
     if (rope) fp.rope = *rope;
     fp.eps = eps;
     fp.status = status;
+    fp.state_out = state_out;
     cudaLaunchAttribute attr[1];
     if (rope) {
         cudaLaunchConfig_t cfg = fused_config<true>(BH, C, stream, attr);
@@ -2657,10 +2673,11 @@ int tc_forward_cluster(int dev, int BH, int N, bool rope, int num_sms) {
 
 cudaError_t launch_tc_fused(const void* q, const void* k, const void* v, const void* g, void* out,
                             int B, int H, int N, int C, const RopeView* rope, float eps,
-                            unsigned* status, cudaStream_t stream) {
+                            unsigned* status, cudaStream_t stream, void* state_out) {
     cudaError_t e = configure(current_device());
     if (e != cudaSuccess) return e;
-    return launch_fused(q, k, v, g, out, B * H, N, C, rope, eps, status, stream);
+    return launch_fused(q, k, v, g, out, B * H, N, C, rope, eps, status, stream,
+                        static_cast<uint8_t*>(state_out));
 }
 
 cudaError_t launch_tc_block_causal(const void* q, const void* k, const void* v, const void* g,
@@ -2704,12 +2721,13 @@ cudaError_t launch_tc_block_causal(const void* q, const void* k, const void* v, 
 cudaError_t launch_tc_two_phase(const void* q, const void* k, const void* v, const void* g,
                                 void* out, int B, int H, int N, const RopeView* rope, float eps,
                                 float* workspace, unsigned* status, int num_sms,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, void* state_out) {
     const int BH = B * H;
     cudaError_t e = configure(current_device());
     if (e != cudaSuccess) return e;
-    uint8_t* state =
-        reinterpret_cast<uint8_t*>(workspace) + tc_state_workspace_bytes(BH, N, num_sms);
+    uint8_t* state = state_out ? static_cast<uint8_t*>(state_out)
+                               : reinterpret_cast<uint8_t*>(workspace) +
+                                     tc_state_workspace_bytes(BH, N, num_sms);
     if ((e = launch_state(k, v, BH, N, rope, workspace, state, status, num_sms, stream)) !=
         cudaSuccess)
         return e;

@@ -240,6 +240,16 @@ __device__ __forceinline__ void bulk_push_cluster(uint32_t dst, uint32_t src, ui
         : "memory");
 }
 
+// Contiguous bulk copy from this CTA's shared memory to global memory (src a
+// shared::cta address; addresses and size 16-byte multiples), in the thread's
+// current bulk group.
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                     reinterpret_cast<uint64_t>(dst)),
+                 "r"(src), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

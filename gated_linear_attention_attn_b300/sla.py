@@ -56,6 +56,10 @@ _BWD_ARGS = [_vp] * 9 + [_int] * 4 + [_vp, _flt, _vp]
 for _name in ("sla_linattn_backward", "sla_linattn_backward_f32"):
     getattr(_lib, _name).argtypes = _BWD_ARGS
     getattr(_lib, _name).restype = _int
+_lib.sla_linattn_forward_keep_state.argtypes = _FWD_ARGS[:-1] + [_vp, _vp]
+_lib.sla_linattn_forward_keep_state.restype = _int
+_lib.sla_linattn_backward_from_state.argtypes = [_vp] * 10 + [_int] * 4 + [_vp, _flt, _vp]
+_lib.sla_linattn_backward_from_state.restype = _int
 _lib.sla_anchor_forward.argtypes = [_vp] * 5 + [_int] * 4 + [_vp, _vp]
 _lib.sla_anchor_forward.restype = _int
 _lib.sla_attnres_aggregate.argtypes = [ctypes.POINTER(_vp), _int, _int, _int, _vp, _flt, _vp,
@@ -75,7 +79,9 @@ EXPORTED = ("sla_rope_table_floats", "sla_rope_table_fill", "sla_rope_table_from
             "sla_linattn_forward_f32", "sla_linattn_state_bytes", "sla_linattn_state",
             "sla_linattn_apply", "sla_linattn_forward_noalloc", "sla_linattn_forward_cluster",
             "sla_linattn_carried_state_bytes", "sla_linattn_forward_block_causal",
-            "sla_linattn_backward", "sla_linattn_backward_f32", "sla_anchor_forward",
+            "sla_linattn_backward", "sla_linattn_backward_f32",
+            "sla_linattn_forward_keep_state", "sla_linattn_backward_from_state",
+            "sla_anchor_forward",
             "sla_attnres_aggregate", "sla_status_string", "sla_last_device_status",
             "sla_selftest_wait_timeout")
 
@@ -336,6 +342,39 @@ def linattn_apply(q: torch.Tensor, g: torch.Tensor, state: torch.Tensor,
     return out
 
 
+def linattn_forward_keep_state(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                               g: torch.Tensor, out: Optional[torch.Tensor] = None,
+                               rope: Optional[RopeTable] = None, eps: float = 1e-6,
+                               state: Optional[torch.Tensor] = None,
+                               stream: Optional[torch.cuda.Stream] = None):
+    """The bf16 forward that also writes the heads' states for the backward
+    (``sla_linattn_forward_keep_state``): returns (out, state), state a uint8 device
+    buffer of ``state_bytes(B, H)`` bytes as ``linattn_state`` writes it."""
+    _check_bf16("q", q)
+    for name, t in (("k", k), ("v", v), ("g", g)):
+        _check_bf16(name, t, like=q)
+    B, H, N, d = q.shape
+    nbytes = state_bytes(B, H, d)
+    if nbytes == 0:
+        raise SlaError(UNSUPPORTED, "linattn_forward_keep_state: shape")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check_bf16("out", out, like=q)
+    if state is None:
+        state = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    elif state.device != q.device or not state.is_contiguous() \
+            or state.numel() * state.element_size() < nbytes:
+        raise SlaError(INVALID_ARG, "linattn_forward_keep_state: state buffer too small")
+    rope_c = _rope_ptr(rope)
+    with torch.cuda.device(q.device):
+        _check(_lib.sla_linattn_forward_keep_state(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(), out.data_ptr(), B, H, N, d,
+            rope_c, float(eps), state.data_ptr(), _stream_handle(stream, q.device)),
+            "sla_linattn_forward_keep_state")
+    return out, state
+
+
 def last_device_status(stream: Optional[torch.cuda.Stream] = None, device="cuda") -> int:
     """Synchronise the stream and read (and clear) the device status word."""
     dev = torch.device(device)
@@ -356,10 +395,13 @@ def selftest_wait_timeout(limit_us: int = 1000, stream: Optional[torch.cuda.Stre
 def linattn_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
                      dout: torch.Tensor, rope: Optional[RopeTable] = None, eps: float = 1e-6,
                      grads: Optional[Sequence[torch.Tensor]] = None,
-                     stream: Optional[torch.cuda.Stream] = None):
+                     stream: Optional[torch.cuda.Stream] = None,
+                     state: Optional[torch.Tensor] = None):
     """(dq, dk, dv, dg) of sum(dout * o) for [B, H, N, d] CUDA tensors (bf16 or fp32;
     ``sla_linattn_backward`` / ``sla_linattn_backward_f32``).  grads: four output
-    tensors to fill, else new ones."""
+    tensors to fill, else new ones.  state (bf16 only): the heads' states of the
+    forward (``linattn_forward_keep_state`` or ``linattn_state``), used instead of
+    recomputing them (``sla_linattn_backward_from_state``)."""
     for name, t in (("k", k), ("v", v), ("g", g), ("dout", dout)):
         if t.shape != q.shape or t.dtype != q.dtype or t.device != q.device \
                 or not t.is_contiguous():
@@ -367,7 +409,14 @@ def linattn_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch
     if q.dim() != 4 or not q.is_contiguous() or q.device.type != "cuda":
         raise SlaError(INVALID_ARG, "linattn_backward: q must be a contiguous [B, H, N, d] "
                                     "CUDA tensor")
-    if q.dtype == torch.bfloat16:
+    if state is not None:
+        if q.dtype != torch.bfloat16:
+            raise SlaError(UNSUPPORTED, "linattn_backward: a given state needs bf16 tensors")
+        if state.device != q.device or not state.is_contiguous() \
+                or state.numel() * state.element_size() < state_bytes(*q.shape[:2], q.shape[3]):
+            raise SlaError(INVALID_ARG, "linattn_backward: state does not match q")
+        fn = _lib.sla_linattn_backward_from_state
+    elif q.dtype == torch.bfloat16:
         fn = _lib.sla_linattn_backward
     elif q.dtype == torch.float32:
         fn = _lib.sla_linattn_backward_f32
@@ -381,9 +430,11 @@ def linattn_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch
             raise SlaError(INVALID_ARG, "linattn_backward: gradient tensors must match q")
     B, H, N, d = q.shape
     rope_c = _rope_ptr(rope)
+    ins = [q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(), dout.data_ptr()]
+    if state is not None:
+        ins.append(state.data_ptr())
     with torch.cuda.device(q.device):
-        _check(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(), dout.data_ptr(),
-                  *(t.data_ptr() for t in grads), B, H, N, d, rope_c, float(eps),
+        _check(fn(*ins, *(t.data_ptr() for t in grads), B, H, N, d, rope_c, float(eps),
                   _stream_handle(stream, q.device)), fn.__name__)
     return tuple(grads)
 

@@ -288,6 +288,32 @@ sla_status_t sla_linattn_backward_f32(const float* q, const float* k, const floa
                                       sla_stream_t stream);
 
 /*
+ * Training without recomputing the state.  A training step runs the forward
+ * and then the backward of the same q, k, v, g; the backward above sums S, z
+ * over k and v again.  sla_linattn_forward_keep_state is sla_linattn_forward
+ * (same launches, same output) that also writes each head's state, as
+ * sla_linattn_state writes it (bf16 S^T, then z in fp32; the two-launch plan
+ * gives the very bytes sla_linattn_state gives, the fused plan the sum of its
+ * cluster's partials in rank order), into `state`: a device buffer of
+ * sla_linattn_state_bytes(B, H, d) bytes, 16-byte aligned, overlapping no
+ * other argument.  sla_linattn_backward_from_state is sla_linattn_backward
+ * (bf16) with that state as S, z instead of its own: one launch and two
+ * tensor passes (k and v) fewer.  Its gradients equal sla_linattn_backward's
+ * bit for bit when the state is the one sla_linattn_state or the two-launch
+ * plan gives for the same k and v; the state is only read, and no output may
+ * overlap it.
+ */
+sla_status_t sla_linattn_forward_keep_state(const void* q, const void* k, const void* v,
+                                            const void* g, void* out, int B, int H, int N, int d,
+                                            const float* rope_table, float eps, void* state,
+                                            sla_stream_t stream);
+sla_status_t sla_linattn_backward_from_state(const void* q, const void* k, const void* v,
+                                             const void* g, const void* dout, const void* state,
+                                             void* dq, void* dk, void* dv, void* dg, int B, int H,
+                                             int N, int d, const float* rope_table, float eps,
+                                             sla_stream_t stream);
+
+/*
  * Forward of the gated-softmax anchor layer ("SANA-Video 2.0", NVlabs/Sana
  * docs/sana_video2.md, section "Architecture": one attention layer in four is
  * a dense softmax layer, 10 heads of 256 in the 5B model, 16 in the 14B

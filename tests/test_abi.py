@@ -234,6 +234,42 @@ def test_backward_rejects_bad_arguments_before_cuda():
             assert bwd(f32=f32, **kw) == want, (f32, kw)
 
 
+def test_training_entries_reject_bad_arguments_before_cuda():
+    lib = sla.raw_lib()
+    sbytes = sla.state_bytes(1, 2)
+    assert sbytes == 2 * (128 * 128 * 2 + 128 * 4)
+
+    def keep(state=A + 5 * STEP, out=A + 4 * STEP, N=256, d=128, eps=1e-6):
+        return lib.sla_linattn_forward_keep_state(A, A + STEP, A + 2 * STEP, A + 3 * STEP, out,
+                                                  1, 2, N, d, None, eps, state, None)
+
+    def bwd(state=A + 9 * STEP, dq=A + 5 * STEP, dv=A + 7 * STEP, N=256, d=128):
+        return lib.sla_linattn_backward_from_state(A, A + STEP, A + 2 * STEP, A + 3 * STEP,
+                                                   A + 4 * STEP, state, dq, A + 6 * STEP, dv,
+                                                   A + 8 * STEP, 1, 2, N, d, None, 1e-6, None)
+
+    for kw, want in [
+        (dict(state=0), sla.INVALID_ARG),
+        (dict(state=A + 5 * STEP + 8), sla.ALIGNMENT),
+        (dict(state=A + 2 * STEP + 4096), sla.INVALID_ARG),      # inside v
+        (dict(state=A + 4 * STEP - sbytes + 16), sla.INVALID_ARG),   # runs into out
+        (dict(N=0), sla.INVALID_ARG),
+        (dict(d=64), sla.UNSUPPORTED),
+        (dict(eps=float("nan")), sla.INVALID_ARG),
+        (dict(out=A + 4 * STEP + 2), sla.ALIGNMENT),
+    ]:
+        assert keep(**kw) == want, kw
+    for kw, want in [
+        (dict(state=0), sla.INVALID_ARG),
+        (dict(state=A + 9 * STEP + 4), sla.ALIGNMENT),
+        (dict(dq=A + 9 * STEP + 1024), sla.INVALID_ARG),         # dq overlaps the state
+        (dict(state=A + 7 * STEP - 16), sla.INVALID_ARG),        # the state runs into dv
+        (dict(N=0), sla.INVALID_ARG),
+        (dict(d=64), sla.UNSUPPORTED),
+    ]:
+        assert bwd(**kw) == want, kw
+
+
 def test_anchor_rejects_bad_arguments_before_cuda():
     lib = sla.raw_lib()
     big = 2 * 256 * 256 * 2                            # one tensor at B=1, H=2, N=256, d=256
