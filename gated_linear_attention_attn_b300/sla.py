@@ -536,3 +536,36 @@ def launches_per_forward(dtype: torch.dtype, B: int = 1, H: int = 1, N: int = 1,
 def raw_lib() -> ctypes.CDLL:
     """The loaded library, for callers that pass raw pointers."""
     return _lib
+
+
+class LinAttnFunction(torch.autograd.Function):
+    """The layer as a torch autograd function, for training: the forward keeps each
+    head's state (bf16: ``linattn_forward_keep_state``) and the backward reuses it
+    (``linattn_backward(..., state=...)``); fp32 tensors take the fp32 forward and the
+    recomputing fp32 backward.  Only argument marshalling happens here; every step runs
+    in the library.  Use ``linattn(q, k, v, g, rope, eps)``."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, g, rope, eps):
+        q, k, v, g = (t.contiguous() for t in (q, k, v, g))
+        if q.dtype == torch.bfloat16:
+            out, state = linattn_forward_keep_state(q, k, v, g, rope=rope, eps=eps)
+        else:
+            out, state = linattn_forward(q, k, v, g, rope=rope, eps=eps), None
+        ctx.save_for_backward(q, k, v, g)
+        ctx.state, ctx.rope, ctx.eps = state, rope, eps
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, g = ctx.saved_tensors
+        grads = linattn_backward(q, k, v, g, dout.contiguous(), rope=ctx.rope, eps=ctx.eps,
+                                 state=ctx.state)
+        ctx.state = None
+        return (*grads, None, None)
+
+
+def linattn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+            rope: Optional[RopeTable] = None, eps: float = 1e-6) -> torch.Tensor:
+    """The layer's forward with autograd support (see ``LinAttnFunction``)."""
+    return LinAttnFunction.apply(q, k, v, g, rope, eps)

@@ -176,3 +176,29 @@ def test_keep_state_rejects_bad_buffers(cuda_device):
         *bargs(state.data_ptr(), state.data_ptr())) == sla.INVALID_ARG
     assert lib.sla_linattn_backward_from_state(*bargs(state.data_ptr(), dq.data_ptr())) == sla.OK
     assert sla.last_device_status(device=cuda_device) == 0
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_autograd_function(dtype, cuda_device):
+    """sla.linattn under torch autograd: its output is the forward's and its
+    gradients the backward's (bit for bit; the two-launch plan for bf16, whose
+    kept state is the recomputed one), and both meet the oracle."""
+    sla = _sla()
+    wl = Workload("autograd", B=2, H=3, grid=(2, 9, 17), dtype=dtype, rope=True)
+    tensors = _inputs(wl, seed=91)
+    q, k, v, g, dout = (t.to(cuda_device) for t in tensors)
+    table = sla.RopeTable(wl.grid, wl.split, wl.base, device=cuda_device)
+    leaves = [t.clone().requires_grad_() for t in (q, k, v, g)]
+    with sla.forward_kernel("split"):
+        out = sla.linattn(*leaves, rope=table, eps=wl.eps)
+        want = sla.linattn_forward(q, k, v, g, rope=table, eps=wl.eps)
+    out.backward(dout)
+    ref = sla.linattn_backward(q, k, v, g, dout, rope=table, eps=wl.eps)
+    assert sla.last_device_status(device=cuda_device) == 0
+    assert torch.equal(out.detach(), want)
+    for name, leaf, r in zip(NAMES, leaves, ref):
+        assert torch.equal(leaf.grad, r), name
+    spec = ol.RopeSpec(*wl.grid, *wl.split, base=wl.base)
+    tol = 1e-5 if dtype == torch.float32 else 1e-2
+    for name, leaf, r in zip(NAMES, leaves, ob.linattn_backward(*tensors, eps=wl.eps, rope=spec)):
+        assert _rel(_np64(leaf.grad), r) <= tol, name
