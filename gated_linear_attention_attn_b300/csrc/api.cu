@@ -8,6 +8,7 @@
 #include <utility>
 
 #include "../../include/sla.h"
+#include "context.h"
 #include "launch.h"
 
 namespace sla {
@@ -220,7 +221,7 @@ static sla_status_t forward(const void* q, const void* k, const void* v, const v
     }
     const RopeView* rp = rope ? &rv : nullptr;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
+    if (bind_current_device(&dev) != cudaSuccess) {
         cudaGetLastError();
         return SLA_ERR_CUDA;
     }
@@ -302,7 +303,7 @@ static sla_status_t backward(const void* q, const void* k, const void* v, const 
     RopeView rv{};
     if ((st = check_rope(rope, N, d, &rv)) != SLA_OK) return st;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
+    if (bind_current_device(&dev) != cudaSuccess) {
         cudaGetLastError();
         return SLA_ERR_CUDA;
     }
@@ -378,7 +379,7 @@ sla_status_t sla_anchor_forward(const void* q, const void* k, const void* v, con
     RopeView rv{};
     if ((st = check_rope(rope_table, N, d, &rv)) != SLA_OK) return st;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
+    if (bind_current_device(&dev) != cudaSuccess) {
         cudaGetLastError();
         return SLA_ERR_CUDA;
     }
@@ -413,7 +414,7 @@ sla_status_t sla_attnres_aggregate(const void* const* sources, int M, int T, int
     }
     if (misaligned(out, 16) || misaligned(w, 16)) return SLA_ERR_ALIGNMENT;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
+    if (bind_current_device(&dev) != cudaSuccess) {
         cudaGetLastError();
         return SLA_ERR_CUDA;
     }
@@ -478,7 +479,7 @@ sla_status_t sla_linattn_forward_block_causal(const void* q, const void* k, cons
     const int nb = N / block_tokens;
     if ((long long)B * H * nb > 0x7fffffffLL / 2) return SLA_ERR_UNSUPPORTED;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
+    if (bind_current_device(&dev) != cudaSuccess) {
         cudaGetLastError();
         return SLA_ERR_CUDA;
     }
@@ -502,7 +503,7 @@ sla_status_t sla_linattn_forward_block_causal(const void* q, const void* k, cons
 int sla_linattn_forward_cluster(int B, int H, int N, int d, int rope) {
     if (check_dims(B, H, N, d) != SLA_OK) return -1;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
+    if (bind_current_device(&dev) != cudaSuccess) {
         cudaGetLastError();
         return -1;
     }
@@ -528,7 +529,7 @@ sla_status_t sla_linattn_state(const void* k, const void* v, void* state, int B,
     RopeView rv{};
     if ((st = check_rope(rope_table, N, d, &rv)) != SLA_OK) return st;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
+    if (bind_current_device(&dev) != cudaSuccess) {
         cudaGetLastError();
         return SLA_ERR_CUDA;
     }
@@ -562,7 +563,7 @@ sla_status_t sla_linattn_apply(const void* q, const void* g, const void* state, 
     RopeView rv{};
     if ((st = check_rope(rope_table, N, d, &rv)) != SLA_OK) return st;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
+    if (bind_current_device(&dev) != cudaSuccess) {
         cudaGetLastError();
         return SLA_ERR_CUDA;
     }
@@ -580,7 +581,7 @@ sla_status_t sla_linattn_apply(const void* q, const void* g, const void* state, 
 sla_status_t sla_selftest_wait_timeout(unsigned int limit_us, sla_stream_t stream) {
     if (limit_us < 1 || limit_us > 1000000u) return SLA_ERR_INVALID_ARG;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
+    if (bind_current_device(&dev) != cudaSuccess) {
         cudaGetLastError();
         return SLA_ERR_CUDA;
     }
@@ -616,7 +617,7 @@ sla_status_t sla_last_device_status(sla_stream_t stream) {
         return SLA_ERR_CUDA;
     }
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return SLA_ERR_CUDA;
+    if (bind_current_device(&dev) != cudaSuccess) return SLA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceState* ds = nullptr;
     sla_status_t st = device_state(dev, &ds);

@@ -9,6 +9,7 @@
 // the address is looked up once per device with cudaGetSymbolAddress.
 #include <mutex>
 
+#include "context.h"
 #include "launch.h"
 
 namespace sla {
@@ -70,7 +71,7 @@ extern "C" sla_status_t sla_linattn_forward_noalloc(const void* q, const void* k
     if (reinterpret_cast<uintptr_t>(device_status) % sizeof(unsigned) != 0)
         return SLA_ERR_ALIGNMENT;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
+    if (bind_current_device(&dev) != cudaSuccess) {
         cudaGetLastError();
         return SLA_ERR_CUDA;
     }

@@ -202,3 +202,42 @@ def test_autograd_function(dtype, cuda_device):
     tol = 1e-5 if dtype == torch.float32 else 1e-2
     for name, leaf, r in zip(NAMES, leaves, ob.linattn_backward(*tensors, eps=wl.eps, rope=spec)):
         assert _rel(_np64(leaf.grad), r) <= tol, name
+
+
+def test_entries_from_a_thread_without_a_current_context(cuda_device):
+    """Calls from a thread that has never made a CUDA context current (as a
+    framework's backward worker may be; torch skips cudaSetDevice when the device
+    number already matches), with the library's workspace already grown so that
+    the call makes no allocation: the library binds the context itself, and the
+    results equal the same calls made from this thread."""
+    import threading
+    sla = _sla()
+    wl = Workload("thread", B=2, H=3, grid=(2, 9, 17), dtype=torch.bfloat16, rope=True)
+    q, k, v, g, dout = (t.to(cuda_device) for t in _inputs(wl, seed=93))
+    table = sla.RopeTable(wl.grid, wl.split, wl.base, device=cuda_device)
+    with sla.forward_kernel("split"):
+        out, state = sla.linattn_forward_keep_state(q, k, v, g, rope=table, eps=wl.eps)
+    want = sla.linattn_backward(q, k, v, g, dout, rope=table, eps=wl.eps, state=state)
+    fwd = sla.linattn_forward(q, k, v, g, rope=table, eps=wl.eps)
+    torch.cuda.synchronize(cuda_device)
+    got = [torch.empty_like(q) for _ in range(4)]
+    got_fwd = torch.empty_like(q)
+    errors = []
+
+    def worker():
+        try:
+            sla.linattn_backward(q, k, v, g, dout, rope=table, eps=wl.eps, grads=got,
+                                 state=state)
+            sla.linattn_forward(q, k, v, g, out=got_fwd, rope=table, eps=wl.eps)
+        except Exception as e:          # reported on the main thread
+            errors.append(e)
+
+    t = threading.Thread(target=worker)
+    t.start()
+    t.join()
+    assert not errors, errors
+    torch.cuda.synchronize(cuda_device)
+    assert sla.last_device_status(device=cuda_device) == 0
+    for name, a, b in zip(NAMES, got, want):
+        assert torch.equal(a, b), name
+    assert torch.equal(got_fwd, fwd)
