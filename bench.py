@@ -1105,12 +1105,13 @@ def time_workloads(args, dev, stream):
     burst, sustained, _ = measured_tensor_peaks()
     scrub = L2Scrub(dev)
 
-    def timed(step, alg_bytes):
+    def timed(step, alg_bytes, on=None):
+        on = on if on is not None else stream
         for _ in range(max(args.warmup, 3)):
             step()
         flush = scrub if alg_bytes < 4 * L2_BYTES else None
-        secs = _time_steps(step, args.steps, stream, flush) / args.steps
-        if sla.last_device_status(stream, dev) != sla.OK:
+        secs = _time_steps(step, args.steps, on, flush) / args.steps
+        if sla.last_device_status(on, dev) != sla.OK:
             raise RuntimeError("device status after a workload")
         return secs, ("L2 flushed between steps" if flush else "inputs larger than L2")
 
@@ -1173,26 +1174,45 @@ def time_workloads(args, dev, stream):
             cluster = sla.forward_cluster(wl.B, wl.H, wl.N, wl.rope, device=dev)
             tensor = wl.B * wl.H * wl.N * wl.d * wl.elem_size
 
-            def bwd():
+            def bwd(on=stream):
                 sla.linattn_backward(q, k, v, g, dout, rope=rope, eps=wl.eps, grads=grads,
-                                     stream=stream, state=state)
+                                     stream=on, state=state)
+            on = stream
             if pass_ == "train_step":
-                def step():
+                # The step's six or seven launches, captured as one CUDA graph and
+                # replayed, as a training loop would run them: eager, the host's
+                # Python and launch overhead per step (two calls) comes close to the
+                # 480p step's device time and would show in it.
+                def eager(s):
                     sla.linattn_forward_keep_state(q, k, v, g, out=out, rope=rope, eps=wl.eps,
-                                                   state=state, stream=stream)
-                    bwd()
+                                                   state=state, stream=s)
+                    bwd(s)
+                on = torch.cuda.Stream(dev)
+                on.wait_stream(stream)
+                with torch.cuda.stream(on):
+                    eager(on)                    # this stream's workspace, before the capture
+                on.synchronize()
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=on):
+                    eager(on)
+
+                def step():
+                    with torch.cuda.stream(on):
+                        graph.replay()
                 alg, launches = 14 * tensor, (1 if cluster > 0 else 2) + BWD_LAUNCHES - 1
                 plan = (_forward_plan(wl, cluster) + ", keeping the state; then "
-                        + BWD_FROM_STATE_PLAN)
+                        + BWD_FROM_STATE_PLAN + "; the step replayed as one CUDA graph")
             else:
                 step, alg, launches = bwd, 9 * tensor, BWD_LAUNCHES - 1
                 plan = BWD_FROM_STATE_PLAN
-            secs, l2 = timed(step, alg)
+            secs, l2 = timed(step, alg, on)
             rec.update(ms=1e3 * secs, value=wl.token_heads / secs, unit=UNIT,
                        hbm_gbs=alg / secs / 1e9, hbm_frac=alg / secs / 1e9 / peak,
                        algorithmic_bytes=alg, launch_plan=plan, l2=l2,
                        gpu_launches_per_step=launches)
             del q, k, v, g, dout, rope, grads, out, state
+            if pass_ == "train_step":
+                del graph
         else:
             q, k, v, g = _device_inputs(wl, dev)
             rope = sla.RopeTable(wl.grid, wl.split, wl.base, device=dev) if wl.rope else None

@@ -2351,11 +2351,16 @@ cudaError_t set_smem(Kernel k, size_t bytes) {
     return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-// Opt-in shared memory is a per-device attribute of a kernel.
+// Opt-in shared memory is a per-device attribute of a kernel.  The entry points
+// call this under locks of their own (the workspace's, the fixed array's), so it
+// takes one of its own too.
 cudaError_t configure(int dev) {
-    static bool done[64] = {};
+    static std::atomic<bool> done[64] = {};
+    static std::mutex mu;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (done[dev]) return cudaSuccess;
+    if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
     cudaError_t e;
     if ((e = set_smem(tc_state_kernel<false>, st_smem<false>())) != cudaSuccess) return e;
     if ((e = set_smem(tc_state_kernel<true>, st_smem<true>())) != cudaSuccess) return e;
@@ -2376,7 +2381,7 @@ cudaError_t configure(int dev) {
         return e;
     if ((e = set_smem(tc_fused_kernel<false>, fu_smem<false>())) != cudaSuccess) return e;
     if ((e = set_smem(tc_fused_kernel<true>, fu_smem<true>())) != cudaSuccess) return e;
-    done[dev] = true;
+    done[dev].store(true, std::memory_order_release);
     return cudaSuccess;
 }
 

@@ -253,3 +253,57 @@ def test_backward_replays_with_new_inputs(cuda_device):
         assert sla.last_device_status(device=cuda_device) == 0
         for name, a, b in zip(("dq", "dk", "dv", "dg"), grads, want):
             assert torch.equal(a, b), (seed, name)
+
+
+@pytest.mark.parametrize("path", ["split", "fused"])
+def test_training_step_replays_with_new_inputs(path, cuda_device):
+    """One training step (the forward keeping its state, then the backward from it:
+    seven or six launches) captured into one graph: with new inputs and upstream
+    gradient copied in before each replay, every replay gives the eager step's output
+    and gradients for those inputs, bit for bit, under both forward plans."""
+    sla = _sla()
+    wl = Workload("graph_train", B=2, H=4, grid=(4, 10, 110), rope=True)
+    rope = sla.RopeTable(wl.grid, wl.split, wl.base, device=cuda_device)
+
+    def inputs(seed):
+        q, k, v, g = make_inputs(wl, seed=seed)
+        gen = torch.Generator().manual_seed(seed + 1000)
+        dout = torch.randn(q.shape, generator=gen).to(wl.dtype)
+        return [t.to(cuda_device) for t in (q, k, v, g, dout)]
+
+    def step(bufs, out, state, grads, stream):
+        q, k, v, g, dout = bufs
+        sla.linattn_forward_keep_state(q, k, v, g, out=out, rope=rope, state=state,
+                                       stream=stream)
+        sla.linattn_backward(q, k, v, g, dout, rope=rope, grads=grads, stream=stream,
+                             state=state)
+
+    bufs = inputs(46)
+    out = torch.full_like(bufs[0], float("nan"))
+    state = torch.zeros(sla.state_bytes(wl.B, wl.H), dtype=torch.uint8, device=cuda_device)
+    grads = [torch.full_like(bufs[0], float("nan")) for _ in range(4)]
+    stream = torch.cuda.Stream(cuda_device)
+    stream.wait_stream(torch.cuda.current_stream(cuda_device))
+    with sla.forward_kernel(path):
+        with torch.cuda.stream(stream):
+            step(bufs, out, state, grads, stream)                 # this stream's workspace
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step(bufs, out, state, grads, stream)
+        for seed in (47, 48):
+            new = inputs(seed)
+            w_out = torch.empty_like(out)
+            w_state = torch.empty_like(state)
+            w_grads = [torch.empty_like(out) for _ in range(4)]
+            with torch.cuda.stream(stream):
+                for dst, src in zip(bufs, new):
+                    dst.copy_(src)
+                graph.replay()
+                step(new, w_out, w_state, w_grads, stream)
+            stream.synchronize()
+            assert sla.last_device_status(device=cuda_device) == 0
+            assert torch.equal(out, w_out), seed
+            assert torch.equal(state, w_state), seed
+            for name, a, b in zip(("dq", "dk", "dv", "dg"), grads, w_grads):
+                assert torch.equal(a, b), (seed, name)
