@@ -404,10 +404,11 @@ cudaError_t launch_backward_bf16(const void* q, const void* k, const void* v, co
                              state ? kPdlNone : kPdlState)) != cudaSuccess)
         return e;
     // dq = [q > 0] (R^T (S a) + dden z), and dz = sum dden phi(q) from its q tiles
-    // (a and dden come from the launch before: nothing is read before it ends)
+    // (a and dden come from the launch before: nothing of them is read before it
+    // ends; the q tiles, inputs of the call, are prefetched)
     if ((e = launch_tc_apply(A, q, S, dq, B, H, N, rope, eps, status, num_sms, stream,
                              kApplyGrad, nullptr, nullptr, dden, nullptr, dzpart,
-                             kPdlWaitAll)) != cudaSuccess)
+                             kPdlWaitAllButG)) != cudaSuccess)
         return e;
     if ((e = launch_tc_ds_merge(dspart, dzpart, dS, B, H, N, num_sms, stream, true)) !=
         cudaSuccess)

@@ -107,8 +107,10 @@ constexpr int kApplyGate = 0, kApplyRaw = 1, kApplyTerms = 2, kApplyGrad = 3;
 // nullable): the dz partials sum_i dden_i phi(g_i), tc_apply_zpart_bytes.
 // pdl: kPdlNone a plain launch; kPdlState a programmatic dependent of a kernel
 // of ours that writes only the state (tiles are prefetched, the state waited
-// for); kPdlWaitAll a programmatic dependent that waits before any read.
-constexpr int kPdlNone = 0, kPdlState = 1, kPdlWaitAll = 2;
+// for); kPdlWaitAll a programmatic dependent that waits before any read;
+// kPdlWaitAllButG the same, except that the G tiles are inputs of the call,
+// which the G producer prefetches without waiting.
+constexpr int kPdlNone = 0, kPdlState = 1, kPdlWaitAll = 2, kPdlWaitAllButG = 3;
 cudaError_t launch_tc_apply(const void* q, const void* g, const void* state, void* out, int B,
                             int H, int N, const RopeView* rope, float eps, unsigned* status,
                             int num_sms, cudaStream_t stream, int mode = kApplyGate,

@@ -98,7 +98,9 @@ struct ApplyParams {
                                     // slot (cta + head) and transform warp, [.][8][128]
     int wait_all;                   // launched as a dependent whose tiles, weights or
                                     // partials the preceding grid writes: every thread
-                                    // waits for it before its first read
+                                    // waits for it before its first read ...
+    int g_inputs;                   // ... but the G producer, when the G tiles are
+                                    // inputs of the call (it prefetches them)
 };
 
 // =================================================================== state ==
@@ -791,7 +793,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    if (p.wait_all) griddep_wait();
+    if (p.wait_all && !(p.g_inputs && warp == 2 + kApXWarps + kApEWarps)) griddep_wait();
 
     if (warp == 0) {
         // ------------------------------------------------ Q producer (+ the heads' states)
@@ -2454,7 +2456,8 @@ cudaError_t launch_apply(const void* q, const void* g, const uint8_t* state, voi
     ap.dden = dden;
     ap.dspart = dspart;
     ap.dzpart = dzpart;
-    ap.wait_all = pdl == kPdlWaitAll ? 1 : 0;
+    ap.wait_all = pdl == kPdlWaitAll || pdl == kPdlWaitAllButG ? 1 : 0;
+    ap.g_inputs = pdl == kPdlWaitAllButG ? 1 : 0;
     if (rope) ap.rope = *rope;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(pl.ap.G);
