@@ -40,3 +40,23 @@ def test_reference_arm_line(workload, unit):
     e2e = line["e2e"]
     assert e2e["value"] == line["value"] and e2e["unit"] == unit
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_headline_line_times_known_workloads_and_passes():
+    """Every entry the headline line times beside the headline names a workload of
+    the table and a pass bench.py knows how to time (forward, backward, the backward
+    from a kept state, the training step); the training passes are on bf16 workloads
+    of the bidirectional layer."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from gated_linear_attention_attn_b300.workloads import WORKLOADS
+    passes = {"", "backward", "backward_from_state", "train_step"}
+    for entry in bench.EXTRA_WORKLOADS:
+        name, _, pass_ = entry.partition(":")
+        assert name in WORKLOADS, entry
+        assert pass_ in passes, entry
+        if pass_:
+            wl = WORKLOADS[name]
+            assert wl.layer == "linear" and not wl.block_frames, entry
+            assert str(wl.dtype) == "torch.bfloat16", entry
+    assert len(set(bench.EXTRA_WORKLOADS)) == len(bench.EXTRA_WORKLOADS)
