@@ -73,6 +73,8 @@ CASES = [
     (2, 3, (1, 1, 1000), False),
     (2, 4, (2, 9, 17), True),
     (1, 1, (4, 32, 32), True),       # 4096 tokens: the fused plan's widest clusters
+    (1, 1, (1, 1, 1), True),         # one token
+    (4, 50, (1, 4, 16), False),      # 200 heads, more than the SMs: the two launches
 ]
 
 
