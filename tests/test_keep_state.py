@@ -91,12 +91,14 @@ def test_keep_state_and_backward_from_it(B, H, grid, rope, plan, cuda_device):
     with sla.forward_kernel(plan):
         want = sla.linattn_forward(q, k, v, g, rope=table, eps=wl.eps)
         out, state = sla.linattn_forward_keep_state(q, k, v, g, rope=table, eps=wl.eps)
+        # the plan the calls took (the fused one does not apply to every shape)
+        split = sla.forward_cluster(B, H, wl.N, rope, device=cuda_device) == 0
     assert sla.last_device_status(device=cuda_device) == 0
     assert torch.equal(out, want)
     assert state.numel() == sla.state_bytes(B, H)
 
     spec = ol.RopeSpec(*wl.grid, *wl.split, base=wl.base) if rope else None
-    if plan == "split":
+    if split:
         assert torch.equal(state, sla.linattn_state(k, v, rope=table))
     else:
         st, z = _decode(state, B, H)
@@ -110,10 +112,15 @@ def test_keep_state_and_backward_from_it(B, H, grid, rope, plan, cuda_device):
 
     got = sla.linattn_backward(q, k, v, g, dout, rope=table, eps=wl.eps, state=state)
     assert sla.last_device_status(device=cuda_device) == 0
-    if plan == "split":
+    if split:
         ref = sla.linattn_backward(q, k, v, g, dout, rope=table, eps=wl.eps)
         for name, a, b in zip(NAMES, got, ref):
             assert torch.equal(a, b), name
+    if wl.N == 1:
+        # one token: dq = phi(k) (v . a) eps / den exactly, a difference of two terms of
+        # size one that cancel to about eps, so the bf16 bound relative to max|ref| does
+        # not apply; the bit-for-bit match with the recomputing backward above stands
+        return
     ref = ob.linattn_backward(*tensors, eps=wl.eps, rope=spec)
     for name, a, b in zip(NAMES, got, ref):
         assert _rel(_np64(a), b) <= 1e-2, name
