@@ -721,7 +721,8 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint64_t* dsfull = rfull + (kTmemRope ? kApXWarps : 0);   // kDS: [2] a segment's dS final
     uint64_t* dsfree = dsfull + (kDS ? 2 : 0);                // kDS: [2] written out
     uint64_t* gread = dsfree + (kDS ? 2 : 0);                 // kDS: [GS] a read by the MMA
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gread + (kDS ? GS : 0));
+    uint64_t* dzread = gread + (kDS ? GS : 0);                // kApGrad: [GS] x read for dz
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dzread + (kGrad ? GS : 0));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -751,6 +752,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int s = 0; s < GS; ++s) {
             mbar_init(&gfull[s], 1);
             mbar_init(&gempty[s], kApEWarps);
+            if (kGrad) mbar_init(&dzread[s], kApXWarps);
         }
         for (int s = 0; s < DS; ++s) {
             mbar_init(&dready[s], kApXWarps);
@@ -1109,6 +1111,10 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tmem_st_wait();
                 tc_fence_before();
             }
+            // the epilogue may start on the tile (its RoPE rows are in TMEM); with
+            // dz it writes over the G slot only once this warp has read it (dzread)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&dready[ds]);
             if (dz) {
                 // the G slot's tile, read before the epilogue writes over it
                 const int h = (int)(u / p.Tq);
@@ -1147,9 +1153,9 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                     for (int j = 0; j < 8; ++j) zacc[j] = 0.f;
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&dzread[gs]);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&dready[ds]);
         }
         // no copy of ours may still be landing when the CTA exits
         if (ROPE && lane == 0 && issued > it) mbar_wait_drain(bar, (uint32_t)((issued - 1) & 1));
@@ -1364,6 +1370,11 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                             csw[4 * sub + 3]);
                         gv[sub] = grad_chunk<ROPE>(gv[sub], v + 8 * sub, cs, w, zw + 8 * sub);
                     }
+                    // with dz, the transform warps read x from the slot: the first
+                    // write over it waits for them
+                    if (ch == 0 && p.dzpart &&
+                        !(ok = warp_wait(&dzread[gs], ground & 1, abort_flag, p.status)))
+                        break;
                 } else {
 #pragma unroll
                     for (int sub = 0; sub < 4; ++sub) {
@@ -1378,6 +1389,7 @@ tc_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                 for (int sub = 0; sub < 4; ++sub) sts128(addr[sub], gv[sub]);
             }
+            if (!ok) break;
             tc_fence_before();
             fence_proxy_async_smem();
             if constexpr (kGrad) {
@@ -2305,7 +2317,7 @@ constexpr size_t ap_smem() {
            kStateBytes +
            ((MODE == kApGrad ? 0 : G::kDS) + (MODE == kApTerms ? 2 : 0)) * kApTok * sizeof(float) +
            (3 * G::kQS + 2 * G::kGS + 2 * G::kDS + 7 + (MODE == kApTerms ? 2 + 4 + G::kGS : 0) +
-            (kTmemRope ? kApXWarps : 0)) *
+            (MODE == kApGrad ? G::kGS : 0) + (kTmemRope ? kApXWarps : 0)) *
                8 +
            16;
 }
