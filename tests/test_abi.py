@@ -134,6 +134,22 @@ def test_binding_rejects_mismatched_tensors():
         sla.linattn_forward(q.to(torch.float16), q, q, q)
 
 
+def test_binding_rejects_bad_training_tensors():
+    import torch
+    q = torch.zeros(1, 2, 8, 128, dtype=torch.bfloat16)
+    with pytest.raises(sla.SlaError):
+        sla.linattn_forward_keep_state(q, q, q, q)           # CPU tensors
+    with pytest.raises(sla.SlaError):
+        sla.linattn_forward_keep_state(q, q, q, q.float())
+    state = torch.zeros(sla.state_bytes(1, 2), dtype=torch.uint8)
+    f = q.float()
+    with pytest.raises(sla.SlaError) as err:
+        sla.linattn_backward(f, f, f, f, f, state=state)     # a kept state needs bf16
+    assert err.value.status in (sla.UNSUPPORTED, sla.INVALID_ARG)
+    with pytest.raises(sla.SlaError):
+        sla.linattn_backward(q, q, q, q, q, state=state[:100])
+
+
 def test_noalloc_forward_rejects_bad_arguments_before_cuda():
     fn = sla.raw_lib().sla_linattn_forward_noalloc
     ok = dict(q=A, k=A + STEP, v=A + 2 * STEP, g=A + 3 * STEP, out=A + 4 * STEP)
